@@ -1,0 +1,411 @@
+"""Benchmark of one paged decode step (slot lookup + K/V write + copy-on-write
+copies + split-context decode + combine) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gqa]
+    python bench.py --impl reference ...     # the CPU oracle, timed the same way
+
+Prints one JSON line.  ``value`` is logical K/V bytes read by decode per second
+over the whole job (inputs resident in HBM, device-timed with CUDA events);
+``e2e`` is the same metric through the public API with the step's inputs
+copied from pinned host memory and the output copied back inside the timed
+region.  The step reads 1 GiB of K/V on the default workload, far more than
+the 129 MB L2, so no L2 flush is needed between steps.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import signal
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+NOMINAL_HBM_GBS = 8000.0
+KERNEL_SOURCES = ["paged_kv_cache_170_gb300/csrc/pa_decode_impl.cuh", "paged_kv_cache_170_gb300/csrc/pa_common.cuh"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per decode-partition launch from the committed ncu summary,
+    if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"decode_partition_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path, encoding="utf-8").read()
+    m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+def workload_inputs(name: str, seed: int, device):
+    from paged_kv_cache_170_gb300 import scenarios, workloads
+
+    if name == "prefix":
+        return scenarios.shared_prefix_inputs(seed, device=device)
+    if name == "longctx":
+        return scenarios.long_context_inputs(seed, device=device)
+    return workloads.make_inputs(workloads.WORKLOADS[name], seed, device=device)
+
+
+def kv_bytes(inp) -> int:
+    """Logical K+V bytes one decode reads: every valid token of every sequence,
+    for every kv head (partial tail blocks count only their valid slots)."""
+    _, Hkv, _, D = inp.k_cache.shape
+    e = inp.k_cache.element_size()
+    return int(inp.context_lens.to(torch.int64).sum().item()) * Hkv * D * e * 2
+
+
+def algorithmic_bytes(inp) -> int:
+    """Bytes the decode kernel must move: K/V + q + out + the table entries it reads + lengths."""
+    B = inp.k_cache.shape[2]
+    lens = inp.context_lens.to(torch.int64)
+    entries = int(((lens + B - 1) // B).sum().item())
+    Hkv = inp.k_cache.shape[1]
+    return kv_bytes(inp) + 2 * inp.q.numel() * inp.q.element_size() + entries * 4 * Hkv + lens.numel() * 4
+
+
+def workload_config(name: str, inp) -> dict:
+    w = inp.workload
+    lens = inp.context_lens.to(torch.int64)
+    return {"workload": f"{name}: {w.note}", "num_seqs": int(inp.q.shape[0]), "block_size": int(inp.k_cache.shape[2]),
+            "num_heads": int(inp.q.shape[1]), "num_kv_heads": int(inp.k_cache.shape[1]),
+            "head_dim": int(inp.q.shape[2]), "pool_blocks": int(inp.k_cache.shape[0]),
+            "context_min": int(lens.min()), "context_max": int(lens.max()), "context_sum": int(lens.sum()),
+            "cow_pairs": int(inp.copy_pairs.shape[0]), "new_tokens": int(inp.new_seq.numel()),
+            "l2_policy": "no flush: each step reads %.2f GB of K/V, larger than the 129 MB L2" % (kv_bytes(inp) / 1e9)}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed loop runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.send_signal(signal.SIGTERM)
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        busy = sorted(sm)[len(sm) // 2:]  # the loaded half of the samples
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def time_cpu_oracle(inp_cpu, max_seconds: float, nthreads: int = 0):
+    """The C oracle on whole sequences of the workload, as many as fit a time
+    budget (at least one).  Returns (GB/s of logical K/V, seconds, sequences, threads)."""
+    from oracle import native
+
+    S = inp_cpu.q.shape[0]
+    tables = inp_cpu.block_tables.numpy()
+    lens = inp_cpu.context_lens.numpy()
+    Hkv, D = inp_cpu.k_cache.shape[1], inp_cpu.k_cache.shape[3]
+    e = inp_cpu.k_cache.element_size()
+    done, t_total, s = 0, 0.0, 0
+    nbytes = 0
+    while s < S and (done == 0 or t_total < max_seconds):
+        t0 = time.perf_counter()
+        native.decode(inp_cpu.q[s:s + 1], inp_cpu.k_cache, inp_cpu.v_cache, tables[s:s + 1], lens[s:s + 1],
+                      inp_cpu.scale, nthreads=nthreads)
+        t_total += time.perf_counter() - t0
+        nbytes += int(lens[s]) * Hkv * D * e * 2
+        done += 1
+        s += 1
+    threads = nthreads if nthreads > 0 else native.max_threads()
+    return nbytes / t_total / 1e9, t_total, done, threads
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return rank, world, local, dist
+    return 0, 1, 0, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(x: float, dist) -> float:
+    if dist is None:
+        return x
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, dist) -> float:
+    if dist is None:
+        return x
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def run_gpu(args) -> dict:
+    from paged_kv_cache_170_gb300 import ops
+
+    rank, world, local, dist = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    # every rank runs its own replica of the workload on different data (weak scaling)
+    inp = workload_inputs(args.workload, args.seed + rank, dev)
+    S, Hq, D = inp.q.shape
+    Hkv, B = inp.k_cache.shape[1], inp.k_cache.shape[2]
+    out = torch.empty_like(inp.q)
+    ws = ops.new_workspace(S, Hq, Hkv, D, dev)
+    slots = torch.empty(inp.new_seq.numel(), dtype=torch.int64, device=dev)
+    err = ops.new_error_word(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev_a=None, ev_b=None):
+        if inp.copy_pairs.numel():
+            ops.pa_copy_blocks(inp.k_cache, inp.v_cache, inp.copy_pairs, err)
+        if inp.new_seq.numel():
+            ops.pa_slot_mapping(inp.block_tables, inp.new_seq, inp.new_pos, B, inp.k_cache.shape[0], slots, err)
+            ops.pa_write_kv(inp.new_key, inp.new_value, inp.k_cache, inp.v_cache, slots, err)
+        if ev_a is not None:
+            ev_a.record(stream)
+        ops.pa_decode_partition(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale,
+                                out, ws, err)
+        if ev_b is not None:
+            ev_b.record(stream)
+        ops.pa_decode_reduce(out, inp.block_tables, inp.context_lens, Hkv, B, ws, err)
+
+    launches_per_step = (1 if inp.copy_pairs.numel() else 0) + (2 if inp.new_seq.numel() else 0) + 2
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert int(err.item()) == 0, ops.error_names(int(err.item()))
+
+    # -- device-timed step loop (inputs resident)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for k in range(args.steps):
+            step(*kev[k])
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(dist)
+    step_ms = start.elapsed_time(end) / args.steps
+    kernel_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
+    step_ms_max = max_over_ranks(step_ms, dist)
+
+    # -- end to end through the public API: pinned host inputs in, output out
+    host = {n: getattr(inp, n).cpu().pin_memory() for n in
+            ("q", "new_key", "new_value", "new_seq", "new_pos", "block_tables", "context_lens", "copy_pairs")}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for n, t in host.items():
+            getattr(inp, n).copy_(t, non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 2000))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist)
+    assert int(err.item()) == 0, ops.error_names(int(err.item()))
+
+    kvb = kv_bytes(inp)
+    total_kv = sum_over_ranks(float(kvb), dist)
+    alg = algorithmic_bytes(inp)
+    peaks = measured_peaks()
+    achieved = alg / (kernel_ms * 1e-3) / 1e9
+    value = total_kv / (step_ms_max * 1e-3) / 1e9
+    line = {
+        "metric": "pa_decode achieved KV GB/s (logical K+V bytes / decode-step time)",
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms_max, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}[inp.q.dtype],
+        "data": "synthetic: seeded N(0,1) q/K/V, random physical placement",
+        "config": workload_config(args.workload, inp),
+        "tokens_per_s": round(sum_over_ranks(float(S), dist) / (step_ms_max * 1e-3), 0),
+        "pct_of_nominal_8000_gbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_hbm": round(100 * value / world / peaks["hbm_gbs"], 2),
+        "decode_kernel_us": round(kernel_ms * 1e3, 2),
+        "roofline": {"kernel": "decode_partition_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
+                     "frac_of_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "algorithmic_bytes_per_launch": alg,
+                     "traffic": profiled_traffic(args.workload)},
+        "e2e": {"value": round(total_kv / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = inp.to("cpu")
+        gbs, secs, nseq, threads = time_cpu_oracle(cpu, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{nseq} of {S} sequences, all {Hq} heads, C float64 oracle, "
+                                          f"{secs:.1f} s"}
+    if dist is not None:
+        dist.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def run_reference(args) -> dict:
+    """The CPU oracle as the reference arm: each step decodes a bounded sample
+    of whole sequences of the same workload on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    from oracle import native
+
+    inp = workload_inputs(args.workload, args.seed, "cuda" if torch.cuda.is_available() else "cpu").to("cpu")
+    S, Hq, D = inp.q.shape
+    Hkv = inp.k_cache.shape[1]
+    e = inp.k_cache.element_size()
+    tables, lens = inp.block_tables.numpy(), inp.context_lens.numpy()
+    # calibrate: seconds per sequence, then size each step for ~90 s over all steps
+    t0 = time.perf_counter()
+    native.decode(inp.q[:1], inp.k_cache, inp.v_cache, tables[:1], lens[:1], inp.scale)
+    per_seq = max(time.perf_counter() - t0, 1e-6)
+    total_steps = args.steps + args.warmup
+    nseq = max(1, min(S, int(90.0 / total_steps / per_seq)))
+    heads_note = "all heads"
+    sample_q = inp.q[:nseq]
+    for _ in range(args.warmup):
+        native.decode(sample_q, inp.k_cache, inp.v_cache, tables[:nseq], lens[:nseq], inp.scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        native.decode(sample_q, inp.k_cache, inp.v_cache, tables[:nseq], lens[:nseq], inp.scale)
+    secs = time.perf_counter() - t0
+    nbytes = int(lens[:nseq].astype("int64").sum()) * Hkv * D * e * 2 * args.steps
+    value = nbytes / secs / 1e9
+    threads = native.max_threads()
+    sample = f"{nseq} of {S} sequences per step, {heads_note}, C float64 oracle"
+    return {
+        "impl": "reference",
+        "metric": "pa_decode achieved KV GB/s (logical K+V bytes / decode-step time)",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args.workload, inp),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=6000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", choices=["tiny", "mha", "gqa", "prefix", "longctx"], default="gqa")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,184 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: paged KV-cache decode attention on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The KV cache is split into fixed-size physical blocks of B tokens; each
+ * sequence owns a block table mapping its logical block i to a physical block
+ * id, so token position t lives in physical block block_table[t / B] at
+ * offset t % B (aiqz.cc "paged-attention-mechanism", section "块表映射机制";
+ * lihaoran.work "auto-20261007-1900", section "块表把逻辑顺序映射到物理位置").
+ *
+ * Layouts (row-major, element type given by pa_dtype):
+ *   q, out            [S][Hq][D]
+ *   k_cache, v_cache  [NB][Hkv][B][D]   one (block, kv head) tile is B*D
+ *                                        contiguous elements
+ *   block_tables      int32 [S][max_blocks_per_seq]; entries past
+ *                     ceil(context_len / B) are never read (may hold -1)
+ *   context_lens      int32 [S]
+ *   slot_mapping      int64 [T]; slot = pid * B + offset, slot < 0 = skip
+ *
+ * Conventions for every call:
+ *   - All pointers are device pointers owned by the caller (allocated by the
+ *     caller, e.g. through PyTorch).  Calls never allocate, never free and
+ *     never synchronise: they enqueue kernels on `stream` (a cudaStream_t,
+ *     NULL = legacy default stream) and return.
+ *   - Host-side scalar arguments are validated; a bad one returns
+ *     PA_ERR_INVALID_ARG (or PA_ERR_UNSUPPORTED for a valid but unsupported
+ *     shape) and enqueues nothing.  A failed launch returns PA_ERR_CUDA.
+ *   - Device-side data (table entries, slots, lengths) is range-checked in the
+ *     kernels: an offending access is skipped and a bit is OR-ed into
+ *     *debug_err (a caller-owned device int; may be NULL to ignore).  Results
+ *     touched by a skipped access are unspecified.  The bits are PA_DEVERR_*.
+ *   - Device pointers must be 16-byte aligned; head_dim must be 64 or 128;
+ *     block_size in [1, 64]; num_heads a multiple of num_kv_heads.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Entry points are exported even when the library hides everything else. */
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,
+  PA_ERR_UNSUPPORTED = 2,
+  PA_ERR_CUDA = 3,
+  PA_ERR_WORKSPACE = 4
+} pa_status;
+
+/* Bits OR-ed into *debug_err by the kernels. */
+#define PA_DEVERR_BLOCK_ID 1u  /* a block id outside [0, num_blocks)          */
+#define PA_DEVERR_SLOT 2u      /* a slot >= num_blocks * block_size           */
+#define PA_DEVERR_CONTEXT 4u   /* context_len < 0 or > max_blocks_per_seq * B */
+#define PA_DEVERR_TIMEOUT 8u   /* an internal pipeline wait gave up (>1 s)    */
+#define PA_DEVERR_POSITION 16u /* a token position outside its block table    */
+
+/* Human-readable name of a status code (static string). */
+PA_API const char *pa_status_string(pa_status status);
+
+/*
+ * a1 -- slot of each new token (the host-side "append" emits it; this is the
+ * same lookup on the device).  Token i belongs to sequence token_seq[i] at
+ * position token_pos[i]:
+ *     slot_mapping[i] = block_tables[seq][pos / B] * B + pos % B
+ * (aiqz.cc, section "块表映射机制").  A negative position gives slot -1
+ * (padding).  A sequence index outside [0, num_seqs), a position past the
+ * table row, or a block id outside [0, num_blocks) gives slot -1 and sets a
+ * PA_DEVERR bit.
+ */
+PA_API pa_status pa_slot_mapping(int64_t *slot_mapping, const int32_t *block_tables,
+                          int max_blocks_per_seq, int num_seqs,
+                          const int32_t *token_seq, const int32_t *token_pos,
+                          int64_t num_tokens, int block_size, int64_t num_blocks,
+                          int *debug_err, void *stream);
+
+/*
+ * a2 -- write each new token's K and V rows into its slot (bit copy):
+ *     k_cache[slot / B][h][slot % B][:] = key[i][h][:]   (same for V)
+ * for every token i and kv head h; slot < 0 skips the token (padding).
+ * Writing the new token is the last step of an append or of a copy-on-write
+ * (aiqz.cc, section "前缀共享机制").  key/value: [T][Hkv][D].  Slots must be
+ * unique within one call.
+ */
+PA_API pa_status pa_write_kv(const void *key, const void *value, void *k_cache,
+                      void *v_cache, const int64_t *slot_mapping,
+                      int64_t num_tokens, int num_kv_heads, int head_dim,
+                      int block_size, int64_t num_blocks, pa_dtype dtype,
+                      int *debug_err, void *stream);
+
+/*
+ * a3 -- copy-on-write block copy: for each pair p, the whole physical block
+ * pairs[p][1] (dst) of K and of V, all heads and all B slots, becomes a copy
+ * of block pairs[p][0] (src) (aiqz.cc, section "前缀共享机制"; cf-1.com
+ * news/5879632, section 4.2).  pairs: device int64 [P][2].  Within one call
+ * every dst must be distinct and no dst may also appear as a src (the host
+ * block manager guarantees this: a copy target is a freshly taken block).
+ */
+PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs,
+                         int64_t num_pairs, int num_kv_heads, int head_dim,
+                         int block_size, int64_t num_blocks, pa_dtype dtype,
+                         int *debug_err, void *stream);
+
+/*
+ * Bytes of device workspace pa_decode needs for this shape on the current
+ * device (depends on its SM count).  Returns 0 for invalid arguments.
+ */
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                int head_dim);
+
+/*
+ * a4 + a5 -- paged decode attention, one query token per sequence:
+ *     out[s][h][:] = sum_t softmax_t(scale * <q[s][h], K_t>) V_t
+ * over the sequence's whole cached history t = 0 .. context_lens[s]-1, with
+ * K_t, V_t read from physical block block_tables[s][t / B], offset t % B, of
+ * kv head h / (num_heads / num_kv_heads).  Every new token attends to the
+ * whole history (aiqz.cc, section "显存痛点"); the kernel looks the table up
+ * before reading each block (cf-1.com news/5879632, section 5.1).  The
+ * formula and the grouped-query head mapping are the textbook definition.
+ * Arithmetic is fp32 on the stored inputs; out is rounded to nearest even.
+ * A sequence with context_len 0 gets a zero row.
+ *
+ * Equivalent to pa_decode_partition followed by pa_decode_reduce on the same
+ * stream.  workspace: device buffer of at least
+ * pa_decode_workspace_size(...) bytes, 256-byte aligned; it holds only
+ * intermediate values and may be reused after the calls complete.
+ */
+PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache,
+                    const void *v_cache, const int32_t *block_tables,
+                    int max_blocks_per_seq, const int32_t *context_lens,
+                    int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                    int block_size, int64_t num_blocks, float scale,
+                    pa_dtype dtype, void *workspace, size_t workspace_bytes,
+                    int *debug_err, void *stream);
+
+/*
+ * a4 alone -- the persistent split-context kernel.  The whole step's
+ * (sequence, kv head, block) tiles are split evenly over one wave of CTAs;
+ * a (sequence, kv head) whose tiles all fall in one CTA is finished there and
+ * written to `out`; otherwise each CTA leaves a partial (max, sum, weighted
+ * values) in the workspace for pa_decode_reduce.
+ */
+PA_API pa_status pa_decode_partition(void *out, const void *q, const void *k_cache,
+                              const void *v_cache, const int32_t *block_tables,
+                              int max_blocks_per_seq,
+                              const int32_t *context_lens, int num_seqs,
+                              int num_heads, int num_kv_heads, int head_dim,
+                              int block_size, int64_t num_blocks, float scale,
+                              pa_dtype dtype, void *workspace,
+                              size_t workspace_bytes, int *debug_err,
+                              void *stream);
+
+/*
+ * a5 alone -- combine the partials of split (sequence, kv head) pairs:
+ *     M = max_p m_p;  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p
+ * and write zero rows for empty sequences.  Must follow pa_decode_partition
+ * with the same shape arguments and workspace on the same stream.
+ */
+PA_API pa_status pa_decode_reduce(void *out, const int32_t *context_lens,
+                           int max_blocks_per_seq, int num_seqs, int num_heads,
+                           int num_kv_heads, int head_dim, int block_size,
+                           pa_dtype dtype, void *workspace,
+                           size_t workspace_bytes, int *debug_err,
+                           void *stream);
+
+/* Number of CTAs the split-context kernel launches on the current device. */
+PA_API int pa_decode_grid_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,175 @@
+// pa_common.cuh -- device helpers shared by the libpagedkv kernels (sm_103a):
+// element conversions, packed fp32x2 FMA, mbarrier and bulk-copy (TMA) PTX.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pagedkv.h"
+
+namespace pagedkv {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// ----------------------------------------------------------------- status
+inline pa_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t dtype_bytes(pa_dtype dt) { return dt == PA_F32 ? 4u : 2u; }
+
+// Number of SMs of the current device (cached per device ordinal).
+int device_sm_count();
+
+// ----------------------------------------------------------------- errors
+__device__ __forceinline__ void raise_error(int *err, unsigned bit) {
+  if (err != nullptr) atomicOr(reinterpret_cast<unsigned *>(err), bit);
+}
+
+// ----------------------------------------------------------------- conversions
+template <typename T> struct Elem;
+
+template <> struct Elem<float> {
+  // 16-byte chunk -> 4 floats as 2 float2
+  static __device__ __forceinline__ void chunk_to_f2(const uint4 &c, float2 *o) {
+    o[0] = make_float2(__uint_as_float(c.x), __uint_as_float(c.y));
+    o[1] = make_float2(__uint_as_float(c.z), __uint_as_float(c.w));
+  }
+  static __device__ __forceinline__ float2 word2_to_f2(uint32_t a, uint32_t b) {
+    return make_float2(__uint_as_float(a), __uint_as_float(b));
+  }
+  static __device__ __forceinline__ float to_float(float x) { return x; }
+  static __device__ __forceinline__ float from_float(float x) { return x; }
+};
+
+template <> struct Elem<__nv_bfloat16> {
+  // bf16 is the high half of an fp32 pattern: unpack with a shift and a mask.
+  static __device__ __forceinline__ float2 word_to_f2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
+  static __device__ __forceinline__ void chunk_to_f2(const uint4 &c, float2 *o) {
+    o[0] = word_to_f2(c.x);
+    o[1] = word_to_f2(c.y);
+    o[2] = word_to_f2(c.z);
+    o[3] = word_to_f2(c.w);
+  }
+  static __device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ __nv_bfloat16 from_float(float x) { return __float2bfloat16_rn(x); }
+};
+
+template <> struct Elem<__half> {
+  static __device__ __forceinline__ float2 word_to_f2(uint32_t w) {
+    __half2 h;
+    *reinterpret_cast<uint32_t *>(&h) = w;
+    return __half22float2(h);
+  }
+  static __device__ __forceinline__ void chunk_to_f2(const uint4 &c, float2 *o) {
+    o[0] = word_to_f2(c.x);
+    o[1] = word_to_f2(c.y);
+    o[2] = word_to_f2(c.z);
+    o[3] = word_to_f2(c.w);
+  }
+  static __device__ __forceinline__ float to_float(__half x) { return __half2float(x); }
+  static __device__ __forceinline__ __half from_float(float x) { return __float2half_rn(x); }
+};
+
+// ----------------------------------------------------------------- packed FMA
+// d.xy += a.xy * b.xy with one fma.rn.f32x2 (two IEEE fp32 FMAs).
+__device__ __forceinline__ void ffma2(float2 &d, const float2 a, const float2 b) {
+  uint64_t dd, aa, bb;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(dd) : "f"(d.x), "f"(d.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(aa) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(bb) : "f"(b.x), "f"(b.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(dd) : "l"(aa), "l"(bb));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(dd));
+}
+
+__device__ __forceinline__ void fmul2(float2 &d, const float2 a) {
+  uint64_t dd, aa;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(dd) : "f"(d.x), "f"(d.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(aa) : "f"(a.x), "f"(a.y));
+  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(dd) : "l"(aa));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(dd));
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ----------------------------------------------------------------- shared memory / mbarrier
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `bar` with the given parity to complete.  Gives up
+// after ~1 s, or at once when *abort is set; returns false then.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// 1-D bulk copy global -> shared (TMA engine), completion counted in bytes on
+// `bar`.  dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+}  // namespace pagedkv

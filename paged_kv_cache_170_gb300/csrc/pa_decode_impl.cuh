@@ -1,0 +1,506 @@
+// pa_decode_impl.cuh -- persistent split-context paged decode kernel (a4).
+//
+// Work decomposition.  The step's work is the ordered list of tiles
+// (sequence s, pair-chunk pc, logical block b), pc = kv head * HC + head
+// chunk, where a head chunk is GT of the G query heads that share one kv head
+// and a tile is one physical block of K plus the same block of V for that kv
+// head (B*D contiguous elements each).  The W tiles are cut into N equal
+// contiguous ranges, one per CTA, N = one full wave (2 CTAs per SM): every
+// CTA streams the same number of bytes whatever the length mix, so no SM
+// idles at the tail.  A CTA finishes any (s, pc) whose tiles all fall in its
+// range and writes `out`; a (s, pc) cut by a range boundary leaves a partial
+// (m, l, acc) for the reduce kernel.
+//
+// Inside a CTA.  One producer warp walks the range in order, reads the block
+// table once per 32 tiles (coalesced, kept in registers: the table is never
+// re-read per token), and issues one 1-D bulk copy (TMA) per K tile and per V
+// tile into a ring of shared-memory slots, completion counted on an mbarrier
+// per slot.  Only the valid rows of a sequence's last, partly filled block are
+// copied.  Four consumer warps take tiles round-robin; each keeps its own
+// running max / sum / accumulator (online softmax, base 2) and the four
+// states are merged when the (s, pc) ends.
+//
+// Per tile and consumer warp (fp32 arithmetic, packed fma.rn.f32x2):
+//   QK: a token is handled by LPT lanes, each owning DPL dimensions of every
+//       query head of the chunk (q pre-scaled by scale*log2(e), in registers);
+//       the partial dots are summed across the LPT lanes with xor shuffles.
+//   softmax: tile max per head (shuffles), rescale of the running state,
+//       p = 2^(x - m) written to a per-warp score buffer.
+//   PV: lanes own D/32 dimensions; every token's p's are broadcast from the
+//       score buffer and accumulated for all GT heads.
+#pragma once
+
+#include <math_constants.h>
+
+#include "pa_common.cuh"
+
+namespace pagedkv {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kCtasPerSm = 2;
+constexpr int kMaxStages = 64;
+constexpr int kMaxBlockSize = 64;
+constexpr int kRingBytes = 80 * 1024;
+
+struct DecodeArgs {
+  void *out;
+  const void *q;
+  const char *k_cache;
+  const char *v_cache;
+  const int32_t *tables;
+  const int32_t *lens;
+  int64_t num_blocks;
+  int max_blocks;
+  int S, Hq, Hkv, B;
+  float qscale;            // scale * log2(e)
+  float *partials;         // [N][2][GT][D + 2]: acc[D], m, l
+  long long *cum;          // [S + 1] tile prefix (written by CTA 0)
+  int *err;
+  int nctas;
+  int nstage;
+  uint32_t slot_stride;    // bytes between ring slots
+};
+
+template <typename T, int D, int GT>
+struct DecodeCfg {
+  static constexpr int EPC = 16 / int(sizeof(T));                 // elements per 16-byte chunk
+  static constexpr int DPL = (D == 128 && GT <= 4) ? 16 : 8;      // dims per lane in QK
+  static constexpr int LPT = D / DPL;                             // lanes per token in QK
+  static constexpr int TS = 32 / LPT;                             // tokens per QK pass
+  static constexpr int CPL = DPL / EPC;                           // 16-byte chunks per lane per token
+  static constexpr int DPV = D / 32;                              // dims per lane in PV
+  static_assert(DPL % EPC == 0, "lane slice must be whole chunks");
+  static_assert(LPT >= 8, "a quarter warp must read one contiguous 128-byte run");
+  static_assert(GT <= LPT, "one score per lane");
+};
+
+// Clamped context length of sequence s (flags out-of-range lengths once).
+__device__ __forceinline__ int clamped_len(const DecodeArgs &a, int s) {
+  int L = a.lens[s];
+  const int cap = a.max_blocks * a.B;
+  return L < 0 ? 0 : (L > cap ? cap : L);
+}
+
+__device__ __forceinline__ int blocks_of(const DecodeArgs &a, int s) {
+  return (clamped_len(a, s) + a.B - 1) / a.B;
+}
+
+// V row slice of a lane: DPV elements starting at dimension lane * DPV.
+template <typename T, int DPV>
+__device__ __forceinline__ void load_v(const char *row, int lane, float2 *vf) {
+  const char *p = row + size_t(lane) * DPV * sizeof(T);
+  if constexpr (sizeof(T) == 4 && DPV == 4) {
+    const uint4 r = *reinterpret_cast<const uint4 *>(p);
+    Elem<float>::chunk_to_f2(r, vf);
+  } else if constexpr (sizeof(T) == 4 && DPV == 2) {
+    const uint2 r = *reinterpret_cast<const uint2 *>(p);
+    vf[0] = make_float2(__uint_as_float(r.x), __uint_as_float(r.y));
+  } else if constexpr (sizeof(T) == 2 && DPV == 4) {
+    const uint2 r = *reinterpret_cast<const uint2 *>(p);
+    vf[0] = Elem<T>::word_to_f2(r.x);
+    vf[1] = Elem<T>::word_to_f2(r.y);
+  } else {
+    static_assert(sizeof(T) == 2 && DPV == 2, "unsupported V slice");
+    vf[0] = Elem<T>::word_to_f2(*reinterpret_cast<const uint32_t *>(p));
+  }
+}
+
+// The GT probabilities of token t from the warp's score buffer.
+template <int GT>
+__device__ __forceinline__ void load_p(const float *sc, int t, float *p) {
+  if constexpr (GT == 8) {
+    const float4 a = *reinterpret_cast<const float4 *>(sc + t * 8);
+    const float4 b = *reinterpret_cast<const float4 *>(sc + t * 8 + 4);
+    p[0] = a.x; p[1] = a.y; p[2] = a.z; p[3] = a.w; p[4] = b.x; p[5] = b.y; p[6] = b.z; p[7] = b.w;
+  } else if constexpr (GT == 4) {
+    const float4 a = *reinterpret_cast<const float4 *>(sc + t * 4);
+    p[0] = a.x; p[1] = a.y; p[2] = a.z; p[3] = a.w;
+  } else if constexpr (GT == 2) {
+    const float2 a = *reinterpret_cast<const float2 *>(sc + t * 2);
+    p[0] = a.x; p[1] = a.y;
+  } else {
+    p[0] = sc[t];
+  }
+}
+
+// Total tile count W (and, in CTA 0, the per-sequence prefix) and the tile
+// where this CTA's range starts.  Run by one whole warp.
+__device__ __forceinline__ void schedule_scan(const DecodeArgs &a, int PC, int lane, long long *W_out,
+                                              int *s0_out, long long *r0_out) {
+  const int cap = a.max_blocks * a.B;
+  long long run = 0;
+  for (int base = 0; base < a.S; base += 32) {
+    const int s = base + lane;
+    long long n = 0;
+    if (s < a.S) {
+      const int L = a.lens[s];
+      if ((L < 0 || L > cap) && blockIdx.x == 0) raise_error(a.err, PA_DEVERR_CONTEXT);
+      n = (long long)blocks_of(a, s) * PC;
+    }
+    long long incl = n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long y = __shfl_up_sync(kFullMask, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (blockIdx.x == 0 && s < a.S) a.cum[s] = run + incl - n;
+    run += __shfl_sync(kFullMask, incl, 31);
+  }
+  if (blockIdx.x == 0 && lane == 0) a.cum[a.S] = run;
+  const long long W = run;
+  const long long w0 = (long long)blockIdx.x * W / a.nctas;
+  int s0 = a.S;
+  long long r0 = 0;
+  run = 0;
+  for (int base = 0; base < a.S && s0 == a.S; base += 32) {
+    const int s = base + lane;
+    const long long n = s < a.S ? (long long)blocks_of(a, s) * PC : 0;
+    long long incl = n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long y = __shfl_up_sync(kFullMask, incl, off);
+      if (lane >= off) incl += y;
+    }
+    const long long excl = run + incl - n;
+    const bool hit = n > 0 && excl <= w0 && w0 < run + incl;
+    const unsigned m = __ballot_sync(kFullMask, hit);
+    if (m) {
+      const int leader = __ffs(m) - 1;
+      s0 = __shfl_sync(kFullMask, s, leader);
+      r0 = __shfl_sync(kFullMask, w0 - excl, leader);
+    }
+    run += __shfl_sync(kFullMask, incl, 31);
+  }
+  *W_out = W;
+  *s0_out = s0;
+  *r0_out = r0;
+}
+
+template <typename T, int D, int GT>
+__global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_kernel(const DecodeArgs a) {
+  using C = DecodeCfg<T, D, GT>;
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(16) float sc_buf[kConsumerWarps][kMaxBlockSize * GT];
+  __shared__ __align__(16) float mrg[kConsumerWarps][GT][D + 2];
+  __shared__ long long sh_W, sh_r0;
+  __shared__ int sh_s0;
+  __shared__ int sh_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = a.Hq / a.Hkv;
+  const int HC = G / GT;
+  const int PC = a.Hkv * HC;
+  const int B = a.B;
+  volatile int *abort_flag = &sh_abort;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.nstage; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    sh_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == kConsumerWarps) {
+    long long W, r0;
+    int s0;
+    schedule_scan(a, PC, lane, &W, &s0, &r0);
+    if (lane == 0) {
+      sh_W = W;
+      sh_s0 = s0;
+      sh_r0 = r0;
+    }
+  }
+  __syncthreads();
+
+  const long long W = sh_W;
+  const long long w0 = (long long)blockIdx.x * W / a.nctas;
+  const long long w1 = (long long)(blockIdx.x + 1) * W / a.nctas;
+  if (w0 >= w1) return;  // empty range (fewer tiles than CTAs)
+  const size_t tile_elems = size_t(B) * D;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    long long e = 0;  // ring entries issued
+    int s = sh_s0;
+    int nb = blocks_of(a, s);
+    int pc = int(sh_r0 / nb);
+    int b = int(sh_r0 % nb);
+    long long w = w0;
+    bool aborted = false;
+    while (w < w1) {
+      const int n = int(min((long long)(nb - b), w1 - w));
+      const int kvh = pc / HC;
+      const int L = clamped_len(a, s);
+      const int32_t *trow = a.tables + (long long)s * a.max_blocks + b;
+      int pid_next = lane < n ? trow[lane] : -1;
+      for (int base = 0; base < n; base += 32) {
+        const int pid_cur = pid_next;
+        const int cnt = min(32, n - base);
+        if (base + 32 < n) pid_next = (base + 32 + lane < n) ? trow[base + 32 + lane] : -1;
+        for (int k = 0; k < cnt; ++k) {
+          const int p = __shfl_sync(kFullMask, pid_cur, k);
+          if (lane == 0) {
+            const int bb = b + base + k;
+            const int nv = min(B, L - bb * B);
+            const uint32_t bytes = uint32_t(nv) * D * sizeof(T);
+            const bool ok = p >= 0 && p < a.num_blocks;
+            if (!ok) raise_error(a.err, PA_DEVERR_BLOCK_ID);
+            const size_t off = ((size_t)(ok ? p : 0) * a.Hkv + kvh) * tile_elems * sizeof(T);
+#pragma unroll
+            for (int kind = 0; kind < 2; ++kind) {
+              const int slot = int(e % a.nstage);
+              const uint32_t u = uint32_t(e / a.nstage);
+              if (!aborted && u > 0 && !mbar_wait(&empty_bar[slot], (u - 1) & 1u, abort_flag)) {
+                aborted = true;
+                *abort_flag = 1;
+                raise_error(a.err, PA_DEVERR_TIMEOUT);
+              }
+              if (aborted) break;  // issue nothing more; e counts issued entries only
+              if (ok) {
+                mbar_arrive_expect_tx(&full_bar[slot], bytes);
+                bulk_g2s(ring + size_t(slot) * a.slot_stride, (kind == 0 ? a.k_cache : a.v_cache) + off, bytes,
+                         &full_bar[slot]);
+              } else {
+                mbar_arrive(&full_bar[slot]);  // complete the phase without data
+              }
+              ++e;
+            }
+          }
+          __syncwarp();
+        }
+      }
+      w += n;
+      b += n;
+      if (b == nb) {
+        b = 0;
+        if (++pc == PC) {
+          pc = 0;
+          do {
+            ++s;
+          } while (s < a.S && blocks_of(a, s) == 0);
+          if (s < a.S) nb = blocks_of(a, s);
+        }
+      }
+    }
+    // Do not leave while a copy into this CTA's shared memory is in flight.
+    if (lane == 0) {
+      const long long first = e > a.nstage ? e - a.nstage : 0;
+      for (long long i = first; i < e; ++i) {
+        int dummy = 0;
+        mbar_wait(&full_bar[i % a.nstage], uint32_t(i / a.nstage) & 1u, &dummy);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  float *sc = sc_buf[warp];
+  const int jl = lane % C::LPT;   // lane within its token group (QK)
+  const int tsub = lane / C::LPT; // token slot of the lane (QK)
+  // Softmax state (m_mine, l_mine) of a lane belongs to head lane % GT.
+
+  int s = sh_s0;
+  int nb = blocks_of(a, s);
+  int pc = int(sh_r0 / nb);
+  int b = int(sh_r0 % nb);
+  long long w = w0;
+  long long j = 0;  // tile index within this CTA's range
+  while (w < w1) {
+    const int n = int(min((long long)(nb - b), w1 - w));
+    const bool complete = (b == 0 && n == nb);
+    const bool first_seg = (w == w0);
+    const int kvh = pc / HC;
+    const int hq0 = kvh * G + (pc % HC) * GT;
+    const int L = clamped_len(a, s);
+
+    float m_mine = -CUDART_INF_F;
+    float l_mine = 0.f;
+    float2 acc[GT][C::DPV / 2];
+#pragma unroll
+    for (int h = 0; h < GT; ++h)
+#pragma unroll
+      for (int i = 0; i < C::DPV / 2; ++i) acc[h][i] = make_float2(0.f, 0.f);
+
+    long long jj = j + ((warp - int(j % kConsumerWarps)) + kConsumerWarps) % kConsumerWarps;
+    if (jj < j + n) {
+      // q slice of this lane, pre-scaled so scores come out in log2 units
+      float2 qreg[GT][C::DPL / 2];
+      const T *qs = static_cast<const T *>(a.q) + ((long long)s * a.Hq + hq0) * D;
+#pragma unroll
+      for (int h = 0; h < GT; ++h)
+#pragma unroll
+        for (int c = 0; c < C::CPL; ++c) {
+          const uint4 raw = *reinterpret_cast<const uint4 *>(qs + h * D + (c * C::LPT + jl) * C::EPC);
+          float2 f[C::EPC / 2];
+          Elem<T>::chunk_to_f2(raw, f);
+#pragma unroll
+          for (int i = 0; i < C::EPC / 2; ++i)
+            qreg[h][c * (C::EPC / 2) + i] = make_float2(f[i].x * a.qscale, f[i].y * a.qscale);
+        }
+
+      for (; jj < j + n; jj += kConsumerWarps) {
+        const int bb = b + int(jj - j);
+        const int nv = min(B, L - bb * B);
+        const long long eK = 2 * jj;
+        const int slotK = int(eK % a.nstage), slotV = int((eK + 1) % a.nstage);
+        const uint32_t parK = uint32_t(eK / a.nstage) & 1u, parV = uint32_t((eK + 1) / a.nstage) & 1u;
+        const char *kt = reinterpret_cast<const char *>(ring) + size_t(slotK) * a.slot_stride;
+        const char *vt = reinterpret_cast<const char *>(ring) + size_t(slotV) * a.slot_stride;
+
+        // ---- QK
+        if (!mbar_wait(&full_bar[slotK], parK, abort_flag)) {
+          if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        __syncwarp();
+        for (int t0 = 0; t0 < nv; t0 += C::TS) {
+          const int t = t0 + tsub;
+          const int tr = t < nv ? t : nv - 1;
+          float2 a2[GT];
+#pragma unroll
+          for (int h = 0; h < GT; ++h) a2[h] = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < C::CPL; ++c) {
+            const uint4 raw =
+                *reinterpret_cast<const uint4 *>(kt + (size_t(tr) * D + (c * C::LPT + jl) * C::EPC) * sizeof(T));
+            float2 kf[C::EPC / 2];
+            Elem<T>::chunk_to_f2(raw, kf);
+#pragma unroll
+            for (int h = 0; h < GT; ++h)
+#pragma unroll
+              for (int i = 0; i < C::EPC / 2; ++i) ffma2(a2[h], qreg[h][c * (C::EPC / 2) + i], kf[i]);
+          }
+          float part[GT];
+#pragma unroll
+          for (int h = 0; h < GT; ++h) part[h] = a2[h].x + a2[h].y;
+#pragma unroll
+          for (int off = C::LPT / 2; off >= 1; off >>= 1)
+#pragma unroll
+            for (int h = 0; h < GT; ++h) part[h] += __shfl_xor_sync(kFullMask, part[h], off);
+          if (t < nv && jl < GT) {
+            float v = part[0];
+#pragma unroll
+            for (int h = 1; h < GT; ++h)
+              if (jl == h) v = part[h];
+            sc[t * GT + jl] = v;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slotK]);
+
+        // ---- online softmax over this tile (base 2)
+        float mx = -CUDART_INF_F;
+        for (int i = lane; i < nv * GT; i += 32) mx = fmaxf(mx, sc[i]);
+#pragma unroll
+        for (int off = GT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, off));
+        const float m_new = fmaxf(m_mine, mx);
+        const float alpha = fast_exp2(m_mine - m_new);
+        float lsum = l_mine * alpha;
+        for (int i = lane; i < nv * GT; i += 32) {
+          const float p = fast_exp2(sc[i] - m_new);
+          sc[i] = p;
+          lsum += p;
+        }
+        l_mine = lsum;
+        m_mine = m_new;
+#pragma unroll
+        for (int h = 0; h < GT; ++h) {
+          const float ah = __shfl_sync(kFullMask, alpha, h);
+          const float2 a2 = make_float2(ah, ah);
+#pragma unroll
+          for (int i = 0; i < C::DPV / 2; ++i) fmul2(acc[h][i], a2);
+        }
+        __syncwarp();
+
+        // ---- PV
+        if (!mbar_wait(&full_bar[slotV], parV, abort_flag)) {
+          if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        __syncwarp();
+#pragma unroll 4
+        for (int t = 0; t < nv; ++t) {
+          float p[GT];
+          load_p<GT>(sc, t, p);
+          float2 vf[C::DPV / 2];
+          load_v<T, C::DPV>(vt + size_t(t) * D * sizeof(T), lane, vf);
+#pragma unroll
+          for (int h = 0; h < GT; ++h) {
+            const float2 pp = make_float2(p[h], p[h]);
+#pragma unroll
+            for (int i = 0; i < C::DPV / 2; ++i) ffma2(acc[h][i], pp, vf[i]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slotV]);
+      }
+    }
+
+    // ---- merge the four warps' states for this (s, pc)
+    float lsum = l_mine;
+#pragma unroll
+    for (int off = GT; off < 32; off <<= 1) lsum += __shfl_xor_sync(kFullMask, lsum, off);
+    if (lane < GT) {
+      mrg[warp][lane][D] = m_mine;
+      mrg[warp][lane][D + 1] = lsum;
+    }
+#pragma unroll
+    for (int h = 0; h < GT; ++h)
+#pragma unroll
+      for (int i = 0; i < C::DPV / 2; ++i) {
+        mrg[warp][h][lane * C::DPV + 2 * i] = acc[h][i].x;
+        mrg[warp][h][lane * C::DPV + 2 * i + 1] = acc[h][i].y;
+      }
+    named_barrier_sync(1, kConsumerWarps * 32);
+    for (int idx = threadIdx.x; idx < GT * D; idx += kConsumerWarps * 32) {
+      const int h = idx / D;
+      const int d = idx - h * D;
+      float M = -CUDART_INF_F;
+#pragma unroll
+      for (int q = 0; q < kConsumerWarps; ++q) M = fmaxf(M, mrg[q][h][D]);
+      float num = 0.f, den = 0.f;
+#pragma unroll
+      for (int q = 0; q < kConsumerWarps; ++q) {
+        const float f = fast_exp2(mrg[q][h][D] - M);
+        num += f * mrg[q][h][d];
+        den += f * mrg[q][h][D + 1];
+      }
+      if (complete) {
+        T *o = static_cast<T *>(a.out) + ((long long)s * a.Hq + hq0 + h) * D + d;
+        *o = Elem<T>::from_float(num / den);
+      } else {
+        float *rec = a.partials + (((long long)blockIdx.x * 2 + (first_seg ? 0 : 1)) * GT + h) * (D + 2);
+        rec[d] = num;
+        if (d == 0) {
+          rec[D] = M;
+          rec[D + 1] = den;
+        }
+      }
+    }
+    named_barrier_sync(1, kConsumerWarps * 32);
+
+    w += n;
+    j += n;
+    b += n;
+    if (b == nb) {
+      b = 0;
+      if (++pc == PC) {
+        pc = 0;
+        do {
+          ++s;
+        } while (s < a.S && blocks_of(a, s) == 0);
+        if (s < a.S) nb = blocks_of(a, s);
+      }
+    }
+  }
+}
+
+template <typename T, int D, int GT>
+pa_status launch_decode_partition(const DecodeArgs &a, size_t ring_bytes, cudaStream_t stream);
+
+}  // namespace pagedkv

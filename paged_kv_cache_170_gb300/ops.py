@@ -1,0 +1,237 @@
+"""Thin Python binding of libpagedkv.so (the C ABI in include/pagedkv.h).
+
+Argument marshalling only: every function checks devices/dtypes/shapes of the
+torch tensors, passes raw device pointers and the current CUDA stream to the
+C entry point of the same name, and raises ``PagedKVError`` on a non-OK
+status.  All arithmetic runs in the library's CUDA kernels; there is no other
+code path.  Importing this module loads the library and raises if it has not
+been built (``python -m paged_kv_cache_170_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libpagedkv.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "pagedkv.h")
+
+PA_OK = 0
+_DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+DEVERR_BITS = {1: "BLOCK_ID", 2: "SLOT", 4: "CONTEXT", 8: "TIMEOUT", 16: "POSITION"}
+
+
+class PagedKVError(RuntimeError):
+    pass
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m paged_kv_cache_170_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    sig = {
+        "pa_slot_mapping": [vp, vp, i32, i32, vp, vp, i64, i32, i64, vp, vp],
+        "pa_write_kv": [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32, vp, vp],
+        "pa_copy_blocks": [vp, vp, vp, i64, i32, i32, i32, i64, i32, vp, vp],
+        "pa_decode": [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, sz, vp, vp],
+        "pa_decode_partition": [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, sz, vp,
+                                vp],
+        "pa_decode_reduce": [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, sz, vp, vp],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = i32
+    lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.pa_decode_workspace_size.restype = sz
+    lib.pa_decode_grid_size.argtypes = []
+    lib.pa_decode_grid_size.restype = i32
+    lib.pa_status_string.argtypes = [i32]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+lib = _load()
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/pagedkv.h declares."""
+    with open(HEADER_PATH, encoding="utf-8") as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:PA_API\s+)?(?:pa_status|size_t|int|const char \*)\s*\*?\s*(pa_\w+)\s*\(", text, re.M)))
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PagedKVError(f"{what}: {lib.pa_status_string(status).decode()}")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, ndim=None, device=None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def new_error_word(device) -> torch.Tensor:
+    """A zeroed device int32 for the kernels' error bits (``debug_err``)."""
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def error_names(word: int) -> list[str]:
+    return [name for bit, name in DEVERR_BITS.items() if word & bit]
+
+
+def pa_slot_mapping(block_tables: torch.Tensor, token_seq: torch.Tensor, token_pos: torch.Tensor,
+                    block_size: int, num_blocks: int, out: Optional[torch.Tensor] = None,
+                    err: Optional[torch.Tensor] = None) -> torch.Tensor:
+    dev = block_tables.device
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(token_seq, "token_seq", torch.int32, 1, dev)
+    _need(token_pos, "token_pos", torch.int32, 1, dev)
+    n = token_seq.numel()
+    if token_pos.numel() != n:
+        raise ValueError("token_seq and token_pos differ in length")
+    if out is None:
+        out = torch.empty(n, dtype=torch.int64, device=dev)
+    _need(out, "out", torch.int64, 1, dev)
+    S, width = block_tables.shape
+    _check(lib.pa_slot_mapping(out.data_ptr(), block_tables.data_ptr(), width, S, token_seq.data_ptr(),
+                               token_pos.data_ptr(), n, block_size, num_blocks, _ptr(err), _stream(dev)),
+           "pa_slot_mapping")
+    return out
+
+
+def _cache_shape(k_cache: torch.Tensor, v_cache: torch.Tensor):
+    _need(k_cache, "k_cache", None, 4)
+    _need(v_cache, "v_cache", k_cache.dtype, 4, k_cache.device)
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache differ in shape")
+    if k_cache.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {k_cache.dtype}")
+    return k_cache.shape  # NB, Hkv, B, D
+
+
+def pa_write_kv(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                slot_mapping: torch.Tensor, err: Optional[torch.Tensor] = None) -> None:
+    NB, Hkv, B, D = _cache_shape(k_cache, v_cache)
+    dev = k_cache.device
+    _need(key, "key", k_cache.dtype, 3, dev)
+    _need(value, "value", k_cache.dtype, 3, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    T = key.shape[0]
+    if key.shape != (T, Hkv, D) or value.shape != key.shape or slot_mapping.numel() != T:
+        raise ValueError("key/value must be [T][Hkv][D] with one slot per token")
+    _check(lib.pa_write_kv(key.data_ptr(), value.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                           slot_mapping.data_ptr(), T, Hkv, D, B, NB, _DTYPES[k_cache.dtype], _ptr(err),
+                           _stream(dev)), "pa_write_kv")
+
+
+def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, pairs: torch.Tensor,
+                   err: Optional[torch.Tensor] = None) -> None:
+    NB, Hkv, B, D = _cache_shape(k_cache, v_cache)
+    dev = k_cache.device
+    _need(pairs, "pairs", torch.int64, None, dev)
+    if pairs.numel() % 2:
+        raise ValueError("pairs must be [P][2]")
+    _check(lib.pa_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), pairs.data_ptr(), pairs.numel() // 2, Hkv,
+                              D, B, NB, _DTYPES[k_cache.dtype], _ptr(err), _stream(dev)), "pa_copy_blocks")
+
+
+def pa_decode_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int) -> int:
+    n = lib.pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim)
+    if n == 0:
+        raise PagedKVError("pa_decode_workspace_size: invalid shape or no CUDA device")
+    return int(n)
+
+
+def pa_decode_grid_size() -> int:
+    return int(lib.pa_decode_grid_size())
+
+
+def new_workspace(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int, device) -> torch.Tensor:
+    n = pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _decode_args(q, k_cache, v_cache, block_tables, context_lens, out, workspace):
+    NB, Hkv, B, D = _cache_shape(k_cache, v_cache)
+    dev = k_cache.device
+    _need(q, "q", k_cache.dtype, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    S, Hq, Dq = q.shape
+    if Dq != D or block_tables.shape[0] != S or context_lens.numel() != S:
+        raise ValueError("q [S][Hq][D], block_tables [S][*], context_lens [S] disagree")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, 3, dev)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if workspace is None:
+        workspace = new_workspace(S, Hq, Hkv, D, dev)
+    _need(workspace, "workspace", torch.uint8, 1, dev)
+    return NB, Hkv, B, D, S, Hq, out, workspace
+
+
+def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+              context_lens: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
+              workspace: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None) -> torch.Tensor:
+    NB, Hkv, B, D, S, Hq, out, ws = _decode_args(q, k_cache, v_cache, block_tables, context_lens, out, workspace)
+    _check(lib.pa_decode(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                         block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), S, Hq, Hkv, D, B,
+                         NB, float(scale), _DTYPES[q.dtype], ws.data_ptr(), ws.numel(), _ptr(err),
+                         _stream(q.device)), "pa_decode")
+    return out
+
+
+def pa_decode_partition(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, workspace=None,
+                        err=None) -> torch.Tensor:
+    NB, Hkv, B, D, S, Hq, out, ws = _decode_args(q, k_cache, v_cache, block_tables, context_lens, out, workspace)
+    _check(lib.pa_decode_partition(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                   block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), S, Hq,
+                                   Hkv, D, B, NB, float(scale), _DTYPES[q.dtype], ws.data_ptr(), ws.numel(),
+                                   _ptr(err), _stream(q.device)), "pa_decode_partition")
+    return out
+
+
+def pa_decode_reduce(out, block_tables, context_lens, num_kv_heads, block_size, workspace, err=None) -> None:
+    _need(out, "out", None, 3)
+    S, Hq, D = out.shape
+    _check(lib.pa_decode_reduce(out.data_ptr(), context_lens.data_ptr(), block_tables.shape[1], S, Hq,
+                                num_kv_heads, D, block_size, _DTYPES[out.dtype], workspace.data_ptr(),
+                                workspace.numel(), _ptr(err), _stream(out.device)), "pa_decode_reduce")
+
+
+def decode_step(inp, out=None, workspace=None, slots=None, err=None) -> torch.Tensor:
+    """One whole decode step on resident inputs: copy-on-write block copies,
+    slot lookup of the new tokens, their K/V write, then decode attention."""
+    if inp.copy_pairs.numel():
+        pa_copy_blocks(inp.k_cache, inp.v_cache, inp.copy_pairs, err)
+    if inp.new_seq.numel():
+        B = inp.k_cache.shape[2]
+        slots = pa_slot_mapping(inp.block_tables, inp.new_seq, inp.new_pos, B, inp.k_cache.shape[0], slots, err)
+        pa_write_kv(inp.new_key, inp.new_value, inp.k_cache, inp.v_cache, slots, err)
+    return pa_decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale, out,
+                     workspace, err)
