@@ -65,14 +65,19 @@ def profiled_traffic(workload: str):
     return float(m_bytes.group(1))
 
 
-def workload_inputs(name: str, seed: int, device):
+def workload_inputs(name: str, seed: int, device, num_seqs=None):
+    """Inputs of a named workload; ``num_seqs`` shrinks the plain workloads (and
+    their pools) to fewer sequences of the same shape, for profiler captures."""
     from paged_kv_cache_170_gb300 import scenarios, workloads
 
     if name == "prefix":
         return scenarios.shared_prefix_inputs(seed, device=device)
     if name == "longctx":
         return scenarios.long_context_inputs(seed, device=device)
-    return workloads.make_inputs(workloads.WORKLOADS[name], seed, device=device)
+    w = workloads.WORKLOADS[name]
+    if num_seqs is not None and name != "tiny":
+        w = workloads.scaled(w, num_seqs=num_seqs, num_blocks=num_seqs * w.max_blocks_per_seq + 64)
+    return workloads.make_inputs(w, seed, device=device)
 
 
 def kv_bytes(inp) -> int:
@@ -226,7 +231,7 @@ def run_gpu(args) -> dict:
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     # every rank runs its own replica of the workload on different data (weak scaling)
-    inp = workload_inputs(args.workload, args.seed + rank, dev)
+    inp = workload_inputs(args.workload, args.seed + rank, dev, args.num_seqs)
     S, Hq, D = inp.q.shape
     Hkv, B = inp.k_cache.shape[1], inp.k_cache.shape[2]
     out = torch.empty_like(inp.q)
@@ -399,6 +404,7 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-seqs", type=int, default=None, help="fewer sequences (profiling captures only)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

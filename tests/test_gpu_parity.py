@@ -248,7 +248,7 @@ def test_host_validation(ops):
     k96 = torch.zeros(4, 1, 4, 96, device=DEV)
     with pytest.raises(ops.PagedKVError, match="UNSUPPORTED"):
         ops.pa_decode(torch.zeros(1, 1, 96, device=DEV), k96, k96, torch.zeros(1, 1, dtype=torch.int32, device=DEV),
-                      torch.ones(1, dtype=torch.int32, device=DEV), 0.1)
+                      torch.ones(1, dtype=torch.int32, device=DEV), 0.1, workspace=small)
     with pytest.raises(ops.PagedKVError):
         ops.pa_decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, float("nan"))
 
