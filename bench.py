@@ -31,7 +31,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 NOMINAL_HBM_GBS = 8000.0
-KERNEL_SOURCES = ["paged_kv_cache_170_gb300/csrc/pa_decode_impl.cuh", "paged_kv_cache_170_gb300/csrc/pa_common.cuh"]
+KERNEL_SOURCES = ["paged_kv_cache_170_gb300/csrc/pa_decode_mma.cuh", "paged_kv_cache_170_gb300/csrc/pa_sched.cuh",
+                  "paged_kv_cache_170_gb300/csrc/pa_common.cuh"]
 
 
 def kernel_source_hash() -> str:

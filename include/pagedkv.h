@@ -63,7 +63,7 @@ typedef enum {
 #define PA_DEVERR_BLOCK_ID 1u  /* a block id outside [0, num_blocks)          */
 #define PA_DEVERR_SLOT 2u      /* a slot >= num_blocks * block_size           */
 #define PA_DEVERR_CONTEXT 4u   /* context_len < 0 or > max_blocks_per_seq * B */
-#define PA_DEVERR_TIMEOUT 8u   /* an internal pipeline wait gave up (>1 s)    */
+#define PA_DEVERR_TIMEOUT 8u   /* an internal pipeline wait gave up (~1.5 s)  */
 #define PA_DEVERR_POSITION 16u /* a token position outside its block table    */
 
 /* Human-readable name of a status code (static string). */

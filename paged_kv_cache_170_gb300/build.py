@@ -18,7 +18,8 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libpagedkv.so")
 SOURCES = ["pa_kv.cu", "pa_decode.cu", "pa_decode_f32.cu", "pa_decode_f16.cu", "pa_decode_bf16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+DEBUG = ["-DPA_DEBUG"] if os.environ.get("PA_DEBUG") == "1" else []
+FLAGS = DEBUG + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]
 
 
@@ -36,7 +37,10 @@ def _deps_mtime() -> float:
 
 def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
+    stamp = os.path.join(OUT_DIR, "flags.txt")
+    flags_now = " ".join(ARCH + FLAGS)
+    same_flags = os.path.exists(stamp) and open(stamp).read() == flags_now
+    if not force and same_flags and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
         return LIB
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
@@ -61,6 +65,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(stamp, "w") as f:
+        f.write(flags_now)
     return LIB
 
 

@@ -2,10 +2,12 @@
 // element conversions, packed fp32x2 FMA, mbarrier and bulk-copy (TMA) PTX.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
 
 #include "../../include/pagedkv.h"
 
@@ -29,6 +31,24 @@ int device_sm_count();
 __device__ __forceinline__ void raise_error(int *err, unsigned bit) {
   if (err != nullptr) atomicOr(reinterpret_cast<unsigned *>(err), bit);
 }
+
+// Debug builds (-DPA_DEBUG) range-check every shared / global address the
+// decode kernels form; an offending one is replaced by a safe one and a bit
+// is raised: 1<<8 shared memory, 1<<9 tensor-copy box, 1<<10 global memory.
+#ifdef PA_DEBUG
+constexpr unsigned kDbgSmem = 1u << 8, kDbgTma = 1u << 9, kDbgGlobal = 1u << 10, kDbgPhase = 1u << 11;
+#define PA_DBG_FIX(cond, bit, fix)  \
+  do {                              \
+    if (!(cond)) {                  \
+      raise_error(a.err, (bit));    \
+      fix;                          \
+    }                               \
+  } while (0)
+#else
+#define PA_DBG_FIX(cond, bit, fix) \
+  do {                             \
+  } while (0)
+#endif
 
 // ----------------------------------------------------------------- conversions
 template <typename T> struct Elem;
@@ -138,23 +158,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
-// after ~1 s, or at once when *abort is set; returns false then.
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// after kWaitLimitCycles SM cycles (>= 1.4 s at the 2.07 GHz maximum clock),
+// or at once when *abort is set; returns false then.  The limit is counted on
+// the SM cycle counter, which only moves forward within a thread: the global
+// nanosecond timer is re-synchronised to host time and can jump forward by
+// more than a second, which would end healthy waits.
+constexpr long long kWaitLimitCycles = 3000000000LL;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long c0 = clock64();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (clock64() - c0 > kWaitLimitCycles) {
+#ifdef PA_DEBUG
+      printf("pagedkv wait gave up: cta %d thread %d bar %u parity %u after %lld cycles\n", blockIdx.x, threadIdx.x,
+             smem_addr(bar), parity, (long long)(clock64() - c0));
+#endif
+      return false;
+    }
   }
 }
 
@@ -167,6 +191,83 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+
+// 2-D tiled bulk copy (TMA tensor) global -> shared: box at element
+// coordinates (x = innermost, y) of `map`, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (bulk copy) accesses of the same bytes.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ----------------------------------------------------------------- warp-level MMA
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+template <typename T> struct Mma;
+
+template <> struct Mma<__nv_bfloat16> {
+  // d += A(16x16, row) * B(16x8, col), fp32 accumulate
+  static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+  // {lo, hi} -> packed pair, round to nearest even
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+  }
+  static __device__ __forceinline__ float2 unpack(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
+};
+
+template <> struct Mma<__half> {
+  static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+  }
+  static __device__ __forceinline__ float2 unpack(uint32_t w) {
+    __half2 h;
+    *reinterpret_cast<uint32_t *>(&h) = w;
+    return __half22float2(h);
+  }
+};
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

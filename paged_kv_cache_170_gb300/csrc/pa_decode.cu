@@ -1,20 +1,23 @@
-// pa_decode.cu -- host entry points of paged decode attention and the
-// split-combine kernel (a5).
+// pa_decode.cu -- host entry points of paged decode attention, the choice
+// between the tensor-core and CUDA-core kernels, and the split-combine kernel
+// (a5).
+#include <cudaTypedefs.h>
 #include <math.h>
 
-#include "pa_decode_impl.cuh"
+#include <mutex>
+
+#include "pa_sched.cuh"
 
 namespace pagedkv {
 
-constexpr float kLog2e = 1.4426950408889634f;
+template <typename T, int D, int GT>
+pa_status launch_decode_simt(const DecodeArgs &a, size_t ring_bytes, cudaStream_t stream);
+template <typename T, int D>
+pa_status launch_decode_mma(const DecodeArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t ring_bytes,
+                            cudaStream_t stream);
 
-// Largest power of two <= 8 dividing the group size: query heads handled by
-// one pass over a kv head's blocks.
-static int pick_head_chunk(int G) {
-  for (int gt = 8; gt > 1; gt >>= 1)
-    if (G % gt == 0) return gt;
-  return 1;
-}
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxRecords = 512;  // partial records one reduce CTA can stage
 
 static int decode_grid() { return device_sm_count() * kCtasPerSm; }
 
@@ -28,6 +31,38 @@ static size_t workspace_bytes_for(int num_seqs, int head_dim, int nctas) {
   return partial_bytes(nctas, head_dim) + round256(size_t(num_seqs + 1) * sizeof(long long));
 }
 
+// ----------------------------------------------------------------- tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A pool [NB][Hkv][B][D] seen as NB*Hkv*B rows of D 16-bit elements; one box
+// is B rows x 64 columns (128 bytes), 128-byte swizzled.
+static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype, int64_t num_blocks, int Hkv,
+                            int B, int D) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(num_blocks) * Hkv * B};
+  const cuuint64_t strides[1] = {cuuint64_t(D) * 2};
+  const cuuint32_t box[2] = {64, cuuint32_t(B)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+             const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ----------------------------------------------------------------- a5: combine
 // CTA whose tile range [c*W/N, (c+1)*W/N) holds tile x.
 __device__ __forceinline__ int cta_of(long long x, long long W, int N) {
   return int(((x + 1) * N + W - 1) / W - 1);
@@ -35,11 +70,18 @@ __device__ __forceinline__ int cta_of(long long x, long long W, int N) {
 
 __device__ __forceinline__ long long range_start(int c, long long W, int N) { return (long long)c * W / N; }
 
+// One CTA per (sequence, pair-chunk).  Thread 0 lists the partial records of
+// the pair (CTAs cf..cl, skipping empty ranges; the first one's record is its
+// last segment when its range starts before the pair); the weights
+// 2^(m_r - M) / sum_r 2^(m_r - M) l_r are computed once per (record, head).
 template <typename T>
 __global__ void __launch_bounds__(128) decode_reduce_kernel(void *out, const int32_t *__restrict__ lens,
                                                             int max_blocks, int S, int Hq, int Hkv, int D, int B,
                                                             int GT, const float *__restrict__ partials,
                                                             const long long *__restrict__ cum, int nctas) {
+  __shared__ int rec_idx[kMaxRecords];
+  __shared__ float wgt[kMaxRecords][8];
+  __shared__ int nrec;
   const int G = Hq / Hkv;
   const int HC = G / GT;
   const int PC = Hkv * HC;
@@ -58,39 +100,69 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(void *out, const int
       continue;
     }
     const long long P0 = cum[s] + (long long)pc * nb;
-    const long long P1 = P0 + nb;
     const int cf = cta_of(P0, W, nctas);
-    const int cl = cta_of(P1 - 1, W, nctas);
+    const int cl = cta_of(P0 + nb - 1, W, nctas);
     if (cf == cl) continue;  // finished inside one CTA by the partition kernel
+    if (threadIdx.x == 0) {
+      int n = 0;
+      for (int c = cf; c <= cl && n < kMaxRecords; ++c) {
+        const long long r0 = range_start(c, W, nctas);
+        if (r0 == range_start(c + 1, W, nctas)) continue;
+        const int slot = (c == cf && r0 < P0) ? 1 : 0;
+        rec_idx[n++] = c * 2 + slot;
+      }
+      nrec = n;
+    }
+    __syncthreads();
+    const int n = nrec;
+    if (threadIdx.x < GT) {
+      const int h = threadIdx.x;
+      float M = -CUDART_INF_F;
+      for (int r = 0; r < n; ++r) M = fmaxf(M, partials[((long long)rec_idx[r] * GT + h) * (D + 2) + D]);
+      float den = 0.f;
+      for (int r = 0; r < n; ++r) {
+        const float *rec = partials + ((long long)rec_idx[r] * GT + h) * (D + 2);
+        const float f = fast_exp2(rec[D] - M);
+        wgt[r][h] = f;
+        den += f * rec[D + 1];
+      }
+      const float inv = 1.f / den;
+      for (int r = 0; r < n; ++r) wgt[r][h] *= inv;
+    }
+    __syncthreads();
     for (int idx = threadIdx.x; idx < GT * D; idx += blockDim.x) {
       const int h = idx / D;
       const int d = idx - h * D;
-      float M = -CUDART_INF_F;
-      for (int c = cf; c <= cl; ++c) {
-        if (range_start(c, W, nctas) == range_start(c + 1, W, nctas)) continue;
-        const int slot = (c == cf && range_start(c, W, nctas) < P0) ? 1 : 0;
-        M = fmaxf(M, partials[(((long long)c * 2 + slot) * GT + h) * (D + 2) + D]);
-      }
-      float num = 0.f, den = 0.f;
-      for (int c = cf; c <= cl; ++c) {
-        if (range_start(c, W, nctas) == range_start(c + 1, W, nctas)) continue;
-        const int slot = (c == cf && range_start(c, W, nctas) < P0) ? 1 : 0;
-        const float *rec = partials + (((long long)c * 2 + slot) * GT + h) * (D + 2);
-        const float f = fast_exp2(rec[D] - M);
-        num += f * rec[d];
-        den += f * rec[D + 1];
-      }
-      o[h * D + d] = Elem<T>::from_float(num / den);
+      float num = 0.f;
+      for (int r = 0; r < n; ++r) num += wgt[r][h] * partials[((long long)rec_idx[r] * GT + h) * (D + 2) + d];
+      o[idx] = Elem<T>::from_float(num);
     }
+    __syncthreads();
   }
 }
 
+// ----------------------------------------------------------------- dispatch
 struct DecodeShape {
   int G, GT, nctas;
+  bool mma;
   size_t ring_bytes;
   uint32_t slot_stride;
   int nstage;
 };
+
+// Largest power of two <= 8 dividing G (CUDA-core kernel, GT is a template
+// parameter there) or largest divisor <= 8 (tensor-core kernel, which covers
+// up to 8 heads with one N = 8 MMA tile).
+static int pick_head_chunk(int G, bool mma) {
+  if (mma) {
+    for (int gt = 8; gt > 1; --gt)
+      if (G % gt == 0) return gt;
+    return 1;
+  }
+  for (int gt = 8; gt > 1; gt >>= 1)
+    if (G % gt == 0) return gt;
+  return 1;
+}
 
 static pa_status check_decode_args(int max_blocks_per_seq, int num_seqs, int num_heads, int num_kv_heads,
                                    int head_dim, int block_size, int64_t num_blocks, pa_dtype dtype,
@@ -102,12 +174,16 @@ static pa_status check_decode_args(int max_blocks_per_seq, int num_seqs, int num
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (block_size > kMaxBlockSize) return PA_ERR_UNSUPPORTED;
   if ((long long)max_blocks_per_seq * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  if (num_blocks * num_kv_heads * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   shape->G = num_heads / num_kv_heads;
-  shape->GT = pick_head_chunk(shape->G);
+  shape->mma = dtype != PA_F32 && block_size % 16 == 0 && tensor_map_encoder() != nullptr;
+  shape->GT = pick_head_chunk(shape->G, shape->mma);
   shape->nctas = decode_grid();
   if (shape->nctas <= 0) return PA_ERR_CUDA;
+  if (shape->nctas > kMaxRecords) return PA_ERR_UNSUPPORTED;
   const size_t slot_bytes = size_t(block_size) * head_dim * dtype_bytes(dtype);
-  shape->slot_stride = uint32_t((slot_bytes + 127) & ~size_t(127));
+  const size_t align = shape->mma ? 1024 : 128;  // the swizzled tiles repeat every 1024 bytes
+  shape->slot_stride = uint32_t((slot_bytes + align - 1) / align * align);
   shape->nstage = int(kRingBytes / shape->slot_stride);
   if (shape->nstage > kMaxStages) shape->nstage = kMaxStages;
   if (shape->nstage < 1) return PA_ERR_UNSUPPORTED;
@@ -116,23 +192,33 @@ static pa_status check_decode_args(int max_blocks_per_seq, int num_seqs, int num
 }
 
 template <typename T>
-static pa_status dispatch_partition(const DecodeArgs &a, int D, int GT, size_t ring, cudaStream_t st) {
+static pa_status dispatch_simt(const DecodeArgs &a, int D, int GT, size_t ring, cudaStream_t st) {
   if (D == 64) {
     switch (GT) {
-      case 1: return launch_decode_partition<T, 64, 1>(a, ring, st);
-      case 2: return launch_decode_partition<T, 64, 2>(a, ring, st);
-      case 4: return launch_decode_partition<T, 64, 4>(a, ring, st);
-      case 8: return launch_decode_partition<T, 64, 8>(a, ring, st);
+      case 1: return launch_decode_simt<T, 64, 1>(a, ring, st);
+      case 2: return launch_decode_simt<T, 64, 2>(a, ring, st);
+      case 4: return launch_decode_simt<T, 64, 4>(a, ring, st);
+      case 8: return launch_decode_simt<T, 64, 8>(a, ring, st);
     }
   } else {
     switch (GT) {
-      case 1: return launch_decode_partition<T, 128, 1>(a, ring, st);
-      case 2: return launch_decode_partition<T, 128, 2>(a, ring, st);
-      case 4: return launch_decode_partition<T, 128, 4>(a, ring, st);
-      case 8: return launch_decode_partition<T, 128, 8>(a, ring, st);
+      case 1: return launch_decode_simt<T, 128, 1>(a, ring, st);
+      case 2: return launch_decode_simt<T, 128, 2>(a, ring, st);
+      case 4: return launch_decode_simt<T, 128, 4>(a, ring, st);
+      case 8: return launch_decode_simt<T, 128, 8>(a, ring, st);
     }
   }
   return PA_ERR_UNSUPPORTED;
+}
+
+template <typename T>
+static pa_status dispatch_mma(const DecodeArgs &a, const void *k_cache, const void *v_cache, pa_dtype dtype, int D,
+                              size_t ring, cudaStream_t st) {
+  CUtensorMap mk, mv;
+  if (!encode_pool_map(&mk, k_cache, dtype, a.num_blocks, a.Hkv, a.B, D) ||
+      !encode_pool_map(&mv, v_cache, dtype, a.num_blocks, a.Hkv, a.B, D))
+    return PA_ERR_CUDA;
+  return D == 64 ? launch_decode_mma<T, 64>(a, mk, mv, ring, st) : launch_decode_mma<T, 128>(a, mk, mv, ring, st);
 }
 
 }  // namespace pagedkv
@@ -187,11 +273,18 @@ extern "C" pa_status pa_decode_partition(void *out, const void *q, const void *k
   a.nctas = sh.nctas;
   a.nstage = sh.nstage;
   a.slot_stride = sh.slot_stride;
+  a.GT = sh.GT;
+  a.ncw = sh.nstage / 2 < kConsumerWarps ? (sh.nstage / 2 > 0 ? sh.nstage / 2 : 1) : kConsumerWarps;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (sh.mma) {
+    return dtype == PA_BF16
+               ? dispatch_mma<__nv_bfloat16>(a, k_cache, v_cache, dtype, head_dim, sh.ring_bytes, s)
+               : dispatch_mma<__half>(a, k_cache, v_cache, dtype, head_dim, sh.ring_bytes, s);
+  }
   switch (dtype) {
-    case PA_F32: return dispatch_partition<float>(a, head_dim, sh.GT, sh.ring_bytes, s);
-    case PA_F16: return dispatch_partition<__half>(a, head_dim, sh.GT, sh.ring_bytes, s);
-    case PA_BF16: return dispatch_partition<__nv_bfloat16>(a, head_dim, sh.GT, sh.ring_bytes, s);
+    case PA_F32: return dispatch_simt<float>(a, head_dim, sh.GT, sh.ring_bytes, s);
+    case PA_F16: return dispatch_simt<__half>(a, head_dim, sh.GT, sh.ring_bytes, s);
+    case PA_BF16: return dispatch_simt<__nv_bfloat16>(a, head_dim, sh.GT, sh.ring_bytes, s);
   }
   return PA_ERR_INVALID_ARG;
 }

@@ -1,6 +1,6 @@
-// pa_decode_f32.cu -- decode kernel instantiations for float elements.
+// pa_decode_f32.cu -- decode kernel instantiations for fp32 caches (CUDA-core path).
 #include "pa_decode_inst.cuh"
 
 namespace pagedkv {
-PAGEDKV_INSTANTIATE_DECODE(float)
+PAGEDKV_INSTANTIATE_SIMT(float)
 }  // namespace pagedkv

@@ -1,35 +1,58 @@
-// pa_decode_inst.cuh -- launcher body shared by the per-dtype translation
-// units (each instantiates the decode kernel for one element type, so the
-// variants compile in parallel).
+// pa_decode_inst.cuh -- launchers shared by the per-dtype translation units
+// (each instantiates the decode kernels for one element type, so the variants
+// compile in parallel).
 #pragma once
 
-#include "pa_decode_impl.cuh"
+#include "pa_decode_mma.cuh"
+#include "pa_decode_simt.cuh"
 
 namespace pagedkv {
 
-template <typename T, int D, int GT>
-pa_status launch_decode_partition(const DecodeArgs &a, size_t ring_bytes, cudaStream_t stream) {
-  auto kern = decode_partition_kernel<T, D, GT>;
-  static int configured[64] = {0};
+// Opt a kernel in to the ring's dynamic shared memory once per device.
+template <typename K>
+inline bool configure_once(K kern, int bytes, int *configured) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (!configured[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kRingBytes)) != cudaSuccess)
-      return PA_ERR_CUDA;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
     configured[dev] = 1;
   }
+  return true;
+}
+
+template <typename T, int D, int GT>
+pa_status launch_decode_simt(const DecodeArgs &a, size_t ring_bytes, cudaStream_t stream) {
+  static int configured[64] = {0};
+  auto kern = decode_partition_kernel<T, D, GT>;
+  if (!configure_once(kern, kRingBytes, configured)) return PA_ERR_CUDA;
   kern<<<a.nctas, kDecodeThreads, ring_bytes, stream>>>(a);
   return launch_status();
 }
 
-#define PAGEDKV_INSTANTIATE_DECODE(T)                                                            \
-  template pa_status launch_decode_partition<T, 64, 1>(const DecodeArgs &, size_t, cudaStream_t);  \
-  template pa_status launch_decode_partition<T, 64, 2>(const DecodeArgs &, size_t, cudaStream_t);  \
-  template pa_status launch_decode_partition<T, 64, 4>(const DecodeArgs &, size_t, cudaStream_t);  \
-  template pa_status launch_decode_partition<T, 64, 8>(const DecodeArgs &, size_t, cudaStream_t);  \
-  template pa_status launch_decode_partition<T, 128, 1>(const DecodeArgs &, size_t, cudaStream_t); \
-  template pa_status launch_decode_partition<T, 128, 2>(const DecodeArgs &, size_t, cudaStream_t); \
-  template pa_status launch_decode_partition<T, 128, 4>(const DecodeArgs &, size_t, cudaStream_t); \
-  template pa_status launch_decode_partition<T, 128, 8>(const DecodeArgs &, size_t, cudaStream_t);
+template <typename T, int D>
+pa_status launch_decode_mma(const DecodeArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t ring_bytes,
+                            cudaStream_t stream) {
+  static int configured[64] = {0};
+  auto kern = decode_partition_mma_kernel<T, D>;
+  if (!configure_once(kern, kRingBytes + 1024, configured)) return PA_ERR_CUDA;
+  kern<<<a.nctas, kDecodeThreads, ring_bytes + 1024, stream>>>(a, mk, mv);
+  return launch_status();
+}
+
+#define PAGEDKV_INSTANTIATE_SIMT(T)                                                           \
+  template pa_status launch_decode_simt<T, 64, 1>(const DecodeArgs &, size_t, cudaStream_t);  \
+  template pa_status launch_decode_simt<T, 64, 2>(const DecodeArgs &, size_t, cudaStream_t);  \
+  template pa_status launch_decode_simt<T, 64, 4>(const DecodeArgs &, size_t, cudaStream_t);  \
+  template pa_status launch_decode_simt<T, 64, 8>(const DecodeArgs &, size_t, cudaStream_t);  \
+  template pa_status launch_decode_simt<T, 128, 1>(const DecodeArgs &, size_t, cudaStream_t); \
+  template pa_status launch_decode_simt<T, 128, 2>(const DecodeArgs &, size_t, cudaStream_t); \
+  template pa_status launch_decode_simt<T, 128, 4>(const DecodeArgs &, size_t, cudaStream_t); \
+  template pa_status launch_decode_simt<T, 128, 8>(const DecodeArgs &, size_t, cudaStream_t);
+
+#define PAGEDKV_INSTANTIATE_MMA(T)                                                                          \
+  template pa_status launch_decode_mma<T, 64>(const DecodeArgs &, const CUtensorMap &, const CUtensorMap &, \
+                                              size_t, cudaStream_t);                                        \
+  template pa_status launch_decode_mma<T, 128>(const DecodeArgs &, const CUtensorMap &, const CUtensorMap &, \
+                                               size_t, cudaStream_t);
 
 }  // namespace pagedkv

@@ -1,0 +1,403 @@
+// pa_decode_mma.cuh -- split-context paged decode kernel on the tensor cores
+// (a4), for fp16 / bf16 caches whose block size is a multiple of 16.
+//
+// Same schedule as the CUDA-core kernel (pa_sched.cuh): one producer warp and
+// four consumer warps per CTA, one CTA range of tiles per CTA.  Differences:
+//
+// * Loads.  Each K or V tile (B rows of D elements, contiguous in the pool) is
+//   brought in by 2-D TMA tensor copies, one per 64-column half, with the
+//   128-byte swizzle: row r's 16-byte chunk c lands at chunk c ^ (r & 7), so
+//   the 8-row fragment loads below never hit the same bank twice.
+//
+// * QK on tensor cores, transposed: S^T = K * Q^T with one mma.m16n8k16 per
+//   16 tokens x 16 dims (M = tokens, N = the <= 8 query heads sharing this kv
+//   head, K = dims).  The K fragment comes from ldmatrix; the q fragment stays
+//   in registers for the whole segment.  Products of two 16-bit inputs are
+//   exact and summed in fp32; the fp32 score is then scaled by scale*log2(e).
+//
+// * Online softmax in registers: each lane holds 2 heads x 2 tokens of every
+//   16-token sub-tile; row maxima come from 3 xor-shuffles.
+//
+// * PV on tensor cores, transposed: O^T += V^T * P^T (M = dims, N = heads,
+//   K = tokens).  V^T comes from ldmatrix.trans.  The accumulator layout of S^T
+//   is the transpose of the operand layout P^T needs, one 8x8 movmatrix.trans
+//   per half turns one into the other.  P is fed as two 16-bit terms
+//   (P = P_hi + P_lo, each rounded to the input type), so the weights carry
+//   ~16 significant bits and PV stays close to an fp32 product.
+#pragma once
+
+#include "pa_sched.cuh"
+
+namespace pagedkv {
+
+// Shared-memory address of (row, 16-byte logical chunk) in a swizzled tile
+// laid out as [D/64 halves][B rows][128 bytes].
+__device__ __forceinline__ uint32_t swz(uint32_t tile, int B, int half, int row, int chunk) {
+  return tile + uint32_t(half * B * 128 + row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
+    decode_partition_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap map_k,
+                                const __grid_constant__ CUtensorMap map_v) {
+  constexpr int KS = D / 16;     // k-steps of QK, m-tiles of PV
+  constexpr int HALVES = D / 64; // 128-byte column halves of a row
+  extern __shared__ __align__(1024) unsigned char ring_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(16) float mrg[kConsumerWarps][8][D + 2];
+  __shared__ long long sh_W, sh_r0;
+  __shared__ int sh_s0;
+  __shared__ int sh_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = a.Hq / a.Hkv;
+  const int GT = a.GT;
+  const int HC = G / GT;
+  const int PC = a.Hkv * HC;
+  const int B = a.B;
+  volatile int *abort_flag = &sh_abort;
+  // the swizzle pattern repeats every 1024 bytes: align the ring to that
+  const uint32_t raw_addr = smem_addr(ring_raw);
+  const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+  unsigned char *ring = ring_raw + pad;
+  const uint32_t ring_addr = raw_addr + pad;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.nstage; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    sh_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == kConsumerWarps) {
+    long long W, r0;
+    int s0;
+    schedule_scan(a, PC, lane, &W, &s0, &r0);
+    if (lane == 0) {
+      sh_W = W;
+      sh_s0 = s0;
+      sh_r0 = r0;
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_k)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_v)) : "memory");
+    }
+  }
+  __syncthreads();
+
+  const long long W = sh_W;
+  const long long w0 = (long long)blockIdx.x * W / a.nctas;
+  const long long w1 = (long long)(blockIdx.x + 1) * W / a.nctas;
+  if (w0 >= w1) return;
+  const uint32_t tile_bytes = uint32_t(B) * D * 2;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    long long e = 0;
+    bool aborted = false;
+    Walk wk;
+    wk.start(a, sh_s0, sh_r0, w0);
+    while (wk.w < w1 && !aborted) {
+      const int n = wk.seg_len(w1);
+      const int kvh = wk.pc / HC;
+      const int32_t *trow = a.tables + (long long)wk.s * a.max_blocks + wk.b;
+      int pid_next = lane < n ? trow[lane] : -1;
+      for (int base = 0; base < n && !aborted; base += 32) {
+        const int pid_cur = pid_next;
+        const int cnt = min(32, n - base);
+        if (base + 32 < n) pid_next = (base + 32 + lane < n) ? trow[base + 32 + lane] : -1;
+        for (int k = 0; k < cnt; ++k) {
+          const int p = __shfl_sync(kFullMask, pid_cur, k);
+          if (lane == 0 && !aborted) {
+            const bool ok = p >= 0 && p < a.num_blocks;
+            if (!ok) raise_error(a.err, PA_DEVERR_BLOCK_ID);
+            const int row = (ok ? p * a.Hkv + kvh : 0) * B;
+#pragma unroll
+            for (int kind = 0; kind < 2; ++kind) {
+              const int slot = int(e % a.nstage);
+              const uint32_t u = uint32_t(e / a.nstage);
+              if (*abort_flag || (u > 0 && !mbar_wait(&empty_bar[slot], (u - 1) & 1u, abort_flag))) {
+#ifdef PA_DEBUG
+                printf("pagedkv producer: cta %d e %lld slot %d u %u seg s %d pc %d b %d n %d k %d base %d range [%lld, "
+                       "%lld) abort %d\n",
+                       blockIdx.x, e, slot, u, wk.s, wk.pc, wk.b, n, k, base, w0, w1, *abort_flag);
+#endif
+                aborted = true;
+                *abort_flag = 1;
+                raise_error(a.err, PA_DEVERR_TIMEOUT);
+                break;
+              }
+#ifdef PA_DEBUG
+              // the slot's previous fill must have landed before it is refilled
+              if (u > 0 && !mbar_try_wait(&full_bar[slot], (u - 1) & 1u)) {
+                raise_error(a.err, kDbgPhase);
+                printf("pagedkv refill of a slot still in flight: cta %d e %lld slot %d u %u\n", blockIdx.x, e, slot, u);
+                int never = 0;
+                mbar_wait(&full_bar[slot], (u - 1) & 1u, &never);  // let it land first
+              }
+#endif
+              if (ok) {
+                mbar_arrive_expect_tx(&full_bar[slot], tile_bytes);
+                unsigned char *dst = ring + size_t(slot) * a.slot_stride;
+#pragma unroll
+                for (int h = 0; h < HALVES; ++h) {
+                  int y = row;
+                  PA_DBG_FIX(y >= 0 && (long long)y + B <= a.num_blocks * a.Hkv * B, kDbgTma, y = 0);
+                  PA_DBG_FIX(smem_addr(dst + h * B * 128) + uint32_t(B) * 128 <= ring_addr + a.nstage * a.slot_stride &&
+                                 (smem_addr(dst + h * B * 128) & 1023u) == 0,
+                             kDbgSmem, break);
+                  tma_load_2d(dst + h * B * 128, kind == 0 ? &map_k : &map_v, 64 * h, y, &full_bar[slot]);
+                }
+              } else {
+                mbar_arrive(&full_bar[slot]);
+              }
+              ++e;
+            }
+          }
+          aborted = __shfl_sync(kFullMask, aborted, 0);
+        }
+      }
+      wk.advance(a, n, PC);
+    }
+    if (lane == 0) {
+      const long long first = e > a.nstage ? e - a.nstage : 0;
+      for (long long i = first; i < e; ++i) {
+        int dummy = 0;
+        mbar_wait(&full_bar[i % a.nstage], uint32_t(i / a.nstage) & 1u, &dummy);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2;      // fragment row group
+  const int c4 = lane & 3;      // fragment column pair
+  const int mj = lane >> 3;     // ldmatrix: which 8x8 matrix this lane addresses
+  const int mr = lane & 7;      // ldmatrix: which row of it
+
+  Walk wk;
+  wk.start(a, sh_s0, sh_r0, w0);
+  long long j = 0;
+  while (wk.w < w1) {
+    const int n = wk.seg_len(w1);
+    const bool complete = (wk.b == 0 && n == wk.nb);
+    const bool first_seg = (wk.w == w0);
+    const int kvh = wk.pc / HC;
+    const int hq0 = kvh * G + (wk.pc % HC) * GT;
+    const int L = clamped_len(a, wk.s);
+
+    // running state: heads h0 = 2*c4 and h1 = 2*c4 + 1 of this lane
+    float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+    float o[KS][4];
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    // this warp's first tile of the segment (warps >= ncw take none)
+    long long jj = warp < a.ncw ? j + ((warp - int(j % a.ncw)) + a.ncw) % a.ncw : j + n;
+    if (jj < j + n) {
+      // q^T fragment (B operand of QK): head g of the chunk, dims 16ks + 2*c4 (+1), (+8)
+      uint32_t qf[KS][2];
+      if (g < GT) {
+        long long qoff = ((long long)wk.s * a.Hq + hq0 + g) * D;
+        PA_DBG_FIX(qoff >= 0 && qoff + D <= (long long)a.S * a.Hq * D, kDbgGlobal, qoff = 0);
+        const T *qrow = static_cast<const T *>(a.q) + qoff;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          qf[ks][0] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c4);
+          qf[ks][1] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * c4);
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) qf[ks][0] = qf[ks][1] = 0u;
+      }
+
+      for (; jj < j + n; jj += a.ncw) {
+        const int bb = wk.b + int(jj - j);
+        const int nv = min(B, L - bb * B);
+        const int nsub = (nv + 15) >> 4;
+        const long long eK = 2 * jj;
+        const int slotK = int(eK % a.nstage), slotV = int((eK + 1) % a.nstage);
+#ifdef PA_DEBUG
+        const uint32_t parK = uint32_t(eK / a.nstage) & 1u, parV = uint32_t((eK + 1) / a.nstage) & 1u;
+#endif
+        const uint32_t kt = ring_addr + uint32_t(slotK) * a.slot_stride;
+        const uint32_t vt = ring_addr + uint32_t(slotV) * a.slot_stride;
+
+        // ---- QK: scores of up to 4 sub-tiles of 16 tokens
+        const bool okK = wait_entry(full_bar, empty_bar, eK, a.nstage, abort_flag);
+#ifdef PA_DEBUG
+        if (okK && lane == 0 && mbar_try_wait(&full_bar[slotK], parK ^ 1u)) {
+          raise_error(a.err, kDbgPhase);  // the barrier ran two phases ahead of this entry
+          printf("pagedkv K phase ahead: cta %d warp %d eK %lld slot %d\n", blockIdx.x, warp, eK, slotK);
+        }
+#endif
+        if (!okK) {
+          if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+#ifdef PA_DEBUG
+          if (lane == 0)
+            printf("pagedkv consumer K: cta %d warp %d jj %lld eK %lld slot %d par %u seg s %d pc %d b %d n %d w %lld "
+                   "range [%lld, %lld) abort %d\n",
+                   blockIdx.x, warp, jj, eK, slotK, parK, wk.s, wk.pc, wk.b, n, wk.w, w0, w1, *abort_flag);
+#endif
+          *abort_flag = 1;
+        }
+        // Lanes leave the wait loop at different iterations: reconverge before
+        // the warp-collective ldmatrix / mma.sync.aligned below.
+        __syncwarp();
+        float sc[4][4];
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+          sc[st][0] = sc[st][1] = sc[st][2] = sc[st][3] = -CUDART_INF_F;
+          if (st < nsub) {
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            const int row = st * 16 + (mj & 1) * 8 + mr;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+              uint32_t af[4];
+              uint32_t ad = swz(kt, B, ks >> 2, row, (ks & 3) * 2 + (mj >> 1));
+              PA_DBG_FIX(ad >= ring_addr && ad + 16 <= ring_addr + a.nstage * a.slot_stride && (ad & 15u) == 0,
+                         kDbgSmem, ad = ring_addr);
+              ldmatrix_x4(af, ad);
+              Mma<T>::run(c, af, qf[ks][0], qf[ks][1]);
+            }
+            const int t0 = st * 16 + g;
+            sc[st][0] = t0 < nv ? c[0] * a.qscale : -CUDART_INF_F;
+            sc[st][1] = t0 < nv ? c[1] * a.qscale : -CUDART_INF_F;
+            sc[st][2] = t0 + 8 < nv ? c[2] * a.qscale : -CUDART_INF_F;
+            sc[st][3] = t0 + 8 < nv ? c[3] * a.qscale : -CUDART_INF_F;
+          }
+        }
+        __syncwarp();
+        if (lane == 0 && okK) mbar_arrive(&empty_bar[slotK]);
+
+        // ---- online softmax (base 2), heads h0 / h1 of this lane
+        float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+          mx0 = fmaxf(mx0, fmaxf(sc[st][0], sc[st][2]));
+          mx1 = fmaxf(mx1, fmaxf(sc[st][1], sc[st][3]));
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        l0 *= al0;
+        l1 *= al1;
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+          sc[st][0] = fast_exp2(sc[st][0] - mn0);
+          sc[st][1] = fast_exp2(sc[st][1] - mn1);
+          sc[st][2] = fast_exp2(sc[st][2] - mn0);
+          sc[st][3] = fast_exp2(sc[st][3] - mn1);
+          l0 += sc[st][0] + sc[st][2];
+          l1 += sc[st][1] + sc[st][3];
+        }
+        if (__any_sync(kFullMask, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+          }
+        }
+
+        // ---- PV
+        const bool okV = wait_entry(full_bar, empty_bar, eK + 1, a.nstage, abort_flag);
+        if (!okV) {
+          if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+#ifdef PA_DEBUG
+          if (lane == 0)
+            printf("pagedkv consumer V: cta %d warp %d jj %lld slot %d par %u seg s %d pc %d b %d n %d abort %d\n",
+                   blockIdx.x, warp, jj, slotV, parV, wk.s, wk.pc, wk.b, n, *abort_flag);
+#endif
+          *abort_flag = 1;
+        }
+        __syncwarp();  // reconverge after the wait (see above)
+        if (nv < nsub * 16) {
+          // rows past the context in the last sub-tile: make them zero so a
+          // zero weight times stale data cannot produce NaN
+          const int rows = nsub * 16 - nv;
+          for (int i = lane; i < rows * HALVES * 8; i += 32) {
+            const int r = nv + i / (HALVES * 8);
+            const int hc = i % (HALVES * 8);
+            size_t zo = (size_t)slotV * a.slot_stride + (hc >> 3) * B * 128 + r * 128 + (hc & 7) * 16;
+            PA_DBG_FIX(zo + 16 <= (size_t)a.nstage * a.slot_stride, kDbgSmem, continue);
+            *reinterpret_cast<uint4 *>(ring + zo) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_shared();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+          if (st < nsub) {
+            const uint32_t hi0 = Mma<T>::pack(sc[st][0], sc[st][1]);  // token g
+            const uint32_t hi1 = Mma<T>::pack(sc[st][2], sc[st][3]);  // token g + 8
+            const float2 f0 = Mma<T>::unpack(hi0), f1 = Mma<T>::unpack(hi1);
+            const uint32_t lo0 = Mma<T>::pack(sc[st][0] - f0.x, sc[st][1] - f0.y);
+            const uint32_t lo1 = Mma<T>::pack(sc[st][2] - f1.x, sc[st][3] - f1.y);
+            const uint32_t bh0 = movmatrix_trans(hi0), bh1 = movmatrix_trans(hi1);
+            const uint32_t bl0 = movmatrix_trans(lo0), bl1 = movmatrix_trans(lo1);
+            const int row = st * 16 + (mj >> 1) * 8 + mr;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+              const int chunk = 2 * mt + (mj & 1);
+              uint32_t af[4];
+              uint32_t ad = swz(vt, B, chunk >> 3, row, chunk & 7);
+              PA_DBG_FIX(ad >= ring_addr && ad + 16 <= ring_addr + a.nstage * a.slot_stride && (ad & 15u) == 0,
+                         kDbgSmem, ad = ring_addr);
+              ldmatrix_x4_trans(af, ad);
+              Mma<T>::run(o[mt], af, bh0, bh1);
+              Mma<T>::run(o[mt], af, bl0, bl1);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0 && okV) mbar_arrive(&empty_bar[slotV]);
+      }
+    }
+
+    // ---- merge the four warps' states for this (s, pc)
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(kFullMask, l0, off);
+      l1 += __shfl_xor_sync(kFullMask, l1, off);
+    }
+    const int h0 = 2 * c4, h1 = 2 * c4 + 1;
+    if (g == 0) {
+      if (h0 < GT) {
+        mrg[warp][h0][D] = m0;
+        mrg[warp][h0][D + 1] = l0;
+      }
+      if (h1 < GT) {
+        mrg[warp][h1][D] = m1;
+        mrg[warp][h1][D + 1] = l1;
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      if (h0 < GT) {
+        mrg[warp][h0][16 * mt + g] = o[mt][0];
+        mrg[warp][h0][16 * mt + g + 8] = o[mt][2];
+      }
+      if (h1 < GT) {
+        mrg[warp][h1][16 * mt + g] = o[mt][1];
+        mrg[warp][h1][16 * mt + g + 8] = o[mt][3];
+      }
+    }
+    named_barrier_sync(1, kConsumerWarps * 32);
+    combine_segment<T>(a, &mrg[0][0][0], 8 * (D + 2), D, GT, complete, first_seg, wk.s, hq0, threadIdx.x,
+                       kConsumerWarps * 32);
+    named_barrier_sync(1, kConsumerWarps * 32);
+    j += n;
+    wk.advance(a, n, PC);
+  }
+}
+
+}  // namespace pagedkv

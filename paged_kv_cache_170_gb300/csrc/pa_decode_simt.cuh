@@ -1,4 +1,5 @@
-// pa_decode_impl.cuh -- persistent split-context paged decode kernel (a4).
+// pa_decode_simt.cuh -- split-context paged decode kernel on CUDA cores (a4):
+// the path for fp32 caches and block sizes that are not a multiple of 16.
 //
 // Work decomposition.  The step's work is the ordered list of tiles
 // (sequence s, pair-chunk pc, logical block b), pc = kv head * HC + head
@@ -30,37 +31,9 @@
 //       score buffer and accumulated for all GT heads.
 #pragma once
 
-#include <math_constants.h>
-
-#include "pa_common.cuh"
+#include "pa_sched.cuh"
 
 namespace pagedkv {
-
-constexpr int kConsumerWarps = 4;
-constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
-constexpr int kCtasPerSm = 2;
-constexpr int kMaxStages = 64;
-constexpr int kMaxBlockSize = 64;
-constexpr int kRingBytes = 80 * 1024;
-
-struct DecodeArgs {
-  void *out;
-  const void *q;
-  const char *k_cache;
-  const char *v_cache;
-  const int32_t *tables;
-  const int32_t *lens;
-  int64_t num_blocks;
-  int max_blocks;
-  int S, Hq, Hkv, B;
-  float qscale;            // scale * log2(e)
-  float *partials;         // [N][2][GT][D + 2]: acc[D], m, l
-  long long *cum;          // [S + 1] tile prefix (written by CTA 0)
-  int *err;
-  int nctas;
-  int nstage;
-  uint32_t slot_stride;    // bytes between ring slots
-};
 
 template <typename T, int D, int GT>
 struct DecodeCfg {
@@ -74,17 +47,6 @@ struct DecodeCfg {
   static_assert(LPT >= 8, "a quarter warp must read one contiguous 128-byte run");
   static_assert(GT <= LPT, "one score per lane");
 };
-
-// Clamped context length of sequence s (flags out-of-range lengths once).
-__device__ __forceinline__ int clamped_len(const DecodeArgs &a, int s) {
-  int L = a.lens[s];
-  const int cap = a.max_blocks * a.B;
-  return L < 0 ? 0 : (L > cap ? cap : L);
-}
-
-__device__ __forceinline__ int blocks_of(const DecodeArgs &a, int s) {
-  return (clamped_len(a, s) + a.B - 1) / a.B;
-}
 
 // V row slice of a lane: DPV elements starting at dimension lane * DPV.
 template <typename T, int DPV>
@@ -122,59 +84,6 @@ __device__ __forceinline__ void load_p(const float *sc, int t, float *p) {
   } else {
     p[0] = sc[t];
   }
-}
-
-// Total tile count W (and, in CTA 0, the per-sequence prefix) and the tile
-// where this CTA's range starts.  Run by one whole warp.
-__device__ __forceinline__ void schedule_scan(const DecodeArgs &a, int PC, int lane, long long *W_out,
-                                              int *s0_out, long long *r0_out) {
-  const int cap = a.max_blocks * a.B;
-  long long run = 0;
-  for (int base = 0; base < a.S; base += 32) {
-    const int s = base + lane;
-    long long n = 0;
-    if (s < a.S) {
-      const int L = a.lens[s];
-      if ((L < 0 || L > cap) && blockIdx.x == 0) raise_error(a.err, PA_DEVERR_CONTEXT);
-      n = (long long)blocks_of(a, s) * PC;
-    }
-    long long incl = n;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const long long y = __shfl_up_sync(kFullMask, incl, off);
-      if (lane >= off) incl += y;
-    }
-    if (blockIdx.x == 0 && s < a.S) a.cum[s] = run + incl - n;
-    run += __shfl_sync(kFullMask, incl, 31);
-  }
-  if (blockIdx.x == 0 && lane == 0) a.cum[a.S] = run;
-  const long long W = run;
-  const long long w0 = (long long)blockIdx.x * W / a.nctas;
-  int s0 = a.S;
-  long long r0 = 0;
-  run = 0;
-  for (int base = 0; base < a.S && s0 == a.S; base += 32) {
-    const int s = base + lane;
-    const long long n = s < a.S ? (long long)blocks_of(a, s) * PC : 0;
-    long long incl = n;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const long long y = __shfl_up_sync(kFullMask, incl, off);
-      if (lane >= off) incl += y;
-    }
-    const long long excl = run + incl - n;
-    const bool hit = n > 0 && excl <= w0 && w0 < run + incl;
-    const unsigned m = __ballot_sync(kFullMask, hit);
-    if (m) {
-      const int leader = __ffs(m) - 1;
-      s0 = __shfl_sync(kFullMask, s, leader);
-      r0 = __shfl_sync(kFullMask, w0 - excl, leader);
-    }
-    run += __shfl_sync(kFullMask, incl, 31);
-  }
-  *W_out = W;
-  *s0_out = s0;
-  *r0_out = r0;
 }
 
 template <typename T, int D, int GT>
@@ -255,7 +164,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
             for (int kind = 0; kind < 2; ++kind) {
               const int slot = int(e % a.nstage);
               const uint32_t u = uint32_t(e / a.nstage);
-              if (!aborted && u > 0 && !mbar_wait(&empty_bar[slot], (u - 1) & 1u, abort_flag)) {
+              if (!aborted && (*abort_flag || (u > 0 && !mbar_wait(&empty_bar[slot], (u - 1) & 1u, abort_flag)))) {
                 aborted = true;
                 *abort_flag = 1;
                 raise_error(a.err, PA_DEVERR_TIMEOUT);
@@ -326,7 +235,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
 #pragma unroll
       for (int i = 0; i < C::DPV / 2; ++i) acc[h][i] = make_float2(0.f, 0.f);
 
-    long long jj = j + ((warp - int(j % kConsumerWarps)) + kConsumerWarps) % kConsumerWarps;
+    // this warp's first tile of the segment (warps >= ncw take none)
+    long long jj = warp < a.ncw ? j + ((warp - int(j % a.ncw)) + a.ncw) % a.ncw : j + n;
     if (jj < j + n) {
       // q slice of this lane, pre-scaled so scores come out in log2 units
       float2 qreg[GT][C::DPL / 2];
@@ -343,17 +253,17 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
             qreg[h][c * (C::EPC / 2) + i] = make_float2(f[i].x * a.qscale, f[i].y * a.qscale);
         }
 
-      for (; jj < j + n; jj += kConsumerWarps) {
+      for (; jj < j + n; jj += a.ncw) {
         const int bb = b + int(jj - j);
         const int nv = min(B, L - bb * B);
         const long long eK = 2 * jj;
         const int slotK = int(eK % a.nstage), slotV = int((eK + 1) % a.nstage);
-        const uint32_t parK = uint32_t(eK / a.nstage) & 1u, parV = uint32_t((eK + 1) / a.nstage) & 1u;
         const char *kt = reinterpret_cast<const char *>(ring) + size_t(slotK) * a.slot_stride;
         const char *vt = reinterpret_cast<const char *>(ring) + size_t(slotV) * a.slot_stride;
 
         // ---- QK
-        if (!mbar_wait(&full_bar[slotK], parK, abort_flag)) {
+        const bool okK = wait_entry(full_bar, empty_bar, eK, a.nstage, abort_flag);
+        if (!okK) {
           if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
           *abort_flag = 1;
         }
@@ -391,7 +301,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[slotK]);
+        if (lane == 0 && okK) mbar_arrive(&empty_bar[slotK]);
 
         // ---- online softmax over this tile (base 2)
         float mx = -CUDART_INF_F;
@@ -418,7 +328,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
         __syncwarp();
 
         // ---- PV
-        if (!mbar_wait(&full_bar[slotV], parV, abort_flag)) {
+        const bool okV = wait_entry(full_bar, empty_bar, eK + 1, a.nstage, abort_flag);
+        if (!okV) {
           if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
           *abort_flag = 1;
         }
@@ -437,7 +348,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[slotV]);
+        if (lane == 0 && okV) mbar_arrive(&empty_bar[slotV]);
       }
     }
 
@@ -457,31 +368,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
         mrg[warp][h][lane * C::DPV + 2 * i + 1] = acc[h][i].y;
       }
     named_barrier_sync(1, kConsumerWarps * 32);
-    for (int idx = threadIdx.x; idx < GT * D; idx += kConsumerWarps * 32) {
-      const int h = idx / D;
-      const int d = idx - h * D;
-      float M = -CUDART_INF_F;
-#pragma unroll
-      for (int q = 0; q < kConsumerWarps; ++q) M = fmaxf(M, mrg[q][h][D]);
-      float num = 0.f, den = 0.f;
-#pragma unroll
-      for (int q = 0; q < kConsumerWarps; ++q) {
-        const float f = fast_exp2(mrg[q][h][D] - M);
-        num += f * mrg[q][h][d];
-        den += f * mrg[q][h][D + 1];
-      }
-      if (complete) {
-        T *o = static_cast<T *>(a.out) + ((long long)s * a.Hq + hq0 + h) * D + d;
-        *o = Elem<T>::from_float(num / den);
-      } else {
-        float *rec = a.partials + (((long long)blockIdx.x * 2 + (first_seg ? 0 : 1)) * GT + h) * (D + 2);
-        rec[d] = num;
-        if (d == 0) {
-          rec[D] = M;
-          rec[D + 1] = den;
-        }
-      }
-    }
+    combine_segment<T>(a, &mrg[0][0][0], GT * (D + 2), D, GT, complete, first_seg, s, hq0, threadIdx.x,
+                       kConsumerWarps * 32);
     named_barrier_sync(1, kConsumerWarps * 32);
 
     w += n;
@@ -500,7 +388,5 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
   }
 }
 
-template <typename T, int D, int GT>
-pa_status launch_decode_partition(const DecodeArgs &a, size_t ring_bytes, cudaStream_t stream);
 
 }  // namespace pagedkv
