@@ -202,6 +202,16 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
       : "memory");
 }
 
+// 3-D tiled bulk copy (TMA tensor) global -> shared at element coordinates
+// (x innermost, y, z).
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (bulk copy) accesses of the same bytes.
 __device__ __forceinline__ void fence_proxy_async_shared() {

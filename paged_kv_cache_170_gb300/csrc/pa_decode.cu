@@ -46,18 +46,32 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A pool [NB][Hkv][B][D] seen as NB*Hkv*B rows of D 16-bit elements; one box
-// is B rows x 64 columns (128 bytes), 128-byte swizzled.
+// A pool [NB][Hkv][B][D] seen as NB*Hkv*B rows of D 16-bit elements, loaded
+// with the 128-byte swizzle into [D/64 halves][B rows][128 bytes].  With
+// three_d (D = 128) the map is (64 elements, rows, 2 halves) with the halves
+// 128 bytes apart, so one box {64, B, 2} brings a whole tile; otherwise one
+// 2-D box {64, B} per half.
 static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype, int64_t num_blocks, int Hkv,
-                            int B, int D) {
+                            int B, int D, bool three_d) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
-  const cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(num_blocks) * Hkv * B};
+  const CUtensorMapDataType ty =
+      dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint64_t rows = cuuint64_t(num_blocks) * Hkv * B;
+  if (three_d) {
+    const cuuint64_t dims[3] = {64, rows, 2};
+    const cuuint64_t strides[2] = {cuuint64_t(D) * 2, 128};
+    const cuuint32_t box[3] = {64, cuuint32_t(B), 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, ty, 3, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  const cuuint64_t dims[2] = {cuuint64_t(D), rows};
   const cuuint64_t strides[1] = {cuuint64_t(D) * 2};
   const cuuint32_t box[2] = {64, cuuint32_t(B)};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-             const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  return enc(map, ty, 2, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -146,8 +160,8 @@ struct DecodeShape {
   int G, GT, nctas;
   bool mma;
   size_t ring_bytes;
-  uint32_t slot_stride;
-  int nstage;
+  uint32_t slot_stride, tile_stride;
+  int nstage, ncw, pg;
 };
 
 // Largest power of two <= 8 dividing G (CUDA-core kernel, GT is a template
@@ -181,12 +195,21 @@ static pa_status check_decode_args(int max_blocks_per_seq, int num_seqs, int num
   shape->nctas = decode_grid();
   if (shape->nctas <= 0) return PA_ERR_CUDA;
   if (shape->nctas > kMaxRecords) return PA_ERR_UNSUPPORTED;
-  const size_t slot_bytes = size_t(block_size) * head_dim * dtype_bytes(dtype);
+  // one ring slot holds the K tile and the V tile of one (block, kv head)
+  const size_t tile_bytes = size_t(block_size) * head_dim * dtype_bytes(dtype);
   const size_t align = shape->mma ? 1024 : 128;  // the swizzled tiles repeat every 1024 bytes
-  shape->slot_stride = uint32_t((slot_bytes + align - 1) / align * align);
+  shape->tile_stride = uint32_t((tile_bytes + align - 1) / align * align);
+  shape->slot_stride = 2 * shape->tile_stride;
   shape->nstage = int(kRingBytes / shape->slot_stride);
   if (shape->nstage > kMaxStages) shape->nstage = kMaxStages;
   if (shape->nstage < 1) return PA_ERR_UNSUPPORTED;
+  // consumer warps and producer group size with ncw + pg <= nstage (the ring's
+  // phase argument needs it; see wait_entry): keep 4 consumers when the ring
+  // allows and give the producer what is left, up to 4 entries at a time
+  shape->ncw = shape->nstage - 1 < kConsumerWarps ? (shape->nstage > 1 ? shape->nstage - 1 : 1) : kConsumerWarps;
+  shape->pg = shape->nstage - shape->ncw;
+  if (shape->pg > 4) shape->pg = 4;
+  if (shape->pg < 1) shape->pg = 1;
   shape->ring_bytes = size_t(shape->nstage) * shape->slot_stride;
   return PA_OK;
 }
@@ -215,10 +238,21 @@ template <typename T>
 static pa_status dispatch_mma(const DecodeArgs &a, const void *k_cache, const void *v_cache, pa_dtype dtype, int D,
                               size_t ring, cudaStream_t st) {
   CUtensorMap mk, mv;
-  if (!encode_pool_map(&mk, k_cache, dtype, a.num_blocks, a.Hkv, a.B, D) ||
-      !encode_pool_map(&mv, v_cache, dtype, a.num_blocks, a.Hkv, a.B, D))
-    return PA_ERR_CUDA;
-  return D == 64 ? launch_decode_mma<T, 64>(a, mk, mv, ring, st) : launch_decode_mma<T, 128>(a, mk, mv, ring, st);
+  DecodeArgs b = a;
+  // one 3-D box per tile when the encoder takes the (rows, halves) stride
+  // order, else one 2-D box per 64-column half
+  b.nops = 1;
+  if (D == 128 && !(encode_pool_map(&mk, k_cache, dtype, a.num_blocks, a.Hkv, a.B, D, true) &&
+                    encode_pool_map(&mv, v_cache, dtype, a.num_blocks, a.Hkv, a.B, D, true))) {
+    b.nops = 2;
+  }
+  if (D == 64 || b.nops == 2) {
+    if (!encode_pool_map(&mk, k_cache, dtype, a.num_blocks, a.Hkv, a.B, D, false) ||
+        !encode_pool_map(&mv, v_cache, dtype, a.num_blocks, a.Hkv, a.B, D, false))
+      return PA_ERR_CUDA;
+    if (D == 64) b.nops = 1;
+  }
+  return D == 64 ? launch_decode_mma<T, 64>(b, mk, mv, ring, st) : launch_decode_mma<T, 128>(b, mk, mv, ring, st);
 }
 
 }  // namespace pagedkv
@@ -273,8 +307,11 @@ extern "C" pa_status pa_decode_partition(void *out, const void *q, const void *k
   a.nctas = sh.nctas;
   a.nstage = sh.nstage;
   a.slot_stride = sh.slot_stride;
+  a.tile_stride = sh.tile_stride;
   a.GT = sh.GT;
-  a.ncw = sh.nstage / 2 < kConsumerWarps ? (sh.nstage / 2 > 0 ? sh.nstage / 2 : 1) : kConsumerWarps;
+  a.ncw = sh.ncw;
+  a.pg = sh.pg;
+  a.nops = 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (sh.mma) {
     return dtype == PA_BF16

@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(16) float mrg[kConsumerWarps][8][D + 2];
   __shared__ long long sh_W, sh_r0;
+  __shared__ uint32_t issued[kMaxStages];
   __shared__ int sh_s0;
   __shared__ int sh_abort;
 
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     for (int i = 0; i < a.nstage; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
+      issued[i] = 0;
     }
     sh_abort = 0;
     fence_barrier_init();
@@ -94,79 +96,42 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    long long e = 0;
-    bool aborted = false;
-    Walk wk;
-    wk.start(a, sh_s0, sh_r0, w0);
-    while (wk.w < w1 && !aborted) {
-      const int n = wk.seg_len(w1);
-      const int kvh = wk.pc / HC;
-      const int32_t *trow = a.tables + (long long)wk.s * a.max_blocks + wk.b;
-      int pid_next = lane < n ? trow[lane] : -1;
-      for (int base = 0; base < n && !aborted; base += 32) {
-        const int pid_cur = pid_next;
-        const int cnt = min(32, n - base);
-        if (base + 32 < n) pid_next = (base + 32 + lane < n) ? trow[base + 32 + lane] : -1;
-        for (int k = 0; k < cnt; ++k) {
-          const int p = __shfl_sync(kFullMask, pid_cur, k);
-          if (lane == 0 && !aborted) {
-            const bool ok = p >= 0 && p < a.num_blocks;
-            if (!ok) raise_error(a.err, PA_DEVERR_BLOCK_ID);
-            const int row = (ok ? p * a.Hkv + kvh : 0) * B;
-#pragma unroll
-            for (int kind = 0; kind < 2; ++kind) {
-              const int slot = int(e % a.nstage);
-              const uint32_t u = uint32_t(e / a.nstage);
-              if (*abort_flag || (u > 0 && !mbar_wait(&empty_bar[slot], (u - 1) & 1u, abort_flag))) {
-#ifdef PA_DEBUG
-                printf("pagedkv producer: cta %d e %lld slot %d u %u seg s %d pc %d b %d n %d k %d base %d range [%lld, "
-                       "%lld) abort %d\n",
-                       blockIdx.x, e, slot, u, wk.s, wk.pc, wk.b, n, k, base, w0, w1, *abort_flag);
+#ifdef PA_TRACE
+    const long long tr_t0 = clock64();
 #endif
-                aborted = true;
-                *abort_flag = 1;
-                raise_error(a.err, PA_DEVERR_TIMEOUT);
-                break;
+    produce(a, PC, HC, sh_s0, sh_r0, w0, w1, lane, full_bar, empty_bar, issued, abort_flag,
+            [&](int slot, int p, int kvh, int bb, int L) {
+              (void)bb;
+              (void)L;
+              if (p < 0 || p >= a.num_blocks) {
+                raise_error(a.err, PA_DEVERR_BLOCK_ID);
+                mbar_arrive(&full_bar[slot]);  // complete the phase without data
+                return;
               }
-#ifdef PA_DEBUG
-              // the slot's previous fill must have landed before it is refilled
-              if (u > 0 && !mbar_try_wait(&full_bar[slot], (u - 1) & 1u)) {
-                raise_error(a.err, kDbgPhase);
-                printf("pagedkv refill of a slot still in flight: cta %d e %lld slot %d u %u\n", blockIdx.x, e, slot, u);
-                int never = 0;
-                mbar_wait(&full_bar[slot], (u - 1) & 1u, &never);  // let it land first
-              }
-#endif
-              if (ok) {
-                mbar_arrive_expect_tx(&full_bar[slot], tile_bytes);
-                unsigned char *dst = ring + size_t(slot) * a.slot_stride;
+              // K and V tiles of one (block, kv head) land in one slot; the full
+              // tile is copied (rows past the context are masked or zeroed later)
+              mbar_arrive_expect_tx(&full_bar[slot], 2 * tile_bytes);
+              unsigned char *dst = ring + size_t(slot) * a.slot_stride;
+              int y = (p * a.Hkv + kvh) * B;
+              PA_DBG_FIX(y >= 0 && (long long)y + B <= a.num_blocks * a.Hkv * B, kDbgTma, y = 0);
+              PA_DBG_FIX(smem_addr(dst) + a.slot_stride <= ring_addr + a.nstage * a.slot_stride &&
+                             (smem_addr(dst) & 1023u) == 0,
+                         kDbgSmem, dst = ring);
+              if (HALVES == 2 && a.nops == 1) {
+                tma_load_3d(dst, &map_k, 0, y, 0, &full_bar[slot]);
+                tma_load_3d(dst + a.tile_stride, &map_v, 0, y, 0, &full_bar[slot]);
+              } else {
 #pragma unroll
                 for (int h = 0; h < HALVES; ++h) {
-                  int y = row;
-                  PA_DBG_FIX(y >= 0 && (long long)y + B <= a.num_blocks * a.Hkv * B, kDbgTma, y = 0);
-                  PA_DBG_FIX(smem_addr(dst + h * B * 128) + uint32_t(B) * 128 <= ring_addr + a.nstage * a.slot_stride &&
-                                 (smem_addr(dst + h * B * 128) & 1023u) == 0,
-                             kDbgSmem, break);
-                  tma_load_2d(dst + h * B * 128, kind == 0 ? &map_k : &map_v, 64 * h, y, &full_bar[slot]);
+                  tma_load_2d(dst + h * B * 128, &map_k, 64 * h, y, &full_bar[slot]);
+                  tma_load_2d(dst + a.tile_stride + h * B * 128, &map_v, 64 * h, y, &full_bar[slot]);
                 }
-              } else {
-                mbar_arrive(&full_bar[slot]);
               }
-              ++e;
-            }
-          }
-          aborted = __shfl_sync(kFullMask, aborted, 0);
-        }
-      }
-      wk.advance(a, n, PC);
-    }
-    if (lane == 0) {
-      const long long first = e > a.nstage ? e - a.nstage : 0;
-      for (long long i = first; i < e; ++i) {
-        int dummy = 0;
-        mbar_wait(&full_bar[i % a.nstage], uint32_t(i / a.nstage) & 1u, &dummy);
-      }
-    }
+            });
+#ifdef PA_TRACE
+    if (lane == 0 && (blockIdx.x % 101) == 0)
+      printf("trace cta %d producer: cycles %lld\n", blockIdx.x, clock64() - tr_t0);
+#endif
     return;
   }
 
@@ -179,6 +144,9 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   Walk wk;
   wk.start(a, sh_s0, sh_r0, w0);
   long long j = 0;
+#ifdef PA_TRACE
+  long long tr_c0 = clock64(), tr_wk = 0, tr_tiles = 0;
+#endif
   while (wk.w < w1) {
     const int n = wk.seg_len(w1);
     const bool complete = (wk.b == 0 && n == wk.nb);
@@ -216,35 +184,40 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         const int bb = wk.b + int(jj - j);
         const int nv = min(B, L - bb * B);
         const int nsub = (nv + 15) >> 4;
-        const long long eK = 2 * jj;
-        const int slotK = int(eK % a.nstage), slotV = int((eK + 1) % a.nstage);
-#ifdef PA_DEBUG
-        const uint32_t parK = uint32_t(eK / a.nstage) & 1u, parV = uint32_t((eK + 1) / a.nstage) & 1u;
-#endif
-        const uint32_t kt = ring_addr + uint32_t(slotK) * a.slot_stride;
-        const uint32_t vt = ring_addr + uint32_t(slotV) * a.slot_stride;
+        const long long ee = jj;  // the pair's ring entry
+        const int slot = int(ee % a.nstage);
+        const uint32_t kt = ring_addr + uint32_t(slot) * a.slot_stride;
+        const uint32_t vt = kt + a.tile_stride;
 
-        // ---- QK: scores of up to 4 sub-tiles of 16 tokens
-        const bool okK = wait_entry(full_bar, empty_bar, eK, a.nstage, abort_flag);
+        // ---- wait for the pair (K and V land together)
+#ifdef PA_TRACE
+        long long tr_a = clock64();
+#endif
+        const bool okE = wait_entry(full_bar, empty_bar, ee, a.nstage, abort_flag);
+#ifdef PA_TRACE
+        tr_wk += clock64() - tr_a;
+        ++tr_tiles;
+#endif
 #ifdef PA_DEBUG
-        if (okK && lane == 0 && mbar_try_wait(&full_bar[slotK], parK ^ 1u)) {
+        if (okE && lane == 0 && mbar_try_wait(&full_bar[slot], (uint32_t(ee / a.nstage) & 1u) ^ 1u)) {
           raise_error(a.err, kDbgPhase);  // the barrier ran two phases ahead of this entry
-          printf("pagedkv K phase ahead: cta %d warp %d eK %lld slot %d\n", blockIdx.x, warp, eK, slotK);
+          printf("pagedkv phase ahead: cta %d warp %d entry %lld slot %d\n", blockIdx.x, warp, ee, slot);
         }
 #endif
-        if (!okK) {
+        if (!okE) {
           if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
 #ifdef PA_DEBUG
           if (lane == 0)
-            printf("pagedkv consumer K: cta %d warp %d jj %lld eK %lld slot %d par %u seg s %d pc %d b %d n %d w %lld "
-                   "range [%lld, %lld) abort %d\n",
-                   blockIdx.x, warp, jj, eK, slotK, parK, wk.s, wk.pc, wk.b, n, wk.w, w0, w1, *abort_flag);
+            printf("pagedkv consumer: cta %d warp %d entry %lld slot %d seg s %d pc %d b %d n %d abort %d\n",
+                   blockIdx.x, warp, ee, slot, wk.s, wk.pc, wk.b, n, *abort_flag);
 #endif
           *abort_flag = 1;
         }
         // Lanes leave the wait loop at different iterations: reconverge before
         // the warp-collective ldmatrix / mma.sync.aligned below.
         __syncwarp();
+
+        // ---- QK: scores of up to 4 sub-tiles of 16 tokens
         float sc[4][4];
 #pragma unroll
         for (int st = 0; st < 4; ++st) {
@@ -268,9 +241,6 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
             sc[st][3] = t0 + 8 < nv ? c[3] * a.qscale : -CUDART_INF_F;
           }
         }
-        __syncwarp();
-        if (lane == 0 && okK) mbar_arrive(&empty_bar[slotK]);
-
         // ---- online softmax (base 2), heads h0 / h1 of this lane
         float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
 #pragma unroll
@@ -309,17 +279,6 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         }
 
         // ---- PV
-        const bool okV = wait_entry(full_bar, empty_bar, eK + 1, a.nstage, abort_flag);
-        if (!okV) {
-          if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
-#ifdef PA_DEBUG
-          if (lane == 0)
-            printf("pagedkv consumer V: cta %d warp %d jj %lld slot %d par %u seg s %d pc %d b %d n %d abort %d\n",
-                   blockIdx.x, warp, jj, slotV, parV, wk.s, wk.pc, wk.b, n, *abort_flag);
-#endif
-          *abort_flag = 1;
-        }
-        __syncwarp();  // reconverge after the wait (see above)
         if (nv < nsub * 16) {
           // rows past the context in the last sub-tile: make them zero so a
           // zero weight times stale data cannot produce NaN
@@ -327,7 +286,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
           for (int i = lane; i < rows * HALVES * 8; i += 32) {
             const int r = nv + i / (HALVES * 8);
             const int hc = i % (HALVES * 8);
-            size_t zo = (size_t)slotV * a.slot_stride + (hc >> 3) * B * 128 + r * 128 + (hc & 7) * 16;
+            size_t zo = (size_t)slot * a.slot_stride + a.tile_stride + (hc >> 3) * B * 128 + r * 128 + (hc & 7) * 16;
             PA_DBG_FIX(zo + 16 <= (size_t)a.nstage * a.slot_stride, kDbgSmem, continue);
             *reinterpret_cast<uint4 *>(ring + zo) = make_uint4(0u, 0u, 0u, 0u);
           }
@@ -359,7 +318,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
           }
         }
         __syncwarp();
-        if (lane == 0 && okV) mbar_arrive(&empty_bar[slotV]);
+        if (lane == 0 && okE) mbar_arrive(&empty_bar[slot]);  // the pair's slot is free again
       }
     }
 
@@ -398,6 +357,11 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     j += n;
     wk.advance(a, n, PC);
   }
+#ifdef PA_TRACE
+  if (lane == 0 && (blockIdx.x % 101) == 0)
+    printf("trace cta %d warp %d: tiles %lld cycles %lld waiting %lld\n", blockIdx.x, warp, tr_tiles,
+           clock64() - tr_c0, tr_wk);
+#endif
 }
 
 }  // namespace pagedkv

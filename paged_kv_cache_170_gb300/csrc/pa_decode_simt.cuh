@@ -14,10 +14,11 @@
 //
 // Inside a CTA.  One producer warp walks the range in order, reads the block
 // table once per 32 tiles (coalesced, kept in registers: the table is never
-// re-read per token), and issues one 1-D bulk copy (TMA) per K tile and per V
-// tile into a ring of shared-memory slots, completion counted on an mbarrier
-// per slot.  Only the valid rows of a sequence's last, partly filled block are
-// copied.  Four consumer warps take tiles round-robin; each keeps its own
+// re-read per token), and fills a ring of shared-memory slots, one slot per
+// (block, kv head): lanes 0 and 1 issue the 1-D bulk copies (TMA) of the K
+// tile and of the V tile in one instruction, completion counted in bytes on
+// the slot's mbarrier.  Only the valid rows of a sequence's last, partly
+// filled block are copied.  Four consumer warps take tiles round-robin; each keeps its own
 // running max / sum / accumulator (online softmax, base 2) and the four
 // states are merged when the (s, pc) ends.
 //
@@ -95,6 +96,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
   __shared__ __align__(16) float sc_buf[kConsumerWarps][kMaxBlockSize * GT];
   __shared__ __align__(16) float mrg[kConsumerWarps][GT][D + 2];
   __shared__ long long sh_W, sh_r0;
+  __shared__ uint32_t issued[kMaxStages];
   __shared__ int sh_s0;
   __shared__ int sh_abort;
 
@@ -110,6 +112,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
     for (int i = 0; i < a.nstage; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
+      issued[i] = 0;
     }
     sh_abort = 0;
     fence_barrier_init();
@@ -134,76 +137,21 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    long long e = 0;  // ring entries issued
-    int s = sh_s0;
-    int nb = blocks_of(a, s);
-    int pc = int(sh_r0 / nb);
-    int b = int(sh_r0 % nb);
-    long long w = w0;
-    bool aborted = false;
-    while (w < w1) {
-      const int n = int(min((long long)(nb - b), w1 - w));
-      const int kvh = pc / HC;
-      const int L = clamped_len(a, s);
-      const int32_t *trow = a.tables + (long long)s * a.max_blocks + b;
-      int pid_next = lane < n ? trow[lane] : -1;
-      for (int base = 0; base < n; base += 32) {
-        const int pid_cur = pid_next;
-        const int cnt = min(32, n - base);
-        if (base + 32 < n) pid_next = (base + 32 + lane < n) ? trow[base + 32 + lane] : -1;
-        for (int k = 0; k < cnt; ++k) {
-          const int p = __shfl_sync(kFullMask, pid_cur, k);
-          if (lane == 0) {
-            const int bb = b + base + k;
-            const int nv = min(B, L - bb * B);
-            const uint32_t bytes = uint32_t(nv) * D * sizeof(T);
-            const bool ok = p >= 0 && p < a.num_blocks;
-            if (!ok) raise_error(a.err, PA_DEVERR_BLOCK_ID);
-            const size_t off = ((size_t)(ok ? p : 0) * a.Hkv + kvh) * tile_elems * sizeof(T);
-#pragma unroll
-            for (int kind = 0; kind < 2; ++kind) {
-              const int slot = int(e % a.nstage);
-              const uint32_t u = uint32_t(e / a.nstage);
-              if (!aborted && (*abort_flag || (u > 0 && !mbar_wait(&empty_bar[slot], (u - 1) & 1u, abort_flag)))) {
-                aborted = true;
-                *abort_flag = 1;
-                raise_error(a.err, PA_DEVERR_TIMEOUT);
-              }
-              if (aborted) break;  // issue nothing more; e counts issued entries only
-              if (ok) {
-                mbar_arrive_expect_tx(&full_bar[slot], bytes);
-                bulk_g2s(ring + size_t(slot) * a.slot_stride, (kind == 0 ? a.k_cache : a.v_cache) + off, bytes,
-                         &full_bar[slot]);
-              } else {
+    produce(a, PC, HC, sh_s0, sh_r0, w0, w1, lane, full_bar, empty_bar, issued, abort_flag,
+            [&](int slot, int p, int kvh, int bb, int L) {
+              if (p < 0 || p >= a.num_blocks) {
+                raise_error(a.err, PA_DEVERR_BLOCK_ID);
                 mbar_arrive(&full_bar[slot]);  // complete the phase without data
+                return;
               }
-              ++e;
-            }
-          }
-          __syncwarp();
-        }
-      }
-      w += n;
-      b += n;
-      if (b == nb) {
-        b = 0;
-        if (++pc == PC) {
-          pc = 0;
-          do {
-            ++s;
-          } while (s < a.S && blocks_of(a, s) == 0);
-          if (s < a.S) nb = blocks_of(a, s);
-        }
-      }
-    }
-    // Do not leave while a copy into this CTA's shared memory is in flight.
-    if (lane == 0) {
-      const long long first = e > a.nstage ? e - a.nstage : 0;
-      for (long long i = first; i < e; ++i) {
-        int dummy = 0;
-        mbar_wait(&full_bar[i % a.nstage], uint32_t(i / a.nstage) & 1u, &dummy);
-      }
-    }
+              const int nv = min(B, L - bb * B);
+              const uint32_t bytes = uint32_t(nv) * D * sizeof(T);  // valid rows only
+              const size_t off = ((size_t)p * a.Hkv + kvh) * tile_elems * sizeof(T);
+              mbar_arrive_expect_tx(&full_bar[slot], 2 * bytes);
+              unsigned char *dst = ring + size_t(slot) * a.slot_stride;
+              bulk_g2s(dst, a.k_cache + off, bytes, &full_bar[slot]);
+              bulk_g2s(dst + a.tile_stride, a.v_cache + off, bytes, &full_bar[slot]);
+            });
     return;
   }
 
@@ -256,14 +204,14 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
       for (; jj < j + n; jj += a.ncw) {
         const int bb = b + int(jj - j);
         const int nv = min(B, L - bb * B);
-        const long long eK = 2 * jj;
-        const int slotK = int(eK % a.nstage), slotV = int((eK + 1) % a.nstage);
-        const char *kt = reinterpret_cast<const char *>(ring) + size_t(slotK) * a.slot_stride;
-        const char *vt = reinterpret_cast<const char *>(ring) + size_t(slotV) * a.slot_stride;
+        const long long ee = jj;  // the pair's ring entry
+        const int slot = int(ee % a.nstage);
+        const char *kt = reinterpret_cast<const char *>(ring) + size_t(slot) * a.slot_stride;
+        const char *vt = kt + a.tile_stride;
 
-        // ---- QK
-        const bool okK = wait_entry(full_bar, empty_bar, eK, a.nstage, abort_flag);
-        if (!okK) {
+        // ---- wait for the pair (K and V land together), then QK
+        const bool okE = wait_entry(full_bar, empty_bar, ee, a.nstage, abort_flag);
+        if (!okE) {
           if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
           *abort_flag = 1;
         }
@@ -301,7 +249,6 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
           }
         }
         __syncwarp();
-        if (lane == 0 && okK) mbar_arrive(&empty_bar[slotK]);
 
         // ---- online softmax over this tile (base 2)
         float mx = -CUDART_INF_F;
@@ -328,12 +275,6 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
         __syncwarp();
 
         // ---- PV
-        const bool okV = wait_entry(full_bar, empty_bar, eK + 1, a.nstage, abort_flag);
-        if (!okV) {
-          if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
-          *abort_flag = 1;
-        }
-        __syncwarp();
 #pragma unroll 4
         for (int t = 0; t < nv; ++t) {
           float p[GT];
@@ -348,7 +289,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
           }
         }
         __syncwarp();
-        if (lane == 0 && okV) mbar_arrive(&empty_bar[slotV]);
+        if (lane == 0 && okE) mbar_arrive(&empty_bar[slot]);  // the pair's slot is free again
       }
     }
 

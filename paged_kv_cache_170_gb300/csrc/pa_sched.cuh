@@ -40,21 +40,25 @@ struct DecodeArgs {
   int *err;
   int nctas;
   int nstage;
-  uint32_t slot_stride;    // bytes between ring slots
+  uint32_t slot_stride;    // bytes between ring slots (one slot = K tile + V tile)
+  uint32_t tile_stride;    // offset of the V tile inside a slot
   int GT;                  // query heads per pair-chunk (<= 8)
-  int ncw;                 // consumer warps that take tiles (<= nstage / 2)
+  int ncw;                 // consumer warps that take tiles
+  int pg;                  // ring entries the producer issues at once (ncw + pg <= nstage)
+  int nops;                // tensor copies per tile (1: one 3-D box; 2: two 2-D halves)
 };
 
 // Wait until ring entry e (slot e % nstage, its u-th use, u = e / nstage) has
-// landed.  Consumer warps take tile pairs round-robin, so the warp waiting for
-// use u of a slot is in general not the one that consumed use u - 1, and an
-// mbarrier parity wait is only unambiguous while the barrier is at most one
-// phase behind.  So first wait until use u - 1 was released (phase u - 1 of
-// the slot's empty barrier): that release implies use u - 1 landed.  With at
-// most nstage / 2 consumer warps the release barrier itself is never more
-// than one phase behind: a warp reaching pair p has consumed pair p - ncw, so
-// every entry up to 2 (p - ncw) + 1 >= e - nstage was issued, which required
-// use u - 2 to be released.
+// landed.  An entry is one tile pair.  Consumer warps take pairs round-robin,
+// so the warp waiting for use u of a slot is in general not the one that
+// consumed use u - 1, and an mbarrier parity wait is only unambiguous while
+// the barrier is at most one phase behind.  So first wait until use u - 1 was
+// released (phase u - 1 of the slot's empty barrier): that release implies
+// use u - 1 landed.  The release barrier itself is never more than one phase
+// behind: a warp reaching pair e has consumed pair e - ncw, so the producer
+// finished every group of pg entries before the one holding e - ncw, which
+// includes e - nstage when ncw + pg <= nstage, and issuing e - nstage
+// required use u - 2 to be released.
 __device__ __forceinline__ bool wait_entry(uint64_t *full, uint64_t *empty, long long e, int nstage,
                                            volatile int *abort) {
   const int slot = int(e % nstage);
@@ -158,6 +162,74 @@ struct Walk {
     }
   }
 };
+
+// The producer warp: walks the CTA's range, reads the block table 32 entries
+// at a time (coalesced, next batch prefetched, kept in registers: never
+// re-read per token) and fills the ring.  Entries are issued in groups of pg:
+// lane i < pg claims entry e + i (waits until its slot's previous use was
+// released) and calls issue(slot, pid, kv head, logical block, context len),
+// which announces the bytes on full_bar[slot] and starts the copies; the lanes
+// of a group wait and issue in parallel.  issued[slot] keeps the last use
+// issued into each slot so the producer can wait for every copy still in
+// flight before it leaves (after an abort too).
+template <class Issue>
+__device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, int s0, long long r0, long long w0,
+                                        long long w1, int lane, uint64_t *full_bar, uint64_t *empty_bar,
+                                        uint32_t *issued, volatile int *abort_flag, Issue issue) {
+  long long e = 0;
+  bool aborted = false;
+  Walk wk;
+  wk.start(a, s0, r0, w0);
+  while (wk.w < w1 && !aborted) {
+    const int n = wk.seg_len(w1);
+    const int kvh = wk.pc / HC;
+    const int L = clamped_len(a, wk.s);
+    const int32_t *trow = a.tables + (long long)wk.s * a.max_blocks + wk.b;
+    int pid_next = lane < n ? trow[lane] : -1;
+    for (int base = 0; base < n && !aborted; base += 32) {
+      const int pid_cur = pid_next;
+      const int cnt = min(32, n - base);
+      if (base + 32 < n) pid_next = (base + 32 + lane < n) ? trow[base + 32 + lane] : -1;
+      for (int k = 0; k < cnt; k += a.pg) {
+        const int t = k + lane;
+        const int p = __shfl_sync(kFullMask, pid_cur, t < 32 ? t : 31);
+        bool fail = false;
+        if (lane < a.pg && t < cnt) {
+          const long long me = e + lane;
+          const int slot = int(me % a.nstage);
+          const uint32_t u = uint32_t(me / a.nstage);
+          if (*abort_flag || (u > 0 && !mbar_wait(&empty_bar[slot], (u - 1) & 1u, abort_flag))) {
+            fail = true;
+          } else {
+            issue(slot, p, kvh, wk.b + base + t, L);
+            issued[slot] = u + 1;
+          }
+        }
+        if (__any_sync(kFullMask, fail)) {
+          aborted = true;
+          if (lane == 0) {
+            *abort_flag = 1;
+            raise_error(a.err, PA_DEVERR_TIMEOUT);
+          }
+          break;
+        }
+        e += min(a.pg, cnt - k);
+      }
+    }
+    wk.advance(a, n, PC);
+  }
+  // Do not leave while a copy into this CTA's shared memory is in flight:
+  // only the last use issued into a slot can be (earlier ones were released,
+  // which needs them landed).
+  __syncwarp();
+  if (lane == 0) {
+    for (int slot = 0; slot < a.nstage; ++slot) {
+      if (issued[slot] == 0) continue;
+      int never = 0;
+      mbar_wait(&full_bar[slot], (issued[slot] - 1) & 1u, &never);
+    }
+  }
+}
 
 // Merge the consumer warps' states of one segment, held in shared memory as
 // mrg[warp][head][0..D-1 acc, D: m, D+1: l] (head stride D + 2), and write the
