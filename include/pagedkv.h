@@ -177,6 +177,34 @@ PA_API pa_status pa_decode_reduce(void *out, const int32_t *context_lens,
 /* Number of CTAs the split-context kernel launches on the current device. */
 PA_API int pa_decode_grid_size(void);
 
+/*
+ * pa_decode for callers that cannot allocate device memory.  The paper has no
+ * counterpart to this call; it exists for the library's users.
+ *
+ * Same arguments and result as pa_decode, without the workspace: the scratch
+ * lives in a static 4 MiB device array inside this library (every GPU that
+ * loads the library keeps it until the process exits).  Meant for callers
+ * that have no device allocator of their own, that must not call cudaMalloc
+ * on their path (it can synchronise the whole device), or that run where all
+ * device memory is already reserved by someone else.
+ *   - Returns PA_ERR_WORKSPACE, and enqueues nothing, when the shape needs more
+ *     scratch than 4 MiB (pa_decode_workspace_size(...) > 4 MiB; on a 152-SM
+ *     GPU with head_dim 128 that is more than about 200 000 sequences).
+ *   - Allocates nothing.  The first call on a device looks up the array's
+ *     device address (cudaGetSymbolAddress), which may load the library's
+ *     device code there; make that first call before any stream capture.
+ *   - All calls on a device share the one array: calls whose kernels may run
+ *     at the same time (unordered streams) race on it.  Nothing in it needs
+ *     clearing between calls.
+ */
+PA_API pa_status pa_decode_noalloc(void *out, const void *q, const void *k_cache,
+                                   const void *v_cache, const int32_t *block_tables,
+                                   int max_blocks_per_seq, const int32_t *context_lens,
+                                   int num_seqs, int num_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int64_t num_blocks,
+                                   float scale, pa_dtype dtype, int *debug_err,
+                                   void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -43,6 +43,7 @@ def _load() -> ctypes.CDLL:
         "pa_decode_partition": [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, sz, vp,
                                 vp],
         "pa_decode_reduce": [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, sz, vp, vp],
+        "pa_decode_noalloc": [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -223,6 +224,28 @@ def pa_decode_reduce(out, block_tables, context_lens, num_kv_heads, block_size, 
     _check(lib.pa_decode_reduce(out.data_ptr(), context_lens.data_ptr(), block_tables.shape[1], S, Hq,
                                 num_kv_heads, D, block_size, _DTYPES[out.dtype], workspace.data_ptr(),
                                 workspace.numel(), _ptr(err), _stream(out.device)), "pa_decode_reduce")
+
+
+def pa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                      context_lens: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
+                      err: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """pa_decode without a workspace, for callers that cannot allocate device
+    memory: the library keeps the scratch in a static 4 MiB device array.
+    ``out`` is still the caller's (allocated here only when not given)."""
+    NB, Hkv, B, D = _cache_shape(k_cache, v_cache)
+    dev = k_cache.device
+    _need(q, "q", k_cache.dtype, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    S, Hq, _ = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, 3, dev)
+    _check(lib.pa_decode_noalloc(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                 block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), S, Hq, Hkv,
+                                 D, B, NB, float(scale), _DTYPES[q.dtype], _ptr(err), _stream(dev)),
+           "pa_decode_noalloc")
+    return out
 
 
 def decode_step(inp, out=None, workspace=None, slots=None, err=None) -> torch.Tensor:
