@@ -114,7 +114,9 @@ PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *pai
 
 /*
  * Bytes of device workspace pa_decode needs for this shape on the current
- * device (depends on its SM count).  Returns 0 for invalid arguments.
+ * device (depends on its SM count): ~2.5 MB of partial results at head_dim
+ * 128 on 152 SMs plus 4 bytes per (sequence, query head).  Returns 0 for
+ * invalid arguments.
  */
 PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                 int head_dim);
@@ -131,10 +133,18 @@ PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_h
  * Arithmetic is fp32 on the stored inputs; out is rounded to nearest even.
  * A sequence with context_len 0 gets a zero row.
  *
- * Equivalent to pa_decode_partition followed by pa_decode_reduce on the same
- * stream.  workspace: device buffer of at least
- * pa_decode_workspace_size(...) bytes, 256-byte aligned; it holds only
- * intermediate values and may be reused after the calls complete.
+ * One kernel launch.  The step's (sequence, kv head, block) tiles are split
+ * evenly over one wave of CTAs (split-context); a (sequence, kv head) whose
+ * tiles fall in one CTA is finished there, and one cut by range boundaries is
+ * combined by the last of its CTAs to finish:
+ *     M = max_p m_p;  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.
+ *
+ * workspace: device buffer of at least pa_decode_workspace_size(...) bytes,
+ * 16-byte aligned, ZERO-FILLED before its first use.  It holds partial
+ * results and per-pair counters; every call leaves the counters at zero
+ * again, so a workspace can be reused by later calls of any shape (except
+ * after a call that reported PA_DEVERR_TIMEOUT: zero it again then).  Calls
+ * that run at the same time need separate workspaces.
  */
 PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache,
                     const void *v_cache, const int32_t *block_tables,
@@ -144,37 +154,7 @@ PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache,
                     pa_dtype dtype, void *workspace, size_t workspace_bytes,
                     int *debug_err, void *stream);
 
-/*
- * a4 alone -- the persistent split-context kernel.  The whole step's
- * (sequence, kv head, block) tiles are split evenly over one wave of CTAs;
- * a (sequence, kv head) whose tiles all fall in one CTA is finished there and
- * written to `out`; otherwise each CTA leaves a partial (max, sum, weighted
- * values) in the workspace for pa_decode_reduce.
- */
-PA_API pa_status pa_decode_partition(void *out, const void *q, const void *k_cache,
-                              const void *v_cache, const int32_t *block_tables,
-                              int max_blocks_per_seq,
-                              const int32_t *context_lens, int num_seqs,
-                              int num_heads, int num_kv_heads, int head_dim,
-                              int block_size, int64_t num_blocks, float scale,
-                              pa_dtype dtype, void *workspace,
-                              size_t workspace_bytes, int *debug_err,
-                              void *stream);
-
-/*
- * a5 alone -- combine the partials of split (sequence, kv head) pairs:
- *     M = max_p m_p;  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p
- * and write zero rows for empty sequences.  Must follow pa_decode_partition
- * with the same shape arguments and workspace on the same stream.
- */
-PA_API pa_status pa_decode_reduce(void *out, const int32_t *context_lens,
-                           int max_blocks_per_seq, int num_seqs, int num_heads,
-                           int num_kv_heads, int head_dim, int block_size,
-                           pa_dtype dtype, void *workspace,
-                           size_t workspace_bytes, int *debug_err,
-                           void *stream);
-
-/* Number of CTAs the split-context kernel launches on the current device. */
+/* Number of CTAs the decode kernel launches on the current device. */
 PA_API int pa_decode_grid_size(void);
 
 /*
@@ -189,13 +169,14 @@ PA_API int pa_decode_grid_size(void);
  * device memory is already reserved by someone else.
  *   - Returns PA_ERR_WORKSPACE, and enqueues nothing, when the shape needs more
  *     scratch than 4 MiB (pa_decode_workspace_size(...) > 4 MiB; on a 152-SM
- *     GPU with head_dim 128 that is more than about 200 000 sequences).
+ *     GPU with head_dim 128, when num_seqs * num_heads exceeds about 400 000).
  *   - Allocates nothing.  The first call on a device looks up the array's
  *     device address (cudaGetSymbolAddress), which may load the library's
  *     device code there; make that first call before any stream capture.
  *   - All calls on a device share the one array: calls whose kernels may run
- *     at the same time (unordered streams) race on it.  Nothing in it needs
- *     clearing between calls.
+ *     at the same time (unordered streams) race on it.  The array starts
+ *     zeroed and every call leaves its counters at zero, so it needs no
+ *     clearing between calls (see pa_decode about PA_DEVERR_TIMEOUT).
  */
 PA_API pa_status pa_decode_noalloc(void *out, const void *q, const void *k_cache,
                                    const void *v_cache, const int32_t *block_tables,

@@ -1,6 +1,5 @@
-// pa_decode.cu -- host entry points of paged decode attention, the choice
-// between the tensor-core and CUDA-core kernels, and the split-combine kernel
-// (a5).
+// pa_decode.cu -- host entry points of paged decode attention and the choice
+// between the tensor-core and CUDA-core kernels.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -17,7 +16,6 @@ pa_status launch_decode_mma(const DecodeArgs &a, const CUtensorMap &mk, const CU
                             cudaStream_t stream);
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxRecords = 512;  // partial records one reduce CTA can stage
 
 static int decode_grid() { return device_sm_count() * kCtasPerSm; }
 
@@ -27,8 +25,10 @@ static size_t partial_bytes(int nctas, int head_dim) {
   return round256(size_t(nctas) * 2 * 8 * (head_dim + 2) * sizeof(float));
 }
 
-static size_t workspace_bytes_for(int num_seqs, int head_dim, int nctas) {
-  return partial_bytes(nctas, head_dim) + round256(size_t(num_seqs + 1) * sizeof(long long));
+// partial records, then one counter per (sequence, query head) (an upper
+// bound of the split pairs)
+static size_t workspace_bytes_for(int num_seqs, int num_heads, int head_dim, int nctas) {
+  return partial_bytes(nctas, head_dim) + round256(size_t(num_seqs) * num_heads * sizeof(unsigned));
 }
 
 // ----------------------------------------------------------------- tensor maps
@@ -76,85 +76,6 @@ static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// ----------------------------------------------------------------- a5: combine
-// CTA whose tile range [c*W/N, (c+1)*W/N) holds tile x.
-__device__ __forceinline__ int cta_of(long long x, long long W, int N) {
-  return int(((x + 1) * N + W - 1) / W - 1);
-}
-
-__device__ __forceinline__ long long range_start(int c, long long W, int N) { return (long long)c * W / N; }
-
-// One CTA per (sequence, pair-chunk).  Thread 0 lists the partial records of
-// the pair (CTAs cf..cl, skipping empty ranges; the first one's record is its
-// last segment when its range starts before the pair); the weights
-// 2^(m_r - M) / sum_r 2^(m_r - M) l_r are computed once per (record, head).
-template <typename T>
-__global__ void __launch_bounds__(128) decode_reduce_kernel(void *out, const int32_t *__restrict__ lens,
-                                                            int max_blocks, int S, int Hq, int Hkv, int D, int B,
-                                                            int GT, const float *__restrict__ partials,
-                                                            const long long *__restrict__ cum, int nctas) {
-  __shared__ int rec_idx[kMaxRecords];
-  __shared__ float wgt[kMaxRecords][8];
-  __shared__ int nrec;
-  const int G = Hq / Hkv;
-  const int HC = G / GT;
-  const int PC = Hkv * HC;
-  const int cap = max_blocks * B;
-  const long long W = cum[S];
-  for (long long pair = blockIdx.x; pair < (long long)S * PC; pair += gridDim.x) {
-    const int s = int(pair / PC);
-    const int pc = int(pair - (long long)s * PC);
-    const int hq0 = (pc / HC) * G + (pc % HC) * GT;
-    int L = lens[s];
-    L = L < 0 ? 0 : (L > cap ? cap : L);
-    const int nb = (L + B - 1) / B;
-    T *o = static_cast<T *>(out) + ((long long)s * Hq + hq0) * D;
-    if (nb == 0) {  // nothing cached: zero row
-      for (int idx = threadIdx.x; idx < GT * D; idx += blockDim.x) o[idx] = Elem<T>::from_float(0.f);
-      continue;
-    }
-    const long long P0 = cum[s] + (long long)pc * nb;
-    const int cf = cta_of(P0, W, nctas);
-    const int cl = cta_of(P0 + nb - 1, W, nctas);
-    if (cf == cl) continue;  // finished inside one CTA by the partition kernel
-    if (threadIdx.x == 0) {
-      int n = 0;
-      for (int c = cf; c <= cl && n < kMaxRecords; ++c) {
-        const long long r0 = range_start(c, W, nctas);
-        if (r0 == range_start(c + 1, W, nctas)) continue;
-        const int slot = (c == cf && r0 < P0) ? 1 : 0;
-        rec_idx[n++] = c * 2 + slot;
-      }
-      nrec = n;
-    }
-    __syncthreads();
-    const int n = nrec;
-    if (threadIdx.x < GT) {
-      const int h = threadIdx.x;
-      float M = -CUDART_INF_F;
-      for (int r = 0; r < n; ++r) M = fmaxf(M, partials[((long long)rec_idx[r] * GT + h) * (D + 2) + D]);
-      float den = 0.f;
-      for (int r = 0; r < n; ++r) {
-        const float *rec = partials + ((long long)rec_idx[r] * GT + h) * (D + 2);
-        const float f = fast_exp2(rec[D] - M);
-        wgt[r][h] = f;
-        den += f * rec[D + 1];
-      }
-      const float inv = 1.f / den;
-      for (int r = 0; r < n; ++r) wgt[r][h] *= inv;
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < GT * D; idx += blockDim.x) {
-      const int h = idx / D;
-      const int d = idx - h * D;
-      float num = 0.f;
-      for (int r = 0; r < n; ++r) num += wgt[r][h] * partials[((long long)rec_idx[r] * GT + h) * (D + 2) + d];
-      o[idx] = Elem<T>::from_float(num);
-    }
-    __syncthreads();
-  }
-}
-
 // ----------------------------------------------------------------- dispatch
 struct DecodeShape {
   int G, GT, nctas;
@@ -194,7 +115,6 @@ static pa_status check_decode_args(int max_blocks_per_seq, int num_seqs, int num
   shape->GT = pick_head_chunk(shape->G, shape->mma);
   shape->nctas = decode_grid();
   if (shape->nctas <= 0) return PA_ERR_CUDA;
-  if (shape->nctas > kMaxRecords) return PA_ERR_UNSUPPORTED;
   // one ring slot holds the K tile and the V tile of one (block, kv head)
   const size_t tile_bytes = size_t(block_size) * head_dim * dtype_bytes(dtype);
   const size_t align = shape->mma ? 1024 : 128;  // the swizzled tiles repeat every 1024 bytes
@@ -266,15 +186,14 @@ extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_
   if (head_dim != 64 && head_dim != 128) return 0;
   const int n = decode_grid();
   if (n <= 0) return 0;
-  return workspace_bytes_for(num_seqs, head_dim, n);
+  return workspace_bytes_for(num_seqs, num_heads, head_dim, n);
 }
 
-extern "C" pa_status pa_decode_partition(void *out, const void *q, const void *k_cache, const void *v_cache,
-                                         const int32_t *block_tables, int max_blocks_per_seq,
-                                         const int32_t *context_lens, int num_seqs, int num_heads,
-                                         int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
-                                         float scale, pa_dtype dtype, void *workspace, size_t workspace_bytes,
-                                         int *debug_err, void *stream) {
+extern "C" pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                               int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                               int64_t num_blocks, float scale, pa_dtype dtype, void *workspace,
+                               size_t workspace_bytes, int *debug_err, void *stream) {
   DecodeShape sh;
   pa_status st = check_decode_args(max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                                    num_blocks, dtype, &sh);
@@ -285,7 +204,7 @@ extern "C" pa_status pa_decode_partition(void *out, const void *q, const void *k
     return PA_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace))
     return PA_ERR_INVALID_ARG;
-  if (workspace_bytes < workspace_bytes_for(num_seqs, head_dim, sh.nctas)) return PA_ERR_WORKSPACE;
+  if (workspace_bytes < workspace_bytes_for(num_seqs, num_heads, head_dim, sh.nctas)) return PA_ERR_WORKSPACE;
 
   DecodeArgs a;
   a.out = out;
@@ -302,7 +221,7 @@ extern "C" pa_status pa_decode_partition(void *out, const void *q, const void *k
   a.B = block_size;
   a.qscale = scale * kLog2e;
   a.partials = static_cast<float *>(workspace);
-  a.cum = reinterpret_cast<long long *>(static_cast<char *>(workspace) + partial_bytes(sh.nctas, head_dim));
+  a.counters = reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + partial_bytes(sh.nctas, head_dim));
   a.err = debug_err;
   a.nctas = sh.nctas;
   a.nstage = sh.nstage;
@@ -324,56 +243,4 @@ extern "C" pa_status pa_decode_partition(void *out, const void *q, const void *k
     case PA_BF16: return dispatch_simt<__nv_bfloat16>(a, head_dim, sh.GT, sh.ring_bytes, s);
   }
   return PA_ERR_INVALID_ARG;
-}
-
-extern "C" pa_status pa_decode_reduce(void *out, const int32_t *context_lens, int max_blocks_per_seq, int num_seqs,
-                                      int num_heads, int num_kv_heads, int head_dim, int block_size, pa_dtype dtype,
-                                      void *workspace, size_t workspace_bytes, int *debug_err, void *stream) {
-  (void)debug_err;
-  DecodeShape sh;
-  pa_status st = check_decode_args(max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
-                                   1, dtype, &sh);
-  if (st != PA_OK) return st;
-  if (num_seqs == 0) return PA_OK;
-  if (!out || !context_lens || !workspace || !aligned16(out) || !aligned16(workspace)) return PA_ERR_INVALID_ARG;
-  if (workspace_bytes < workspace_bytes_for(num_seqs, head_dim, sh.nctas)) return PA_ERR_WORKSPACE;
-  const float *partials = static_cast<const float *>(workspace);
-  const long long *cum =
-      reinterpret_cast<const long long *>(static_cast<const char *>(workspace) + partial_bytes(sh.nctas, head_dim));
-  const long long pairs = (long long)num_seqs * num_kv_heads * (sh.G / sh.GT);
-  long long grid = pairs;
-  const long long cap = (long long)device_sm_count() * 8;
-  if (grid > cap) grid = cap;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  switch (dtype) {
-    case PA_F32:
-      decode_reduce_kernel<float><<<unsigned(grid), 128, 0, s>>>(out, context_lens, max_blocks_per_seq, num_seqs,
-                                                                 num_heads, num_kv_heads, head_dim, block_size,
-                                                                 sh.GT, partials, cum, sh.nctas);
-      break;
-    case PA_F16:
-      decode_reduce_kernel<__half><<<unsigned(grid), 128, 0, s>>>(out, context_lens, max_blocks_per_seq, num_seqs,
-                                                                  num_heads, num_kv_heads, head_dim, block_size,
-                                                                  sh.GT, partials, cum, sh.nctas);
-      break;
-    case PA_BF16:
-      decode_reduce_kernel<__nv_bfloat16><<<unsigned(grid), 128, 0, s>>>(
-          out, context_lens, max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, head_dim, block_size, sh.GT,
-          partials, cum, sh.nctas);
-      break;
-  }
-  return launch_status();
-}
-
-extern "C" pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
-                               const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
-                               int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                               int64_t num_blocks, float scale, pa_dtype dtype, void *workspace,
-                               size_t workspace_bytes, int *debug_err, void *stream) {
-  pa_status st = pa_decode_partition(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                                     num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
-                                     dtype, workspace, workspace_bytes, debug_err, stream);
-  if (st != PA_OK) return st;
-  return pa_decode_reduce(out, context_lens, max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, head_dim,
-                          block_size, dtype, workspace, workspace_bytes, debug_err, stream);
 }

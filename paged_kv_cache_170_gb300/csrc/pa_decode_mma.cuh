@@ -46,10 +46,11 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(16) float mrg[kConsumerWarps][8][D + 2];
-  __shared__ long long sh_W, sh_r0;
+  __shared__ Plan sh_plan;
   __shared__ uint32_t issued[kMaxStages];
-  __shared__ int sh_s0;
   __shared__ int sh_abort;
+  __shared__ __align__(8) uint64_t st_full, st_free;  // consumers -> merger hand-off of mrg
+  __shared__ float sh_mw[kMergeRecords * 8];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -71,35 +72,36 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
       mbar_init(&empty_bar[i], 1);
       issued[i] = 0;
     }
+    mbar_init(&st_full, kConsumerWarps);
+    mbar_init(&st_free, 1);
     sh_abort = 0;
     fence_barrier_init();
   }
-  if (warp == kConsumerWarps) {
-    long long W, r0;
-    int s0;
-    schedule_scan(a, PC, lane, &W, &s0, &r0);
+  if (warp == kProducerWarp) {
+    Plan plan;
+    schedule_scan(a, PC, lane, &plan);
     if (lane == 0) {
-      sh_W = W;
-      sh_s0 = s0;
-      sh_r0 = r0;
+      sh_plan = plan;
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_k)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_v)) : "memory");
     }
   }
   __syncthreads();
 
-  const long long W = sh_W;
-  const long long w0 = (long long)blockIdx.x * W / a.nctas;
-  const long long w1 = (long long)(blockIdx.x + 1) * W / a.nctas;
-  if (w0 >= w1) return;
+  const Plan plan = sh_plan;
+  const long long W = plan.W, w0 = plan.w0, w1 = plan.w1;
+  if (w0 >= w1) {  // fewer tiles than CTAs: nothing to stream, only empty rows to zero
+    if (warp == kMergerWarp) zero_empty_rows<T>(a, D, lane, 32);
+    return;
+  }
   const uint32_t tile_bytes = uint32_t(B) * D * 2;
 
-  if (warp == kConsumerWarps) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
 #ifdef PA_TRACE
     const long long tr_t0 = clock64();
 #endif
-    produce(a, PC, HC, sh_s0, sh_r0, w0, w1, lane, full_bar, empty_bar, issued, abort_flag,
+    produce(a, PC, HC, plan, lane, full_bar, empty_bar, issued, abort_flag,
             [&](int slot, int p, int kvh, int bb, int L) {
               (void)bb;
               (void)L;
@@ -135,232 +137,254 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     return;
   }
 
+  if (warp == kMergerWarp) {
+    // -------------------------------------------------------------- merger
+    run_merger<T>(a, plan, PC, HC, G, D, lane, &mrg[0][0][0], 8 * (D + 2), &st_full, &st_free, sh_mw, abort_flag);
+    zero_empty_rows<T>(a, D, lane, 32);
+    return;
+  }
+
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2;      // fragment row group
   const int c4 = lane & 3;      // fragment column pair
   const int mj = lane >> 3;     // ldmatrix: which 8x8 matrix this lane addresses
   const int mr = lane & 7;      // ldmatrix: which row of it
 
-  Walk wk;
-  wk.start(a, sh_s0, sh_r0, w0);
-  long long j = 0;
+  long long j = 0;      // tiles, in this CTA's processing order
+  long long seg_k = 0;  // segments deposited to the merger
 #ifdef PA_TRACE
-  long long tr_c0 = clock64(), tr_wk = 0, tr_tiles = 0;
+  long long tr_c0 = clock64(), tr_wk = 0, tr_tiles = 0, tr_seg = 0, tr_nseg = 0;
 #endif
-  while (wk.w < w1) {
-    const int n = wk.seg_len(w1);
-    const bool complete = (wk.b == 0 && n == wk.nb);
-    const bool first_seg = (wk.w == w0);
-    const int kvh = wk.pc / HC;
-    const int hq0 = kvh * G + (wk.pc % HC) * GT;
-    const int L = clamped_len(a, wk.s);
+  // rotated processing order (see Plan); j counts tiles in that order
+  for (int ph = 0; ph < 2; ++ph) {
+    long long from, to;
+    if (!phase_range(plan, ph, &from, &to)) continue;
+    Walk wk;
+    if (ph == 0)
+      wk.start(a, plan.sA, plan.rA, from);
+    else
+      wk.start(a, plan.s0, plan.r0, from);
+    while (wk.w < to) {
+      const int n = wk.seg_len(to);
+      const bool complete = (wk.b == 0 && n == wk.nb);
+      const bool first_seg = (wk.w == w0);
+      const int kvh = wk.pc / HC;
+      const int hq0 = kvh * G + (wk.pc % HC) * GT;
+      const int L = clamped_len(a, wk.s);
 
-    // running state: heads h0 = 2*c4 and h1 = 2*c4 + 1 of this lane
-    float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
-    float o[KS][4];
+      // running state: heads h0 = 2*c4 and h1 = 2*c4 + 1 of this lane
+      float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+      float o[KS][4];
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
-    // this warp's first tile of the segment (warps >= ncw take none)
-    long long jj = warp < a.ncw ? j + ((warp - int(j % a.ncw)) + a.ncw) % a.ncw : j + n;
-    if (jj < j + n) {
-      // q^T fragment (B operand of QK): head g of the chunk, dims 16ks + 2*c4 (+1), (+8)
-      uint32_t qf[KS][2];
-      if (g < GT) {
-        long long qoff = ((long long)wk.s * a.Hq + hq0 + g) * D;
-        PA_DBG_FIX(qoff >= 0 && qoff + D <= (long long)a.S * a.Hq * D, kDbgGlobal, qoff = 0);
-        const T *qrow = static_cast<const T *>(a.q) + qoff;
+      // this warp's first tile of the segment (warps >= ncw take none)
+      long long jj = warp < a.ncw ? j + ((warp - int(j % a.ncw)) + a.ncw) % a.ncw : j + n;
+      if (jj < j + n) {
+        // q^T fragment (B operand of QK): head g of the chunk, dims 16ks + 2*c4 (+1), (+8)
+        uint32_t qf[KS][2];
+        if (g < GT) {
+          long long qoff = ((long long)wk.s * a.Hq + hq0 + g) * D;
+          PA_DBG_FIX(qoff >= 0 && qoff + D <= (long long)a.S * a.Hq * D, kDbgGlobal, qoff = 0);
+          const T *qrow = static_cast<const T *>(a.q) + qoff;
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          qf[ks][0] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c4);
-          qf[ks][1] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * c4);
+          for (int ks = 0; ks < KS; ++ks) {
+            qf[ks][0] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c4);
+            qf[ks][1] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * c4);
+          }
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) qf[ks][0] = qf[ks][1] = 0u;
         }
-      } else {
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) qf[ks][0] = qf[ks][1] = 0u;
-      }
 
-      for (; jj < j + n; jj += a.ncw) {
-        const int bb = wk.b + int(jj - j);
-        const int nv = min(B, L - bb * B);
-        const int nsub = (nv + 15) >> 4;
-        const long long ee = jj;  // the pair's ring entry
-        const int slot = int(ee % a.nstage);
-        const uint32_t kt = ring_addr + uint32_t(slot) * a.slot_stride;
-        const uint32_t vt = kt + a.tile_stride;
+        for (; jj < j + n; jj += a.ncw) {
+          const int bb = wk.b + int(jj - j);
+          const int nv = min(B, L - bb * B);
+          const int nsub = (nv + 15) >> 4;
+          const long long ee = jj;  // the pair's ring entry
+          const int slot = int(ee % a.nstage);
+          const uint32_t kt = ring_addr + uint32_t(slot) * a.slot_stride;
+          const uint32_t vt = kt + a.tile_stride;
 
-        // ---- wait for the pair (K and V land together)
+          // ---- wait for the pair (K and V land together)
 #ifdef PA_TRACE
-        long long tr_a = clock64();
+          long long tr_a = clock64();
 #endif
-        const bool okE = wait_entry(full_bar, empty_bar, ee, a.nstage, abort_flag);
+          const bool okE = wait_entry(full_bar, empty_bar, ee, a.nstage, abort_flag);
 #ifdef PA_TRACE
-        tr_wk += clock64() - tr_a;
-        ++tr_tiles;
+          tr_wk += clock64() - tr_a;
+          ++tr_tiles;
 #endif
 #ifdef PA_DEBUG
-        if (okE && lane == 0 && mbar_try_wait(&full_bar[slot], (uint32_t(ee / a.nstage) & 1u) ^ 1u)) {
-          raise_error(a.err, kDbgPhase);  // the barrier ran two phases ahead of this entry
-          printf("pagedkv phase ahead: cta %d warp %d entry %lld slot %d\n", blockIdx.x, warp, ee, slot);
-        }
+          if (okE && lane == 0 && mbar_try_wait(&full_bar[slot], (uint32_t(ee / a.nstage) & 1u) ^ 1u)) {
+            raise_error(a.err, kDbgPhase);  // the barrier ran two phases ahead of this entry
+            printf("pagedkv phase ahead: cta %d warp %d entry %lld slot %d\n", blockIdx.x, warp, ee, slot);
+          }
 #endif
-        if (!okE) {
-          if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+          if (!okE) {
+            if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
 #ifdef PA_DEBUG
-          if (lane == 0)
-            printf("pagedkv consumer: cta %d warp %d entry %lld slot %d seg s %d pc %d b %d n %d abort %d\n",
-                   blockIdx.x, warp, ee, slot, wk.s, wk.pc, wk.b, n, *abort_flag);
+            if (lane == 0)
+              printf("pagedkv consumer: cta %d warp %d entry %lld slot %d seg s %d pc %d b %d n %d abort %d\n",
+                     blockIdx.x, warp, ee, slot, wk.s, wk.pc, wk.b, n, *abort_flag);
 #endif
-          *abort_flag = 1;
-        }
-        // Lanes leave the wait loop at different iterations: reconverge before
-        // the warp-collective ldmatrix / mma.sync.aligned below.
-        __syncwarp();
-
-        // ---- QK: scores of up to 4 sub-tiles of 16 tokens
-        float sc[4][4];
-#pragma unroll
-        for (int st = 0; st < 4; ++st) {
-          sc[st][0] = sc[st][1] = sc[st][2] = sc[st][3] = -CUDART_INF_F;
-          if (st < nsub) {
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-            const int row = st * 16 + (mj & 1) * 8 + mr;
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-              uint32_t af[4];
-              uint32_t ad = swz(kt, B, ks >> 2, row, (ks & 3) * 2 + (mj >> 1));
-              PA_DBG_FIX(ad >= ring_addr && ad + 16 <= ring_addr + a.nstage * a.slot_stride && (ad & 15u) == 0,
-                         kDbgSmem, ad = ring_addr);
-              ldmatrix_x4(af, ad);
-              Mma<T>::run(c, af, qf[ks][0], qf[ks][1]);
-            }
-            const int t0 = st * 16 + g;
-            sc[st][0] = t0 < nv ? c[0] * a.qscale : -CUDART_INF_F;
-            sc[st][1] = t0 < nv ? c[1] * a.qscale : -CUDART_INF_F;
-            sc[st][2] = t0 + 8 < nv ? c[2] * a.qscale : -CUDART_INF_F;
-            sc[st][3] = t0 + 8 < nv ? c[3] * a.qscale : -CUDART_INF_F;
+            *abort_flag = 1;
           }
-        }
-        // ---- online softmax (base 2), heads h0 / h1 of this lane
-        float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
-#pragma unroll
-        for (int st = 0; st < 4; ++st) {
-          mx0 = fmaxf(mx0, fmaxf(sc[st][0], sc[st][2]));
-          mx1 = fmaxf(mx1, fmaxf(sc[st][1], sc[st][3]));
-        }
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
-        }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
-        l0 *= al0;
-        l1 *= al1;
-#pragma unroll
-        for (int st = 0; st < 4; ++st) {
-          sc[st][0] = fast_exp2(sc[st][0] - mn0);
-          sc[st][1] = fast_exp2(sc[st][1] - mn1);
-          sc[st][2] = fast_exp2(sc[st][2] - mn0);
-          sc[st][3] = fast_exp2(sc[st][3] - mn1);
-          l0 += sc[st][0] + sc[st][2];
-          l1 += sc[st][1] + sc[st][3];
-        }
-        if (__any_sync(kFullMask, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-          for (int mt = 0; mt < KS; ++mt) {
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
-          }
-        }
-
-        // ---- PV
-        if (nv < nsub * 16) {
-          // rows past the context in the last sub-tile: make them zero so a
-          // zero weight times stale data cannot produce NaN
-          const int rows = nsub * 16 - nv;
-          for (int i = lane; i < rows * HALVES * 8; i += 32) {
-            const int r = nv + i / (HALVES * 8);
-            const int hc = i % (HALVES * 8);
-            size_t zo = (size_t)slot * a.slot_stride + a.tile_stride + (hc >> 3) * B * 128 + r * 128 + (hc & 7) * 16;
-            PA_DBG_FIX(zo + 16 <= (size_t)a.nstage * a.slot_stride, kDbgSmem, continue);
-            *reinterpret_cast<uint4 *>(ring + zo) = make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async_shared();
+          // Lanes leave the wait loop at different iterations: reconverge before
+          // the warp-collective ldmatrix / mma.sync.aligned below.
           __syncwarp();
-        }
+
+          // ---- QK: scores of up to 4 sub-tiles of 16 tokens
+          float sc[4][4];
 #pragma unroll
-        for (int st = 0; st < 4; ++st) {
-          if (st < nsub) {
-            const uint32_t hi0 = Mma<T>::pack(sc[st][0], sc[st][1]);  // token g
-            const uint32_t hi1 = Mma<T>::pack(sc[st][2], sc[st][3]);  // token g + 8
-            const float2 f0 = Mma<T>::unpack(hi0), f1 = Mma<T>::unpack(hi1);
-            const uint32_t lo0 = Mma<T>::pack(sc[st][0] - f0.x, sc[st][1] - f0.y);
-            const uint32_t lo1 = Mma<T>::pack(sc[st][2] - f1.x, sc[st][3] - f1.y);
-            const uint32_t bh0 = movmatrix_trans(hi0), bh1 = movmatrix_trans(hi1);
-            const uint32_t bl0 = movmatrix_trans(lo0), bl1 = movmatrix_trans(lo1);
-            const int row = st * 16 + (mj >> 1) * 8 + mr;
+          for (int st = 0; st < 4; ++st) {
+            sc[st][0] = sc[st][1] = sc[st][2] = sc[st][3] = -CUDART_INF_F;
+            if (st < nsub) {
+              float c[4] = {0.f, 0.f, 0.f, 0.f};
+              const int row = st * 16 + (mj & 1) * 8 + mr;
+#pragma unroll
+              for (int ks = 0; ks < KS; ++ks) {
+                uint32_t af[4];
+                uint32_t ad = swz(kt, B, ks >> 2, row, (ks & 3) * 2 + (mj >> 1));
+                PA_DBG_FIX(ad >= ring_addr && ad + 16 <= ring_addr + a.nstage * a.slot_stride && (ad & 15u) == 0,
+                           kDbgSmem, ad = ring_addr);
+                ldmatrix_x4(af, ad);
+                Mma<T>::run(c, af, qf[ks][0], qf[ks][1]);
+              }
+              const int t0 = st * 16 + g;
+              sc[st][0] = t0 < nv ? c[0] * a.qscale : -CUDART_INF_F;
+              sc[st][1] = t0 < nv ? c[1] * a.qscale : -CUDART_INF_F;
+              sc[st][2] = t0 + 8 < nv ? c[2] * a.qscale : -CUDART_INF_F;
+              sc[st][3] = t0 + 8 < nv ? c[3] * a.qscale : -CUDART_INF_F;
+            }
+          }
+          // ---- online softmax (base 2), heads h0 / h1 of this lane
+          float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+          for (int st = 0; st < 4; ++st) {
+            mx0 = fmaxf(mx0, fmaxf(sc[st][0], sc[st][2]));
+            mx1 = fmaxf(mx1, fmaxf(sc[st][1], sc[st][3]));
+          }
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
+          }
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+          m0 = mn0;
+          m1 = mn1;
+          l0 *= al0;
+          l1 *= al1;
+#pragma unroll
+          for (int st = 0; st < 4; ++st) {
+            sc[st][0] = fast_exp2(sc[st][0] - mn0);
+            sc[st][1] = fast_exp2(sc[st][1] - mn1);
+            sc[st][2] = fast_exp2(sc[st][2] - mn0);
+            sc[st][3] = fast_exp2(sc[st][3] - mn1);
+            l0 += sc[st][0] + sc[st][2];
+            l1 += sc[st][1] + sc[st][3];
+          }
+          if (__any_sync(kFullMask, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
-              const int chunk = 2 * mt + (mj & 1);
-              uint32_t af[4];
-              uint32_t ad = swz(vt, B, chunk >> 3, row, chunk & 7);
-              PA_DBG_FIX(ad >= ring_addr && ad + 16 <= ring_addr + a.nstage * a.slot_stride && (ad & 15u) == 0,
-                         kDbgSmem, ad = ring_addr);
-              ldmatrix_x4_trans(af, ad);
-              Mma<T>::run(o[mt], af, bh0, bh1);
-              Mma<T>::run(o[mt], af, bl0, bl1);
+              o[mt][0] *= al0;
+              o[mt][1] *= al1;
+              o[mt][2] *= al0;
+              o[mt][3] *= al1;
             }
           }
-        }
-        __syncwarp();
-        if (lane == 0 && okE) mbar_arrive(&empty_bar[slot]);  // the pair's slot is free again
-      }
-    }
 
-    // ---- merge the four warps' states for this (s, pc)
+          // ---- PV
+          if (nv < nsub * 16) {
+            // rows past the context in the last sub-tile: make them zero so a
+            // zero weight times stale data cannot produce NaN
+            const int rows = nsub * 16 - nv;
+            for (int i = lane; i < rows * HALVES * 8; i += 32) {
+              const int r = nv + i / (HALVES * 8);
+              const int hc = i % (HALVES * 8);
+              size_t zo = (size_t)slot * a.slot_stride + a.tile_stride + (hc >> 3) * B * 128 + r * 128 + (hc & 7) * 16;
+              PA_DBG_FIX(zo + 16 <= (size_t)a.nstage * a.slot_stride, kDbgSmem, continue);
+              *reinterpret_cast<uint4 *>(ring + zo) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+          }
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l0 += __shfl_xor_sync(kFullMask, l0, off);
-      l1 += __shfl_xor_sync(kFullMask, l1, off);
-    }
-    const int h0 = 2 * c4, h1 = 2 * c4 + 1;
-    if (g == 0) {
-      if (h0 < GT) {
-        mrg[warp][h0][D] = m0;
-        mrg[warp][h0][D + 1] = l0;
-      }
-      if (h1 < GT) {
-        mrg[warp][h1][D] = m1;
-        mrg[warp][h1][D + 1] = l1;
-      }
-    }
+          for (int st = 0; st < 4; ++st) {
+            if (st < nsub) {
+              const uint32_t hi0 = Mma<T>::pack(sc[st][0], sc[st][1]);  // token g
+              const uint32_t hi1 = Mma<T>::pack(sc[st][2], sc[st][3]);  // token g + 8
+              const float2 f0 = Mma<T>::unpack(hi0), f1 = Mma<T>::unpack(hi1);
+              const uint32_t lo0 = Mma<T>::pack(sc[st][0] - f0.x, sc[st][1] - f0.y);
+              const uint32_t lo1 = Mma<T>::pack(sc[st][2] - f1.x, sc[st][3] - f1.y);
+              const uint32_t bh0 = movmatrix_trans(hi0), bh1 = movmatrix_trans(hi1);
+              const uint32_t bl0 = movmatrix_trans(lo0), bl1 = movmatrix_trans(lo1);
+              const int row = st * 16 + (mj >> 1) * 8 + mr;
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-      if (h0 < GT) {
-        mrg[warp][h0][16 * mt + g] = o[mt][0];
-        mrg[warp][h0][16 * mt + g + 8] = o[mt][2];
+              for (int mt = 0; mt < KS; ++mt) {
+                const int chunk = 2 * mt + (mj & 1);
+                uint32_t af[4];
+                uint32_t ad = swz(vt, B, chunk >> 3, row, chunk & 7);
+                PA_DBG_FIX(ad >= ring_addr && ad + 16 <= ring_addr + a.nstage * a.slot_stride && (ad & 15u) == 0,
+                           kDbgSmem, ad = ring_addr);
+                ldmatrix_x4_trans(af, ad);
+                Mma<T>::run(o[mt], af, bh0, bh1);
+                Mma<T>::run(o[mt], af, bl0, bl1);
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0 && okE) mbar_arrive(&empty_bar[slot]);  // the pair's slot is free again
+        }
       }
-      if (h1 < GT) {
-        mrg[warp][h1][16 * mt + g] = o[mt][1];
-        mrg[warp][h1][16 * mt + g + 8] = o[mt][3];
+
+#ifdef PA_TRACE
+      const long long tr_s0 = clock64();
+#endif
+      // ---- hand this warp's state for the segment to the merger warp
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(kFullMask, l0, off);
+        l1 += __shfl_xor_sync(kFullMask, l1, off);
       }
+      const int h0 = 2 * c4, h1 = 2 * c4 + 1;
+      deposit_state(a, seg_k, lane, &st_full, &st_free, abort_flag, [&]() {
+        if (g == 0) {
+          if (h0 < GT) {
+            mrg[warp][h0][D] = m0;
+            mrg[warp][h0][D + 1] = l0;
+          }
+          if (h1 < GT) {
+            mrg[warp][h1][D] = m1;
+            mrg[warp][h1][D + 1] = l1;
+          }
+        }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          if (h0 < GT) {
+            mrg[warp][h0][16 * mt + g] = o[mt][0];
+            mrg[warp][h0][16 * mt + g + 8] = o[mt][2];
+          }
+          if (h1 < GT) {
+            mrg[warp][h1][16 * mt + g] = o[mt][1];
+            mrg[warp][h1][16 * mt + g + 8] = o[mt][3];
+          }
+        }
+      });
+      ++seg_k;
+#ifdef PA_TRACE
+      tr_seg += clock64() - tr_s0;
+      ++tr_nseg;
+#endif
+      j += n;
+      wk.advance(a, n, PC);
     }
-    named_barrier_sync(1, kConsumerWarps * 32);
-    combine_segment<T>(a, &mrg[0][0][0], 8 * (D + 2), D, GT, complete, first_seg, wk.s, hq0, threadIdx.x,
-                       kConsumerWarps * 32);
-    named_barrier_sync(1, kConsumerWarps * 32);
-    j += n;
-    wk.advance(a, n, PC);
   }
 #ifdef PA_TRACE
   if (lane == 0 && (blockIdx.x % 101) == 0)
-    printf("trace cta %d warp %d: tiles %lld cycles %lld waiting %lld\n", blockIdx.x, warp, tr_tiles,
-           clock64() - tr_c0, tr_wk);
+    printf("trace cta %d warp %d: tiles %lld cycles %lld waiting %lld segment-ends %lld (%lld cycles)\n",
+           blockIdx.x, warp, tr_tiles, clock64() - tr_c0, tr_wk, tr_nseg, tr_seg);
 #endif
 }
 

@@ -14,9 +14,9 @@
 // library holds its kStaticScratchBytes until the process exits.  Every call
 // on a device uses the same array, so two calls whose kernels overlap on the
 // GPU (different streams, no ordering between them) corrupt each other's
-// scratch; calls on one stream, or otherwise ordered, are safe.  Nothing in
-// the scratch has to start at zero: each call writes every value it reads
-// before reading it, so what a previous call left there does not matter.
+// scratch; calls on one stream, or otherwise ordered, are safe.  The array
+// starts zeroed (static device storage), which is what pa_decode's workspace
+// contract asks for, and each call leaves its counters at zero again.
 #include <mutex>
 
 #include "pa_common.cuh"

@@ -95,10 +95,11 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(16) float sc_buf[kConsumerWarps][kMaxBlockSize * GT];
   __shared__ __align__(16) float mrg[kConsumerWarps][GT][D + 2];
-  __shared__ long long sh_W, sh_r0;
+  __shared__ Plan sh_plan;
   __shared__ uint32_t issued[kMaxStages];
-  __shared__ int sh_s0;
   __shared__ int sh_abort;
+  __shared__ __align__(8) uint64_t st_full, st_free;  // consumers -> merger hand-off of mrg
+  __shared__ float sh_mw[kMergeRecords * 8];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -114,30 +115,31 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
       mbar_init(&empty_bar[i], 1);
       issued[i] = 0;
     }
+    mbar_init(&st_full, kConsumerWarps);
+    mbar_init(&st_free, 1);
     sh_abort = 0;
     fence_barrier_init();
   }
-  if (warp == kConsumerWarps) {
-    long long W, r0;
-    int s0;
-    schedule_scan(a, PC, lane, &W, &s0, &r0);
+  if (warp == kProducerWarp) {
+    Plan plan;
+    schedule_scan(a, PC, lane, &plan);
     if (lane == 0) {
-      sh_W = W;
-      sh_s0 = s0;
-      sh_r0 = r0;
+      sh_plan = plan;
     }
   }
   __syncthreads();
 
-  const long long W = sh_W;
-  const long long w0 = (long long)blockIdx.x * W / a.nctas;
-  const long long w1 = (long long)(blockIdx.x + 1) * W / a.nctas;
-  if (w0 >= w1) return;  // empty range (fewer tiles than CTAs)
+  const Plan plan = sh_plan;
+  const long long W = plan.W, w0 = plan.w0, w1 = plan.w1;
+  if (w0 >= w1) {  // fewer tiles than CTAs: nothing to stream, only empty rows to zero
+    if (warp == kMergerWarp) zero_empty_rows<T>(a, D, lane, 32);
+    return;
+  }
   const size_t tile_elems = size_t(B) * D;
 
-  if (warp == kConsumerWarps) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    produce(a, PC, HC, sh_s0, sh_r0, w0, w1, lane, full_bar, empty_bar, issued, abort_flag,
+    produce(a, PC, HC, plan, lane, full_bar, empty_bar, issued, abort_flag,
             [&](int slot, int p, int kvh, int bb, int L) {
               if (p < 0 || p >= a.num_blocks) {
                 raise_error(a.err, PA_DEVERR_BLOCK_ID);
@@ -155,179 +157,180 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
     return;
   }
 
+  if (warp == kMergerWarp) {
+    // -------------------------------------------------------------- merger
+    run_merger<T>(a, plan, PC, HC, G, D, lane, &mrg[0][0][0], GT * (D + 2), &st_full, &st_free, sh_mw, abort_flag);
+    zero_empty_rows<T>(a, D, lane, 32);
+    return;
+  }
+
   // -------------------------------------------------------------- consumers
   float *sc = sc_buf[warp];
   const int jl = lane % C::LPT;   // lane within its token group (QK)
   const int tsub = lane / C::LPT; // token slot of the lane (QK)
   // Softmax state (m_mine, l_mine) of a lane belongs to head lane % GT.
 
-  int s = sh_s0;
-  int nb = blocks_of(a, s);
-  int pc = int(sh_r0 / nb);
-  int b = int(sh_r0 % nb);
-  long long w = w0;
-  long long j = 0;  // tile index within this CTA's range
-  while (w < w1) {
-    const int n = int(min((long long)(nb - b), w1 - w));
-    const bool complete = (b == 0 && n == nb);
-    const bool first_seg = (w == w0);
-    const int kvh = pc / HC;
-    const int hq0 = kvh * G + (pc % HC) * GT;
-    const int L = clamped_len(a, s);
+  long long j = 0;      // tiles, in this CTA's processing order
+  long long seg_k = 0;  // segments deposited to the merger
+  // rotated processing order (see Plan)
+  for (int ph = 0; ph < 2; ++ph) {
+    long long from, to;
+    if (!phase_range(plan, ph, &from, &to)) continue;
+    Walk wk;
+    if (ph == 0)
+      wk.start(a, plan.sA, plan.rA, from);
+    else
+      wk.start(a, plan.s0, plan.r0, from);
+    while (wk.w < to) {
+      const int n = wk.seg_len(to);
+      const int s = wk.s, nb = wk.nb, pc = wk.pc, b = wk.b;
+      const long long w = wk.w;
+      const bool complete = (b == 0 && n == nb);
+      const bool first_seg = (w == w0);
+      const int kvh = pc / HC;
+      const int hq0 = kvh * G + (pc % HC) * GT;
+      const int L = clamped_len(a, s);
 
-    float m_mine = -CUDART_INF_F;
-    float l_mine = 0.f;
-    float2 acc[GT][C::DPV / 2];
-#pragma unroll
-    for (int h = 0; h < GT; ++h)
-#pragma unroll
-      for (int i = 0; i < C::DPV / 2; ++i) acc[h][i] = make_float2(0.f, 0.f);
-
-    // this warp's first tile of the segment (warps >= ncw take none)
-    long long jj = warp < a.ncw ? j + ((warp - int(j % a.ncw)) + a.ncw) % a.ncw : j + n;
-    if (jj < j + n) {
-      // q slice of this lane, pre-scaled so scores come out in log2 units
-      float2 qreg[GT][C::DPL / 2];
-      const T *qs = static_cast<const T *>(a.q) + ((long long)s * a.Hq + hq0) * D;
+      float m_mine = -CUDART_INF_F;
+      float l_mine = 0.f;
+      float2 acc[GT][C::DPV / 2];
 #pragma unroll
       for (int h = 0; h < GT; ++h)
 #pragma unroll
-        for (int c = 0; c < C::CPL; ++c) {
-          const uint4 raw = *reinterpret_cast<const uint4 *>(qs + h * D + (c * C::LPT + jl) * C::EPC);
-          float2 f[C::EPC / 2];
-          Elem<T>::chunk_to_f2(raw, f);
-#pragma unroll
-          for (int i = 0; i < C::EPC / 2; ++i)
-            qreg[h][c * (C::EPC / 2) + i] = make_float2(f[i].x * a.qscale, f[i].y * a.qscale);
-        }
+        for (int i = 0; i < C::DPV / 2; ++i) acc[h][i] = make_float2(0.f, 0.f);
 
-      for (; jj < j + n; jj += a.ncw) {
-        const int bb = b + int(jj - j);
-        const int nv = min(B, L - bb * B);
-        const long long ee = jj;  // the pair's ring entry
-        const int slot = int(ee % a.nstage);
-        const char *kt = reinterpret_cast<const char *>(ring) + size_t(slot) * a.slot_stride;
-        const char *vt = kt + a.tile_stride;
-
-        // ---- wait for the pair (K and V land together), then QK
-        const bool okE = wait_entry(full_bar, empty_bar, ee, a.nstage, abort_flag);
-        if (!okE) {
-          if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
-          *abort_flag = 1;
-        }
-        __syncwarp();
-        for (int t0 = 0; t0 < nv; t0 += C::TS) {
-          const int t = t0 + tsub;
-          const int tr = t < nv ? t : nv - 1;
-          float2 a2[GT];
+      // this warp's first tile of the segment (warps >= ncw take none)
+      long long jj = warp < a.ncw ? j + ((warp - int(j % a.ncw)) + a.ncw) % a.ncw : j + n;
+      if (jj < j + n) {
+        // q slice of this lane, pre-scaled so scores come out in log2 units
+        float2 qreg[GT][C::DPL / 2];
+        const T *qs = static_cast<const T *>(a.q) + ((long long)s * a.Hq + hq0) * D;
 #pragma unroll
-          for (int h = 0; h < GT; ++h) a2[h] = make_float2(0.f, 0.f);
+        for (int h = 0; h < GT; ++h)
 #pragma unroll
           for (int c = 0; c < C::CPL; ++c) {
-            const uint4 raw =
-                *reinterpret_cast<const uint4 *>(kt + (size_t(tr) * D + (c * C::LPT + jl) * C::EPC) * sizeof(T));
-            float2 kf[C::EPC / 2];
-            Elem<T>::chunk_to_f2(raw, kf);
+            const uint4 raw = *reinterpret_cast<const uint4 *>(qs + h * D + (c * C::LPT + jl) * C::EPC);
+            float2 f[C::EPC / 2];
+            Elem<T>::chunk_to_f2(raw, f);
 #pragma unroll
-            for (int h = 0; h < GT; ++h)
-#pragma unroll
-              for (int i = 0; i < C::EPC / 2; ++i) ffma2(a2[h], qreg[h][c * (C::EPC / 2) + i], kf[i]);
+            for (int i = 0; i < C::EPC / 2; ++i)
+              qreg[h][c * (C::EPC / 2) + i] = make_float2(f[i].x * a.qscale, f[i].y * a.qscale);
           }
-          float part[GT];
-#pragma unroll
-          for (int h = 0; h < GT; ++h) part[h] = a2[h].x + a2[h].y;
-#pragma unroll
-          for (int off = C::LPT / 2; off >= 1; off >>= 1)
-#pragma unroll
-            for (int h = 0; h < GT; ++h) part[h] += __shfl_xor_sync(kFullMask, part[h], off);
-          if (t < nv && jl < GT) {
-            float v = part[0];
-#pragma unroll
-            for (int h = 1; h < GT; ++h)
-              if (jl == h) v = part[h];
-            sc[t * GT + jl] = v;
+
+        for (; jj < j + n; jj += a.ncw) {
+          const int bb = b + int(jj - j);
+          const int nv = min(B, L - bb * B);
+          const long long ee = jj;  // the pair's ring entry
+          const int slot = int(ee % a.nstage);
+          const char *kt = reinterpret_cast<const char *>(ring) + size_t(slot) * a.slot_stride;
+          const char *vt = kt + a.tile_stride;
+
+          // ---- wait for the pair (K and V land together), then QK
+          const bool okE = wait_entry(full_bar, empty_bar, ee, a.nstage, abort_flag);
+          if (!okE) {
+            if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+            *abort_flag = 1;
           }
-        }
-        __syncwarp();
+          __syncwarp();
+          for (int t0 = 0; t0 < nv; t0 += C::TS) {
+            const int t = t0 + tsub;
+            const int tr = t < nv ? t : nv - 1;
+            float2 a2[GT];
+#pragma unroll
+            for (int h = 0; h < GT; ++h) a2[h] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < C::CPL; ++c) {
+              const uint4 raw =
+                  *reinterpret_cast<const uint4 *>(kt + (size_t(tr) * D + (c * C::LPT + jl) * C::EPC) * sizeof(T));
+              float2 kf[C::EPC / 2];
+              Elem<T>::chunk_to_f2(raw, kf);
+#pragma unroll
+              for (int h = 0; h < GT; ++h)
+#pragma unroll
+                for (int i = 0; i < C::EPC / 2; ++i) ffma2(a2[h], qreg[h][c * (C::EPC / 2) + i], kf[i]);
+            }
+            float part[GT];
+#pragma unroll
+            for (int h = 0; h < GT; ++h) part[h] = a2[h].x + a2[h].y;
+#pragma unroll
+            for (int off = C::LPT / 2; off >= 1; off >>= 1)
+#pragma unroll
+              for (int h = 0; h < GT; ++h) part[h] += __shfl_xor_sync(kFullMask, part[h], off);
+            if (t < nv && jl < GT) {
+              float v = part[0];
+#pragma unroll
+              for (int h = 1; h < GT; ++h)
+                if (jl == h) v = part[h];
+              sc[t * GT + jl] = v;
+            }
+          }
+          __syncwarp();
 
-        // ---- online softmax over this tile (base 2)
-        float mx = -CUDART_INF_F;
-        for (int i = lane; i < nv * GT; i += 32) mx = fmaxf(mx, sc[i]);
+          // ---- online softmax over this tile (base 2)
+          float mx = -CUDART_INF_F;
+          for (int i = lane; i < nv * GT; i += 32) mx = fmaxf(mx, sc[i]);
 #pragma unroll
-        for (int off = GT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, off));
-        const float m_new = fmaxf(m_mine, mx);
-        const float alpha = fast_exp2(m_mine - m_new);
-        float lsum = l_mine * alpha;
-        for (int i = lane; i < nv * GT; i += 32) {
-          const float p = fast_exp2(sc[i] - m_new);
-          sc[i] = p;
-          lsum += p;
-        }
-        l_mine = lsum;
-        m_mine = m_new;
-#pragma unroll
-        for (int h = 0; h < GT; ++h) {
-          const float ah = __shfl_sync(kFullMask, alpha, h);
-          const float2 a2 = make_float2(ah, ah);
-#pragma unroll
-          for (int i = 0; i < C::DPV / 2; ++i) fmul2(acc[h][i], a2);
-        }
-        __syncwarp();
-
-        // ---- PV
-#pragma unroll 4
-        for (int t = 0; t < nv; ++t) {
-          float p[GT];
-          load_p<GT>(sc, t, p);
-          float2 vf[C::DPV / 2];
-          load_v<T, C::DPV>(vt + size_t(t) * D * sizeof(T), lane, vf);
+          for (int off = GT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, off));
+          const float m_new = fmaxf(m_mine, mx);
+          const float alpha = fast_exp2(m_mine - m_new);
+          float lsum = l_mine * alpha;
+          for (int i = lane; i < nv * GT; i += 32) {
+            const float p = fast_exp2(sc[i] - m_new);
+            sc[i] = p;
+            lsum += p;
+          }
+          l_mine = lsum;
+          m_mine = m_new;
 #pragma unroll
           for (int h = 0; h < GT; ++h) {
-            const float2 pp = make_float2(p[h], p[h]);
+            const float ah = __shfl_sync(kFullMask, alpha, h);
+            const float2 a2 = make_float2(ah, ah);
 #pragma unroll
-            for (int i = 0; i < C::DPV / 2; ++i) ffma2(acc[h][i], pp, vf[i]);
+            for (int i = 0; i < C::DPV / 2; ++i) fmul2(acc[h][i], a2);
           }
+          __syncwarp();
+
+          // ---- PV
+#pragma unroll 4
+          for (int t = 0; t < nv; ++t) {
+            float p[GT];
+            load_p<GT>(sc, t, p);
+            float2 vf[C::DPV / 2];
+            load_v<T, C::DPV>(vt + size_t(t) * D * sizeof(T), lane, vf);
+#pragma unroll
+            for (int h = 0; h < GT; ++h) {
+              const float2 pp = make_float2(p[h], p[h]);
+#pragma unroll
+              for (int i = 0; i < C::DPV / 2; ++i) ffma2(acc[h][i], pp, vf[i]);
+            }
+          }
+          __syncwarp();
+          if (lane == 0 && okE) mbar_arrive(&empty_bar[slot]);  // the pair's slot is free again
         }
-        __syncwarp();
-        if (lane == 0 && okE) mbar_arrive(&empty_bar[slot]);  // the pair's slot is free again
       }
-    }
 
-    // ---- merge the four warps' states for this (s, pc)
-    float lsum = l_mine;
+      // ---- hand this warp's state for the segment to the merger warp
+      float lsum = l_mine;
 #pragma unroll
-    for (int off = GT; off < 32; off <<= 1) lsum += __shfl_xor_sync(kFullMask, lsum, off);
-    if (lane < GT) {
-      mrg[warp][lane][D] = m_mine;
-      mrg[warp][lane][D + 1] = lsum;
-    }
+      for (int off = GT; off < 32; off <<= 1) lsum += __shfl_xor_sync(kFullMask, lsum, off);
+      deposit_state(a, seg_k, lane, &st_full, &st_free, abort_flag, [&]() {
+        if (lane < GT) {
+          mrg[warp][lane][D] = m_mine;
+          mrg[warp][lane][D + 1] = lsum;
+        }
 #pragma unroll
-    for (int h = 0; h < GT; ++h)
+        for (int h = 0; h < GT; ++h)
 #pragma unroll
-      for (int i = 0; i < C::DPV / 2; ++i) {
-        mrg[warp][h][lane * C::DPV + 2 * i] = acc[h][i].x;
-        mrg[warp][h][lane * C::DPV + 2 * i + 1] = acc[h][i].y;
-      }
-    named_barrier_sync(1, kConsumerWarps * 32);
-    combine_segment<T>(a, &mrg[0][0][0], GT * (D + 2), D, GT, complete, first_seg, s, hq0, threadIdx.x,
-                       kConsumerWarps * 32);
-    named_barrier_sync(1, kConsumerWarps * 32);
-
-    w += n;
-    j += n;
-    b += n;
-    if (b == nb) {
-      b = 0;
-      if (++pc == PC) {
-        pc = 0;
-        do {
-          ++s;
-        } while (s < a.S && blocks_of(a, s) == 0);
-        if (s < a.S) nb = blocks_of(a, s);
-      }
+          for (int i = 0; i < C::DPV / 2; ++i) {
+            mrg[warp][h][lane * C::DPV + 2 * i] = acc[h][i].x;
+            mrg[warp][h][lane * C::DPV + 2 * i + 1] = acc[h][i].y;
+          }
+      });
+      ++seg_k;
+      j += n;
+      wk.advance(a, n, PC);
     }
   }
 }
-
 
 }  // namespace pagedkv

@@ -8,7 +8,8 @@
 // SM): every CTA streams the same number of bytes whatever the length mix.
 // A CTA finishes any (s, pc) whose tiles all fall in its range and writes
 // `out`; a (s, pc) cut by a range boundary leaves a partial (acc, m, l) for
-// the reduce kernel: slot 0 for the CTA's first segment, slot 1 for its last.
+// the pair's last contributor to merge: slot 0 for the CTA's first segment,
+// slot 1 for its last.
 #pragma once
 
 #include <math_constants.h>
@@ -18,11 +19,14 @@
 namespace pagedkv {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kProducerWarp = kConsumerWarps;       // fills the ring
+constexpr int kMergerWarp = kConsumerWarps + 1;     // combines the consumers' states
+constexpr int kDecodeThreads = (kConsumerWarps + 2) * 32;
 constexpr int kCtasPerSm = 2;
 constexpr int kMaxStages = 64;
 constexpr int kMaxBlockSize = 64;
 constexpr int kRingBytes = 80 * 1024;
+constexpr int kMergeRecords = 32;  // records whose merge weights are staged in shared memory
 
 struct DecodeArgs {
   void *out;
@@ -36,7 +40,7 @@ struct DecodeArgs {
   int S, Hq, Hkv, B;
   float qscale;            // scale * log2(e)
   float *partials;         // [N][2][GT][D + 2]: acc[D], m, l
-  long long *cum;          // [S + 1] tile prefix (written by CTA 0)
+  unsigned *counters;      // [S * PC] contributors seen per split pair; zero between calls
   int *err;
   int nctas;
   int nstage;
@@ -79,10 +83,47 @@ __device__ __forceinline__ int blocks_of(const DecodeArgs &a, int s) {
   return (clamped_len(a, s) + a.B - 1) / a.B;
 }
 
-// Total tile count W (and, in CTA 0, the per-sequence prefix) and the tile
-// where this CTA's range starts.  Run by one whole warp.
-__device__ __forceinline__ void schedule_scan(const DecodeArgs &a, int PC, int lane, long long *W_out,
-                                              int *s0_out, long long *r0_out) {
+// Sequence holding flattened tile x, and x's offset inside that sequence's
+// tiles.  Run by one whole warp; x must be < W.
+__device__ __forceinline__ void locate_tile(const DecodeArgs &a, int PC, int lane, long long x, int *s_out,
+                                            long long *r_out) {
+  int sx = a.S;
+  long long rx = 0, run = 0;
+  for (int base = 0; base < a.S && sx == a.S; base += 32) {
+    const int s = base + lane;
+    const long long n = s < a.S ? (long long)blocks_of(a, s) * PC : 0;
+    long long incl = n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long y = __shfl_up_sync(kFullMask, incl, off);
+      if (lane >= off) incl += y;
+    }
+    const long long excl = run + incl - n;
+    const unsigned m = __ballot_sync(kFullMask, n > 0 && excl <= x && x < run + incl);
+    if (m) {
+      const int leader = __ffs(m) - 1;
+      sx = __shfl_sync(kFullMask, s, leader);
+      rx = __shfl_sync(kFullMask, x - excl, leader);
+    }
+    run += __shfl_sync(kFullMask, incl, 31);
+  }
+  *s_out = sx;
+  *r_out = rx;
+}
+
+// The CTA's plan.  W = total tiles of the step; the CTA owns [w0, w1).  It
+// processes its range rotated: first [Ls, w1), the segment that ends the
+// range (usually the head of a (s, pc) cut by the range end), then
+// [w0, Ls).  Both ends of a cut (s, pc) are then worked on early by the two
+// CTAs that share it, so their merge overlaps with streaming instead of
+// piling up at the end of the kernel.  (sA, rA) / (s0, r0) locate Ls / w0.
+struct Plan {
+  long long W, w0, w1, Ls;
+  int sA, s0;
+  long long rA, r0;
+};
+
+__device__ __forceinline__ void schedule_scan(const DecodeArgs &a, int PC, int lane, Plan *plan) {
   const int cap = a.max_blocks * a.B;
   long long run = 0;
   for (int base = 0; base < a.S; base += 32) {
@@ -99,37 +140,39 @@ __device__ __forceinline__ void schedule_scan(const DecodeArgs &a, int PC, int l
       const long long y = __shfl_up_sync(kFullMask, incl, off);
       if (lane >= off) incl += y;
     }
-    if (blockIdx.x == 0 && s < a.S) a.cum[s] = run + incl - n;
     run += __shfl_sync(kFullMask, incl, 31);
   }
-  if (blockIdx.x == 0 && lane == 0) a.cum[a.S] = run;
-  const long long W = run;
-  const long long w0 = (long long)blockIdx.x * W / a.nctas;
-  int s0 = a.S;
-  long long r0 = 0;
-  run = 0;
-  for (int base = 0; base < a.S && s0 == a.S; base += 32) {
-    const int s = base + lane;
-    const long long n = s < a.S ? (long long)blocks_of(a, s) * PC : 0;
-    long long incl = n;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const long long y = __shfl_up_sync(kFullMask, incl, off);
-      if (lane >= off) incl += y;
+  Plan p;
+  p.W = run;
+  p.w0 = (long long)blockIdx.x * p.W / a.nctas;
+  p.w1 = (long long)(blockIdx.x + 1) * p.W / a.nctas;
+  p.Ls = p.w0;
+  p.sA = p.s0 = a.S;
+  p.rA = p.r0 = 0;
+  if (p.w0 < p.w1) {
+    locate_tile(a, PC, lane, p.w0, &p.s0, &p.r0);
+    int sl;
+    long long rl;
+    locate_tile(a, PC, lane, p.w1 - 1, &sl, &rl);
+    const int nb = blocks_of(a, sl);
+    const long long pair_start = (p.w1 - 1) - rl % nb;
+    if (pair_start > p.w0) {
+      p.Ls = pair_start;
+      p.sA = sl;
+      p.rA = rl - rl % nb;
+    } else {
+      p.sA = p.s0;
+      p.rA = p.r0;
     }
-    const long long excl = run + incl - n;
-    const bool hit = n > 0 && excl <= w0 && w0 < run + incl;
-    const unsigned m = __ballot_sync(kFullMask, hit);
-    if (m) {
-      const int leader = __ffs(m) - 1;
-      s0 = __shfl_sync(kFullMask, s, leader);
-      r0 = __shfl_sync(kFullMask, w0 - excl, leader);
-    }
-    run += __shfl_sync(kFullMask, incl, 31);
   }
-  *W_out = W;
-  *s0_out = s0;
-  *r0_out = r0;
+  *plan = p;
+}
+
+// Processing order of a CTA's range: phase 0 walks [Ls, w1), phase 1 [w0, Ls).
+__device__ __forceinline__ bool phase_range(const Plan &p, int ph, long long *from, long long *to) {
+  *from = ph == 0 ? p.Ls : p.w0;
+  *to = ph == 0 ? p.w1 : p.Ls;
+  return *from < *to;
 }
 
 // Cursor over a CTA's tile range, one segment (consecutive tiles of one
@@ -173,50 +216,57 @@ struct Walk {
 // issued into each slot so the producer can wait for every copy still in
 // flight before it leaves (after an abort too).
 template <class Issue>
-__device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, int s0, long long r0, long long w0,
-                                        long long w1, int lane, uint64_t *full_bar, uint64_t *empty_bar,
-                                        uint32_t *issued, volatile int *abort_flag, Issue issue) {
+__device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, const Plan &plan, int lane,
+                                        uint64_t *full_bar, uint64_t *empty_bar, uint32_t *issued,
+                                        volatile int *abort_flag, Issue issue) {
   long long e = 0;
   bool aborted = false;
-  Walk wk;
-  wk.start(a, s0, r0, w0);
-  while (wk.w < w1 && !aborted) {
-    const int n = wk.seg_len(w1);
-    const int kvh = wk.pc / HC;
-    const int L = clamped_len(a, wk.s);
-    const int32_t *trow = a.tables + (long long)wk.s * a.max_blocks + wk.b;
-    int pid_next = lane < n ? trow[lane] : -1;
-    for (int base = 0; base < n && !aborted; base += 32) {
-      const int pid_cur = pid_next;
-      const int cnt = min(32, n - base);
-      if (base + 32 < n) pid_next = (base + 32 + lane < n) ? trow[base + 32 + lane] : -1;
-      for (int k = 0; k < cnt; k += a.pg) {
-        const int t = k + lane;
-        const int p = __shfl_sync(kFullMask, pid_cur, t < 32 ? t : 31);
-        bool fail = false;
-        if (lane < a.pg && t < cnt) {
-          const long long me = e + lane;
-          const int slot = int(me % a.nstage);
-          const uint32_t u = uint32_t(me / a.nstage);
-          if (*abort_flag || (u > 0 && !mbar_wait(&empty_bar[slot], (u - 1) & 1u, abort_flag))) {
-            fail = true;
-          } else {
-            issue(slot, p, kvh, wk.b + base + t, L);
-            issued[slot] = u + 1;
+  for (int ph = 0; ph < 2 && !aborted; ++ph) {
+    long long from, to;
+    if (!phase_range(plan, ph, &from, &to)) continue;
+    Walk wk;
+    if (ph == 0)
+      wk.start(a, plan.sA, plan.rA, from);
+    else
+      wk.start(a, plan.s0, plan.r0, from);
+    while (wk.w < to && !aborted) {
+      const int n = wk.seg_len(to);
+      const int kvh = wk.pc / HC;
+      const int L = clamped_len(a, wk.s);
+      const int32_t *trow = a.tables + (long long)wk.s * a.max_blocks + wk.b;
+      int pid_next = lane < n ? trow[lane] : -1;
+      for (int base = 0; base < n && !aborted; base += 32) {
+        const int pid_cur = pid_next;
+        const int cnt = min(32, n - base);
+        if (base + 32 < n) pid_next = (base + 32 + lane < n) ? trow[base + 32 + lane] : -1;
+        for (int k = 0; k < cnt; k += a.pg) {
+          const int t = k + lane;
+          const int p = __shfl_sync(kFullMask, pid_cur, t < 32 ? t : 31);
+          bool fail = false;
+          if (lane < a.pg && t < cnt) {
+            const long long me = e + lane;
+            const int slot = int(me % a.nstage);
+            const uint32_t u = uint32_t(me / a.nstage);
+            if (*abort_flag || (u > 0 && !mbar_wait(&empty_bar[slot], (u - 1) & 1u, abort_flag))) {
+              fail = true;
+            } else {
+              issue(slot, p, kvh, wk.b + base + t, L);
+              issued[slot] = u + 1;
+            }
           }
-        }
-        if (__any_sync(kFullMask, fail)) {
-          aborted = true;
-          if (lane == 0) {
-            *abort_flag = 1;
-            raise_error(a.err, PA_DEVERR_TIMEOUT);
+          if (__any_sync(kFullMask, fail)) {
+            aborted = true;
+            if (lane == 0) {
+              *abort_flag = 1;
+              raise_error(a.err, PA_DEVERR_TIMEOUT);
+            }
+            break;
           }
-          break;
+          e += min(a.pg, cnt - k);
         }
-        e += min(a.pg, cnt - k);
       }
+      wk.advance(a, n, PC);
     }
-    wk.advance(a, n, PC);
   }
   // Do not leave while a copy into this CTA's shared memory is in flight:
   // only the last use issued into a slot can be (earlier ones were released,
@@ -231,43 +281,208 @@ __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, int
   }
 }
 
-// Merge the consumer warps' states of one segment, held in shared memory as
-// mrg[warp][head][0..D-1 acc, D: m, D+1: l] (head stride D + 2), and write the
-// final rows (segment covers the whole (s, pc)) or this CTA's partial record.
+// CTA whose tile range [c*W/N, (c+1)*W/N) holds tile x.
+__device__ __forceinline__ int cta_of(long long x, long long W, int N) {
+  return int(((x + 1) * N + W - 1) / W - 1);
+}
+
+__device__ __forceinline__ long long range_start(int c, long long W, int N) { return (long long)c * W / N; }
+
+// Zero output rows of the sequences with nothing cached, spread over CTAs.
 template <typename T>
-__device__ __forceinline__ void combine_segment(const DecodeArgs &a, const float *mrg, int warp_stride, int D,
-                                                int GT, bool complete, bool first_seg, int s, int hq0, int tid,
-                                                int nthreads) {
-  for (int idx = tid; idx < GT * D; idx += nthreads) {
-    const int h = idx / D;
-    const int d = idx - h * D;
-    float M = -CUDART_INF_F;
-#pragma unroll
-    for (int q = 0; q < kConsumerWarps; ++q) M = fmaxf(M, mrg[q * warp_stride + h * (D + 2) + D]);
-    float num = 0.f, den = 0.f;
-#pragma unroll
-    for (int q = 0; q < kConsumerWarps; ++q) {
-      const float *row = mrg + q * warp_stride + h * (D + 2);
-      const float f = fast_exp2(row[D] - M);
-      num += f * row[d];
-      den += f * row[D + 1];
-    }
-    if (complete) {
-      long long oo = ((long long)s * a.Hq + hq0 + h) * D + d;
-      PA_DBG_FIX(oo >= 0 && oo < (long long)a.S * a.Hq * D, kDbgGlobal, continue);
-      T *o = static_cast<T *>(a.out) + oo;
-      *o = Elem<T>::from_float(num / den);
-    } else {
-      long long ro = (((long long)blockIdx.x * 2 + (first_seg ? 0 : 1)) * GT + h) * (D + 2);
-      PA_DBG_FIX(ro >= 0 && ro + D + 2 <= (long long)a.nctas * 2 * 8 * (D + 2), kDbgGlobal, continue);
-      float *rec = a.partials + ro;
-      rec[d] = num;
-      if (d == 0) {
-        rec[D] = M;
-        rec[D + 1] = den;
+__device__ __forceinline__ void zero_empty_rows(const DecodeArgs &a, int D, int tid, int nthreads) {
+  for (int s = blockIdx.x; s < a.S; s += a.nctas) {
+    if (clamped_len(a, s) != 0) continue;
+    T *o = static_cast<T *>(a.out) + (long long)s * a.Hq * D;
+    for (int i = tid; i < a.Hq * D; i += nthreads) o[i] = Elem<T>::from_float(0.f);
+  }
+}
+
+// The merger warp.  It walks the same plan as the consumers, one segment at
+// a time: waits until the four consumer warps have deposited their running
+// states (m, l, acc per head; head stride D + 2, warp stride warp_stride) in
+// `mrg` (mbarrier st_full, four arrivals), combines them,
+//     M = max_w m_w;  num = sum_w 2^(m_w - M) acc_w;  den = sum_w 2^(m_w - M) l_w,
+// and writes num / den as the output rows (the segment is a whole (s, pc)) or
+// this CTA's partial record (acc, m, l) for a (s, pc) cut by a range boundary,
+// then hands the buffer back (st_free).  For a cut (s, pc) it counts this CTA
+// in; the CTA that completes the count merges the records of all CTAs that
+// share the pair (the a5 step) and sets the counter back to zero:
+//     M = max_r m_r;  out = sum_r 2^(m_r - M) acc_r / sum_r 2^(m_r - M) l_r.
+// Running this off the consumer warps keeps every fence, atomic and remote
+// read of a segment end out of the streaming path.
+template <typename T>
+__device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan, int PC, int HC, int G, int D,
+                                           int lane, const float *mrg, int warp_stride, uint64_t *st_full,
+                                           uint64_t *st_free, float *sh_w, volatile int *abort_flag) {
+  const int GT = a.GT;
+  const int N = a.nctas;
+  const long long W = plan.W;
+  long long k = 0;  // segments handled
+#ifdef PA_TRACE
+  long long tr_t0 = clock64(), tr_wait = 0;
+#endif
+  for (int ph = 0; ph < 2; ++ph) {
+    long long from, to;
+    if (!phase_range(plan, ph, &from, &to)) continue;
+    Walk wk;
+    if (ph == 0)
+      wk.start(a, plan.sA, plan.rA, from);
+    else
+      wk.start(a, plan.s0, plan.r0, from);
+    while (wk.w < to) {
+      const int n = wk.seg_len(to);
+      const bool complete = (wk.b == 0 && n == wk.nb);
+      const bool first_seg = (wk.w == plan.w0);
+      const int s = wk.s, pc = wk.pc;
+      const int hq0 = (pc / HC) * G + (pc % HC) * GT;
+#ifdef PA_TRACE
+      const long long tr_w0 = clock64();
+#endif
+      if (!mbar_wait(st_full, uint32_t(k) & 1u, abort_flag)) {
+        if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
       }
+#ifdef PA_TRACE
+      tr_wait += clock64() - tr_w0;
+#endif
+      __syncwarp();
+      // ---- combine the four warps' states
+      for (int idx = lane; idx < GT * D; idx += 32) {
+        const int h = idx / D;
+        const int d = idx - h * D;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int q = 0; q < kConsumerWarps; ++q) M = fmaxf(M, mrg[q * warp_stride + h * (D + 2) + D]);
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int q = 0; q < kConsumerWarps; ++q) {
+          const float *row = mrg + q * warp_stride + h * (D + 2);
+          const float f = fast_exp2(row[D] - M);
+          num += f * row[d];
+          den += f * row[D + 1];
+        }
+        if (complete) {
+          long long oo = ((long long)s * a.Hq + hq0 + h) * D + d;
+          PA_DBG_FIX(oo >= 0 && oo < (long long)a.S * a.Hq * D, kDbgGlobal, continue);
+          static_cast<T *>(a.out)[oo] = Elem<T>::from_float(num / den);
+        } else {
+          long long ro = (((long long)blockIdx.x * 2 + (first_seg ? 0 : 1)) * GT + h) * (D + 2);
+          PA_DBG_FIX(ro >= 0 && ro + D + 2 <= (long long)N * 2 * 8 * (D + 2), kDbgGlobal, continue);
+          float *rec = a.partials + ro;
+          rec[d] = num;
+          if (d == 0) {
+            rec[D] = M;
+            rec[D + 1] = den;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(st_free);  // the consumers may overwrite mrg now
+      if (!complete) {
+        // ---- count this CTA in; the last of the pair's CTAs merges
+        __threadfence();  // publish this CTA's record before it is counted
+        __syncwarp();
+        const long long P0 = wk.w - wk.b;
+        const int nb = wk.nb;
+        const int cf = cta_of(P0, W, N);
+        const int cl = cta_of(P0 + nb - 1, W, N);
+        int last = 0;
+        if (lane == 0) {
+          int kc = 0;
+          if (W >= N) {
+            kc = cl - cf + 1;
+          } else {
+            for (int c = cf; c <= cl; ++c) kc += range_start(c, W, N) < range_start(c + 1, W, N);
+          }
+          unsigned *ctr = a.counters + (long long)s * PC + pc;
+          const unsigned seen = atomicAdd(ctr, 1u) + 1u;
+          last = seen == unsigned(kc);
+          if (last) {
+            *ctr = 0u;        // ready for the next call
+            __threadfence();  // the other records were published before their counts
+          }
+        }
+        last = __shfl_sync(kFullMask, last, 0);
+        if (last) {
+          const bool cf_last_seg = range_start(cf, W, N) < P0;
+          auto rec_of = [&](int c, int h) {
+            const int slot = (c == cf && cf_last_seg) ? 1 : 0;
+            return a.partials + (((long long)c * 2 + slot) * GT + h) * (D + 2);
+          };
+          const int nrec = cl - cf + 1;
+          if (W >= N && nrec <= kMergeRecords) {
+            if (lane < GT) {  // weights 2^(m_r - M) / sum_r 2^(m_r - M) l_r, once per (record, head)
+              const int h = lane;
+              float M = -CUDART_INF_F;
+              for (int r = 0; r < nrec; ++r) M = fmaxf(M, __ldcg(rec_of(cf + r, h) + D));
+              float den = 0.f;
+              for (int r = 0; r < nrec; ++r) {
+                const float *rec = rec_of(cf + r, h);
+                const float f = fast_exp2(__ldcg(rec + D) - M);
+                sh_w[r * 8 + h] = f;
+                den += f * __ldcg(rec + D + 1);
+              }
+              const float inv = 1.f / den;
+              for (int r = 0; r < nrec; ++r) sh_w[r * 8 + h] *= inv;
+            }
+            __syncwarp();
+            for (int idx = lane; idx < GT * D; idx += 32) {
+              const int h = idx / D;
+              const int d = idx - h * D;
+              float num = 0.f;
+              for (int r = 0; r < nrec; ++r) num += sh_w[r * 8 + h] * __ldcg(rec_of(cf + r, h) + d);
+              static_cast<T *>(a.out)[((long long)s * a.Hq + hq0 + h) * D + d] = Elem<T>::from_float(num);
+            }
+            __syncwarp();
+          } else {
+            // many records (or empty CTA ranges): per element, straight from the records
+            for (int idx = lane; idx < GT * D; idx += 32) {
+              const int h = idx / D;
+              const int d = idx - h * D;
+              float M = -CUDART_INF_F;
+              for (int c = cf; c <= cl; ++c) {
+                if (W < N && range_start(c, W, N) == range_start(c + 1, W, N)) continue;
+                M = fmaxf(M, __ldcg(rec_of(c, h) + D));
+              }
+              float num = 0.f, den = 0.f;
+              for (int c = cf; c <= cl; ++c) {
+                if (W < N && range_start(c, W, N) == range_start(c + 1, W, N)) continue;
+                const float *rec = rec_of(c, h);
+                const float f = fast_exp2(__ldcg(rec + D) - M);
+                num += f * __ldcg(rec + d);
+                den += f * __ldcg(rec + D + 1);
+              }
+              static_cast<T *>(a.out)[((long long)s * a.Hq + hq0 + h) * D + d] = Elem<T>::from_float(num / den);
+            }
+          }
+        }
+      }
+      ++k;
+      wk.advance(a, n, PC);
     }
   }
+#ifdef PA_TRACE
+  if (lane == 0 && (blockIdx.x % 101) == 0)
+    printf("trace cta %d merger: segments %lld cycles %lld waiting %lld\n", blockIdx.x, k, clock64() - tr_t0, tr_wait);
+#endif
+}
+
+// A consumer warp's end of a segment: wait until the merger took the previous
+// segment's states (mbarrier st_free, phase k - 1: the merger hands buffers
+// back in order, so the parity test is exact), then let `write` store this
+// warp's state into the buffer and announce it (st_full).
+template <class Write>
+__device__ __forceinline__ void deposit_state(const DecodeArgs &a, long long k, int lane, uint64_t *st_full,
+                                              uint64_t *st_free, volatile int *abort_flag, Write write) {
+  if (k > 0 && !mbar_wait(st_free, uint32_t(k - 1) & 1u, abort_flag)) {
+    if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+    *abort_flag = 1;
+  }
+  __syncwarp();
+  write();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(st_full);
 }
 
 }  // namespace pagedkv

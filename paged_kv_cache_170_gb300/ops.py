@@ -40,9 +40,6 @@ def _load() -> ctypes.CDLL:
         "pa_write_kv": [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32, vp, vp],
         "pa_copy_blocks": [vp, vp, vp, i64, i32, i32, i32, i64, i32, vp, vp],
         "pa_decode": [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, sz, vp, vp],
-        "pa_decode_partition": [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, sz, vp,
-                                vp],
-        "pa_decode_reduce": [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, sz, vp, vp],
         "pa_decode_noalloc": [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp],
     }
     for name, args in sig.items():
@@ -173,8 +170,9 @@ def pa_decode_grid_size() -> int:
 
 
 def new_workspace(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int, device) -> torch.Tensor:
+    """A decode workspace, zero-filled as pa_decode requires before first use."""
     n = pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim)
-    return torch.empty(n, dtype=torch.uint8, device=device)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
 def _decode_args(q, k_cache, v_cache, block_tables, context_lens, out, workspace):
@@ -206,24 +204,6 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, blo
                          NB, float(scale), _DTYPES[q.dtype], ws.data_ptr(), ws.numel(), _ptr(err),
                          _stream(q.device)), "pa_decode")
     return out
-
-
-def pa_decode_partition(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, workspace=None,
-                        err=None) -> torch.Tensor:
-    NB, Hkv, B, D, S, Hq, out, ws = _decode_args(q, k_cache, v_cache, block_tables, context_lens, out, workspace)
-    _check(lib.pa_decode_partition(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                                   block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), S, Hq,
-                                   Hkv, D, B, NB, float(scale), _DTYPES[q.dtype], ws.data_ptr(), ws.numel(),
-                                   _ptr(err), _stream(q.device)), "pa_decode_partition")
-    return out
-
-
-def pa_decode_reduce(out, block_tables, context_lens, num_kv_heads, block_size, workspace, err=None) -> None:
-    _need(out, "out", None, 3)
-    S, Hq, D = out.shape
-    _check(lib.pa_decode_reduce(out.data_ptr(), context_lens.data_ptr(), block_tables.shape[1], S, Hq,
-                                num_kv_heads, D, block_size, _DTYPES[out.dtype], workspace.data_ptr(),
-                                workspace.numel(), _ptr(err), _stream(out.device)), "pa_decode_reduce")
 
 
 def pa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
