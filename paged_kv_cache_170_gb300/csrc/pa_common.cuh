@@ -64,6 +64,8 @@ template <> struct Elem<float> {
   }
   static __device__ __forceinline__ float to_float(float x) { return x; }
   static __device__ __forceinline__ float from_float(float x) { return x; }
+  // 4 consecutive outputs (16-byte aligned)
+  static __device__ __forceinline__ void store4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
 };
 
 template <> struct Elem<__nv_bfloat16> {
@@ -79,6 +81,12 @@ template <> struct Elem<__nv_bfloat16> {
   }
   static __device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
   static __device__ __forceinline__ __nv_bfloat16 from_float(float x) { return __float2bfloat16_rn(x); }
+  // 4 consecutive outputs, rounded to nearest even (8-byte aligned)
+  static __device__ __forceinline__ void store4(__nv_bfloat16 *p, float4 v) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    *reinterpret_cast<uint2 *>(p) =
+        make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+  }
 };
 
 template <> struct Elem<__half> {
@@ -95,6 +103,12 @@ template <> struct Elem<__half> {
   }
   static __device__ __forceinline__ float to_float(__half x) { return __half2float(x); }
   static __device__ __forceinline__ __half from_float(float x) { return __float2half_rn(x); }
+  // 4 consecutive outputs, rounded to nearest even (8-byte aligned)
+  static __device__ __forceinline__ void store4(__half *p, float4 v) {
+    const __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
+    *reinterpret_cast<uint2 *>(p) =
+        make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+  }
 };
 
 // ----------------------------------------------------------------- packed FMA

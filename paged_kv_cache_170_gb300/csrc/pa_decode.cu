@@ -22,7 +22,7 @@ static int decode_grid() { return device_sm_count() * kCtasPerSm; }
 static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static size_t partial_bytes(int nctas, int head_dim) {
-  return round256(size_t(nctas) * 2 * 8 * (head_dim + 2) * sizeof(float));
+  return round256(size_t(nctas) * 2 * 8 * state_row(head_dim) * sizeof(float));
 }
 
 // partial records, then one counter per (sequence, query head) (an upper

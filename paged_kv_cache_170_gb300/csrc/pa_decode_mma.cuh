@@ -45,12 +45,12 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   extern __shared__ __align__(1024) unsigned char ring_raw[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ __align__(16) float mrg[kConsumerWarps][8][D + 2];
+  __shared__ __align__(16) float mrg[kConsumerWarps][8][state_row(D)];
   __shared__ Plan sh_plan;
   __shared__ uint32_t issued[kMaxStages];
   __shared__ int sh_abort;
   __shared__ __align__(8) uint64_t st_full, st_free;  // consumers -> merger hand-off of mrg
-  __shared__ float sh_mw[kMergeRecords * 8];
+  __shared__ float sh_mw[2 * kMergeRecords * 8];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
 
   if (warp == kMergerWarp) {
     // -------------------------------------------------------------- merger
-    run_merger<T>(a, plan, PC, HC, G, D, lane, &mrg[0][0][0], 8 * (D + 2), &st_full, &st_free, sh_mw, abort_flag);
+    run_merger<T, D>(a, plan, PC, HC, G, lane, &mrg[0][0][0], 8 * state_row(D), &st_full, &st_free, sh_mw, abort_flag);
     zero_empty_rows<T>(a, D, lane, 32);
     return;
   }
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
               const int r = nv + i / (HALVES * 8);
               const int hc = i % (HALVES * 8);
               size_t zo = (size_t)slot * a.slot_stride + a.tile_stride + (hc >> 3) * B * 128 + r * 128 + (hc & 7) * 16;
-              PA_DBG_FIX(zo + 16 <= (size_t)a.nstage * a.slot_stride, kDbgSmem, continue);
+              PA_DBG_FIX(zo + 16 <= (size_t)a.nstage * a.slot_stride, kDbgSmem, zo = 0);
               *reinterpret_cast<uint4 *>(ring + zo) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_shared();

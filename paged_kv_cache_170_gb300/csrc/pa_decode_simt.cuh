@@ -94,12 +94,12 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(16) float sc_buf[kConsumerWarps][kMaxBlockSize * GT];
-  __shared__ __align__(16) float mrg[kConsumerWarps][GT][D + 2];
+  __shared__ __align__(16) float mrg[kConsumerWarps][GT][state_row(D)];
   __shared__ Plan sh_plan;
   __shared__ uint32_t issued[kMaxStages];
   __shared__ int sh_abort;
   __shared__ __align__(8) uint64_t st_full, st_free;  // consumers -> merger hand-off of mrg
-  __shared__ float sh_mw[kMergeRecords * 8];
+  __shared__ float sh_mw[2 * kMergeRecords * 8];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
 
   if (warp == kMergerWarp) {
     // -------------------------------------------------------------- merger
-    run_merger<T>(a, plan, PC, HC, G, D, lane, &mrg[0][0][0], GT * (D + 2), &st_full, &st_free, sh_mw, abort_flag);
+    run_merger<T, D>(a, plan, PC, HC, G, lane, &mrg[0][0][0], GT * state_row(D), &st_full, &st_free, sh_mw, abort_flag);
     zero_empty_rows<T>(a, D, lane, 32);
     return;
   }

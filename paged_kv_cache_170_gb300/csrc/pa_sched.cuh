@@ -39,7 +39,7 @@ struct DecodeArgs {
   int max_blocks;
   int S, Hq, Hkv, B;
   float qscale;            // scale * log2(e)
-  float *partials;         // [N][2][GT][D + 2]: acc[D], m, l
+  float *partials;         // [N][2][8][state_row(D)]: acc[D], m, l per head
   unsigned *counters;      // [S * PC] contributors seen per split pair; zero between calls
   int *err;
   int nctas;
@@ -298,26 +298,38 @@ __device__ __forceinline__ void zero_empty_rows(const DecodeArgs &a, int D, int 
   }
 }
 
+// Floats per head in a warp state or a partial record: acc[D], m, l, and two
+// pad floats so that every head row starts on a 16-byte boundary.
+__host__ __device__ constexpr int state_row(int D) { return D + 4; }
+
 // The merger warp.  It walks the same plan as the consumers, one segment at
 // a time: waits until the four consumer warps have deposited their running
-// states (m, l, acc per head; head stride D + 2, warp stride warp_stride) in
-// `mrg` (mbarrier st_full, four arrivals), combines them,
+// states (acc[D], m, l per head; head stride state_row(D), warp stride
+// warp_stride) in `mrg` (mbarrier st_full, four arrivals), combines them,
 //     M = max_w m_w;  num = sum_w 2^(m_w - M) acc_w;  den = sum_w 2^(m_w - M) l_w,
 // and writes num / den as the output rows (the segment is a whole (s, pc)) or
-// this CTA's partial record (acc, m, l) for a (s, pc) cut by a range boundary,
-// then hands the buffer back (st_free).  For a cut (s, pc) it counts this CTA
-// in; the CTA that completes the count merges the records of all CTAs that
-// share the pair (the a5 step) and sets the counter back to zero:
+// this CTA's partial record (num, M, den) for a (s, pc) cut by a range
+// boundary, then hands the buffer back (st_free).  For a cut (s, pc) it counts
+// this CTA in; the CTA that completes the count merges the records of all CTAs
+// that share the pair (the a5 step) and sets the counter back to zero:
 //     M = max_r m_r;  out = sum_r 2^(m_r - M) acc_r / sum_r 2^(m_r - M) l_r.
 // Running this off the consumer warps keeps every fence, atomic and remote
-// read of a segment end out of the streaming path.
-template <typename T>
-__device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan, int PC, int HC, int G, int D,
-                                           int lane, const float *mrg, int warp_stride, uint64_t *st_full,
-                                           uint64_t *st_free, float *sh_w, volatile int *abort_flag) {
+// read of a segment end out of the streaming path.  The weights are formed
+// once per (warp or record, head); the rows then move as 16-byte vectors, so
+// a merge costs one L2 round trip per record rather than one per element.
+template <typename T, int D>
+__device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan, int PC, int HC, int G, int lane,
+                                           const float *mrg, int warp_stride, uint64_t *st_full, uint64_t *st_free,
+                                           float *sh_w, volatile int *abort_flag) {
+  constexpr int R = state_row(D);
+  constexpr int C4 = D / 4;            // 16-byte chunks per head row
+  constexpr int kIters = 8 * C4 / 32;  // chunks per lane for 8 heads
+  static_assert(kConsumerWarps == 4 && (8 * C4) % 32 == 0, "lane = 4 * head + warp below");
   const int GT = a.GT;
   const int N = a.nctas;
   const long long W = plan.W;
+  const int lh = lane >> 2, lq = lane & 3;  // the (head, warp) whose weight this lane forms
+  float *sh_m = sh_w, *sh_l = sh_w + kMergeRecords * 8;
   long long k = 0;  // segments handled
 #ifdef PA_TRACE
   long long tr_t0 = clock64(), tr_wait = 0;
@@ -347,33 +359,53 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
       tr_wait += clock64() - tr_w0;
 #endif
       __syncwarp();
-      // ---- combine the four warps' states
-      for (int idx = lane; idx < GT * D; idx += 32) {
-        const int h = idx / D;
-        const int d = idx - h * D;
-        float M = -CUDART_INF_F;
-#pragma unroll
-        for (int q = 0; q < kConsumerWarps; ++q) M = fmaxf(M, mrg[q * warp_stride + h * (D + 2) + D]);
-        float num = 0.f, den = 0.f;
-#pragma unroll
-        for (int q = 0; q < kConsumerWarps; ++q) {
-          const float *row = mrg + q * warp_stride + h * (D + 2);
-          const float f = fast_exp2(row[D] - M);
-          num += f * row[d];
-          den += f * row[D + 1];
+      // ---- combine the four warps' states: weights per (warp, head) ...
+      float m = -CUDART_INF_F, l = 0.f;
+      if (lh < GT) {
+        m = mrg[lq * warp_stride + lh * R + D];
+        l = mrg[lq * warp_stride + lh * R + D + 1];
+      }
+      float M = fmaxf(m, __shfl_xor_sync(kFullMask, m, 1));
+      M = fmaxf(M, __shfl_xor_sync(kFullMask, M, 2));
+      const float f = lh < GT ? fast_exp2(m - M) : 0.f;
+      float den = f * l;
+      den += __shfl_xor_sync(kFullMask, den, 1);
+      den += __shfl_xor_sync(kFullMask, den, 2);
+      const float wt = complete ? (lh < GT ? f / den : 0.f) : f;
+      float *rec = nullptr;
+      if (!complete) {
+        long long ro = ((long long)blockIdx.x * 2 + (first_seg ? 0 : 1)) * 8 * R;
+        PA_DBG_FIX(ro >= 0 && ro + 8 * R <= (long long)N * 2 * 8 * R, kDbgGlobal, ro = 0);
+        rec = a.partials + ro;
+        if (lq == 0 && lh < GT) {
+          rec[lh * R + D] = M;
+          rec[lh * R + D + 1] = den;
         }
-        if (complete) {
-          long long oo = ((long long)s * a.Hq + hq0 + h) * D + d;
-          PA_DBG_FIX(oo >= 0 && oo < (long long)a.S * a.Hq * D, kDbgGlobal, continue);
-          static_cast<T *>(a.out)[oo] = Elem<T>::from_float(num / den);
-        } else {
-          long long ro = (((long long)blockIdx.x * 2 + (first_seg ? 0 : 1)) * GT + h) * (D + 2);
-          PA_DBG_FIX(ro >= 0 && ro + D + 2 <= (long long)N * 2 * 8 * (D + 2), kDbgGlobal, continue);
-          float *rec = a.partials + ro;
-          rec[d] = num;
-          if (d == 0) {
-            rec[D] = M;
-            rec[D + 1] = den;
+      }
+      // ... then the rows, 4 floats per lane and step
+#pragma unroll
+      for (int i = 0; i < kIters; ++i) {
+        const int c = lane + 32 * i;
+        const int h = c / C4, d = (c % C4) * 4;
+        float w[kConsumerWarps];
+#pragma unroll
+        for (int q = 0; q < kConsumerWarps; ++q) w[q] = __shfl_sync(kFullMask, wt, 4 * h + q);
+        if (h < GT) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int q = 0; q < kConsumerWarps; ++q) {
+            const float4 v = *reinterpret_cast<const float4 *>(mrg + q * warp_stride + h * R + d);
+            acc.x += w[q] * v.x;
+            acc.y += w[q] * v.y;
+            acc.z += w[q] * v.z;
+            acc.w += w[q] * v.w;
+          }
+          if (complete) {
+            long long oo = ((long long)s * a.Hq + hq0 + h) * D + d;
+            PA_DBG_FIX(oo >= 0 && oo + 4 <= (long long)a.S * a.Hq * D, kDbgGlobal, oo = 0);
+            Elem<T>::store4(static_cast<T *>(a.out) + oo, acc);
+          } else {
+            *reinterpret_cast<float4 *>(rec + h * R + d) = acc;
           }
         }
       }
@@ -406,54 +438,80 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
         last = __shfl_sync(kFullMask, last, 0);
         if (last) {
           const bool cf_last_seg = range_start(cf, W, N) < P0;
-          auto rec_of = [&](int c, int h) {
+          auto rec_of = [&](int c) {
             const int slot = (c == cf && cf_last_seg) ? 1 : 0;
-            return a.partials + (((long long)c * 2 + slot) * GT + h) * (D + 2);
+            return a.partials + ((long long)c * 2 + slot) * 8 * R;
           };
           const int nrec = cl - cf + 1;
           if (W >= N && nrec <= kMergeRecords) {
-            if (lane < GT) {  // weights 2^(m_r - M) / sum_r 2^(m_r - M) l_r, once per (record, head)
+            // every record's (m, l) per head at once, then the weights
+            //     2^(m_r - M) / sum_r 2^(m_r - M) l_r   (in place of m_r)
+            for (int i = lane; i < nrec * GT; i += 32) {
+              const int r = i / GT, h = i - r * GT;
+              const float *rr = rec_of(cf + r) + h * R;
+              sh_m[r * 8 + h] = __ldcg(rr + D);
+              sh_l[r * 8 + h] = __ldcg(rr + D + 1);
+            }
+            __syncwarp();
+            if (lane < GT) {
               const int h = lane;
-              float M = -CUDART_INF_F;
-              for (int r = 0; r < nrec; ++r) M = fmaxf(M, __ldcg(rec_of(cf + r, h) + D));
-              float den = 0.f;
+              float Mr = -CUDART_INF_F;
+              for (int r = 0; r < nrec; ++r) Mr = fmaxf(Mr, sh_m[r * 8 + h]);
+              float dr = 0.f;
               for (int r = 0; r < nrec; ++r) {
-                const float *rec = rec_of(cf + r, h);
-                const float f = fast_exp2(__ldcg(rec + D) - M);
-                sh_w[r * 8 + h] = f;
-                den += f * __ldcg(rec + D + 1);
+                const float fr = fast_exp2(sh_m[r * 8 + h] - Mr);
+                sh_m[r * 8 + h] = fr;
+                dr += fr * sh_l[r * 8 + h];
               }
-              const float inv = 1.f / den;
-              for (int r = 0; r < nrec; ++r) sh_w[r * 8 + h] *= inv;
+              const float inv = 1.f / dr;
+              for (int r = 0; r < nrec; ++r) sh_m[r * 8 + h] *= inv;
             }
             __syncwarp();
-            for (int idx = lane; idx < GT * D; idx += 32) {
-              const int h = idx / D;
-              const int d = idx - h * D;
-              float num = 0.f;
-              for (int r = 0; r < nrec; ++r) num += sh_w[r * 8 + h] * __ldcg(rec_of(cf + r, h) + d);
-              static_cast<T *>(a.out)[((long long)s * a.Hq + hq0 + h) * D + d] = Elem<T>::from_float(num);
+            float4 acc[kIters];
+#pragma unroll
+            for (int i = 0; i < kIters; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int r = 0; r < nrec; ++r) {
+              const float *rr = rec_of(cf + r);
+#pragma unroll
+              for (int i = 0; i < kIters; ++i) {
+                const int c = lane + 32 * i;
+                const int h = c / C4, d = (c % C4) * 4;
+                if (h < GT) {
+                  const float wr = sh_m[r * 8 + h];
+                  const float4 v = __ldcg(reinterpret_cast<const float4 *>(rr + h * R + d));
+                  acc[i].x += wr * v.x;
+                  acc[i].y += wr * v.y;
+                  acc[i].z += wr * v.z;
+                  acc[i].w += wr * v.w;
+                }
+              }
             }
-            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < kIters; ++i) {
+              const int c = lane + 32 * i;
+              const int h = c / C4, d = (c % C4) * 4;
+              if (h < GT) Elem<T>::store4(static_cast<T *>(a.out) + ((long long)s * a.Hq + hq0 + h) * D + d, acc[i]);
+            }
+            __syncwarp();  // sh_m / sh_l are reused by the next merge
           } else {
             // many records (or empty CTA ranges): per element, straight from the records
             for (int idx = lane; idx < GT * D; idx += 32) {
               const int h = idx / D;
               const int d = idx - h * D;
-              float M = -CUDART_INF_F;
+              float Mr = -CUDART_INF_F;
               for (int c = cf; c <= cl; ++c) {
                 if (W < N && range_start(c, W, N) == range_start(c + 1, W, N)) continue;
-                M = fmaxf(M, __ldcg(rec_of(c, h) + D));
+                Mr = fmaxf(Mr, __ldcg(rec_of(c) + h * R + D));
               }
-              float num = 0.f, den = 0.f;
+              float num = 0.f, dr = 0.f;
               for (int c = cf; c <= cl; ++c) {
                 if (W < N && range_start(c, W, N) == range_start(c + 1, W, N)) continue;
-                const float *rec = rec_of(c, h);
-                const float f = fast_exp2(__ldcg(rec + D) - M);
-                num += f * __ldcg(rec + d);
-                den += f * __ldcg(rec + D + 1);
+                const float *rr = rec_of(c) + h * R;
+                const float fr = fast_exp2(__ldcg(rr + D) - Mr);
+                num += fr * __ldcg(rr + d);
+                dr += fr * __ldcg(rr + D + 1);
               }
-              static_cast<T *>(a.out)[((long long)s * a.Hq + hq0 + h) * D + d] = Elem<T>::from_float(num / den);
+              static_cast<T *>(a.out)[((long long)s * a.Hq + hq0 + h) * D + d] = Elem<T>::from_float(num / dr);
             }
           }
         }
