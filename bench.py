@@ -270,26 +270,13 @@ def run_gpu(args) -> dict:
     # every rank runs its own replica of the workload on different data (weak scaling)
     inp = workload_inputs(args.workload, args.seed + rank, dev, args.num_seqs)
     S, Hq, D = inp.q.shape
-    Hkv, B = inp.k_cache.shape[1], inp.k_cache.shape[2]
-    out = torch.empty_like(inp.q)
-    ws = ops.new_workspace(S, Hq, Hkv, D, dev)
-    slots = torch.empty(inp.new_seq.numel(), dtype=torch.int64, device=dev)
-    err = ops.new_error_word(dev)
     stream = torch.cuda.current_stream(dev)
+    from paged_kv_cache_170_gb300.step import DecodeStep
 
-    def step(ev_a=None, ev_b=None):
-        if inp.copy_pairs.numel():
-            ops.pa_copy_blocks(inp.k_cache, inp.v_cache, inp.copy_pairs, err)
-        if inp.new_seq.numel():
-            ops.pa_slot_mapping(inp.block_tables, inp.new_seq, inp.new_pos, B, inp.k_cache.shape[0], slots, err)
-            ops.pa_write_kv(inp.new_key, inp.new_value, inp.k_cache, inp.v_cache, slots, err)
-        if ev_a is not None:
-            ev_a.record(stream)
-        ops.pa_decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale, out, ws, err)
-        if ev_b is not None:
-            ev_b.record(stream)
-
-    launches_per_step = (1 if inp.copy_pairs.numel() else 0) + (2 if inp.new_seq.numel() else 0) + 1
+    runner = DecodeStep(inp, graphs=not args.no_graph)
+    out, err = runner.out, runner.err
+    step = runner.run
+    launches_per_step = runner.launches_per_step
 
     for _ in range(args.warmup):
         step()
@@ -372,7 +359,9 @@ def run_gpu(args) -> dict:
         "vs_baseline": None,
         "dtype": {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}[inp.q.dtype],
         "data": "synthetic: seeded N(0,1) q/K/V, random physical placement",
-        "config": workload_config(args.workload, inp),
+        "config": dict(workload_config(args.workload, inp),
+                       step_launch="eager, kernel by kernel" if args.no_graph
+                       else "CUDA graphs: pre (copies, slots, write) then decode"),
         "tokens_per_s": round(sum_over_ranks(float(S), dist) / (step_ms_max * 1e-3), 0),
         "pct_of_nominal_8000_gbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / peaks["hbm_gbs"], 2),
@@ -457,6 +446,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-seqs", type=int, default=None, help="fewer sequences (profiling captures only)")
+    ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -21,6 +21,10 @@ SOURCES = ["pa_kv.cu", "pa_decode.cu", "pa_decode_f32.cu", "pa_decode_f16.cu", "
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 DEBUG = (["-DPA_DEBUG"] if os.environ.get("PA_DEBUG") == "1" else []) + \
     (["-DPA_TRACE"] if os.environ.get("PA_TRACE") == "1" else [])
+if os.environ.get("PA_TRACE") == "1" and os.environ.get("PA_TRACE_CTAS"):
+    # comma-separated CTA indices whose warps print their trace counters
+    _ctas = [int(c) for c in os.environ["PA_TRACE_CTAS"].split(",")]
+    DEBUG.append("-DPA_TRACE_CTA(c)=(" + "||".join(f"(c)=={c}" for c in _ctas) + ")")
 FLAGS = DEBUG + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]
 

@@ -81,7 +81,7 @@ struct DecodeShape {
   int G, GT, nctas;
   bool mma;
   size_t ring_bytes;
-  uint32_t slot_stride, tile_stride;
+  uint32_t slot_stride, tile_stride, q_offset, q_bytes;
   int nstage, ncw, pg;
 };
 
@@ -115,12 +115,15 @@ static pa_status check_decode_args(int max_blocks_per_seq, int num_seqs, int num
   shape->GT = pick_head_chunk(shape->G, shape->mma);
   shape->nctas = decode_grid();
   if (shape->nctas <= 0) return PA_ERR_CUDA;
-  // one ring slot holds the K tile and the V tile of one (block, kv head)
+  // one ring slot holds the K tile and the V tile of one (block, kv head);
+  // on the tensor-core path also room for the q rows of one pair chunk
   const size_t tile_bytes = size_t(block_size) * head_dim * dtype_bytes(dtype);
   const size_t align = shape->mma ? 1024 : 128;  // the swizzled tiles repeat every 1024 bytes
   shape->tile_stride = uint32_t((tile_bytes + align - 1) / align * align);
-  shape->slot_stride = 2 * shape->tile_stride;
-  shape->nstage = int(kRingBytes / shape->slot_stride);
+  shape->q_offset = 2 * shape->tile_stride;
+  shape->q_bytes = shape->mma ? uint32_t(shape->GT * head_dim * dtype_bytes(dtype)) : 0u;
+  shape->slot_stride = uint32_t((shape->q_offset + shape->q_bytes + align - 1) / align * align);
+  shape->nstage = int((shape->mma ? kRingBytesMma : kRingBytes) / shape->slot_stride);
   if (shape->nstage > kMaxStages) shape->nstage = kMaxStages;
   if (shape->nstage < 1) return PA_ERR_UNSUPPORTED;
   // consumer warps and producer group size with ncw + pg <= nstage (the ring's
@@ -231,6 +234,8 @@ extern "C" pa_status pa_decode(void *out, const void *q, const void *k_cache, co
   a.ncw = sh.ncw;
   a.pg = sh.pg;
   a.nops = 1;
+  a.q_offset = sh.q_offset;
+  a.q_bytes = sh.q_bytes;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (sh.mma) {
     return dtype == PA_BF16

@@ -34,7 +34,7 @@ pa_status launch_decode_mma(const DecodeArgs &a, const CUtensorMap &mk, const CU
                             cudaStream_t stream) {
   static int configured[64] = {0};
   auto kern = decode_partition_mma_kernel<T, D>;
-  if (!configure_once(kern, kRingBytes + 1024, configured)) return PA_ERR_CUDA;
+  if (!configure_once(kern, kRingBytesMma + 1024, configured)) return PA_ERR_CUDA;
   kern<<<a.nctas, kDecodeThreads, ring_bytes + 1024, stream>>>(a, mk, mv);
   return launch_status();
 }

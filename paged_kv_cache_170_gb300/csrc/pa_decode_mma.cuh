@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   __shared__ Plan sh_plan;
   __shared__ uint32_t issued[kMaxStages];
   __shared__ int sh_abort;
-  __shared__ __align__(8) uint64_t st_full, st_free;  // consumers -> merger hand-off of mrg
+  __shared__ __align__(8) uint64_t st_full[kConsumerWarps], st_free[kConsumerWarps];  // hand-off of mrg[w]
   __shared__ float sh_mw[2 * kMergeRecords * 8];
 
   const int warp = threadIdx.x >> 5;
@@ -66,14 +66,20 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   unsigned char *ring = ring_raw + pad;
   const uint32_t ring_addr = raw_addr + pad;
 
+#ifdef PA_TRACE
+  __shared__ unsigned long long tr_start;
+  if (threadIdx.x == 0) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tr_start));
+#endif
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.nstage; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
       issued[i] = 0;
     }
-    mbar_init(&st_full, kConsumerWarps);
-    mbar_init(&st_free, 1);
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      mbar_init(&st_full[w], 1);
+      mbar_init(&st_free[w], 1);
+    }
     sh_abort = 0;
     fence_barrier_init();
   }
@@ -102,7 +108,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     const long long tr_t0 = clock64();
 #endif
     produce(a, PC, HC, plan, lane, full_bar, empty_bar, issued, abort_flag,
-            [&](int slot, int p, int kvh, int bb, int L) {
+            [&](int slot, int p, int kvh, int bb, int L, int s, int pc, bool lead) {
               (void)bb;
               (void)L;
               if (p < 0 || p >= a.num_blocks) {
@@ -111,9 +117,16 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
                 return;
               }
               // K and V tiles of one (block, kv head) land in one slot; the full
-              // tile is copied (rows past the context are masked or zeroed later)
-              mbar_arrive_expect_tx(&full_bar[slot], 2 * tile_bytes);
+              // tile is copied (rows past the context are masked or zeroed later).
+              // A segment's lead entries also bring the chunk's q rows, so a
+              // consumer never waits on a global load when it starts a segment.
+              mbar_arrive_expect_tx(&full_bar[slot], 2 * tile_bytes + (lead ? a.q_bytes : 0u));
               unsigned char *dst = ring + size_t(slot) * a.slot_stride;
+              if (lead) {
+                long long qoff = ((long long)s * a.Hq + kvh * G + (pc % HC) * GT) * D;
+                PA_DBG_FIX(qoff >= 0 && qoff + (long long)GT * D <= (long long)a.S * a.Hq * D, kDbgGlobal, qoff = 0);
+                bulk_g2s(dst + a.q_offset, static_cast<const T *>(a.q) + qoff, a.q_bytes, &full_bar[slot]);
+              }
               int y = (p * a.Hkv + kvh) * B;
               PA_DBG_FIX(y >= 0 && (long long)y + B <= a.num_blocks * a.Hkv * B, kDbgTma, y = 0);
               PA_DBG_FIX(smem_addr(dst) + a.slot_stride <= ring_addr + a.nstage * a.slot_stride &&
@@ -131,7 +144,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
               }
             });
 #ifdef PA_TRACE
-    if (lane == 0 && (blockIdx.x % 101) == 0)
+    if (lane == 0 && PA_TRACE_CTA(blockIdx.x))
       printf("trace cta %d producer: cycles %lld\n", blockIdx.x, clock64() - tr_t0);
 #endif
     return;
@@ -139,8 +152,18 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
 
   if (warp == kMergerWarp) {
     // -------------------------------------------------------------- merger
-    run_merger<T, D>(a, plan, PC, HC, G, lane, &mrg[0][0][0], 8 * state_row(D), &st_full, &st_free, sh_mw, abort_flag);
+    run_merger<T, D, true>(a, plan, PC, HC, G, lane, &mrg[0][0][0], 8 * state_row(D), st_full, st_free, sh_mw,
+                           abort_flag);
     zero_empty_rows<T>(a, D, lane, 32);
+#ifdef PA_TRACE
+    if (lane == 0) {
+      unsigned long long t1;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+      unsigned smid;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+      printf("tracet %d %u %llu %llu %lld\n", blockIdx.x, smid, tr_start, t1, w1 - w0);
+    }
+#endif
     return;
   }
 
@@ -151,7 +174,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   const int mr = lane & 7;      // ldmatrix: which row of it
 
   long long j = 0;      // tiles, in this CTA's processing order
-  long long seg_k = 0;  // segments deposited to the merger
+  long long dep = 0;    // states this warp deposited for the merger
 #ifdef PA_TRACE
   long long tr_c0 = clock64(), tr_wk = 0, tr_tiles = 0, tr_seg = 0, tr_nseg = 0;
 #endif
@@ -170,7 +193,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
       const bool first_seg = (wk.w == w0);
       const int kvh = wk.pc / HC;
       const int hq0 = kvh * G + (wk.pc % HC) * GT;
-      const int L = clamped_len(a, wk.s);
+      const int L = wk.L;
 
       // running state: heads h0 = 2*c4 and h1 = 2*c4 + 1 of this lane
       float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
@@ -179,30 +202,18 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
       for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
       // this warp's first tile of the segment (warps >= ncw take none)
-      long long jj = warp < a.ncw ? j + ((warp - int(j % a.ncw)) + a.ncw) % a.ncw : j + n;
+      long long jj = warp < a.ncw ? j + ((warp - int(uint32_t(j) % uint32_t(a.ncw))) + a.ncw) % a.ncw : j + n;
+      const long long jj0 = jj;
       if (jj < j + n) {
-        // q^T fragment (B operand of QK): head g of the chunk, dims 16ks + 2*c4 (+1), (+8)
+        // q^T fragment (B operand of QK): head g of the chunk, dims 16ks + 2*c4
+        // (+1), (+8); taken from the slot of the warp's first tile (a lead entry)
         uint32_t qf[KS][2];
-        if (g < GT) {
-          long long qoff = ((long long)wk.s * a.Hq + hq0 + g) * D;
-          PA_DBG_FIX(qoff >= 0 && qoff + D <= (long long)a.S * a.Hq * D, kDbgGlobal, qoff = 0);
-          const T *qrow = static_cast<const T *>(a.q) + qoff;
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            qf[ks][0] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c4);
-            qf[ks][1] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * c4);
-          }
-        } else {
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks) qf[ks][0] = qf[ks][1] = 0u;
-        }
-
         for (; jj < j + n; jj += a.ncw) {
           const int bb = wk.b + int(jj - j);
           const int nv = min(B, L - bb * B);
           const int nsub = (nv + 15) >> 4;
-          const long long ee = jj;  // the pair's ring entry
-          const int slot = int(ee % a.nstage);
+          const uint32_t ee = uint32_t(jj);  // the pair's ring entry (a CTA's count fits 32 bits)
+          const int slot = int(ee % uint32_t(a.nstage));
           const uint32_t kt = ring_addr + uint32_t(slot) * a.slot_stride;
           const uint32_t vt = kt + a.tile_stride;
 
@@ -216,7 +227,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
           ++tr_tiles;
 #endif
 #ifdef PA_DEBUG
-          if (okE && lane == 0 && mbar_try_wait(&full_bar[slot], (uint32_t(ee / a.nstage) & 1u) ^ 1u)) {
+          if (okE && lane == 0 && mbar_try_wait(&full_bar[slot], ((ee / uint32_t(a.nstage)) & 1u) ^ 1u)) {
             raise_error(a.err, kDbgPhase);  // the barrier ran two phases ahead of this entry
             printf("pagedkv phase ahead: cta %d warp %d entry %lld slot %d\n", blockIdx.x, warp, ee, slot);
           }
@@ -233,6 +244,14 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
           // Lanes leave the wait loop at different iterations: reconverge before
           // the warp-collective ldmatrix / mma.sync.aligned below.
           __syncwarp();
+          if (jj == jj0) {
+            const unsigned char *qs = ring + size_t(slot) * a.slot_stride + a.q_offset;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+              qf[ks][0] = g < GT ? *reinterpret_cast<const uint32_t *>(qs + (g * D + 16 * ks + 2 * c4) * 2) : 0u;
+              qf[ks][1] = g < GT ? *reinterpret_cast<const uint32_t *>(qs + (g * D + 16 * ks + 8 + 2 * c4) * 2) : 0u;
+            }
+          }
 
           // ---- QK: scores of up to 4 sub-tiles of 16 tokens
           float sc[4][4];
@@ -342,37 +361,57 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
 #ifdef PA_TRACE
       const long long tr_s0 = clock64();
 #endif
-      // ---- hand this warp's state for the segment to the merger warp
+      // ---- this warp's state for the segment: written out directly when the
+      // warp alone covered a whole (s, pc), else handed to the merger warp
+      if (jj0 < j + n) {
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(kFullMask, l0, off);
-        l1 += __shfl_xor_sync(kFullMask, l1, off);
+        for (int off = 4; off < 32; off <<= 1) {
+          l0 += __shfl_xor_sync(kFullMask, l0, off);
+          l1 += __shfl_xor_sync(kFullMask, l1, off);
+        }
+        const int h0 = 2 * c4, h1 = 2 * c4 + 1;
+        if (complete && __popc(participants(j, n, a.ncw)) == 1) {
+          // same arithmetic as the merger's one-state combine: o * (1 / l)
+          const float i0 = 1.f / l0, i1 = 1.f / l1;
+          T *orow = static_cast<T *>(a.out) + ((long long)wk.s * a.Hq + hq0) * D;
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            if (h0 < GT) {
+              orow[h0 * D + 16 * mt + g] = Elem<T>::from_float(o[mt][0] * i0);
+              orow[h0 * D + 16 * mt + g + 8] = Elem<T>::from_float(o[mt][2] * i0);
+            }
+            if (h1 < GT) {
+              orow[h1 * D + 16 * mt + g] = Elem<T>::from_float(o[mt][1] * i1);
+              orow[h1 * D + 16 * mt + g + 8] = Elem<T>::from_float(o[mt][3] * i1);
+            }
+          }
+        } else {
+          deposit_state(a, dep, lane, &st_full[warp], &st_free[warp], abort_flag, [&]() {
+            if (g == 0) {
+              if (h0 < GT) {
+                mrg[warp][h0][D] = m0;
+                mrg[warp][h0][D + 1] = l0;
+              }
+              if (h1 < GT) {
+                mrg[warp][h1][D] = m1;
+                mrg[warp][h1][D + 1] = l1;
+              }
+            }
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+              if (h0 < GT) {
+                mrg[warp][h0][16 * mt + g] = o[mt][0];
+                mrg[warp][h0][16 * mt + g + 8] = o[mt][2];
+              }
+              if (h1 < GT) {
+                mrg[warp][h1][16 * mt + g] = o[mt][1];
+                mrg[warp][h1][16 * mt + g + 8] = o[mt][3];
+              }
+            }
+          });
+          ++dep;
+        }
       }
-      const int h0 = 2 * c4, h1 = 2 * c4 + 1;
-      deposit_state(a, seg_k, lane, &st_full, &st_free, abort_flag, [&]() {
-        if (g == 0) {
-          if (h0 < GT) {
-            mrg[warp][h0][D] = m0;
-            mrg[warp][h0][D + 1] = l0;
-          }
-          if (h1 < GT) {
-            mrg[warp][h1][D] = m1;
-            mrg[warp][h1][D + 1] = l1;
-          }
-        }
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          if (h0 < GT) {
-            mrg[warp][h0][16 * mt + g] = o[mt][0];
-            mrg[warp][h0][16 * mt + g + 8] = o[mt][2];
-          }
-          if (h1 < GT) {
-            mrg[warp][h1][16 * mt + g] = o[mt][1];
-            mrg[warp][h1][16 * mt + g + 8] = o[mt][3];
-          }
-        }
-      });
-      ++seg_k;
 #ifdef PA_TRACE
       tr_seg += clock64() - tr_s0;
       ++tr_nseg;
@@ -382,7 +421,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     }
   }
 #ifdef PA_TRACE
-  if (lane == 0 && (blockIdx.x % 101) == 0)
+  if (lane == 0 && PA_TRACE_CTA(blockIdx.x))
     printf("trace cta %d warp %d: tiles %lld cycles %lld waiting %lld segment-ends %lld (%lld cycles)\n",
            blockIdx.x, warp, tr_tiles, clock64() - tr_c0, tr_wk, tr_nseg, tr_seg);
 #endif

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
   __shared__ Plan sh_plan;
   __shared__ uint32_t issued[kMaxStages];
   __shared__ int sh_abort;
-  __shared__ __align__(8) uint64_t st_full, st_free;  // consumers -> merger hand-off of mrg
+  __shared__ __align__(8) uint64_t st_full[kConsumerWarps], st_free[kConsumerWarps];  // hand-off of mrg[w]
   __shared__ float sh_mw[2 * kMergeRecords * 8];
 
   const int warp = threadIdx.x >> 5;
@@ -115,8 +115,10 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
       mbar_init(&empty_bar[i], 1);
       issued[i] = 0;
     }
-    mbar_init(&st_full, kConsumerWarps);
-    mbar_init(&st_free, 1);
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      mbar_init(&st_full[w], 1);
+      mbar_init(&st_free[w], 1);
+    }
     sh_abort = 0;
     fence_barrier_init();
   }
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     produce(a, PC, HC, plan, lane, full_bar, empty_bar, issued, abort_flag,
-            [&](int slot, int p, int kvh, int bb, int L) {
+            [&](int slot, int p, int kvh, int bb, int L, int, int, bool) {
               if (p < 0 || p >= a.num_blocks) {
                 raise_error(a.err, PA_DEVERR_BLOCK_ID);
                 mbar_arrive(&full_bar[slot]);  // complete the phase without data
@@ -159,7 +161,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
 
   if (warp == kMergerWarp) {
     // -------------------------------------------------------------- merger
-    run_merger<T, D>(a, plan, PC, HC, G, lane, &mrg[0][0][0], GT * state_row(D), &st_full, &st_free, sh_mw, abort_flag);
+    run_merger<T, D, false>(a, plan, PC, HC, G, lane, &mrg[0][0][0], GT * state_row(D), st_full, st_free, sh_mw,
+                            abort_flag);
     zero_empty_rows<T>(a, D, lane, 32);
     return;
   }
@@ -171,7 +174,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
   // Softmax state (m_mine, l_mine) of a lane belongs to head lane % GT.
 
   long long j = 0;      // tiles, in this CTA's processing order
-  long long seg_k = 0;  // segments deposited to the merger
+  long long dep = 0;    // states this warp deposited for the merger
   // rotated processing order (see Plan)
   for (int ph = 0; ph < 2; ++ph) {
     long long from, to;
@@ -189,7 +192,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
       const bool first_seg = (w == w0);
       const int kvh = pc / HC;
       const int hq0 = kvh * G + (pc % HC) * GT;
-      const int L = clamped_len(a, s);
+      const int L = wk.L;
 
       float m_mine = -CUDART_INF_F;
       float l_mine = 0.f;
@@ -200,7 +203,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
         for (int i = 0; i < C::DPV / 2; ++i) acc[h][i] = make_float2(0.f, 0.f);
 
       // this warp's first tile of the segment (warps >= ncw take none)
-      long long jj = warp < a.ncw ? j + ((warp - int(j % a.ncw)) + a.ncw) % a.ncw : j + n;
+      long long jj = warp < a.ncw ? j + ((warp - int(uint32_t(j) % uint32_t(a.ncw))) + a.ncw) % a.ncw : j + n;
+      const long long jj0 = jj;
       if (jj < j + n) {
         // q slice of this lane, pre-scaled so scores come out in log2 units
         float2 qreg[GT][C::DPL / 2];
@@ -220,8 +224,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
         for (; jj < j + n; jj += a.ncw) {
           const int bb = b + int(jj - j);
           const int nv = min(B, L - bb * B);
-          const long long ee = jj;  // the pair's ring entry
-          const int slot = int(ee % a.nstage);
+          const uint32_t ee = uint32_t(jj);  // the pair's ring entry (a CTA's count fits 32 bits)
+          const int slot = int(ee % uint32_t(a.nstage));
           const char *kt = reinterpret_cast<const char *>(ring) + size_t(slot) * a.slot_stride;
           const char *vt = kt + a.tile_stride;
 
@@ -309,24 +313,27 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
         }
       }
 
-      // ---- hand this warp's state for the segment to the merger warp
-      float lsum = l_mine;
+      // ---- hand this warp's state for the segment to the merger warp (only
+      // warps that took a tile of it)
+      if (jj0 < j + n) {
+        float lsum = l_mine;
 #pragma unroll
-      for (int off = GT; off < 32; off <<= 1) lsum += __shfl_xor_sync(kFullMask, lsum, off);
-      deposit_state(a, seg_k, lane, &st_full, &st_free, abort_flag, [&]() {
-        if (lane < GT) {
-          mrg[warp][lane][D] = m_mine;
-          mrg[warp][lane][D + 1] = lsum;
-        }
-#pragma unroll
-        for (int h = 0; h < GT; ++h)
-#pragma unroll
-          for (int i = 0; i < C::DPV / 2; ++i) {
-            mrg[warp][h][lane * C::DPV + 2 * i] = acc[h][i].x;
-            mrg[warp][h][lane * C::DPV + 2 * i + 1] = acc[h][i].y;
+        for (int off = GT; off < 32; off <<= 1) lsum += __shfl_xor_sync(kFullMask, lsum, off);
+        deposit_state(a, dep, lane, &st_full[warp], &st_free[warp], abort_flag, [&]() {
+          if (lane < GT) {
+            mrg[warp][lane][D] = m_mine;
+            mrg[warp][lane][D + 1] = lsum;
           }
-      });
-      ++seg_k;
+#pragma unroll
+          for (int h = 0; h < GT; ++h)
+#pragma unroll
+            for (int i = 0; i < C::DPV / 2; ++i) {
+              mrg[warp][h][lane * C::DPV + 2 * i] = acc[h][i].x;
+              mrg[warp][h][lane * C::DPV + 2 * i + 1] = acc[h][i].y;
+            }
+        });
+        ++dep;
+      }
       j += n;
       wk.advance(a, n, PC);
     }

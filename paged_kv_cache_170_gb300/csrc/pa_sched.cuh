@@ -16,6 +16,12 @@
 
 #include "pa_common.cuh"
 
+#ifdef PA_TRACE
+#ifndef PA_TRACE_CTA
+#define PA_TRACE_CTA(c) ((c) % 101 == 0)  // CTAs whose warps print their counters
+#endif
+#endif
+
 namespace pagedkv {
 
 constexpr int kConsumerWarps = 4;
@@ -25,7 +31,8 @@ constexpr int kDecodeThreads = (kConsumerWarps + 2) * 32;
 constexpr int kCtasPerSm = 2;
 constexpr int kMaxStages = 64;
 constexpr int kMaxBlockSize = 64;
-constexpr int kRingBytes = 80 * 1024;
+constexpr int kRingBytes = 80 * 1024;      // CUDA-core kernel: ring of K + V tile pairs
+constexpr int kRingBytesMma = 90 * 1024;   // tensor-core kernel: K + V tiles + the segment's q rows
 constexpr int kMergeRecords = 32;  // records whose merge weights are staged in shared memory
 
 struct DecodeArgs {
@@ -50,6 +57,8 @@ struct DecodeArgs {
   int ncw;                 // consumer warps that take tiles
   int pg;                  // ring entries the producer issues at once (ncw + pg <= nstage)
   int nops;                // tensor copies per tile (1: one 3-D box; 2: two 2-D halves)
+  uint32_t q_offset;       // tensor-core kernel: offset of the q rows inside a slot
+  uint32_t q_bytes;        // tensor-core kernel: bytes of q rows of one pair chunk (GT * D * e)
 };
 
 // Wait until ring entry e (slot e % nstage, its u-th use, u = e / nstage) has
@@ -63,10 +72,10 @@ struct DecodeArgs {
 // finished every group of pg entries before the one holding e - ncw, which
 // includes e - nstage when ncw + pg <= nstage, and issuing e - nstage
 // required use u - 2 to be released.
-__device__ __forceinline__ bool wait_entry(uint64_t *full, uint64_t *empty, long long e, int nstage,
+__device__ __forceinline__ bool wait_entry(uint64_t *full, uint64_t *empty, uint32_t e, int nstage,
                                            volatile int *abort) {
-  const int slot = int(e % nstage);
-  const uint32_t u = uint32_t(e / nstage);
+  const int slot = int(e % uint32_t(nstage));
+  const uint32_t u = e / uint32_t(nstage);
   if (u > 0 && !mbar_wait(&empty[slot], (u - 1) & 1u, abort)) return false;
   return mbar_wait(&full[slot], u & 1u, abort);
 }
@@ -178,11 +187,12 @@ __device__ __forceinline__ bool phase_range(const Plan &p, int ph, long long *fr
 // Cursor over a CTA's tile range, one segment (consecutive tiles of one
 // (s, pc)) at a time.  Producer and consumers walk identical sequences.
 struct Walk {
-  int s, pc, b, nb;
+  int s, pc, b, nb, L;  // L: clamped context length of s (read once per sequence)
   long long w;
   __device__ __forceinline__ void start(const DecodeArgs &a, int s0, long long r0, long long w0) {
     s = s0;
-    nb = blocks_of(a, s);
+    L = clamped_len(a, s);
+    nb = (L + a.B - 1) / a.B;
     pc = int(r0 / nb);
     b = int(r0 % nb);
     w = w0;
@@ -200,7 +210,10 @@ struct Walk {
         do {
           ++s;
         } while (s < a.S && blocks_of(a, s) == 0);
-        if (s < a.S) nb = blocks_of(a, s);
+        if (s < a.S) {
+          L = clamped_len(a, s);
+          nb = (L + a.B - 1) / a.B;
+        }
       }
     }
   }
@@ -210,9 +223,12 @@ struct Walk {
 // at a time (coalesced, next batch prefetched, kept in registers: never
 // re-read per token) and fills the ring.  Entries are issued in groups of pg:
 // lane i < pg claims entry e + i (waits until its slot's previous use was
-// released) and calls issue(slot, pid, kv head, logical block, context len),
-// which announces the bytes on full_bar[slot] and starts the copies; the lanes
-// of a group wait and issue in parallel.  issued[slot] keeps the last use
+// released) and calls issue(slot, pid, kv head, logical block, context len,
+// s, pc, lead), which announces the bytes on full_bar[slot] and starts the
+// copies; the lanes of a group wait and issue in parallel.  `lead` marks the
+// first ncw entries of a segment: every consumer warp that takes part in the
+// segment meets one of them first, so a kernel can ship per-segment data
+// (the q rows) with those entries only.  issued[slot] keeps the last use
 // issued into each slot so the producer can wait for every copy still in
 // flight before it leaves (after an abort too).
 template <class Issue>
@@ -221,6 +237,9 @@ __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, con
                                         volatile int *abort_flag, Issue issue) {
   long long e = 0;
   bool aborted = false;
+#ifdef PA_TRACE
+  long long tr_t0 = clock64(), tr_tab = 0, tr_empty = 0, tr_segs = 0;
+#endif
   for (int ph = 0; ph < 2 && !aborted; ++ph) {
     long long from, to;
     if (!phase_range(plan, ph, &from, &to)) continue;
@@ -232,9 +251,17 @@ __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, con
     while (wk.w < to && !aborted) {
       const int n = wk.seg_len(to);
       const int kvh = wk.pc / HC;
-      const int L = clamped_len(a, wk.s);
+      const int L = wk.L;
       const int32_t *trow = a.tables + (long long)wk.s * a.max_blocks + wk.b;
       int pid_next = lane < n ? trow[lane] : -1;
+#ifdef PA_TRACE
+      {
+        const long long t = clock64();
+        pid_next = __shfl_sync(kFullMask, pid_next, lane);  // wait for the table load
+        tr_tab += clock64() - t;
+        ++tr_segs;
+      }
+#endif
       for (int base = 0; base < n && !aborted; base += 32) {
         const int pid_cur = pid_next;
         const int cnt = min(32, n - base);
@@ -244,13 +271,19 @@ __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, con
           const int p = __shfl_sync(kFullMask, pid_cur, t < 32 ? t : 31);
           bool fail = false;
           if (lane < a.pg && t < cnt) {
-            const long long me = e + lane;
-            const int slot = int(me % a.nstage);
-            const uint32_t u = uint32_t(me / a.nstage);
+            const uint32_t me = uint32_t(e) + uint32_t(lane);  // a CTA's entry count fits 32 bits
+            const int slot = int(me % uint32_t(a.nstage));
+            const uint32_t u = me / uint32_t(a.nstage);
+#ifdef PA_TRACE
+            const long long t = clock64();
+#endif
             if (*abort_flag || (u > 0 && !mbar_wait(&empty_bar[slot], (u - 1) & 1u, abort_flag))) {
               fail = true;
             } else {
-              issue(slot, p, kvh, wk.b + base + t, L);
+#ifdef PA_TRACE
+              if (lane == 0) tr_empty += clock64() - t;
+#endif
+              issue(slot, p, kvh, wk.b + base + t, L, wk.s, wk.pc, base + t < a.ncw);
               issued[slot] = u + 1;
             }
           }
@@ -268,6 +301,11 @@ __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, con
       wk.advance(a, n, PC);
     }
   }
+#ifdef PA_TRACE
+  if (lane == 0 && PA_TRACE_CTA(blockIdx.x))
+    printf("trace cta %d producer: segments %lld cycles %lld table-wait %lld slot-wait(lane0) %lld\n", blockIdx.x,
+           tr_segs, clock64() - tr_t0, tr_tab, tr_empty);
+#endif
   // Do not leave while a copy into this CTA's shared memory is in flight:
   // only the last use issued into a slot can be (earlier ones were released,
   // which needs them landed).
@@ -288,6 +326,15 @@ __device__ __forceinline__ int cta_of(long long x, long long W, int N) {
 
 __device__ __forceinline__ long long range_start(int c, long long W, int N) { return (long long)c * W / N; }
 
+// Consumer warps that take at least one tile of the segment [j, j + n) of a
+// CTA's processing order (tile j goes to warp j % ncw), as a bit mask.
+__device__ __forceinline__ unsigned participants(long long j, int n, int ncw) {
+  if (n >= ncw) return (1u << ncw) - 1u;
+  const int w0 = int(uint32_t(j) % uint32_t(ncw));  // a CTA's tile count fits 32 bits
+  const unsigned run = (1u << n) - 1u;
+  return ((run << w0) | (run >> (ncw - w0))) & ((1u << ncw) - 1u);
+}
+
 // Zero output rows of the sequences with nothing cached, spread over CTAs.
 template <typename T>
 __device__ __forceinline__ void zero_empty_rows(const DecodeArgs &a, int D, int tid, int nthreads) {
@@ -303,21 +350,27 @@ __device__ __forceinline__ void zero_empty_rows(const DecodeArgs &a, int D, int 
 __host__ __device__ constexpr int state_row(int D) { return D + 4; }
 
 // The merger warp.  It walks the same plan as the consumers, one segment at
-// a time: waits until the four consumer warps have deposited their running
-// states (acc[D], m, l per head; head stride state_row(D), warp stride
-// warp_stride) in `mrg` (mbarrier st_full, four arrivals), combines them,
+// a time.  Only the consumer warps that took a tile of a segment (the
+// participants) hand it a state: warp w deposits (acc[D], m, l per head; head
+// stride state_row(D), warp stride warp_stride) in its own buffer of `mrg` and
+// arrives on st_full[w]; the merger waits for the participants, combines
 //     M = max_w m_w;  num = sum_w 2^(m_w - M) acc_w;  den = sum_w 2^(m_w - M) l_w,
 // and writes num / den as the output rows (the segment is a whole (s, pc)) or
 // this CTA's partial record (num, M, den) for a (s, pc) cut by a range
-// boundary, then hands the buffer back (st_free).  For a cut (s, pc) it counts
-// this CTA in; the CTA that completes the count merges the records of all CTAs
-// that share the pair (the a5 step) and sets the counter back to zero:
+// boundary, then hands each buffer back (st_free[w]).  Each warp has its own
+// pair of barriers, so warps never wait for one another's segments: a run of
+// one-tile segments (short sequences) spreads over the four warps.  With
+// kSoloWrites, a whole (s, pc) taken by a single warp is normalised and
+// written by that warp and never reaches the merger.  For a cut (s, pc) the
+// merger counts this CTA in; the CTA that completes the count merges the
+// records of all CTAs that share the pair (the a5 step) and sets the counter
+// back to zero:
 //     M = max_r m_r;  out = sum_r 2^(m_r - M) acc_r / sum_r 2^(m_r - M) l_r.
 // Running this off the consumer warps keeps every fence, atomic and remote
 // read of a segment end out of the streaming path.  The weights are formed
 // once per (warp or record, head); the rows then move as 16-byte vectors, so
 // a merge costs one L2 round trip per record rather than one per element.
-template <typename T, int D>
+template <typename T, int D, bool kSoloWrites>
 __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan, int PC, int HC, int G, int lane,
                                            const float *mrg, int warp_stride, uint64_t *st_full, uint64_t *st_free,
                                            float *sh_w, volatile int *abort_flag) {
@@ -331,6 +384,8 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
   const int lh = lane >> 2, lq = lane & 3;  // the (head, warp) whose weight this lane forms
   float *sh_m = sh_w, *sh_l = sh_w + kMergeRecords * 8;
   long long k = 0;  // segments handled
+  long long j = 0;  // tiles before the current segment, in processing order
+  uint32_t taken[kConsumerWarps] = {0u, 0u, 0u, 0u};  // deposits taken from each warp
 #ifdef PA_TRACE
   long long tr_t0 = clock64(), tr_wait = 0;
 #endif
@@ -351,27 +406,37 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
 #ifdef PA_TRACE
       const long long tr_w0 = clock64();
 #endif
-      if (!mbar_wait(st_full, uint32_t(k) & 1u, abort_flag)) {
-        if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
-        *abort_flag = 1;
+      const unsigned pm = participants(j, n, a.ncw);
+      if (kSoloWrites && complete && __popc(pm) == 1) {  // the warp wrote the rows itself
+        j += n;
+        wk.advance(a, n, PC);
+        continue;
+      }
+#pragma unroll
+      for (int q = 0; q < kConsumerWarps; ++q) {
+        if (((pm >> q) & 1u) && !mbar_wait(&st_full[q], taken[q] & 1u, abort_flag)) {
+          if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+        }
       }
 #ifdef PA_TRACE
       tr_wait += clock64() - tr_w0;
 #endif
       __syncwarp();
-      // ---- combine the four warps' states: weights per (warp, head) ...
+      // ---- combine the participants' states: weights per (warp, head) ...
+      const bool mine = lh < GT && ((pm >> lq) & 1u);
       float m = -CUDART_INF_F, l = 0.f;
-      if (lh < GT) {
+      if (mine) {
         m = mrg[lq * warp_stride + lh * R + D];
         l = mrg[lq * warp_stride + lh * R + D + 1];
       }
       float M = fmaxf(m, __shfl_xor_sync(kFullMask, m, 1));
       M = fmaxf(M, __shfl_xor_sync(kFullMask, M, 2));
-      const float f = lh < GT ? fast_exp2(m - M) : 0.f;
+      const float f = mine ? fast_exp2(m - M) : 0.f;
       float den = f * l;
       den += __shfl_xor_sync(kFullMask, den, 1);
       den += __shfl_xor_sync(kFullMask, den, 2);
-      const float wt = complete ? (lh < GT ? f / den : 0.f) : f;
+      const float wt = complete ? (mine ? f / den : 0.f) : f;
       float *rec = nullptr;
       if (!complete) {
         long long ro = ((long long)blockIdx.x * 2 + (first_seg ? 0 : 1)) * 8 * R;
@@ -394,6 +459,7 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int q = 0; q < kConsumerWarps; ++q) {
+            if (!((pm >> q) & 1u)) continue;  // a buffer that got no state this segment
             const float4 v = *reinterpret_cast<const float4 *>(mrg + q * warp_stride + h * R + d);
             acc.x += w[q] * v.x;
             acc.y += w[q] * v.y;
@@ -410,7 +476,13 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(st_free);  // the consumers may overwrite mrg now
+#pragma unroll
+      for (int q = 0; q < kConsumerWarps; ++q) {
+        if ((pm >> q) & 1u) {
+          if (lane == 0) mbar_arrive(&st_free[q]);  // warp q may overwrite its buffer now
+          ++taken[q];
+        }
+      }
       if (!complete) {
         // ---- count this CTA in; the last of the pair's CTAs merges
         __threadfence();  // publish this CTA's record before it is counted
@@ -517,23 +589,25 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
         }
       }
       ++k;
+      j += n;
       wk.advance(a, n, PC);
     }
   }
 #ifdef PA_TRACE
-  if (lane == 0 && (blockIdx.x % 101) == 0)
+  if (lane == 0 && PA_TRACE_CTA(blockIdx.x))
     printf("trace cta %d merger: segments %lld cycles %lld waiting %lld\n", blockIdx.x, k, clock64() - tr_t0, tr_wait);
 #endif
 }
 
-// A consumer warp's end of a segment: wait until the merger took the previous
-// segment's states (mbarrier st_free, phase k - 1: the merger hands buffers
-// back in order, so the parity test is exact), then let `write` store this
-// warp's state into the buffer and announce it (st_full).
+// A consumer warp's hand-off of its state for a segment it took tiles of:
+// wait until the merger took this warp's previous deposit (its st_free, phase
+// dep - 1: the merger frees one warp's deposits in order, so the parity test
+// is exact), then let `write` store the state into the warp's buffer and
+// announce it (its st_full).
 template <class Write>
-__device__ __forceinline__ void deposit_state(const DecodeArgs &a, long long k, int lane, uint64_t *st_full,
+__device__ __forceinline__ void deposit_state(const DecodeArgs &a, long long dep, int lane, uint64_t *st_full,
                                               uint64_t *st_free, volatile int *abort_flag, Write write) {
-  if (k > 0 && !mbar_wait(st_free, uint32_t(k - 1) & 1u, abort_flag)) {
+  if (dep > 0 && !mbar_wait(st_free, uint32_t(dep - 1) & 1u, abort_flag)) {
     if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
     *abort_flag = 1;
   }

@@ -1,0 +1,91 @@
+"""A whole decode step recorded once as CUDA graphs and replayed.
+
+One step is: copy-on-write block copies (when the step has any), slot lookup of
+the new tokens, their K/V write, then split-context decode attention over every
+sequence.  Launched one by one from Python, each call pays host-side argument
+checks and a launch, and the GPU idles whenever the host falls behind; small
+batches are then launch-bound.  Here the step's kernels are captured into two
+CUDA graphs on first use: ``pre`` (copies, slots, write) and ``decode``.  A
+replay launches them back to back with no host work in between.  Two graphs
+rather than one so a caller can put CUDA events around the decode alone.
+
+The graphs hold the device addresses of the step's tensors, so the caller
+updates inputs in place (``q``, ``new_key`` / ``new_value``, the tables, ...)
+and must not reallocate them.  Shapes are fixed at capture: a different batch
+needs a new ``DecodeStep``.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import ops
+
+
+class DecodeStep:
+    """The decode step of one set of resident inputs, as CUDA graphs.
+
+    ``inp`` carries q, k_cache, v_cache, block_tables, context_lens, scale,
+    new_key, new_value, new_seq, new_pos and copy_pairs (the layout of
+    ``workloads.DecodeInputs``).  ``graphs=False`` launches the kernels one by
+    one instead (same results, for comparison).
+    """
+
+    def __init__(self, inp, graphs: bool = True):
+        self.inp = inp
+        dev = inp.q.device
+        S, Hq, D = inp.q.shape
+        Hkv = inp.k_cache.shape[1]
+        self.out = torch.empty_like(inp.q)
+        self.workspace = ops.new_workspace(S, Hq, Hkv, D, dev)
+        self.slots = torch.empty(inp.new_seq.numel(), dtype=torch.int64, device=dev)
+        self.err = ops.new_error_word(dev)
+        self.launches_per_step = (1 if inp.copy_pairs.numel() else 0) + (2 if inp.new_seq.numel() else 0) + 1
+        self.graphs = graphs
+        self._pre: Optional[torch.cuda.CUDAGraph] = None
+        self._dec: Optional[torch.cuda.CUDAGraph] = None
+        if graphs:
+            # one eager pass first: the library sets its kernels' attributes and
+            # caches device properties outside the capture
+            self._run_pre()
+            self._run_decode()
+            torch.cuda.synchronize(dev)
+            self._pre = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self._pre):
+                self._run_pre()
+            self._dec = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self._dec):
+                self._run_decode()
+
+    def _run_pre(self):
+        inp = self.inp
+        if inp.copy_pairs.numel():
+            ops.pa_copy_blocks(inp.k_cache, inp.v_cache, inp.copy_pairs, self.err)
+        if inp.new_seq.numel():
+            ops.pa_slot_mapping(inp.block_tables, inp.new_seq, inp.new_pos, inp.k_cache.shape[2],
+                                inp.k_cache.shape[0], self.slots, self.err)
+            ops.pa_write_kv(inp.new_key, inp.new_value, inp.k_cache, inp.v_cache, self.slots, self.err)
+
+    def _run_decode(self):
+        inp = self.inp
+        ops.pa_decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale, self.out,
+                      self.workspace, self.err)
+
+    def run(self, ev_decode_start=None, ev_decode_end=None) -> torch.Tensor:
+        """Enqueue one step on the current stream; optional events bracket the
+        decode.  Returns ``out`` (written when the stream reaches it)."""
+        stream = torch.cuda.current_stream(self.inp.q.device)
+        if self._pre is not None:
+            self._pre.replay()
+        else:
+            self._run_pre()
+        if ev_decode_start is not None:
+            ev_decode_start.record(stream)
+        if self._dec is not None:
+            self._dec.replay()
+        else:
+            self._run_decode()
+        if ev_decode_end is not None:
+            ev_decode_end.record(stream)
+        return self.out
