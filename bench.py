@@ -273,7 +273,7 @@ def run_gpu(args) -> dict:
     stream = torch.cuda.current_stream(dev)
     from paged_kv_cache_170_gb300.step import DecodeStep
 
-    runner = DecodeStep(inp, graphs=not args.no_graph)
+    runner = DecodeStep(inp, graphs=not args.no_graph, shared=args.shared)
     out, err = runner.out, runner.err
     step = runner.run
     launches_per_step = runner.launches_per_step
@@ -316,12 +316,16 @@ def run_gpu(args) -> dict:
     host = {n: getattr(inp, n).cpu().pin_memory() for n in
             ("q", "new_key", "new_value", "new_seq", "new_pos", "block_tables", "context_lens", "copy_pairs")}
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    plan_host = runner.plan.pin_memory() if args.shared else None  # the plan travels with the tables
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + \
+        (plan_host.numel() * plan_host.element_size() if args.shared else 0)
     d2h = out_host.numel() * out_host.element_size()
 
     def e2e_step():
         for n, t in host.items():
             getattr(inp, n).copy_(t, non_blocking=True)
+        if args.shared:
+            runner.plan_dev.copy_(plan_host, non_blocking=True)
         step()
         out_host.copy_(out, non_blocking=True)
 
@@ -361,7 +365,10 @@ def run_gpu(args) -> dict:
         "data": "synthetic: seeded N(0,1) q/K/V, random physical placement",
         "config": dict(workload_config(args.workload, inp),
                        step_launch="eager, kernel by kernel" if args.no_graph
-                       else "CUDA graphs: pre (copies, slots, write) then decode"),
+                       else "CUDA graphs: pre (copies, slots, write) then decode",
+                       decode="pa_decode_shared (plan: %d groups, %d pieces)" % (
+                           runner.plan_info["num_groups"], runner.plan_info["num_pieces"]) if args.shared
+                       else "pa_decode"),
         "tokens_per_s": round(sum_over_ranks(float(S), dist) / (step_ms_max * 1e-3), 0),
         "pct_of_nominal_8000_gbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / peaks["hbm_gbs"], 2),
@@ -447,6 +454,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-seqs", type=int, default=None, help="fewer sequences (profiling captures only)")
     ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one")
+    ap.add_argument("--shared", action="store_true",
+                    help="decode with pa_decode_shared (each shared block read once per group of sharers)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -186,6 +186,65 @@ PA_API pa_status pa_decode_noalloc(void *out, const void *q, const void *k_cache
                                    float scale, pa_dtype dtype, int *debug_err,
                                    void *stream);
 
+/*
+ * Plan of a shared-block decode (host, no GPU work).  Sequences that hold the
+ * same physical blocks for a common history -- forks of one prompt, whose
+ * shared blocks the prefix-sharing passages keep read-only under reference
+ * counts (aiqz.cc, section "前缀共享机制"; cf-1.com news/5879632, section
+ * 4.1) -- are found from the block tables: groups of two or more sequences
+ * whose tables agree on a run of blocks that are full for every member.  The
+ * pages read a shared block once per sharer; pa_decode_shared reads it once
+ * per group.  The plan also splits the groups' work evenly over `nctas` CTAs
+ * (pass pa_decode_grid_size()).
+ *
+ * block_tables, context_lens: HOST int32 arrays [num_seqs][max_blocks_per_seq]
+ * and [num_seqs], the same contents the decode will see.  plan: host int32
+ * buffer of plan_capacity ints, or NULL to only compute the size.  On return
+ * *plan_ints holds the plan's size in ints; PA_ERR_WORKSPACE if plan_capacity
+ * is smaller.  The plan stays valid while the tables and lengths keep those
+ * contents (or change only in private blocks of the same count) and for the
+ * same head counts and nctas.
+ */
+PA_API pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *context_lens, int num_seqs, int block_size,
+                               int num_heads, int num_kv_heads, int nctas, int32_t *plan,
+                               size_t plan_capacity, size_t *plan_ints);
+
+/*
+ * Bytes of device workspace pa_decode_shared needs with this plan (host copy)
+ * on the current device; 0 for invalid arguments.
+ */
+PA_API size_t pa_decode_shared_workspace_size(const int32_t *plan_host, int num_seqs,
+                                              int num_heads, int num_kv_heads, int head_dim);
+
+/*
+ * pa_decode with each shared block read once per group of sharers.  Same
+ * arguments and the same result (up to fp32 rounding order) as pa_decode,
+ * plus the plan that pa_share_plan built from these tables: plan_host (host
+ * copy, read for its sizes) and plan_dev (device copy of the same ints,
+ * 16-byte aligned).  fp16 / bf16 caches with block_size a multiple of 16
+ * only (else PA_ERR_UNSUPPORTED).  Two launches on `stream`:
+ *   1. every group's blocks against the query rows of all its members (a
+ *      group is a shared run of full blocks, or one sequence's own blocks):
+ *      the four consumer warps of a CTA share each tile, 8 query rows each,
+ *      and each piece of the work leaves a partial state (acc, m, l) per row;
+ *   2. per (sequence, head), the merge of the partial states of every group
+ *      it belongs to:
+ *      M = max_i m_i;  out = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i.
+ * workspace: at least pa_decode_shared_workspace_size(...) bytes, 16-byte
+ * aligned (the partial states; zero-filled before first use when the plan has
+ * no shared group, as pa_decode then runs with it).  A plan without shared
+ * groups runs pa_decode.
+ */
+PA_API pa_status pa_decode_shared(void *out, const void *q, const void *k_cache,
+                                  const void *v_cache, const int32_t *block_tables,
+                                  int max_blocks_per_seq, const int32_t *context_lens,
+                                  int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int64_t num_blocks, float scale,
+                                  pa_dtype dtype, const int32_t *plan_host,
+                                  const int32_t *plan_dev, void *workspace,
+                                  size_t workspace_bytes, int *debug_err, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

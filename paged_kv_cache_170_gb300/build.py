@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libpagedkv.so")
 SOURCES = ["pa_kv.cu", "pa_decode.cu", "pa_decode_f32.cu", "pa_decode_f16.cu", "pa_decode_bf16.cu",
-           "pa_decode_noalloc.cu"]
+           "pa_decode_noalloc.cu", "pa_share.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 DEBUG = (["-DPA_DEBUG"] if os.environ.get("PA_DEBUG") == "1" else []) + \
     (["-DPA_TRACE"] if os.environ.get("PA_TRACE") == "1" else [])

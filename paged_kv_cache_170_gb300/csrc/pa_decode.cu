@@ -5,6 +5,7 @@
 
 #include <mutex>
 
+#include "pa_decode_shared.cuh"
 #include "pa_sched.cuh"
 
 namespace pagedkv {
@@ -14,6 +15,11 @@ pa_status launch_decode_simt(const DecodeArgs &a, size_t ring_bytes, cudaStream_
 template <typename T, int D>
 pa_status launch_decode_mma(const DecodeArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t ring_bytes,
                             cudaStream_t stream);
+template <typename T, int D>
+pa_status launch_decode_shared(const SharedArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t ring_bytes,
+                               cudaStream_t stream);
+template <typename T, int D>
+pa_status launch_merge_shared(const MergeArgs &a, cudaStream_t stream);
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -157,24 +163,28 @@ static pa_status dispatch_simt(const DecodeArgs &a, int D, int GT, size_t ring, 
   return PA_ERR_UNSUPPORTED;
 }
 
+// Tensor maps of the K and V pools: one 3-D box per tile when the encoder
+// takes the (rows, halves) stride order, else one 2-D box per 64-column half
+// (*nops = copies per tile; D = 64 is always one 2-D box).
+static bool encode_pool_maps(const void *k_cache, const void *v_cache, pa_dtype dtype, int64_t num_blocks, int Hkv,
+                             int B, int D, CUtensorMap *mk, CUtensorMap *mv, int *nops) {
+  *nops = 1;
+  if (D == 128 && encode_pool_map(mk, k_cache, dtype, num_blocks, Hkv, B, D, true) &&
+      encode_pool_map(mv, v_cache, dtype, num_blocks, Hkv, B, D, true))
+    return true;
+  if (!encode_pool_map(mk, k_cache, dtype, num_blocks, Hkv, B, D, false) ||
+      !encode_pool_map(mv, v_cache, dtype, num_blocks, Hkv, B, D, false))
+    return false;
+  *nops = D == 64 ? 1 : 2;
+  return true;
+}
+
 template <typename T>
 static pa_status dispatch_mma(const DecodeArgs &a, const void *k_cache, const void *v_cache, pa_dtype dtype, int D,
                               size_t ring, cudaStream_t st) {
   CUtensorMap mk, mv;
   DecodeArgs b = a;
-  // one 3-D box per tile when the encoder takes the (rows, halves) stride
-  // order, else one 2-D box per 64-column half
-  b.nops = 1;
-  if (D == 128 && !(encode_pool_map(&mk, k_cache, dtype, a.num_blocks, a.Hkv, a.B, D, true) &&
-                    encode_pool_map(&mv, v_cache, dtype, a.num_blocks, a.Hkv, a.B, D, true))) {
-    b.nops = 2;
-  }
-  if (D == 64 || b.nops == 2) {
-    if (!encode_pool_map(&mk, k_cache, dtype, a.num_blocks, a.Hkv, a.B, D, false) ||
-        !encode_pool_map(&mv, v_cache, dtype, a.num_blocks, a.Hkv, a.B, D, false))
-      return PA_ERR_CUDA;
-    if (D == 64) b.nops = 1;
-  }
+  if (!encode_pool_maps(k_cache, v_cache, dtype, a.num_blocks, a.Hkv, a.B, D, &mk, &mv, &b.nops)) return PA_ERR_CUDA;
   return D == 64 ? launch_decode_mma<T, 64>(b, mk, mv, ring, st) : launch_decode_mma<T, 128>(b, mk, mv, ring, st);
 }
 
@@ -192,11 +202,15 @@ extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_
   return workspace_bytes_for(num_seqs, num_heads, head_dim, n);
 }
 
-extern "C" pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
-                               const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
-                               int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                               int64_t num_blocks, float scale, pa_dtype dtype, void *workspace,
-                               size_t workspace_bytes, int *debug_err, void *stream) {
+namespace pagedkv {
+
+// pa_decode, optionally over each sequence's blocks from start_block[s] on,
+// with fp32 output rows (out_f32) and their log2-sum-exp (lse).
+static pa_status decode_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                             int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                             int64_t num_blocks, float scale, pa_dtype dtype, void *workspace, size_t workspace_bytes,
+                             int *debug_err, void *stream, const int32_t *start_block, float *out_f32, float *lse) {
   DecodeShape sh;
   pa_status st = check_decode_args(max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                                    num_blocks, dtype, &sh);
@@ -236,6 +250,9 @@ extern "C" pa_status pa_decode(void *out, const void *q, const void *k_cache, co
   a.nops = 1;
   a.q_offset = sh.q_offset;
   a.q_bytes = sh.q_bytes;
+  a.start_block = start_block;
+  a.out_f32 = out_f32;
+  a.lse = lse;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (sh.mma) {
     return dtype == PA_BF16
@@ -248,4 +265,155 @@ extern "C" pa_status pa_decode(void *out, const void *q, const void *k_cache, co
     case PA_BF16: return dispatch_simt<__nv_bfloat16>(a, head_dim, sh.GT, sh.ring_bytes, s);
   }
   return PA_ERR_INVALID_ARG;
+}
+
+}  // namespace pagedkv
+
+extern "C" pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                               int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                               int64_t num_blocks, float scale, pa_dtype dtype, void *workspace,
+                               size_t workspace_bytes, int *debug_err, void *stream) {
+  return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_heads,
+                     num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace, workspace_bytes,
+                     debug_err, stream, nullptr, nullptr, nullptr);
+}
+
+// ------------------------------------------------------ shared-block decode
+namespace pagedkv {
+
+// The plan's header if it belongs to these arguments, else null.
+static const SharePlanHeader *check_plan(const int32_t *plan_host, int num_seqs, int num_heads, int num_kv_heads,
+                                         int block_size, int max_blocks_per_seq) {
+  if (plan_host == nullptr) return nullptr;
+  const SharePlanHeader *h = reinterpret_cast<const SharePlanHeader *>(plan_host);
+  if (h->magic != kSharePlanMagic || h->num_seqs != num_seqs || num_kv_heads <= 0 ||
+      h->group_size * num_kv_heads != num_heads || h->num_kv_heads != num_kv_heads || h->block_size != block_size ||
+      h->max_blocks != max_blocks_per_seq || h->nctas <= 0 || h->num_pieces < 0 || h->total_ints < kSharePlanHeaderInts)
+    return nullptr;
+  return h;
+}
+
+// Workspace of the shared-block decode: the private-block decode's own
+// workspace (partials, counters), its fp32 rows and log2-sum-exp, then the
+// shared kernel's partial states [num_pieces][kSharePassRows][state_row(D)].
+struct SharedWorkspace {
+  size_t out_f32, lse, records, total;  // byte offsets of each part, and the total
+};
+
+static SharedWorkspace shared_workspace(const SharePlanHeader &h, int num_seqs, int num_heads, int head_dim,
+                                        int nctas) {
+  SharedWorkspace w;
+  w.out_f32 = round256(workspace_bytes_for(num_seqs, num_heads, head_dim, nctas));
+  w.lse = w.out_f32 + round256(size_t(num_seqs) * num_heads * head_dim * sizeof(float));
+  w.records = w.lse + round256(size_t(num_seqs) * num_heads * sizeof(float));
+  w.total = w.records + round256(size_t(h.num_pieces) * kSharePassRows * state_row(head_dim) * sizeof(float));
+  return w;
+}
+
+template <typename T>
+static pa_status shared_step(const SharedArgs &sa, const void *k_cache, const void *v_cache, pa_dtype dtype, int D,
+                             size_t ring, cudaStream_t st) {
+  CUtensorMap mk, mv;
+  SharedArgs b = sa;
+  if (!encode_pool_maps(k_cache, v_cache, dtype, sa.num_blocks, sa.Hkv, sa.B, D, &mk, &mv, &b.nops))
+    return PA_ERR_CUDA;
+  return D == 64 ? launch_decode_shared<T, 64>(b, mk, mv, ring, st) : launch_decode_shared<T, 128>(b, mk, mv, ring, st);
+}
+
+template <typename T>
+static pa_status merge_step(const MergeArgs &ma, int D, cudaStream_t st) {
+  return D == 64 ? launch_merge_shared<T, 64>(ma, st) : launch_merge_shared<T, 128>(ma, st);
+}
+
+}  // namespace pagedkv
+
+extern "C" size_t pa_decode_shared_workspace_size(const int32_t *plan_host, int num_seqs, int num_heads,
+                                                  int num_kv_heads, int head_dim) {
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads) return 0;
+  if (head_dim != 64 && head_dim != 128) return 0;
+  const SharePlanHeader *h = reinterpret_cast<const SharePlanHeader *>(plan_host);
+  if (h == nullptr || h->magic != kSharePlanMagic || h->num_seqs != num_seqs) return 0;
+  const int n = decode_grid();
+  if (n <= 0) return 0;
+  return shared_workspace(*h, num_seqs, num_heads, head_dim, n).total;
+}
+
+extern "C" pa_status pa_decode_shared(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                      const int32_t *block_tables, int max_blocks_per_seq,
+                                      const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                      int head_dim, int block_size, int64_t num_blocks, float scale, pa_dtype dtype,
+                                      const int32_t *plan_host, const int32_t *plan_dev, void *workspace,
+                                      size_t workspace_bytes, int *debug_err, void *stream) {
+  DecodeShape sh;
+  pa_status st = check_decode_args(max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                   num_blocks, dtype, &sh);
+  if (st != PA_OK) return st;
+  if (!sh.mma) return PA_ERR_UNSUPPORTED;  // fp16 / bf16 with block_size % 16 == 0 only
+  if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+  const SharePlanHeader *h =
+      check_plan(plan_host, num_seqs, num_heads, num_kv_heads, block_size, max_blocks_per_seq);
+  if (h == nullptr) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (h->num_groups == 0)  // nothing shared: the plain decode
+    return pa_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_heads,
+                     num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace, workspace_bytes,
+                     debug_err, stream);
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace || !plan_dev)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace) ||
+      !aligned16(plan_dev))
+    return PA_ERR_INVALID_ARG;
+  const SharedWorkspace w = shared_workspace(*h, num_seqs, num_heads, head_dim, sh.nctas);
+  if (workspace_bytes < w.total) return PA_ERR_WORKSPACE;
+  char *ws = static_cast<char *>(workspace);
+  float *out_f32 = reinterpret_cast<float *>(ws + w.out_f32);
+  float *lse = reinterpret_cast<float *>(ws + w.lse);
+  float *records = reinterpret_cast<float *>(ws + w.records);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  // 1. shared blocks, once per group of sharers
+  SharedArgs sa;
+  sa.q = q;
+  sa.tables = block_tables;
+  sa.plan = plan_dev;
+  sa.h = *h;
+  sa.num_blocks = num_blocks;
+  sa.max_blocks = max_blocks_per_seq;
+  sa.S = num_seqs;
+  sa.Hq = num_heads;
+  sa.Hkv = num_kv_heads;
+  sa.B = block_size;
+  sa.qscale = scale * kLog2e;
+  sa.records = records;
+  sa.err = debug_err;
+  sa.tile_stride = sh.tile_stride;
+  sa.slot_stride = 2 * sh.tile_stride;
+  sa.nstage = int(kRingBytesShared / sa.slot_stride);
+  if (sa.nstage > kMaxStages) sa.nstage = kMaxStages;
+  if (sa.nstage < 1) return PA_ERR_UNSUPPORTED;
+  sa.pg = sa.nstage < 4 ? sa.nstage : 4;
+  sa.nops = 1;
+  const size_t ring = size_t(sa.nstage) * sa.slot_stride;
+  MergeArgs ma;
+  ma.out = out;
+  ma.out_f32 = out_f32;
+  ma.lse = lse;
+  ma.records = records;
+  ma.plan = plan_dev;
+  ma.h = *h;
+  ma.S = num_seqs;
+  ma.Hq = num_heads;
+  if (h->num_pieces > 0) {
+    st = dtype == PA_BF16 ? shared_step<__nv_bfloat16>(sa, k_cache, v_cache, dtype, head_dim, ring, s)
+                          : shared_step<__half>(sa, k_cache, v_cache, dtype, head_dim, ring, s);
+    if (st != PA_OK) return st;
+  }
+  // 2. each sequence's own blocks: fp32 rows and their log2-sum-exp
+  st = decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_heads,
+                   num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace, w.out_f32, debug_err,
+                   stream, plan_dev + h->s_start, out_f32, lse);
+  if (st != PA_OK) return st;
+  // 3. merge
+  return dtype == PA_BF16 ? merge_step<__nv_bfloat16>(ma, head_dim, s) : merge_step<__half>(ma, head_dim, s);
 }

@@ -5,4 +5,5 @@
 namespace pagedkv {
 PAGEDKV_INSTANTIATE_SIMT(__half)
 PAGEDKV_INSTANTIATE_MMA(__half)
+PAGEDKV_INSTANTIATE_SHARED(__half)
 }  // namespace pagedkv

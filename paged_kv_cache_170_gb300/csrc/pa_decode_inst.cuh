@@ -4,6 +4,7 @@
 #pragma once
 
 #include "pa_decode_mma.cuh"
+#include "pa_decode_shared.cuh"
 #include "pa_decode_simt.cuh"
 
 namespace pagedkv {
@@ -38,6 +39,32 @@ pa_status launch_decode_mma(const DecodeArgs &a, const CUtensorMap &mk, const CU
   kern<<<a.nctas, kDecodeThreads, ring_bytes + 1024, stream>>>(a, mk, mv);
   return launch_status();
 }
+
+template <typename T, int D>
+pa_status launch_decode_shared(const SharedArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t ring_bytes,
+                               cudaStream_t stream) {
+  static int configured[64] = {0};
+  auto kern = decode_shared_mma_kernel<T, D>;
+  if (!configure_once(kern, kRingBytesShared + 1024, configured)) return PA_ERR_CUDA;
+  kern<<<a.h.nctas, kSharedThreads, ring_bytes + 1024, stream>>>(a, mk, mv);
+  return launch_status();
+}
+
+template <typename T, int D>
+pa_status launch_merge_shared(const MergeArgs &a, cudaStream_t stream) {
+  const long long rows = (long long)a.S * a.Hq;
+  if (rows == 0) return PA_OK;
+  merge_shared_kernel<T, D><<<unsigned((rows + kMergeWarps - 1) / kMergeWarps), kMergeWarps * 32, 0, stream>>>(a);
+  return launch_status();
+}
+
+#define PAGEDKV_INSTANTIATE_SHARED(T)                                                                         \
+  template pa_status launch_decode_shared<T, 64>(const SharedArgs &, const CUtensorMap &, const CUtensorMap &, \
+                                                 size_t, cudaStream_t);                                        \
+  template pa_status launch_decode_shared<T, 128>(const SharedArgs &, const CUtensorMap &,                     \
+                                                  const CUtensorMap &, size_t, cudaStream_t);                  \
+  template pa_status launch_merge_shared<T, 64>(const MergeArgs &, cudaStream_t);                              \
+  template pa_status launch_merge_shared<T, 128>(const MergeArgs &, cudaStream_t);
 
 #define PAGEDKV_INSTANTIATE_SIMT(T)                                                           \
   template pa_status launch_decode_simt<T, 64, 1>(const DecodeArgs &, size_t, cudaStream_t);  \

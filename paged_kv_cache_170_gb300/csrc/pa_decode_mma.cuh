@@ -26,15 +26,10 @@
 //   ~16 significant bits and PV stays close to an fp32 product.
 #pragma once
 
+#include "pa_mma_tile.cuh"
 #include "pa_sched.cuh"
 
 namespace pagedkv {
-
-// Shared-memory address of (row, 16-byte logical chunk) in a swizzled tile
-// laid out as [D/64 halves][B rows][128 bytes].
-__device__ __forceinline__ uint32_t swz(uint32_t tile, int B, int half, int row, int chunk) {
-  return tile + uint32_t(half * B * 128 + row * 128 + ((chunk ^ (row & 7)) << 4));
-}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
@@ -95,7 +90,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   __syncthreads();
 
   const Plan plan = sh_plan;
-  const long long W = plan.W, w0 = plan.w0, w1 = plan.w1;
+  const long long w0 = plan.w0, w1 = plan.w1;
   if (w0 >= w1) {  // fewer tiles than CTAs: nothing to stream, only empty rows to zero
     if (warp == kMergerWarp) zero_empty_rows<T>(a, D, lane, 32);
     return;
@@ -170,8 +165,6 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2;      // fragment row group
   const int c4 = lane & 3;      // fragment column pair
-  const int mj = lane >> 3;     // ldmatrix: which 8x8 matrix this lane addresses
-  const int mr = lane & 7;      // ldmatrix: which row of it
 
   long long j = 0;      // tiles, in this CTA's processing order
   long long dep = 0;    // states this warp deposited for the merger
@@ -190,7 +183,6 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     while (wk.w < to) {
       const int n = wk.seg_len(to);
       const bool complete = (wk.b == 0 && n == wk.nb);
-      const bool first_seg = (wk.w == w0);
       const int kvh = wk.pc / HC;
       const int hq0 = kvh * G + (wk.pc % HC) * GT;
       const int L = wk.L;
@@ -253,68 +245,6 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
             }
           }
 
-          // ---- QK: scores of up to 4 sub-tiles of 16 tokens
-          float sc[4][4];
-#pragma unroll
-          for (int st = 0; st < 4; ++st) {
-            sc[st][0] = sc[st][1] = sc[st][2] = sc[st][3] = -CUDART_INF_F;
-            if (st < nsub) {
-              float c[4] = {0.f, 0.f, 0.f, 0.f};
-              const int row = st * 16 + (mj & 1) * 8 + mr;
-#pragma unroll
-              for (int ks = 0; ks < KS; ++ks) {
-                uint32_t af[4];
-                uint32_t ad = swz(kt, B, ks >> 2, row, (ks & 3) * 2 + (mj >> 1));
-                PA_DBG_FIX(ad >= ring_addr && ad + 16 <= ring_addr + a.nstage * a.slot_stride && (ad & 15u) == 0,
-                           kDbgSmem, ad = ring_addr);
-                ldmatrix_x4(af, ad);
-                Mma<T>::run(c, af, qf[ks][0], qf[ks][1]);
-              }
-              const int t0 = st * 16 + g;
-              sc[st][0] = t0 < nv ? c[0] * a.qscale : -CUDART_INF_F;
-              sc[st][1] = t0 < nv ? c[1] * a.qscale : -CUDART_INF_F;
-              sc[st][2] = t0 + 8 < nv ? c[2] * a.qscale : -CUDART_INF_F;
-              sc[st][3] = t0 + 8 < nv ? c[3] * a.qscale : -CUDART_INF_F;
-            }
-          }
-          // ---- online softmax (base 2), heads h0 / h1 of this lane
-          float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
-#pragma unroll
-          for (int st = 0; st < 4; ++st) {
-            mx0 = fmaxf(mx0, fmaxf(sc[st][0], sc[st][2]));
-            mx1 = fmaxf(mx1, fmaxf(sc[st][1], sc[st][3]));
-          }
-#pragma unroll
-          for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
-          }
-          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-          const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
-          m0 = mn0;
-          m1 = mn1;
-          l0 *= al0;
-          l1 *= al1;
-#pragma unroll
-          for (int st = 0; st < 4; ++st) {
-            sc[st][0] = fast_exp2(sc[st][0] - mn0);
-            sc[st][1] = fast_exp2(sc[st][1] - mn1);
-            sc[st][2] = fast_exp2(sc[st][2] - mn0);
-            sc[st][3] = fast_exp2(sc[st][3] - mn1);
-            l0 += sc[st][0] + sc[st][2];
-            l1 += sc[st][1] + sc[st][3];
-          }
-          if (__any_sync(kFullMask, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-              o[mt][0] *= al0;
-              o[mt][1] *= al1;
-              o[mt][2] *= al0;
-              o[mt][3] *= al1;
-            }
-          }
-
-          // ---- PV
           if (nv < nsub * 16) {
             // rows past the context in the last sub-tile: make them zero so a
             // zero weight times stale data cannot produce NaN
@@ -329,30 +259,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
             fence_proxy_async_shared();
             __syncwarp();
           }
-#pragma unroll
-          for (int st = 0; st < 4; ++st) {
-            if (st < nsub) {
-              const uint32_t hi0 = Mma<T>::pack(sc[st][0], sc[st][1]);  // token g
-              const uint32_t hi1 = Mma<T>::pack(sc[st][2], sc[st][3]);  // token g + 8
-              const float2 f0 = Mma<T>::unpack(hi0), f1 = Mma<T>::unpack(hi1);
-              const uint32_t lo0 = Mma<T>::pack(sc[st][0] - f0.x, sc[st][1] - f0.y);
-              const uint32_t lo1 = Mma<T>::pack(sc[st][2] - f1.x, sc[st][3] - f1.y);
-              const uint32_t bh0 = movmatrix_trans(hi0), bh1 = movmatrix_trans(hi1);
-              const uint32_t bl0 = movmatrix_trans(lo0), bl1 = movmatrix_trans(lo1);
-              const int row = st * 16 + (mj >> 1) * 8 + mr;
-#pragma unroll
-              for (int mt = 0; mt < KS; ++mt) {
-                const int chunk = 2 * mt + (mj & 1);
-                uint32_t af[4];
-                uint32_t ad = swz(vt, B, chunk >> 3, row, chunk & 7);
-                PA_DBG_FIX(ad >= ring_addr && ad + 16 <= ring_addr + a.nstage * a.slot_stride && (ad & 15u) == 0,
-                           kDbgSmem, ad = ring_addr);
-                ldmatrix_x4_trans(af, ad);
-                Mma<T>::run(o[mt], af, bh0, bh1);
-                Mma<T>::run(o[mt], af, bl0, bl1);
-              }
-            }
-          }
+          mma_tile<T, D>(a, kt, vt, B, nv, qf, a.qscale, m0, m1, l0, l1, o, lane, ring_addr,
+                         ring_addr + uint32_t(a.nstage) * a.slot_stride);
           __syncwarp();
           if (lane == 0 && okE) mbar_arrive(&empty_bar[slot]);  // the pair's slot is free again
         }
@@ -373,17 +281,21 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         if (complete && __popc(participants(j, n, a.ncw)) == 1) {
           // same arithmetic as the merger's one-state combine: o * (1 / l)
           const float i0 = 1.f / l0, i1 = 1.f / l1;
-          T *orow = static_cast<T *>(a.out) + ((long long)wk.s * a.Hq + hq0) * D;
+          const long long row0 = (long long)wk.s * a.Hq + hq0;
 #pragma unroll
           for (int mt = 0; mt < KS; ++mt) {
             if (h0 < GT) {
-              orow[h0 * D + 16 * mt + g] = Elem<T>::from_float(o[mt][0] * i0);
-              orow[h0 * D + 16 * mt + g + 8] = Elem<T>::from_float(o[mt][2] * i0);
+              store_out1<T>(a, row0 + h0, 16 * mt + g, D, o[mt][0] * i0);
+              store_out1<T>(a, row0 + h0, 16 * mt + g + 8, D, o[mt][2] * i0);
             }
             if (h1 < GT) {
-              orow[h1 * D + 16 * mt + g] = Elem<T>::from_float(o[mt][1] * i1);
-              orow[h1 * D + 16 * mt + g + 8] = Elem<T>::from_float(o[mt][3] * i1);
+              store_out1<T>(a, row0 + h1, 16 * mt + g, D, o[mt][1] * i1);
+              store_out1<T>(a, row0 + h1, 16 * mt + g + 8, D, o[mt][3] * i1);
             }
+          }
+          if (g == 0) {
+            if (h0 < GT) store_lse(a, row0 + h0, m0, l0);
+            if (h1 < GT) store_lse(a, row0 + h1, m1, l1);
           }
         } else {
           deposit_state(a, dep, lane, &st_full[warp], &st_free[warp], abort_flag, [&]() {

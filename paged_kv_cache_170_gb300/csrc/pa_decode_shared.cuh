@@ -1,0 +1,405 @@
+// pa_decode_shared.cuh -- the two kernels of the shared-block decode:
+//
+// decode_shared_mma_kernel (step 1): every group's shared blocks against the
+//   query rows of all its members.  A CTA walks its pieces (plan: c_poff) in
+//   order; one producer warp streams each piece's K and V tiles into a ring by
+//   TMA.  The four consumer warps take the unit's pass of up to 32 query rows
+//   (row = member * G + head) as wr row-warps of 8 rows times 4 / wr
+//   tile-lanes: with 32 rows all four warps work on every tile, so a tile read
+//   once serves 32 rows of up to 32 sequences; with 8 rows each warp takes
+//   every fourth tile, and the tile-lanes' states are combined in shared
+//   memory at the piece's end.  Each piece leaves one partial state (acc, m,
+//   l) per row of its pass in `records`.
+//   Every consumer waits for every entry in order, so the ring's mbarrier
+//   parity waits are exact (no warp can lag a full ring behind another).
+//
+// merge_shared_kernel (step 3): per output row (s, h), the row the
+//   split-context decode computed over the sequence's own blocks (fp32 o and
+//   its log2-sum-exp) and the partial states of every piece of every group s
+//   belongs to, merged with a running maximum:
+//     M = max_i m_i;  out = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i,
+//   where the own-block row enters as acc = o, m = lse, l = 1.
+#pragma once
+
+#include "pa_mma_tile.cuh"
+#include "pa_sched.cuh"
+#include "pa_share_plan.h"
+
+namespace pagedkv {
+
+struct SharedArgs {
+  const void *q;
+  const int32_t *tables;
+  const int32_t *plan;  // device copy of the plan
+  SharePlanHeader h;    // its header
+  int64_t num_blocks;
+  int max_blocks, S, Hq, Hkv, B;
+  float qscale;      // scale * log2(e)
+  float *records;    // [num_pieces][kSharePassRows][state_row(D)]
+  int *err;
+  int nstage, pg, nops;
+  uint32_t slot_stride, tile_stride;
+};
+
+constexpr int kSharedThreads = (kConsumerWarps + 1) * 32;
+
+// Row-warps (8 rows each) a pass of `rows` query rows takes: 1, 2 or 4.
+__host__ __device__ __forceinline__ int share_row_warps(int rows) { return rows <= 8 ? 1 : (rows <= 16 ? 2 : 4); }
+constexpr int kRingBytesShared = 88 * 1024;  // ring of K + V tile pairs
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
+    decode_shared_mma_kernel(const SharedArgs a, const __grid_constant__ CUtensorMap map_k,
+                             const __grid_constant__ CUtensorMap map_v) {
+  constexpr int KS = D / 16;
+  constexpr int HALVES = D / 64;
+  constexpr int R = state_row(D);
+  extern __shared__ __align__(1024) unsigned char ring_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ uint32_t issued[kMaxStages];
+  __shared__ int sh_abort;
+  __shared__ __align__(16) float st[kConsumerWarps][8][R];  // tile-lane states of a piece's rows
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int32_t *P = a.plan;
+  const SharePlanHeader &h = a.h;
+  const int Gq = h.group_size;
+  const int B = a.B;
+  volatile int *abort_flag = &sh_abort;
+  const uint32_t raw_addr = smem_addr(ring_raw);
+  const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+  unsigned char *ring = ring_raw + pad;
+  const uint32_t ring_addr = raw_addr + pad;
+  const uint32_t ring_end = ring_addr + uint32_t(a.nstage) * a.slot_stride;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.nstage; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], kConsumerWarps);
+      issued[i] = 0;
+    }
+    sh_abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const int p0 = P[h.c_poff + blockIdx.x], p1 = P[h.c_poff + blockIdx.x + 1];
+  const uint32_t tile_bytes = uint32_t(B) * D * 2;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_k)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_v)) : "memory");
+    }
+    uint32_t e = 0;
+    bool aborted = false;
+    for (int p = p0; p < p1 && !aborted; ++p) {
+      const int u = P[h.p_unit + p];
+      const int t0 = P[h.p_t0 + p], t1 = P[h.p_t1 + p];
+      const int g = P[h.u_group + u];
+      const int kvh = P[h.u_kvh + u];
+      const int leader = P[h.g_members + P[h.g_moff + g]];
+      const int32_t *trow = a.tables + (long long)leader * a.max_blocks + P[h.g_b0 + g] + t0;
+      const int n = t1 - t0;
+      for (int base = 0; base < n && !aborted; base += 32) {
+        const int cnt = min(32, n - base);
+        const int pid_cur = lane < cnt ? trow[base + lane] : -1;
+        for (int k = 0; k < cnt; k += a.pg) {
+          const int t = k + lane;
+          const int pid = __shfl_sync(kFullMask, pid_cur, t < 32 ? t : 31);
+          bool fail = false;
+          if (lane < a.pg && t < cnt) {
+            const uint32_t me = e + uint32_t(lane);
+            const int slot = int(me % uint32_t(a.nstage));
+            const uint32_t use = me / uint32_t(a.nstage);
+            if (*abort_flag || (use > 0 && !mbar_wait(&empty_bar[slot], (use - 1) & 1u, abort_flag))) {
+              fail = true;
+            } else if (pid < 0 || pid >= a.num_blocks) {
+              raise_error(a.err, PA_DEVERR_BLOCK_ID);
+              mbar_arrive(&full_bar[slot]);  // complete the phase without data
+              issued[slot] = use + 1;
+            } else {
+              mbar_arrive_expect_tx(&full_bar[slot], 2 * tile_bytes);
+              unsigned char *dst = ring + size_t(slot) * a.slot_stride;
+              const int y = (pid * a.Hkv + kvh) * B;
+              if (HALVES == 2 && a.nops == 1) {
+                tma_load_3d(dst, &map_k, 0, y, 0, &full_bar[slot]);
+                tma_load_3d(dst + a.tile_stride, &map_v, 0, y, 0, &full_bar[slot]);
+              } else {
+#pragma unroll
+                for (int hh = 0; hh < HALVES; ++hh) {
+                  tma_load_2d(dst + hh * B * 128, &map_k, 64 * hh, y, &full_bar[slot]);
+                  tma_load_2d(dst + a.tile_stride + hh * B * 128, &map_v, 64 * hh, y, &full_bar[slot]);
+                }
+              }
+              issued[slot] = use + 1;
+            }
+          }
+          if (__any_sync(kFullMask, fail)) {
+            aborted = true;
+            if (lane == 0) {
+              *abort_flag = 1;
+              raise_error(a.err, PA_DEVERR_TIMEOUT);
+            }
+            break;
+          }
+          e += uint32_t(min(a.pg, cnt - k));
+        }
+      }
+    }
+    // leave only when no copy into this CTA's shared memory is in flight
+    __syncwarp();
+    if (lane == 0) {
+      for (int slot = 0; slot < a.nstage; ++slot) {
+        if (issued[slot] == 0) continue;
+        int never = 0;
+        mbar_wait(&full_bar[slot], (issued[slot] - 1) & 1u, &never);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  // All four consumer warps walk every entry in the same order and meet at
+  // the same named barriers (id 1, 128 threads); after a timeout they keep
+  // walking without waiting or computing, so no warp is left at a barrier.
+  const int g8 = lane >> 2;  // fragment row group: this lane's query column
+  const int c4 = lane & 3;
+  int slot = 0;         // ring slot of the next entry
+  uint32_t parity = 0;  // its use's parity; entries are consumed in order, one by one
+#ifdef PA_TRACE
+  long long tr_c0 = clock64(), tr_setup = 0, tr_wait = 0, tr_math = 0, tr_end = 0, tr_tiles = 0;
+#endif
+  for (int p = p0; p < p1; ++p) {
+#ifdef PA_TRACE
+    const long long tr_p0 = clock64();
+#endif
+    const int u = P[h.p_unit + p];
+    const int t0 = P[h.p_t0 + p];
+    const int n = P[h.p_t1 + p] - t0;
+    const int g = P[h.u_group + u];
+    const int kvh = P[h.u_kvh + u];
+    const int moff = P[h.g_moff + g];
+    const int rows = (P[h.g_moff + g + 1] - moff) * Gq;
+    // wr row-warps cover the pass's rows (8 each); the 4 / wr tile-lanes take
+    // every (4 / wr)-th tile, so a pass of few rows still keeps all warps busy
+    const int prow = P[h.u_pass + u] * kSharePassRows;
+    const int wr = share_row_warps(rows - prow);
+    const int rw = warp % wr, tl = warp / wr, nl = kConsumerWarps / wr;
+    const int rb = prow + rw * 8;  // this warp's first row
+    const int myrows = tl < nl ? max(0, min(8, rows - rb)) : 0;
+
+    uint32_t qf[KS][2];
+    if (g8 < myrows) {
+      const int r = rb + g8;
+      const int seq = P[h.g_members + moff + r / Gq];
+      const T *qrow = static_cast<const T *>(a.q) + ((long long)seq * a.Hq + kvh * Gq + r % Gq) * D;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qf[ks][0] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c4);
+        qf[ks][1] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * c4);
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) qf[ks][0] = qf[ks][1] = 0u;
+    }
+    float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+    float o[KS][4];
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+#ifdef PA_TRACE
+    qf[0][0] = __shfl_sync(kFullMask, qf[0][0], lane);  // wait for the q loads
+    tr_setup += clock64() - tr_p0;
+#endif
+    for (int t = 0; t < n; ++t) {
+#ifdef PA_TRACE
+      const long long tr_w0 = clock64();
+#endif
+      bool ok = !*abort_flag;
+      if (ok && !mbar_wait(&full_bar[slot], parity, abort_flag)) {
+        if (lane == 0 && !*abort_flag) raise_error(a.err, PA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+        ok = false;
+      }
+      __syncwarp();
+      ok = __all_sync(kFullMask, ok);
+      const uint32_t kt = ring_addr + uint32_t(slot) * a.slot_stride;
+#ifdef PA_TRACE
+      const long long tr_m0 = clock64();
+      tr_wait += tr_m0 - tr_w0;
+#endif
+      if (ok && myrows > 0 && t % nl == tl) {  // shared blocks are full: B valid rows
+        mma_tile<T, D>(a, kt, kt + a.tile_stride, B, B, qf, a.qscale, m0, m1, l0, l1, o, lane, ring_addr,
+                       ring_end);
+#ifdef PA_TRACE
+        o[0][0] = __shfl_sync(kFullMask, o[0][0], lane);
+        tr_math += clock64() - tr_m0;
+        ++tr_tiles;
+#endif
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[slot]);
+      if (++slot == a.nstage) {
+        slot = 0;
+        parity ^= 1u;
+      }
+    }
+
+#ifdef PA_TRACE
+    const long long tr_e0 = clock64();
+#endif
+    // ---- the piece's partial state per row (acc, m, l): straight to the
+    // record (one tile-lane), or through shared memory, combining the
+    // tile-lanes of each row first
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(kFullMask, l0, off);
+      l1 += __shfl_xor_sync(kFullMask, l1, off);
+    }
+    const int h0 = 2 * c4, h1 = 2 * c4 + 1;
+    float *dst = nl == 1 ? a.records + ((long long)p * kSharePassRows + rw * 8) * R : &st[warp][0][0];
+    if (myrows > 0) {
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        if (h0 < myrows) {
+          dst[h0 * R + 16 * mt + g8] = o[mt][0];
+          dst[h0 * R + 16 * mt + g8 + 8] = o[mt][2];
+        }
+        if (h1 < myrows) {
+          dst[h1 * R + 16 * mt + g8] = o[mt][1];
+          dst[h1 * R + 16 * mt + g8 + 8] = o[mt][3];
+        }
+      }
+      if (g8 == 0) {
+        if (h0 < myrows) {
+          dst[h0 * R + D] = m0;
+          dst[h0 * R + D + 1] = l0;
+        }
+        if (h1 < myrows) {
+          dst[h1 * R + D] = m1;
+          dst[h1 * R + D + 1] = l1;
+        }
+      }
+    }
+    if (nl > 1) {
+      named_barrier_sync(1, kConsumerWarps * 32);
+      if (tl == 0 && myrows > 0) {
+        // lane (j, hh) = (lane / 8, lane % 8): weight of tile-lane j for row hh
+        const int j = lane >> 3, hh = lane & 7;
+        const bool mine = j < nl && hh < myrows;
+        const float *sj = &st[j * wr + rw][0][0];
+        const float m = mine ? sj[hh * R + D] : -CUDART_INF_F;
+        const float lv = mine ? sj[hh * R + D + 1] : 0.f;
+        float M = fmaxf(m, __shfl_xor_sync(kFullMask, m, 8));
+        M = fmaxf(M, __shfl_xor_sync(kFullMask, M, 16));
+        const float f = (mine && M > -CUDART_INF_F) ? fast_exp2(m - M) : 0.f;
+        float den = f * lv;
+        den += __shfl_xor_sync(kFullMask, den, 8);
+        den += __shfl_xor_sync(kFullMask, den, 16);
+        float *rec = a.records + ((long long)p * kSharePassRows + rw * 8) * R;
+        if (j == 0 && hh < myrows) {
+          rec[hh * R + D] = M;
+          rec[hh * R + D + 1] = den;
+        }
+        constexpr int C4 = D / 4;
+#pragma unroll
+        for (int i = 0; i < 8 * C4 / 32; ++i) {
+          const int idx = lane + 32 * i;
+          const int row = idx / C4, d = (idx % C4) * 4;
+          float w[kConsumerWarps];
+#pragma unroll
+          for (int jj = 0; jj < kConsumerWarps; ++jj) w[jj] = __shfl_sync(kFullMask, f, jj * 8 + row);
+          if (row < myrows) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int jj = 0; jj < nl; ++jj) {
+              const float4 v = *reinterpret_cast<const float4 *>(&st[jj * wr + rw][row][d]);
+              acc.x += w[jj] * v.x;
+              acc.y += w[jj] * v.y;
+              acc.z += w[jj] * v.z;
+              acc.w += w[jj] * v.w;
+            }
+            *reinterpret_cast<float4 *>(rec + row * R + d) = acc;
+          }
+        }
+      }
+      named_barrier_sync(1, kConsumerWarps * 32);  // st is free for the next piece
+    }
+#ifdef PA_TRACE
+    tr_end += clock64() - tr_e0;
+#endif
+  }
+#ifdef PA_TRACE
+  if (lane == 0 && PA_TRACE_CTA(blockIdx.x))
+    printf("trace shared cta %d warp %d: pieces %d tiles %lld cycles %lld setup %lld wait %lld math %lld end %lld\n",
+           blockIdx.x, warp, p1 - p0, tr_tiles, clock64() - tr_c0, tr_setup, tr_wait, tr_math, tr_end);
+#endif
+}
+
+struct MergeArgs {
+  void *out;             // [S][Hq][D], element type T
+  const float *out_f32;  // [S][Hq][D] the own-block rows, normalised
+  const float *lse;      // [S][Hq] their log2-sum-exp (-inf: no own tokens)
+  const float *records;  // step 1's partial states
+  const int32_t *plan;
+  SharePlanHeader h;
+  int S, Hq;
+};
+
+constexpr int kMergeWarps = 8;
+
+// One warp per output row; lane i owns dims 4i .. 4i+3 (D = 128) or
+// 2i .. 2i+1 (D = 64).  A row with no state at all (empty sequence) is zero.
+template <typename T, int D>
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_shared_kernel(const MergeArgs a) {
+  constexpr int R = state_row(D);
+  constexpr int V = D / 32;  // dims per lane
+  const long long row = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= (long long)a.S * a.Hq) return;
+  const int32_t *P = a.plan;
+  const SharePlanHeader &h = a.h;
+  const int s = int(row / a.Hq), hq = int(row % a.Hq);
+  const int Gq = h.group_size;
+  const int kvh = hq / Gq, hh = hq % Gq;
+
+  float M = a.lse[row];
+  const bool own = M > -CUDART_INF_F;
+  float den = own ? 1.f : 0.f;
+  float num[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) num[v] = own ? a.out_f32[row * D + lane * V + v] : 0.f;
+  for (int k = P[h.s_moff + s]; k < P[h.s_moff + s + 1]; ++k) {
+    const int g = P[h.s_mgroup + k];
+    const int r = P[h.s_midx + k] * Gq + hh;
+    const int u = P[h.g_ubase + g] + kvh * P[h.g_passes + g] + r / kSharePassRows;
+    for (int p = P[h.u_poff + u]; p < P[h.u_poff + u + 1]; ++p) {
+      const float *rec = a.records + ((long long)p * kSharePassRows + r % kSharePassRows) * R;
+      const float m = __ldcg(rec + D), l = __ldcg(rec + D + 1);
+      float acc[V];
+#pragma unroll
+      for (int v = 0; v < V; ++v) acc[v] = __ldcg(rec + lane * V + v);
+      if (m > M) {
+        const float sc = fast_exp2(M - m);  // 0 while M is still -inf
+#pragma unroll
+        for (int v = 0; v < V; ++v) num[v] = num[v] * sc + acc[v];
+        den = den * sc + l;
+        M = m;
+      } else if (m > -CUDART_INF_F) {
+        const float f = fast_exp2(m - M);
+#pragma unroll
+        for (int v = 0; v < V; ++v) num[v] += f * acc[v];
+        den += f * l;
+      }
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  T *o = static_cast<T *>(a.out) + row * D + lane * V;
+#pragma unroll
+  for (int v = 0; v < V; ++v) o[v] = Elem<T>::from_float(num[v] * inv);
+}
+
+}  // namespace pagedkv

@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
   __syncthreads();
 
   const Plan plan = sh_plan;
-  const long long W = plan.W, w0 = plan.w0, w1 = plan.w1;
+  const long long w0 = plan.w0, w1 = plan.w1;
   if (w0 >= w1) {  // fewer tiles than CTAs: nothing to stream, only empty rows to zero
     if (warp == kMergerWarp) zero_empty_rows<T>(a, D, lane, 32);
     return;
@@ -186,10 +186,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
       wk.start(a, plan.s0, plan.r0, from);
     while (wk.w < to) {
       const int n = wk.seg_len(to);
-      const int s = wk.s, nb = wk.nb, pc = wk.pc, b = wk.b;
-      const long long w = wk.w;
-      const bool complete = (b == 0 && n == nb);
-      const bool first_seg = (w == w0);
+      const int s = wk.s, pc = wk.pc, b = wk.b;
       const int kvh = pc / HC;
       const int hq0 = kvh * G + (pc % HC) * GT;
       const int L = wk.L;

@@ -41,6 +41,9 @@ def _load() -> ctypes.CDLL:
         "pa_copy_blocks": [vp, vp, vp, i64, i32, i32, i32, i64, i32, vp, vp],
         "pa_decode": [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, sz, vp, vp],
         "pa_decode_noalloc": [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp],
+        "pa_share_plan": [vp, i32, vp, i32, i32, i32, i32, i32, vp, sz, ctypes.POINTER(sz)],
+        "pa_decode_shared": [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp, vp, sz,
+                             vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -48,6 +51,8 @@ def _load() -> ctypes.CDLL:
         fn.restype = i32
     lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
     lib.pa_decode_workspace_size.restype = sz
+    lib.pa_decode_shared_workspace_size.argtypes = [vp, i32, i32, i32, i32]
+    lib.pa_decode_shared_workspace_size.restype = sz
     lib.pa_decode_grid_size.argtypes = []
     lib.pa_decode_grid_size.restype = i32
     lib.pa_status_string.argtypes = [i32]
@@ -225,6 +230,81 @@ def pa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                                  block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), S, Hq, Hkv,
                                  D, B, NB, float(scale), _DTYPES[q.dtype], _ptr(err), _stream(dev)),
            "pa_decode_noalloc")
+    return out
+
+
+# Field order of the plan header (csrc/pa_share_plan.h); each array field is
+# the array's offset in ints from the start of the plan.
+PLAN_FIELDS = ["magic", "total_ints", "num_seqs", "num_groups", "num_units", "num_pieces", "nctas", "group_size",
+               "num_kv_heads", "block_size", "max_blocks", "total_members", "total_memberships", "g_moff",
+               "g_members", "g_b0", "g_b1", "g_ubase", "g_passes", "u_group", "u_kvh", "u_pass", "u_poff", "p_unit",
+               "p_t0", "p_t1", "c_poff", "s_start", "s_moff", "s_mgroup", "s_midx"]
+
+
+def share_plan(block_tables: torch.Tensor, context_lens: torch.Tensor, block_size: int, num_heads: int,
+               num_kv_heads: int, nctas: Optional[int] = None) -> torch.Tensor:
+    """pa_share_plan on host copies of the tables: the plan as a CPU int32
+    tensor (copy it to the device for pa_decode_shared)."""
+    tables = block_tables.detach().to("cpu", torch.int32).contiguous()
+    lens = context_lens.detach().to("cpu", torch.int32).contiguous()
+    S, width = tables.shape
+    if lens.numel() != S:
+        raise ValueError("context_lens and block_tables differ in rows")
+    n = lib.pa_decode_grid_size() if nctas is None else int(nctas)
+    need = ctypes.c_size_t(0)
+    _check(lib.pa_share_plan(tables.data_ptr(), width, lens.data_ptr(), S, block_size, num_heads, num_kv_heads, n,
+                             None, 0, ctypes.byref(need)), "pa_share_plan")
+    plan = torch.zeros(int(need.value), dtype=torch.int32)
+    _check(lib.pa_share_plan(tables.data_ptr(), width, lens.data_ptr(), S, block_size, num_heads, num_kv_heads, n,
+                             plan.data_ptr(), plan.numel(), ctypes.byref(need)), "pa_share_plan")
+    return plan
+
+
+def plan_fields(plan: torch.Tensor) -> dict:
+    """The plan's header as a dict, and its arrays (numpy) under their names."""
+    p = plan.numpy()
+    hdr = {k: int(p[i]) for i, k in enumerate(PLAN_FIELDS)}
+    n = {"g_moff": hdr["num_groups"] + 1, "g_members": hdr["total_members"], "g_b0": hdr["num_groups"],
+         "g_b1": hdr["num_groups"], "g_ubase": hdr["num_groups"], "g_passes": hdr["num_groups"],
+         "u_group": hdr["num_units"], "u_kvh": hdr["num_units"], "u_pass": hdr["num_units"],
+         "u_poff": hdr["num_units"] + 1, "p_unit": hdr["num_pieces"], "p_t0": hdr["num_pieces"],
+         "p_t1": hdr["num_pieces"], "c_poff": hdr["nctas"] + 1, "s_start": hdr["num_seqs"],
+         "s_moff": hdr["num_seqs"] + 1, "s_mgroup": hdr["total_memberships"], "s_midx": hdr["total_memberships"]}
+    out = dict(hdr)
+    for k, cnt in n.items():
+        out[k + "_arr"] = p[hdr[k]:hdr[k] + cnt]
+    return out
+
+
+def new_shared_workspace(plan_host: torch.Tensor, num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                         device) -> torch.Tensor:
+    nbytes = lib.pa_decode_shared_workspace_size(plan_host.data_ptr(), num_seqs, num_heads, num_kv_heads, head_dim)
+    if nbytes == 0:
+        raise PagedKVError("pa_decode_shared_workspace_size: invalid arguments")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+def pa_decode_shared(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                     context_lens: torch.Tensor, scale: float, plan_host: torch.Tensor, plan_dev: torch.Tensor,
+                     out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                     err: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """pa_decode reading each shared block once per group of sharers, with a
+    plan from ``share_plan`` (host copy and a device copy of it)."""
+    if plan_host.device.type != "cpu" or plan_host.dtype != torch.int32 or not plan_host.is_contiguous():
+        raise ValueError("plan_host must be a contiguous CPU int32 tensor")
+    if workspace is None:
+        S, Hq, D = q.shape
+        workspace = new_shared_workspace(plan_host, S, Hq, k_cache.shape[1], D, q.device)
+    NB, Hkv, B, D, S, Hq, out, workspace = _decode_args(q, k_cache, v_cache, block_tables, context_lens, out,
+                                                        workspace)
+    _need(plan_dev, "plan_dev", torch.int32, 1, q.device)
+    if plan_dev.numel() != plan_host.numel():
+        raise ValueError("plan_dev and plan_host differ in size")
+    _check(lib.pa_decode_shared(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), S, Hq, Hkv,
+                                D, B, NB, float(scale), _DTYPES[q.dtype], plan_host.data_ptr(), plan_dev.data_ptr(),
+                                workspace.data_ptr(), workspace.numel(), _ptr(err), _stream(q.device)),
+           "pa_decode_shared")
     return out
 
 

@@ -29,19 +29,34 @@ class DecodeStep:
     ``inp`` carries q, k_cache, v_cache, block_tables, context_lens, scale,
     new_key, new_value, new_seq, new_pos and copy_pairs (the layout of
     ``workloads.DecodeInputs``).  ``graphs=False`` launches the kernels one by
-    one instead (same results, for comparison).
+    one instead (same results, for comparison).  ``shared=True`` decodes with
+    pa_decode_shared, reading each block that several sequences share once
+    per group (the plan is built here from the tables).
     """
 
-    def __init__(self, inp, graphs: bool = True):
+    def __init__(self, inp, graphs: bool = True, shared: bool = False):
         self.inp = inp
         dev = inp.q.device
         S, Hq, D = inp.q.shape
-        Hkv = inp.k_cache.shape[1]
+        Hkv, B = inp.k_cache.shape[1], inp.k_cache.shape[2]
         self.out = torch.empty_like(inp.q)
-        self.workspace = ops.new_workspace(S, Hq, Hkv, D, dev)
+        self.shared = shared
+        decode_launches = 1
+        if shared:
+            # the plan follows the tables as the decode sees them; this step
+            # only writes into private blocks, so it stays valid across replays
+            self.plan = ops.share_plan(inp.block_tables, inp.context_lens, B, Hq, Hkv)
+            self.plan_dev = self.plan.to(dev)
+            self.plan_info = {k: v for k, v in ops.plan_fields(self.plan).items() if not k.endswith("_arr")}
+            self.workspace = ops.new_shared_workspace(self.plan, S, Hq, Hkv, D, dev)
+            if self.plan_info["num_groups"] > 0:
+                decode_launches = 3  # shared blocks, own blocks, merge
+        else:
+            self.workspace = ops.new_workspace(S, Hq, Hkv, D, dev)
         self.slots = torch.empty(inp.new_seq.numel(), dtype=torch.int64, device=dev)
         self.err = ops.new_error_word(dev)
-        self.launches_per_step = (1 if inp.copy_pairs.numel() else 0) + (2 if inp.new_seq.numel() else 0) + 1
+        self.launches_per_step = (1 if inp.copy_pairs.numel() else 0) + (2 if inp.new_seq.numel() else 0) + \
+            decode_launches
         self.graphs = graphs
         self._pre: Optional[torch.cuda.CUDAGraph] = None
         self._dec: Optional[torch.cuda.CUDAGraph] = None
@@ -69,8 +84,12 @@ class DecodeStep:
 
     def _run_decode(self):
         inp = self.inp
-        ops.pa_decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale, self.out,
-                      self.workspace, self.err)
+        if self.shared:
+            ops.pa_decode_shared(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale,
+                                 self.plan, self.plan_dev, self.out, self.workspace, self.err)
+        else:
+            ops.pa_decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale, self.out,
+                          self.workspace, self.err)
 
     def run(self, ev_decode_start=None, ev_decode_end=None) -> torch.Tensor:
         """Enqueue one step on the current stream; optional events bracket the

@@ -1,0 +1,159 @@
+"""pa_decode_shared: the decode that reads each shared block once per group of
+sharers (plan from pa_share_plan), against the float64 oracle, on the
+shared-prefix and long-context workloads (small and full size), a nested
+beam-like trie, and edge cases.  It must also agree with pa_decode."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_utils import assert_attention_close, oracle_step
+from oracle import native
+from paged_kv_cache_170_gb300 import scenarios
+from paged_kv_cache_170_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def ops():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_170_gb300 import build
+
+    build.build()
+    from paged_kv_cache_170_gb300 import ops as _ops
+
+    return _ops
+
+
+def _pre_step(ops, inp):
+    """The step's copies, slot lookup and writes (the state the decode reads)."""
+    err = ops.new_error_word(inp.q.device)
+    if inp.copy_pairs.numel():
+        ops.pa_copy_blocks(inp.k_cache, inp.v_cache, inp.copy_pairs, err)
+    if inp.new_seq.numel():
+        slots = ops.pa_slot_mapping(inp.block_tables, inp.new_seq, inp.new_pos, inp.k_cache.shape[2],
+                                    inp.k_cache.shape[0], None, err)
+        ops.pa_write_kv(inp.new_key, inp.new_value, inp.k_cache, inp.v_cache, slots, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+
+
+def _shared(ops, q, kc, vc, tables, lens, scale, workspace=None):
+    plan = ops.share_plan(tables, lens, kc.shape[2], q.shape[1], kc.shape[1])
+    plan_dev = plan.to(q.device)
+    err = ops.new_error_word(q.device)
+    out = ops.pa_decode_shared(q, kc, vc, tables, lens, scale, plan, plan_dev, workspace=workspace, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, ops.error_names(int(err.item()))
+    return out, ops.plan_fields(plan)
+
+
+def _small(name, seed=0):
+    if name == "prefix":
+        return scenarios.shared_prefix_inputs(seed, num_parents=4, prefix_tokens=256, suffix_max=300,
+                                              w=W.scaled(W.PREFIX, num_blocks=300, max_blocks_per_seq=40))
+    if name == "longctx":
+        return scenarios.long_context_inputs(seed, num_prompts=2, branches=3, prompt_tokens=2048, suffix_max=200,
+                                             w=W.scaled(W.LONGCTX, num_blocks=200, max_blocks_per_seq=80))
+    if name == "prefix_wide":  # 20 sharers x 4 heads = 80 rows: three passes per kv head
+        return scenarios.shared_prefix_inputs(seed, num_parents=10, prefix_tokens=320, suffix_max=100,
+                                              w=W.scaled(W.PREFIX, num_blocks=400, max_blocks_per_seq=40))
+    raise KeyError(name)
+
+
+@pytest.mark.parametrize("name", ["prefix", "longctx", "prefix_wide"])
+def test_shared_decode_small_matches_oracle_and_plain_decode(ops, name):
+    cpu = _small(name)
+    inp = cpu.to(DEV)
+    _pre_step(ops, inp)
+    out, f = _shared(ops, inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale)
+    assert f["num_groups"] > 0
+    _, _, _, ref = oracle_step(cpu)
+    assert_attention_close(out, ref, strict=True)
+    plain = ops.pa_decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale)
+    torch.cuda.synchronize()
+    assert (out.float() - plain.float()).abs().max().item() <= 4e-3
+
+
+@pytest.mark.parametrize("name,sample", [("prefix", None), ("longctx", [0, 3, 6, 13, 22, 31])])
+def test_shared_decode_full_size(ops, name, sample):
+    inp = scenarios.shared_prefix_inputs(0, device=DEV) if name == "prefix" else \
+        scenarios.long_context_inputs(0, device=DEV)
+    cpu = inp.to("cpu")
+    _pre_step(ops, inp)
+    out, f = _shared(ops, inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale)
+    assert f["num_groups"] > 0
+    _, _, _, ref = oracle_step(cpu, seqs=sample)
+    got = out if sample is None else out[torch.as_tensor(sample, device=out.device)]
+    print(name, assert_attention_close(got, ref, strict=True), "groups", f["num_groups"], "pieces", f["num_pieces"])
+
+
+def _random_pool(S, Hq, Hkv, D, B, NB, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(S, Hq, D, generator=g).to(dtype)
+    kc = torch.randn(NB, Hkv, B, D, generator=g).to(dtype)
+    vc = torch.randn(NB, Hkv, B, D, generator=g).to(dtype)
+    return q, kc, vc
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_shared_decode_edge_cases(ops, dtype):
+    """Identical tables with a partial tail, an empty sequence, a sequence
+    shorter than one block, a sequence whose blocks are all shared, and a
+    sequence outside every group; head_dim 64 and 128."""
+    for D in (64, 128):
+        S, Hq, Hkv, B, NB = 6, 8, 2, 16, 64
+        q, kc, vc = _random_pool(S, Hq, Hkv, D, B, NB, dtype, seed=D)
+        row = list(range(10))
+        tables = torch.tensor([row, row, row, row, row, list(range(20, 30))], dtype=torch.int32)
+        lens = torch.tensor([150, 150, 0, 7, 144, 150], dtype=torch.int32)
+        scale = 1.0 / math.sqrt(D)
+        args = [x.to(DEV) for x in (q, kc, vc, tables, lens)]
+        out, f = _shared(ops, *args, scale)
+        assert f["num_groups"] >= 1
+        ref = native.decode(q, kc, vc, tables.numpy(), lens.numpy(), scale)
+        assert_attention_close(out, ref, strict=False)
+        assert torch.count_nonzero(out[2]) == 0  # empty sequence: zero row
+
+
+def test_shared_decode_deterministic_reusable_workspace_and_no_group_plan(ops):
+    cpu = _small("prefix", seed=1)
+    inp = cpu.to(DEV)
+    _pre_step(ops, inp)
+    plan = ops.share_plan(inp.block_tables, inp.context_lens, 16, inp.q.shape[1], inp.k_cache.shape[1])
+    ws = ops.new_shared_workspace(plan, inp.q.shape[0], inp.q.shape[1], inp.k_cache.shape[1], inp.q.shape[2], DEV)
+    pd = plan.to(DEV)
+    a = ops.pa_decode_shared(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale, plan,
+                             pd, workspace=ws).clone()
+    b = ops.pa_decode_shared(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale, plan,
+                             pd, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    # tables without sharing: the plan has no groups and the call is pa_decode
+    g = W.make_inputs(W.scaled(W.GQA, num_seqs=3, num_blocks=3 * 256 + 5), 0).to(DEV)
+    out, f = _shared(ops, g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale)
+    assert f["num_groups"] == 0
+    plain = ops.pa_decode(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out, plain)
+
+
+def test_shared_decode_rejects_fp32_and_mismatched_plans(ops):
+    q, kc, vc = _random_pool(2, 4, 2, 64, 16, 8, torch.float32, seed=0)
+    tables = torch.tensor([[0, 1], [0, 1]], dtype=torch.int32)
+    lens = torch.tensor([32, 32], dtype=torch.int32)
+    plan = ops.share_plan(tables, lens, 16, 4, 2)
+    with pytest.raises(ops.PagedKVError, match="UNSUPPORTED"):
+        ops.pa_decode_shared(q.to(DEV), kc.to(DEV), vc.to(DEV), tables.to(DEV), lens.to(DEV), 0.1, plan,
+                             plan.to(DEV))
+    q16 = q.to(torch.bfloat16).to(DEV)
+    other = ops.share_plan(tables, lens, 16, 8, 2)  # built for 8 query heads
+    with pytest.raises(ops.PagedKVError, match="INVALID"):
+        ops.pa_decode_shared(q16, kc.to(torch.bfloat16).to(DEV), vc.to(torch.bfloat16).to(DEV), tables.to(DEV),
+                             lens.to(DEV), 0.1, other, other.to(DEV), workspace=torch.zeros(1 << 22,
+                                                                                             dtype=torch.uint8,
+                                                                                             device=DEV))

@@ -74,3 +74,16 @@ def test_graph_step_follows_inputs_updated_in_place(step_mod):
         assert torch.equal(out_g, ref)
         _, _, _, oref = oracle_step(dev_in.to("cpu"))
         assert_attention_close(out_g, oref, strict=False)
+
+
+@pytest.mark.parametrize("name", ["prefix"])
+def test_graph_step_with_shared_decode(step_mod, name):
+    inp_cpu = _case(name)
+    _, _, _, ref = oracle_step(inp_cpu)
+    runner = step_mod.DecodeStep(inp_cpu.to("cuda"), graphs=True, shared=True)
+    assert runner.plan_info["num_groups"] > 0
+    for _ in range(2):
+        out = runner.run()
+    torch.cuda.synchronize()
+    assert int(runner.err.item()) == 0
+    assert_attention_close(out, ref, strict=True)

@@ -1,0 +1,254 @@
+"""The shared-block decode plan (pa_share_plan, host code: no GPU needed).
+
+Structural checks of the plan against the block tables it was built from,
+and a float64 numpy walk through the plan -- partial states per piece and
+row, the private part per sequence, then the merge -- that must reproduce
+the oracle's decode: the plan's split of the work is complete and does not
+overlap.  (The GPU tests then check the kernels that follow the plan.)
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import reference
+from paged_kv_cache_170_gb300 import build, scenarios
+from paged_kv_cache_170_gb300 import workloads as W
+from paged_kv_cache_170_gb300.block_manager import BlockManager
+
+PASS_ROWS = 32
+
+
+@pytest.fixture(scope="module")
+def ops():
+    build.build()
+    from paged_kv_cache_170_gb300 import ops as _ops
+
+    return _ops
+
+
+def _prefix_small(seed=0):
+    return scenarios.shared_prefix_inputs(seed, num_parents=4, prefix_tokens=256, suffix_max=300,
+                                          w=W.scaled(W.PREFIX, num_blocks=300, max_blocks_per_seq=40))
+
+
+def _longctx_small(seed=0):
+    return scenarios.long_context_inputs(seed, num_prompts=2, branches=3, prompt_tokens=2048, suffix_max=200,
+                                         w=W.scaled(W.LONGCTX, num_blocks=200, max_blocks_per_seq=80))
+
+
+def _beam_like(seed=0):
+    """A deeper trie: one root prompt, forked twice, each child forked again,
+    with appends between forks (groups nest three levels)."""
+    B, Hkv, Hq, D, NB = 16, 2, 8, 64, 400
+    g = torch.Generator().manual_seed(seed)
+    mgr = BlockManager(NB, B, free_order=torch.randperm(NB, generator=g).tolist())
+    mgr.allocate(0, 16 * 6)  # 6 full blocks
+    for child, parent in [(1, 0), (2, 0)]:
+        mgr.fork(child, parent)
+    for s in (0, 1, 2):
+        for _ in range(16 * (s + 1) + 3):
+            mgr.append_slot(s)
+    for child, parent in [(3, 1), (4, 2), (5, 2)]:
+        mgr.fork(child, parent)
+    for s in range(6):
+        for _ in range(5 + 7 * s):
+            mgr.append_slot(s)
+    S = 6
+    tables = torch.as_tensor(mgr.block_tables(list(range(S)), 40, pad=0), dtype=torch.int32)
+    lens = torch.as_tensor(mgr.context_lens(list(range(S))), dtype=torch.int32)
+    q = torch.randn(S, Hq, D, generator=g).to(torch.bfloat16)
+    kc = torch.randn(NB, Hkv, B, D, generator=g).to(torch.bfloat16)
+    vc = torch.randn(NB, Hkv, B, D, generator=g).to(torch.bfloat16)
+    return q, kc, vc, tables, lens, 1.0 / math.sqrt(D)
+
+
+def _case(name):
+    if name == "beam":
+        return _beam_like()
+    inp = _prefix_small() if name == "prefix" else _longctx_small()
+    # the plan is built from the tables as the decode sees them (after the step's copies / writes)
+    return inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale
+
+
+def _check_structure(f, tables, lens, B, Hq, Hkv):
+    S = tables.shape[0]
+    Gq = Hq // Hkv
+    full = [int(L) // B for L in lens]
+    nb = [-(-int(L) // B) for L in lens]
+    moff, mem = f["g_moff_arr"], f["g_members_arr"]
+    b0, b1 = f["g_b0_arr"], f["g_b1_arr"]
+    start = f["s_start_arr"]
+    for g in range(f["num_groups"]):
+        members = mem[moff[g]:moff[g + 1]]
+        assert len(members) >= 2 and list(members) == sorted(set(members))
+        assert 0 <= b0[g] < b1[g]
+        for s in members:
+            assert full[s] >= b1[g], "a group block must be full for every member"
+            assert np.array_equal(tables[s, b0[g]:b1[g]], tables[members[0], b0[g]:b1[g]])
+        # maximal: the run cannot be extended by one block
+        e = b1[g]
+        extendable = all(full[s] > e for s in members) and len({int(tables[s, e]) for s in members}) == 1
+        assert not extendable, f"group {g} could extend past block {e}"
+        assert f["g_passes_arr"][g] == -(-len(members) * Gq // PASS_ROWS)
+    # memberships of each sequence chain from block 0 to its private start
+    for s in range(S):
+        ks = range(f["s_moff_arr"][s], f["s_moff_arr"][s + 1])
+        runs = sorted((b0[f["s_mgroup_arr"][k]], b1[f["s_mgroup_arr"][k]]) for k in ks)
+        at = 0
+        for x, y in runs:
+            assert x == at
+            at = y
+        assert at == start[s] <= full[s] <= nb[s]
+        for k in ks:  # member index points back at s
+            g, i = f["s_mgroup_arr"][k], f["s_midx_arr"][k]
+            assert mem[moff[g] + i] == s
+    # trie property: two sequences with identical full blocks [0, k) share groups covering [0, k)
+    for s1 in range(S):
+        for s2 in range(s1 + 1, S):
+            k = 0
+            while k < min(full[s1], full[s2]) and tables[s1, k] == tables[s2, k]:
+                k += 1
+            g1 = {f["s_mgroup_arr"][j] for j in range(f["s_moff_arr"][s1], f["s_moff_arr"][s1 + 1])}
+            g2 = {f["s_mgroup_arr"][j] for j in range(f["s_moff_arr"][s2], f["s_moff_arr"][s2 + 1])}
+            covered = sum(b1[g] - b0[g] for g in g1 & g2)
+            assert covered == k, (s1, s2, covered, k)
+    # pieces: each unit's tiles exactly once, in order; CTA ranges balanced
+    U, P, N = f["num_units"], f["num_pieces"], f["nctas"]
+    poff = f["u_poff_arr"]
+    for u in range(U):
+        g = f["u_group_arr"][u]
+        ps = range(poff[u], poff[u + 1])
+        assert all(f["p_unit_arr"][p] == u for p in ps)
+        t = 0
+        for p in ps:
+            assert f["p_t0_arr"][p] == t and f["p_t1_arr"][p] > t
+            t = f["p_t1_arr"][p]
+        assert t == b1[g] - b0[g]
+        assert u == f["g_ubase_arr"][g] + f["u_kvh_arr"][u] * f["g_passes_arr"][g] + f["u_pass_arr"][u]
+    # CTA ranges: contiguous, covering all tiles, balanced in cost (a tile of a
+    # unit whose pass has <= 8, <= 16 or more rows costs 3, 4 or 5), to within
+    # one tile of the dearest unit
+    def cost(u):
+        g = f["u_group_arr"][u]
+        rows = (moff[g + 1] - moff[g]) * Gq - f["u_pass_arr"][u] * PASS_ROWS
+        return 3 if rows <= 8 else (4 if rows <= 16 else 5)
+
+    per_cta = [sum((f["p_t1_arr"][p] - f["p_t0_arr"][p]) * cost(f["p_unit_arr"][p])
+                   for p in range(f["c_poff_arr"][c], f["c_poff_arr"][c + 1])) for c in range(N)]
+    total = sum((b1[f["u_group_arr"][u]] - b0[f["u_group_arr"][u]]) * cost(u) for u in range(U))
+    assert f["c_poff_arr"][N] == P and sum(per_cta) == total
+    if U:
+        assert max(per_cta) - total / N <= max(cost(u) for u in range(U))
+
+
+def _softmax_state(qv, keys, vals):
+    """(acc, m, l) of one query row over some tokens, natural-log domain."""
+    s = keys @ qv
+    m = s.max()
+    w = np.exp(s - m)
+    return w @ vals, m, w.sum()
+
+
+def _emulate(f, q, kc, vc, tables, lens, scale):
+    """The three steps of the shared decode, in float64, driven by the plan."""
+    q, K, V = (x.double().numpy() for x in (q, kc, vc))
+    tables, lens = tables.numpy(), lens.numpy()
+    S, Hq, D = q.shape
+    Hkv, B = K.shape[1], K.shape[2]
+    Gq = Hq // Hkv
+    moff, mem = f["g_moff_arr"], f["g_members_arr"]
+    records = {}
+    for p in range(f["num_pieces"]):
+        u = f["p_unit_arr"][p]
+        g, kvh, ps = f["u_group_arr"][u], f["u_kvh_arr"][u], f["u_pass_arr"][u]
+        members = mem[moff[g]:moff[g + 1]]
+        first = f["g_b0_arr"][g] + f["p_t0_arr"][p]
+        blocks = tables[members[0], first:f["g_b0_arr"][g] + f["p_t1_arr"][p]]
+        ntok = min(len(blocks) * B, int(lens[members[0]]) - first * B)  # a last block may be partly filled
+        keys = np.concatenate([K[b, kvh] for b in blocks])[:ntok]
+        vals = np.concatenate([V[b, kvh] for b in blocks])[:ntok]
+        for r in range(ps * PASS_ROWS, min(ps * PASS_ROWS + PASS_ROWS, len(members) * Gq)):
+            s, hh = members[r // Gq], r % Gq
+            records[(p, r % PASS_ROWS)] = _softmax_state(q[s, kvh * Gq + hh] * scale, keys, vals)
+    out = np.zeros_like(q)
+    for s in range(S):
+        L, st = int(lens[s]), int(f["s_start_arr"][s])
+        for h in range(Hq):
+            kvh, hh = h // Gq, h % Gq
+            states = []
+            if L > st * B:  # the sequence's own tokens st*B .. L-1
+                toks = range(st * B, L)
+                keys = np.stack([K[tables[s, t // B], kvh, t % B] for t in toks])
+                vals = np.stack([V[tables[s, t // B], kvh, t % B] for t in toks])
+                states.append(_softmax_state(q[s, h] * scale, keys, vals))
+            for k in range(f["s_moff_arr"][s], f["s_moff_arr"][s + 1]):
+                g, mi = f["s_mgroup_arr"][k], f["s_midx_arr"][k]
+                r = mi * Gq + hh
+                u = f["g_ubase_arr"][g] + kvh * f["g_passes_arr"][g] + r // PASS_ROWS
+                for p in range(f["u_poff_arr"][u], f["u_poff_arr"][u + 1]):
+                    states.append(records[(p, r % PASS_ROWS)])
+            if states:
+                M = max(m for _, m, _ in states)
+                num = sum(a * np.exp(m - M) for a, m, _ in states)
+                den = sum(l * np.exp(m - M) for _, m, l in states)
+                out[s, h] = num / den
+    return out
+
+
+@pytest.mark.parametrize("name,nctas", [("prefix", 7), ("prefix", 304), ("longctx", 5), ("beam", 3)])
+def test_plan_structure_and_emulated_decode_match_oracle(ops, name, nctas):
+    q, kc, vc, tables, lens, scale = _case(name)
+    B, Hq, Hkv = kc.shape[2], q.shape[1], kc.shape[1]
+    plan = ops.share_plan(tables, lens, B, Hq, Hkv, nctas=nctas)
+    f = ops.plan_fields(plan)
+    assert f["num_groups"] > 0
+    _check_structure(f, tables.numpy(), lens.numpy(), B, Hq, Hkv)
+    got = _emulate(f, q, kc, vc, tables, lens, scale)
+    ref = reference.decode(q, kc, vc, tables.numpy(), lens.numpy(), scale)
+    np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_plan_of_unshared_tables_has_no_groups(ops):
+    inp = W.make_inputs(W.scaled(W.GQA, num_seqs=4, num_blocks=4 * 256 + 3), 0)
+    plan = ops.share_plan(inp.block_tables, inp.context_lens, 16, 32, 8, nctas=11)
+    f = ops.plan_fields(plan)
+    assert f["num_groups"] == 0 and f["num_pieces"] == 0
+    assert list(f["s_start_arr"]) == [0] * 4
+    _check_structure(f, inp.block_tables.numpy(), inp.context_lens.numpy(), 16, 32, 8)
+
+
+def test_plan_edge_cases(ops):
+    # identical tables: one group over all full blocks; the partial tail, an
+    # empty sequence and a one-token sequence stay private
+    B = 16
+    row = list(range(10))
+    tables = torch.tensor([row, row, row, row], dtype=torch.int32)
+    lens = torch.tensor([150, 150, 0, 7], dtype=torch.int32)  # 9 full blocks + 6 tokens
+    f = ops.plan_fields(ops.share_plan(tables, lens, B, 4, 2, nctas=3))
+    assert f["num_groups"] == 1
+    assert list(f["g_members_arr"]) == [0, 1] and (f["g_b0_arr"][0], f["g_b1_arr"][0]) == (0, 9)
+    assert list(f["s_start_arr"]) == [9, 9, 0, 0]
+    _check_structure(f, tables.numpy(), lens.numpy(), B, 4, 2)
+    # 40 members x 4 heads = 160 rows: 5 passes per kv head
+    tables = torch.tensor([row] * 40, dtype=torch.int32)
+    lens = torch.full((40,), 64, dtype=torch.int32)
+    f = ops.plan_fields(ops.share_plan(tables, lens, B, 8, 2, nctas=9))
+    assert f["num_groups"] == 1 and f["g_passes_arr"][0] == 5 and f["num_units"] == 10
+    assert list(f["s_start_arr"]) == [4] * 40  # every block shared: nothing of their own
+
+
+def test_plan_rejects_bad_arguments_and_small_buffers(ops):
+    import ctypes
+
+    tables = torch.zeros(2, 4, dtype=torch.int32)
+    lens = torch.tensor([16, 16], dtype=torch.int32)
+    need = ctypes.c_size_t(0)
+    assert ops.lib.pa_share_plan(tables.data_ptr(), 4, lens.data_ptr(), 2, 16, 6, 4, 8, None, 0,
+                                 ctypes.byref(need)) == 1  # heads not a multiple of kv heads
+    assert ops.lib.pa_share_plan(tables.data_ptr(), 4, lens.data_ptr(), 2, 16, 8, 4, 8, None, 0,
+                                 ctypes.byref(need)) == 0
+    small = torch.zeros(int(need.value) - 1, dtype=torch.int32)
+    assert ops.lib.pa_share_plan(tables.data_ptr(), 4, lens.data_ptr(), 2, 16, 8, 4, 8, small.data_ptr(),
+                                 small.numel(), ctypes.byref(need)) == 4  # PA_ERR_WORKSPACE
