@@ -68,16 +68,18 @@ def profiled_traffic(workload: str):
     return float(m_bytes.group(1))
 
 
-def workload_inputs(name: str, seed: int, device, num_seqs=None):
+def workload_inputs(name: str, seed: int, device, num_seqs=None, placement: str = "random"):
     """Inputs of a named workload; ``num_seqs`` shrinks the plain workloads (and
-    their pools) to fewer sequences of the same shape, for profiler captures."""
+    their pools) to fewer sequences of the same shape, for profiler captures;
+    ``placement`` "contiguous" gives each sequence of a plain workload one run
+    of consecutive physical blocks instead of random ones."""
     from paged_kv_cache_170_gb300 import scenarios, workloads
 
     if name == "prefix":
         return scenarios.shared_prefix_inputs(seed, device=device)
     if name == "longctx":
         return scenarios.long_context_inputs(seed, device=device)
-    w = workloads.WORKLOADS[name]
+    w = workloads.scaled(workloads.WORKLOADS[name], placement=placement)
     if num_seqs is not None and name != "tiny":
         w = workloads.scaled(w, num_seqs=num_seqs, num_blocks=num_seqs * w.max_blocks_per_seq + 64)
     return workloads.make_inputs(w, seed, device=device)
@@ -127,6 +129,18 @@ def algorithmic_bytes(inp) -> int:
     return kv_bytes(inp) + 2 * inp.q.numel() * inp.q.element_size() + entries * 4 * Hkv + lens.numel() * 4
 
 
+def memory_report(inp) -> dict:
+    """The pages' memory figures (waste ratio, its half-block estimate, memory
+    saved by sharing, use against a contiguous max-length reservation) for
+    this step's block tables."""
+    from paged_kv_cache_170_gb300.block_manager import pool_report
+
+    _, Hkv, B, D = inp.k_cache.shape
+    rep = pool_report(inp.block_tables.cpu().numpy(), inp.context_lens.cpu().numpy(), B,
+                      2 * Hkv * D * inp.k_cache.element_size(), max_len=inp.block_tables.shape[1] * B)
+    return {k: round(v, 6) if isinstance(v, float) else v for k, v in rep.items()}
+
+
 def workload_config(name: str, inp) -> dict:
     w = inp.workload
     lens = inp.context_lens.to(torch.int64)
@@ -141,7 +155,7 @@ def workload_config(name: str, inp) -> dict:
             "head_dim": int(inp.q.shape[2]), "pool_blocks": int(inp.k_cache.shape[0]),
             "context_min": int(lens.min()), "context_max": int(lens.max()), "context_sum": int(lens.sum()),
             "cow_pairs": int(inp.copy_pairs.shape[0]), "new_tokens": int(inp.new_seq.numel()),
-            "l2_policy": l2}
+            "l2_policy": l2, "placement": w.placement, "memory": memory_report(inp)}
 
 
 class ClockSampler:
@@ -268,7 +282,7 @@ def run_gpu(args) -> dict:
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     # every rank runs its own replica of the workload on different data (weak scaling)
-    inp = workload_inputs(args.workload, args.seed + rank, dev, args.num_seqs)
+    inp = workload_inputs(args.workload, args.seed + rank, dev, args.num_seqs, args.placement)
     S, Hq, D = inp.q.shape
     stream = torch.cuda.current_stream(dev)
     from paged_kv_cache_170_gb300.step import DecodeStep
@@ -454,6 +468,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-seqs", type=int, default=None, help="fewer sequences (profiling captures only)")
     ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one")
+    ap.add_argument("--placement", choices=["random", "contiguous"], default="random",
+                    help="physical placement of the plain workloads' blocks")
     ap.add_argument("--shared", action="store_true",
                     help="decode with pa_decode_shared (each shared block read once per group of sharers)")
     args = ap.parse_args(argv)

@@ -35,6 +35,7 @@ class Workload:
     ctx_max: int
     fixed_lens: tuple = field(default=())   # explicit context lengths (overrides the draw)
     note: str = ""
+    placement: str = "random"  # physical ids of a row: "random" permutation, or "contiguous" runs
 
 
 TINY = Workload("tiny", 4, 4, 2, 2, 64, torch.float32, 16, 4, 1, 16, fixed_lens=(10, 3, 16, 1),
@@ -74,12 +75,20 @@ def draw_lengths(w: Workload, gen: torch.Generator) -> torch.Tensor:
 
 
 def draw_full_tables(w: Workload, gen: torch.Generator) -> torch.Tensor:
-    """Rows of ``max_blocks_per_seq`` distinct physical ids from a random permutation of the pool."""
+    """Rows of ``max_blocks_per_seq`` distinct physical ids: from a random
+    permutation of the pool, or (placement "contiguous") each row one run of
+    consecutive ids, as an allocator that keeps a sequence's blocks together
+    would give on a fresh pool."""
     need = w.num_seqs * w.max_blocks_per_seq
     if need > w.num_blocks:
         raise ValueError(f"{w.name}: {need} table entries do not fit a pool of {w.num_blocks}")
-    perm = torch.randperm(w.num_blocks, generator=gen)[:need]
-    return perm.view(w.num_seqs, w.max_blocks_per_seq).to(torch.int32).contiguous()
+    if w.placement == "contiguous":
+        ids = torch.arange(need)
+    elif w.placement == "random":
+        ids = torch.randperm(w.num_blocks, generator=gen)[:need]
+    else:
+        raise ValueError(f"unknown placement {w.placement!r}")
+    return ids.view(w.num_seqs, w.max_blocks_per_seq).to(torch.int32).contiguous()
 
 
 def draw_tiny_tables(gen: torch.Generator) -> torch.Tensor:
