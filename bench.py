@@ -116,7 +116,12 @@ L2_BYTES = 129 * 1024 * 1024
 FLUSH_BYTES = 512 * 1024 * 1024  # written between timed steps when a step's distinct K/V would sit in L2
 
 
-def needs_l2_flush(inp) -> bool:
+def needs_l2_flush(inp, mode: str = "auto") -> bool:
+    """auto: flush when a step's distinct K/V is under 4x the L2; "flush" /
+    "warm" force it on / off ("warm" numbers are for analysis, not the line's
+    headline)."""
+    if mode != "auto":
+        return mode == "flush"
     return unique_kv_bytes(inp) < 4 * L2_BYTES
 
 
@@ -141,10 +146,13 @@ def memory_report(inp) -> dict:
     return {k: round(v, 6) if isinstance(v, float) else v for k, v in rep.items()}
 
 
-def workload_config(name: str, inp) -> dict:
+def workload_config(name: str, inp, l2_mode: str = "auto") -> dict:
     w = inp.workload
     lens = inp.context_lens.to(torch.int64)
-    if needs_l2_flush(inp):
+    if l2_mode == "warm":
+        l2 = "warm: no flush between steps (forced for analysis; the step's distinct K/V is %.2f GB)" % (
+            unique_kv_bytes(inp) / 1e9)
+    elif needs_l2_flush(inp, l2_mode):
         l2 = ("flush: %d MiB written between timed steps (outside the timed intervals); the step's distinct "
               "K/V is %.2f GB" % (FLUSH_BYTES >> 20, unique_kv_bytes(inp) / 1e9))
     else:
@@ -298,7 +306,7 @@ def run_gpu(args) -> dict:
     assert int(err.item()) == 0, ops.error_names(int(err.item()))
 
     # -- device-timed step loop (inputs resident)
-    flush = needs_l2_flush(inp)
+    flush = needs_l2_flush(inp, args.l2)
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)] \
@@ -377,7 +385,7 @@ def run_gpu(args) -> dict:
         "vs_baseline": None,
         "dtype": {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}[inp.q.dtype],
         "data": "synthetic: seeded N(0,1) q/K/V, random physical placement",
-        "config": dict(workload_config(args.workload, inp),
+        "config": dict(workload_config(args.workload, inp, args.l2),
                        step_launch="eager, kernel by kernel" if args.no_graph
                        else "CUDA graphs: pre (copies, slots, write) then decode",
                        decode="pa_decode_shared (plan: %d groups, %d pieces)" % (
@@ -468,6 +476,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-seqs", type=int, default=None, help="fewer sequences (profiling captures only)")
     ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one")
+    ap.add_argument("--l2", choices=["auto", "flush", "warm"], default="auto",
+                    help="L2 between timed steps: auto (flush when the distinct K/V is under 4x L2), "
+                         "flush, or warm (no flush; analysis only)")
     ap.add_argument("--placement", choices=["random", "contiguous"], default="random",
                     help="physical placement of the plain workloads' blocks")
     ap.add_argument("--shared", action="store_true",

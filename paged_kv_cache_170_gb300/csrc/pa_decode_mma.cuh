@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   __shared__ uint32_t issued[kMaxStages];
   __shared__ int sh_abort;
   __shared__ __align__(8) uint64_t st_full[kConsumerWarps], st_free[kConsumerWarps];  // hand-off of mrg[w]
-  __shared__ float sh_mw[2 * kMergeRecords * 8];
+  __shared__ float sh_mw[kMergeScratch];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;

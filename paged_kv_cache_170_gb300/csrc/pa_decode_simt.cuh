@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
   __shared__ uint32_t issued[kMaxStages];
   __shared__ int sh_abort;
   __shared__ __align__(8) uint64_t st_full[kConsumerWarps], st_free[kConsumerWarps];  // hand-off of mrg[w]
-  __shared__ float sh_mw[2 * kMergeRecords * 8];
+  __shared__ float sh_mw[kMergeScratch];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -109,6 +109,10 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
   const int B = a.B;
   volatile int *abort_flag = &sh_abort;
 
+#ifdef PA_TRACE
+  __shared__ unsigned long long tr_start;
+  if (threadIdx.x == 0) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tr_start));
+#endif
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.nstage; ++i) {
       mbar_init(&full_bar[i], 1);
@@ -164,6 +168,13 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
     run_merger<T, D, false>(a, plan, PC, HC, G, lane, &mrg[0][0][0], GT * state_row(D), st_full, st_free, sh_mw,
                             abort_flag);
     zero_empty_rows<T>(a, D, lane, 32);
+#ifdef PA_TRACE
+    if (lane == 0) {
+      unsigned long long t1;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+      printf("tracet %d %u %llu %llu %lld\n", blockIdx.x, 0u, tr_start, t1, w1 - w0);
+    }
+#endif
     return;
   }
 

@@ -34,6 +34,7 @@ constexpr int kMaxBlockSize = 64;
 constexpr int kRingBytes = 80 * 1024;      // CUDA-core kernel: ring of K + V tile pairs
 constexpr int kRingBytesMma = 90 * 1024;   // tensor-core kernel: K + V tiles + the segment's q rows
 constexpr int kMergeRecords = 32;  // records whose merge weights are staged in shared memory
+constexpr int kMergeScratch = 2 * kMergeRecords * 8 + kMergeRecords;  // floats: m, l per (record, head); record ids
 
 struct DecodeArgs {
   void *out;
@@ -426,6 +427,7 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
   const long long W = plan.W;
   const int lh = lane >> 2, lq = lane & 3;  // the (head, warp) whose weight this lane forms
   float *sh_m = sh_w, *sh_l = sh_w + kMergeRecords * 8;
+  int *sh_rec = reinterpret_cast<int *>(sh_w + 2 * kMergeRecords * 8);  // contributors of a cut pair
   long long k = 0;  // segments handled
   long long j = 0;  // tiles before the current segment, in processing order
   uint32_t taken[kConsumerWarps] = {0u, 0u, 0u, 0u};  // deposits taken from each warp
@@ -535,14 +537,26 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
         const int nb = wk.nb;
         const int cf = cta_of(P0, W, N);
         const int cl = cta_of(P0 + nb - 1, W, N);
+        // the pair's contributors: the CTAs of [cf, cl] with a non-empty range
+        // (all of them when W >= N), found 32 at a time; the first
+        // kMergeRecords are listed in sh_rec
+        int kc = 0;
+        if (W >= N) {
+          kc = cl - cf + 1;
+          for (int r = lane; r < min(kc, kMergeRecords); r += 32) sh_rec[r] = cf + r;
+        } else {
+          for (int base = cf; base <= cl; base += 32) {
+            const int c = base + lane;
+            const bool has = c <= cl && range_start(c, W, N) < range_start(c + 1, W, N);
+            const unsigned mk = __ballot_sync(kFullMask, has);
+            const int pos = kc + __popc(mk & ((1u << lane) - 1u));
+            if (has && pos < kMergeRecords) sh_rec[pos] = c;
+            kc += __popc(mk);
+          }
+        }
+        __syncwarp();
         int last = 0;
         if (lane == 0) {
-          int kc = 0;
-          if (W >= N) {
-            kc = cl - cf + 1;
-          } else {
-            for (int c = cf; c <= cl; ++c) kc += range_start(c, W, N) < range_start(c + 1, W, N);
-          }
           unsigned *ctr = a.counters + (long long)s * PC + pc;
           const unsigned seen = atomicAdd(ctr, 1u) + 1u;
           last = seen == unsigned(kc);
@@ -558,13 +572,13 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
             const int slot = (c == cf && cf_last_seg) ? 1 : 0;
             return a.partials + ((long long)c * 2 + slot) * 8 * R;
           };
-          const int nrec = cl - cf + 1;
-          if (W >= N && nrec <= kMergeRecords) {
+          const int nrec = kc;
+          if (nrec <= kMergeRecords) {
             // every record's (m, l) per head at once, then the weights
             //     2^(m_r - M) / sum_r 2^(m_r - M) l_r   (in place of m_r)
             for (int i = lane; i < nrec * GT; i += 32) {
               const int r = i / GT, h = i - r * GT;
-              const float *rr = rec_of(cf + r) + h * R;
+              const float *rr = rec_of(sh_rec[r]) + h * R;
               sh_m[r * 8 + h] = __ldcg(rr + D);
               sh_l[r * 8 + h] = __ldcg(rr + D + 1);
             }
@@ -588,7 +602,7 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
 #pragma unroll
             for (int i = 0; i < kIters; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int r = 0; r < nrec; ++r) {
-              const float *rr = rec_of(cf + r);
+              const float *rr = rec_of(sh_rec[r]);
 #pragma unroll
               for (int i = 0; i < kIters; ++i) {
                 const int c = lane + 32 * i;
@@ -609,9 +623,9 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
               const int h = c / C4, d = (c % C4) * 4;
               if (h < GT) store_out4<T>(a, (long long)s * a.Hq + hq0 + h, d, D, acc[i]);
             }
-            __syncwarp();  // sh_m / sh_l are reused by the next merge
+            __syncwarp();  // sh_m / sh_l / sh_rec are reused by the next merge
           } else {
-            // many records (or empty CTA ranges): per element, straight from the records
+            // more than kMergeRecords contributors: per element, straight from the records
             for (int idx = lane; idx < GT * D; idx += 32) {
               const int h = idx / D;
               const int d = idx - h * D;
