@@ -56,6 +56,9 @@ def lib() -> ctypes.CDLL:
         L.oracle_decode.argtypes = [vp, vp, vp, vp, vp, i64, vp, i32, i32, i32, i32, i32, i64,
                                     dbl, i32, i32]
         L.oracle_decode.restype = i32
+        L.oracle_prefill.argtypes = [vp, vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, i32, i64,
+                                     dbl, i32, i32]
+        L.oracle_prefill.restype = i32
         L.oracle_max_threads.argtypes = []
         L.oracle_max_threads.restype = i32
         _lib = L
@@ -132,6 +135,28 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, nthrea
                              _DTYPE_CODE[q.dtype], int(nthreads))
     if rc:
         raise ValueError("oracle_decode: invalid argument or index")
+    return out
+
+
+def prefill(q, k_cache, v_cache, block_tables, context_lens, q_start, scale: float,
+            nthreads: int = 0) -> np.ndarray:
+    """float64 [T][Hq][D] (see ``pa_oracle.c``, oracle_prefill)."""
+    q, k_cache, v_cache = _cpu(q), _cpu(k_cache), _cpu(v_cache)
+    T, Hq, D = q.shape
+    NB, Hkv, B, _ = k_cache.shape
+    tables = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    lens = np.ascontiguousarray(np.asarray(context_lens, dtype=np.int32))
+    qs = np.ascontiguousarray(np.asarray(q_start, dtype=np.int32))
+    S = lens.size
+    if qs.size != S + 1 or (S and int(qs[-1]) != T):
+        raise ValueError("q_start must have num_seqs + 1 entries ending at the number of query rows")
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    rc = lib().oracle_prefill(out.ctypes.data, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                              tables.ctypes.data, tables.shape[1] if tables.ndim == 2 else 0, lens.ctypes.data,
+                              qs.ctypes.data, S, Hq, Hkv, D, B, NB, float(scale), _DTYPE_CODE[q.dtype],
+                              int(nthreads))
+    if rc:
+        raise ValueError("oracle_prefill: invalid argument or index")
     return out
 
 

@@ -1,5 +1,6 @@
 /*
- * pa_oracle.c -- plain fp64 CPU oracle for paged KV-cache decode attention.
+ * pa_oracle.c -- plain fp64 CPU oracle for paged KV-cache attention (decode
+ * and prefill).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
  * call this file: only the test-suite, the smoke check and the CPU-baseline leg
@@ -23,6 +24,11 @@
  *    kv_head = h / (Hq/Hkv) are not printed on the pages; they are the plain
  *    textbook definition, evaluated here in double precision on the stored
  *    (already rounded) input values, in logical token order.
+ *  - Prefill: the prompt's tokens are written into blocks taken as the
+ *    request enters (cf-1.com news/5879632, section 3.2) and each attends to
+ *    all history before it (aiqz.cc, section "显存痛点"); the causal mask
+ *    (a prompt token sees the history and the prompt up to itself) is again
+ *    the textbook definition.
  *
  * Layouts (all row-major):
  *   q, out        [S][Hq][D]
@@ -157,17 +163,17 @@ int oracle_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs,
   return 0;
 }
 
-/* Decode attention for one (sequence, query head).  Returns 0 or -1. */
-static int orc_decode_one(double *out_row, const void *q, const void *k_cache,
+/* Attention of one query row (element offset qrow in q, query head h) over
+ * the first L tokens of a sequence, in logical order.  Returns 0 or -1. */
+static int orc_attend_one(double *out_row, const void *q, size_t qrow, const void *k_cache,
                           const void *v_cache, const int32_t *table_row,
-                          int64_t max_blocks, int64_t L, int s, int h, int Hq,
+                          int64_t max_blocks, int64_t L, int h, int Hq,
                           int Hkv, int D, int B, int64_t NB, double scale,
                           int dtype, double *x) {
   for (int d = 0; d < D; ++d) out_row[d] = 0.0;
   if (L == 0) return 0; /* no cached tokens: nothing to attend to */
   int G = Hq / Hkv;
   int g = h / G; /* query heads are grouped contiguously per KV head */
-  size_t qrow = ((size_t)s * (size_t)Hq + (size_t)h) * (size_t)D;
   double m = -INFINITY;
   for (int64_t t = 0; t < L; ++t) {
     int64_t pid, off;
@@ -223,8 +229,59 @@ int oracle_decode(double *out, const void *q, const void *k_cache,
       if (!x) continue;
       int s = (int)(w / Hq), h = (int)(w % Hq);
       double *row = out + (size_t)w * (size_t)D;
-      if (orc_decode_one(row, q, k_cache, v_cache, block_tables + (size_t)s * (size_t)max_blocks,
-                         max_blocks, context_lens[s], s, h, Hq, Hkv, D, B, NB, scale, dtype, x))
+      if (orc_attend_one(row, q, (size_t)w * (size_t)D, k_cache, v_cache,
+                         block_tables + (size_t)s * (size_t)max_blocks, max_blocks, context_lens[s], h, Hq,
+                         Hkv, D, B, NB, scale, dtype, x))
+        err |= 1;
+    }
+    free(x);
+  }
+  (void)nthreads;
+  return err ? -1 : 0;
+}
+
+/* Prefill (prompt) attention.  Sequence s owns the query rows
+ * q_start[s] .. q_start[s+1]-1 of q / out ([T][Hq][D]); they are the last
+ * n = q_start[s+1] - q_start[s] positions of its context, whose length
+ * context_lens[s] counts them.  Row i (position p = L - n + i) attends over
+ * tokens 0 .. p: the whole cached history, then the prompt up to itself
+ * (causal).  Returns 0, or -1 on an invalid argument or index. */
+int oracle_prefill(double *out, const void *q, const void *k_cache, const void *v_cache,
+                   const int32_t *block_tables, int64_t max_blocks, const int32_t *context_lens,
+                   const int32_t *q_start, int S, int Hq, int Hkv, int D, int B, int64_t NB, double scale,
+                   int dtype, int nthreads) {
+  if (S < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || B <= 0) return -1;
+  if (S > 0 && q_start[0] != 0) return -1;
+  int64_t maxL = 0;
+  for (int s = 0; s < S; ++s) {
+    int64_t n = (int64_t)q_start[s + 1] - q_start[s];
+    if (n < 0 || context_lens[s] < n || (int64_t)context_lens[s] > max_blocks * B) return -1;
+    if (context_lens[s] > maxL) maxL = context_lens[s];
+  }
+  int64_t T = S > 0 ? q_start[S] : 0;
+  int err = 0;
+  int64_t work = T * Hq;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel reduction(| : err)
+#endif
+  {
+    double *x = (double *)malloc(sizeof(double) * (size_t)(maxL > 0 ? maxL : 1));
+    if (!x) err |= 1;
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 16)
+#endif
+    for (int64_t w = 0; w < work; ++w) {
+      if (!x) continue;
+      int64_t row = w / Hq;
+      int h = (int)(w % Hq);
+      int s = 0;
+      while (s + 1 < S && q_start[s + 1] <= row) ++s; /* the sequence owning query row `row` */
+      int64_t n = (int64_t)q_start[s + 1] - q_start[s];
+      int64_t p = (int64_t)context_lens[s] - n + (row - q_start[s]);
+      if (orc_attend_one(out + (size_t)w * (size_t)D, q, (size_t)w * (size_t)D, k_cache, v_cache,
+                         block_tables + (size_t)s * (size_t)max_blocks, max_blocks, p + 1, h, Hq, Hkv, D, B,
+                         NB, scale, dtype, x))
         err |= 1;
     }
     free(x);

@@ -24,6 +24,10 @@ Sources (pages, by title and section):
     kv_head = h // (Hq // Hkv) are not printed on the pages: they are the
     textbook definition, evaluated in float64 on the stored input values in
     logical token order.                                     -> decode
+  * Prefill: the prompt's tokens enter blocks as the request arrives
+    (cf-1.com news/5879632, section 3.2) and each attends to all history
+    before it (aiqz.cc, section "显存痛点"); causally, prompt token i sees
+    the history and prompt tokens 0 .. i.               -> prefill
 
 Layouts: q/out [S][Hq][D]; K/V pools [NB][Hkv][B][D]; block_tables int32
 [S][max_blocks]; context_lens int32 [S]; slot_mapping int64 [T]; copy pairs
@@ -130,6 +134,41 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
             x = scale * (K @ qd[s, h])        # [L]
             w = np.exp(x - x.max())
             out[s, h] = (w @ V) / w.sum()
+    return out
+
+
+def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+            block_tables, context_lens, q_start, scale: float) -> np.ndarray:
+    """float64 [T][Hq][D] prompt attention through the block table.
+
+    Sequence s owns query rows q_start[s] .. q_start[s+1]-1: the last n of its
+    context_lens[s] positions.  Row i, at position p = L - n + i, attends to
+    tokens 0 .. p (the history, then the prompt up to itself).
+    """
+    T, Hq, D = q.shape
+    Hkv, B = k_cache.shape[1], k_cache.shape[2]
+    qd, kd, vd = _f64(q), _f64(k_cache), _f64(v_cache)
+    tables = np.asarray(block_tables)
+    lens = np.asarray(context_lens).tolist()
+    qs = np.asarray(q_start).tolist()
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    for s in range(len(lens)):
+        L, n = int(lens[s]), int(qs[s + 1] - qs[s])
+        if n == 0:
+            continue
+        addr = [locate(tables[s], tok, B) for tok in range(L)]
+        pid = np.array([a[0] for a in addr], dtype=np.int64)
+        off = np.array([a[1] for a in addr], dtype=np.int64)
+        for i in range(n):
+            p = L - n + i      # this query row's position in the sequence
+            end = p + 1        # it sees tokens 0 .. p
+            for h in range(Hq):
+                g = kv_head(h, Hq, Hkv)
+                Kc = kd[pid[:end], g, off[:end], :]
+                Vc = vd[pid[:end], g, off[:end], :]
+                z = scale * (Kc @ qd[qs[s] + i, h])
+                e = np.exp(z - np.max(z))
+                out[qs[s] + i, h] = (e @ Vc) / np.sum(e)
     return out
 
 

@@ -31,6 +31,11 @@ MUTATIONS = {
     "write_transposed": ("pid, off = divmod(slot, B)", "off, pid = divmod(slot, B)"),
     "copy_reversed": ("k_cache[dst] = k_cache[src].clone()", "k_cache[src] = k_cache[dst].clone()"),
     "write_skips_zero_slot": ("if slot < 0:", "if slot <= 0:"),
+    "prefill_not_causal": ("end = p + 1        # it sees tokens 0 .. p", "end = L"),
+    "prefill_excludes_itself": ("end = p + 1        # it sees tokens 0 .. p", "end = p"),
+    "prefill_position_from_start": ("p = L - n + i      # this query row's position", "p = i      # this query row's position"),
+    "prefill_wrong_query_row": ("z = scale * (Kc @ qd[qs[s] + i, h])", "z = scale * (Kc @ qd[qs[s], h])"),
+    "prefill_scale_dropped": ("z = scale * (Kc @ qd[qs[s] + i, h])", "z = (Kc @ qd[qs[s] + i, h])"),
 }
 
 PIN_TESTS = [
@@ -45,6 +50,8 @@ PIN_TESTS = [
     (pins.test_write_kv_identity_slots, {"dtype": pins.torch.float16}),
     (pins.test_write_kv_skips_negative_and_rejects_outside, {}),
     (pins.test_copy_blocks, {}),
+    (pins.test_prefill_identity_layout_matches_sdpa, {"Hq": 8, "Hkv": 2}),
+    (pins.test_prefill_closed_forms, {}),
 ]
 
 

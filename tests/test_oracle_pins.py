@@ -262,3 +262,99 @@ def test_copy_blocks(orc):
     assert torch.equal(kc[1], k0[0]) and torch.equal(vc[3], v0[0])
     with pytest.raises(IndexError):
         orc.copy_blocks(kc, vc, np.array([[0, NB]], dtype=np.int64))
+
+
+# ------------------------------------------------------------------ prefill
+def _sdpa_prefill(q, k, v, lens, q_start, scale):
+    """Library routine with an explicit causal mask on contiguous K/V: query row
+    i of sequence s (position L - n + i) may see keys 0 .. L - n + i."""
+    T, Hq, D = q.shape
+    NB, Hkv, B, _ = k.shape
+    S = len(lens)
+    nb = NB // S
+    out = torch.zeros(T, Hq, D, dtype=torch.float64)
+    for s in range(S):
+        L, a, b = int(lens[s]), int(q_start[s]), int(q_start[s + 1])
+        n = b - a
+        if n == 0:
+            continue
+        Ks = k[s * nb:(s + 1) * nb].to(torch.float64).permute(1, 0, 2, 3).reshape(Hkv, nb * B, D)[:, :L]
+        Vs = v[s * nb:(s + 1) * nb].to(torch.float64).permute(1, 0, 2, 3).reshape(Hkv, nb * B, D)[:, :L]
+        Ks = Ks.repeat_interleave(Hq // Hkv, dim=0)
+        Vs = Vs.repeat_interleave(Hq // Hkv, dim=0)
+        mask = torch.arange(L)[None, :] <= (L - n + torch.arange(n))[:, None]   # [n][L], True = visible
+        qs = q[a:b].to(torch.float64).transpose(0, 1)                             # [Hq][n][D]
+        out[a:b] = F.scaled_dot_product_attention(qs, Ks, Vs, attn_mask=mask, scale=scale).transpose(0, 1)
+    return out.numpy()
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2)])
+def test_prefill_identity_layout_matches_sdpa(orc, Hq, Hkv):
+    S, D, B, nb = 3, 16, 4, 6
+    q_all, k, v, _ = _identity_case(S, Hq, Hkv, D, B, nb, dtype=torch.float32, seed=5 + Hq)
+    tables = np.arange(S * nb, dtype=np.int32).reshape(S, nb)
+    lens = np.array([17, 24, 5], dtype=np.int32)        # history + prompt
+    q_start = np.array([0, 9, 9 + 24, 9 + 24 + 1], dtype=np.int32)  # prompts of 9, 24 (no history), 1
+    q = torch.randn(int(q_start[-1]), Hq, D, generator=torch.Generator().manual_seed(Hq)).to(torch.float32)
+    got = orc.prefill(q, k, v, tables, lens, q_start, 0.29)
+    want = _sdpa_prefill(q, k, v, lens, q_start, 0.29)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-13)
+
+
+def test_prefill_closed_forms(orc):
+    # all keys equal: row i (position p) is the mean of V over 0 .. p
+    S, Hq, Hkv, D, B, NB = 1, 2, 1, 8, 4, 3
+    k = torch.zeros(NB, Hkv, B, D)
+    v = torch.randn(NB, Hkv, B, D, generator=torch.Generator().manual_seed(2))
+    tables = np.array([[2, 0, 1]], dtype=np.int32)
+    L, n = 11, 4
+    q = torch.randn(n, Hq, D, generator=torch.Generator().manual_seed(3))
+    got = orc.prefill(q, k, v, tables, np.array([L], np.int32), np.array([0, n], np.int32), 1.0)
+    rows = torch.cat([v[p, 0] for p in tables[0]])  # logical order [12][D]
+    for i in range(n):
+        p = L - n + i
+        want = rows[:p + 1].double().mean(0).numpy()
+        for h in range(Hq):
+            np.testing.assert_allclose(got[i, h], want, rtol=1e-12, atol=1e-14)
+    # a prompt of one token at position 0 returns its own value row
+    got1 = orc.prefill(q[:1], k, v, tables, np.array([1], np.int32), np.array([0, 1], np.int32), 1.0)
+    np.testing.assert_allclose(got1[0, 0], rows[0].double().numpy(), rtol=0, atol=0)
+
+
+def test_prefill_last_row_is_the_decode_of_its_sequence(orc):
+    S, Hq, Hkv, D, B, NB = 2, 4, 2, 16, 4, 24
+    lens = np.array([14, 7], dtype=np.int32)
+    qd, k, v, tables = _random_paged(S, Hq, Hkv, D, B, NB, lens, torch.float32, seed=8)
+    q_start = np.array([0, 5, 12], dtype=np.int32)
+    q = torch.randn(12, Hq, D, generator=torch.Generator().manual_seed(9))
+    got = orc.prefill(q, k, v, tables, lens, q_start, 0.4)
+    last = q[torch.as_tensor(q_start[1:] - 1, dtype=torch.long)]
+    np.testing.assert_allclose(got[q_start[1:] - 1], orc.decode(last, k, v, tables, lens, 0.4), rtol=1e-12,
+                               atol=1e-14)
+
+
+def test_prefill_invariant_under_block_relabelling(orc):
+    S, Hq, Hkv, D, B, NB = 2, 4, 2, 8, 4, 30
+    lens = np.array([19, 9], dtype=np.int32)
+    qd, k, v, tables = _random_paged(S, Hq, Hkv, D, B, NB, lens, torch.bfloat16, seed=12)
+    q_start = np.array([0, 6, 15], dtype=np.int32)
+    q = torch.randn(15, Hq, D, generator=torch.Generator().manual_seed(13)).to(torch.bfloat16)
+    base = orc.prefill(q, k, v, tables, lens, q_start, 0.3)
+    pi = torch.randperm(NB, generator=torch.Generator().manual_seed(14))
+    k2, v2 = torch.empty_like(k), torch.empty_like(v)
+    k2[pi], v2[pi] = k, v
+    again = orc.prefill(q, k2, v2, pi.numpy().astype(np.int32)[tables], lens, q_start, 0.3)
+    assert np.array_equal(base, again)
+
+
+def test_prefill_implementations_agree_and_reject_bad_offsets():
+    S, Hq, Hkv, D, B, NB = 3, 8, 2, 32, 16, 40
+    lens = np.array([70, 33, 16], dtype=np.int32)
+    _, k, v, tables = _random_paged(S, Hq, Hkv, D, B, NB, lens, torch.float16, seed=21)
+    q_start = np.array([0, 20, 53, 54], dtype=np.int32)
+    q = torch.randn(54, Hq, D, generator=torch.Generator().manual_seed(22)).to(torch.float16)
+    a = reference.prefill(q, k, v, tables, lens, q_start, 0.18)
+    b = native.prefill(q, k, v, tables, lens, q_start, 0.18)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-13)
+    with pytest.raises(ValueError):  # a prompt longer than its context
+        native.prefill(q, k, v, tables, np.array([10, 33, 16], np.int32), q_start, 0.18)
