@@ -27,6 +27,7 @@ import subprocess
 import sys
 import time
 
+import numpy as np
 import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -50,8 +51,9 @@ def measured_peaks() -> dict:
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d.get("bf16_tflops", 1900.0)),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
 def profiled_traffic(workload: str):
@@ -420,6 +422,151 @@ def run_gpu(args) -> dict:
     return line if rank == 0 else None
 
 
+def prefill_flops(inp) -> int:
+    """Causal attention flops of a prompt step: 4 * D per (query row, head,
+    visible token); the row at position p sees p + 1 tokens."""
+    lens = inp.context_lens.to(torch.int64).cpu()
+    qs = inp.q_start.to(torch.int64).cpu()
+    n = qs[1:] - qs[:-1]
+    # sum over rows of (p + 1), p = L - n + i, i = 0 .. n-1
+    visible = int((n * (lens - n) + n * (n + 1) // 2).sum())
+    return 4 * inp.q.shape[2] * inp.q.shape[1] * visible
+
+
+def prefill_config(name: str, inp, l2: str) -> dict:
+    w = inp.workload
+    lens = inp.context_lens.to(torch.int64)
+    n = (inp.q_start[1:] - inp.q_start[:-1]).to(torch.int64)
+    return {"workload": f"{name}: {w.note}", "num_seqs": int(lens.numel()), "block_size": int(inp.k_cache.shape[2]),
+            "num_heads": int(inp.q.shape[1]), "num_kv_heads": int(inp.k_cache.shape[1]),
+            "head_dim": int(inp.q.shape[2]), "pool_blocks": int(inp.k_cache.shape[0]),
+            "context_sum": int(lens.sum()), "prompt_tokens": int(n.sum()), "placement": w.placement, "l2_policy": l2}
+
+
+def run_prefill_gpu(args) -> dict:
+    """The prompt step: pa_prefill over every sequence's prompt (its K/V
+    already in the cache), timed with CUDA events around each launch."""
+    from paged_kv_cache_170_gb300 import ops, workloads
+
+    rank, world, local, dist = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = workloads.make_prefill_inputs(workloads.WORKLOADS[args.workload], args.seed + rank, device=dev)
+    out = torch.empty_like(inp.q)
+    err = ops.new_error_word(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev_a=None, ev_b=None):
+        if ev_a is not None:
+            ev_a.record(stream)
+        ops.pa_prefill(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.q_start,
+                       inp.max_q_len, inp.scale, out, err)
+        if ev_b is not None:
+            ev_b.record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert int(err.item()) == 0, ops.error_names(int(err.item()))
+    _, Hkv, _, D = inp.k_cache.shape
+    distinct = int(inp.context_lens.to(torch.int64).sum()) * Hkv * D * inp.k_cache.element_size() * 2
+    flush = args.l2 == "flush" or (args.l2 == "auto" and distinct < 4 * L2_BYTES)
+    l2 = ("flush: %d MiB written between timed steps (outside the timed intervals); the step's K/V is %.3f GB"
+          % (FLUSH_BYTES >> 20, distinct / 1e9)) if flush else "no flush (%s)" % args.l2
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        for k in range(args.steps):
+            if flush:
+                flush_buf.fill_(k & 255)
+            step(*kev[k])
+        torch.cuda.synchronize(dev)
+    barrier(dist)
+    times = [a.elapsed_time(b) for a, b in kev]
+    step_ms = max_over_ranks(sum(times) / args.steps, dist)
+    flops = prefill_flops(inp)
+    total_flops = sum_over_ranks(float(flops), dist)
+    peaks = measured_peaks()
+    tflops = total_flops / (step_ms * 1e-3) / 1e12
+    # end to end: the prompts' queries in from pinned host memory, the outputs back
+    host = {n: getattr(inp, n).cpu().pin_memory() for n in ("q", "block_tables", "context_lens", "q_start")}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_steps = max(1, min(args.steps, 200))
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for n, t in host.items():
+            getattr(inp, n).copy_(t, non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist)
+    assert int(err.item()) == 0, ops.error_names(int(err.item()))
+    bf16 = float(peaks.get("bf16_tflops", 1900.0))
+    line = {
+        "metric": "pa_prefill causal attention TFLOP/s (4*D flops per query row, head and visible token)",
+        "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {torch.bfloat16: "bf16", torch.float16: "f16"}[inp.q.dtype],
+        "data": "synthetic: seeded N(0,1) q/K/V, random physical placement",
+        "config": prefill_config(args.workload, inp, l2),
+        "tokens_per_s": round(sum_over_ranks(float(inp.q.shape[0]), dist) / (step_ms * 1e-3), 0),
+        "prefill_kernel_us": round(step_ms * 1e3, 2),
+        "roofline": {"kernel": "prefill_mma_kernel", "bound": "tensor", "achieved": round(tflops / world, 2),
+                     "peak": bf16, "unit": "TFLOP/s", "frac": round(tflops / world / bf16, 4),
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops, cuBLAS bf16 GEMM burst)",
+                     "algorithmic_flops_per_launch": flops, "traffic": None},
+        "e2e": {"value": round(total_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = inp.to("cpu")
+        v, secs, rows, threads = time_cpu_prefill(cpu, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(v, 4), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{rows} query rows (all heads) of the workload's prompts, C float64 "
+                                          f"oracle, {secs:.1f} s"}
+    if dist is not None:
+        dist.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def time_cpu_prefill(inp_cpu, max_seconds: float):
+    """The C oracle on one-row prompts cut from the workload (row i of a prompt
+    is position p of its sequence: a one-token prompt on the context cut
+    after p), cycling until the time budget is spent.  Returns (TFLOP/s,
+    seconds, rows, threads)."""
+    from oracle import native
+
+    lens = inp_cpu.context_lens.numpy()
+    qs = inp_cpu.q_start.numpy()
+    tables = inp_cpu.block_tables.numpy()
+    D, Hq = inp_cpu.q.shape[2], inp_cpu.q.shape[1]
+    order = [(s, r) for s in range(len(lens)) for r in range(int(qs[s]), int(qs[s + 1]))]
+    step = max(1, len(order) // 97)
+    picks = order[::step]
+    t_total, flops, done = 0.0, 0, 0
+    while done == 0 or t_total < max_seconds:
+        s, r = picks[done % len(picks)]
+        p = int(lens[s]) - int(qs[s + 1] - qs[s]) + (r - int(qs[s]))
+        t0 = time.perf_counter()
+        native.prefill(inp_cpu.q[r:r + 1], inp_cpu.k_cache, inp_cpu.v_cache, tables[s:s + 1],
+                       np.array([p + 1], np.int32), np.array([0, 1], np.int32), inp_cpu.scale)
+        t_total += time.perf_counter() - t0
+        flops += 4 * D * Hq * (p + 1)
+        done += 1
+    return flops / t_total / 1e12, t_total, done, native.max_threads()
+
+
 def run_reference(args) -> dict:
     """The CPU oracle as the reference arm: each step decodes a bounded sample
     of whole sequences of the same workload on the host cores."""
@@ -428,6 +575,8 @@ def run_reference(args) -> dict:
         return None
     from oracle import native
 
+    if args.workload.startswith("prefill"):
+        return run_prefill_reference(args)
     inp = workload_inputs(args.workload, args.seed, "cuda" if torch.cuda.is_available() else "cpu").to("cpu")
     S, Hq, D = inp.q.shape
     Hkv = inp.k_cache.shape[1]
@@ -464,13 +613,44 @@ def run_reference(args) -> dict:
     }
 
 
+def run_prefill_reference(args) -> dict:
+    """The CPU oracle as the reference arm of a prompt workload: each step a
+    bounded sample of one-row prompts cut from the workload."""
+    from paged_kv_cache_170_gb300 import workloads
+
+    inp = workloads.make_prefill_inputs(workloads.WORKLOADS[args.workload], args.seed, device="cpu")
+    budget = max(0.5, 90.0 / (args.steps + args.warmup))
+    for _ in range(args.warmup):
+        time_cpu_prefill(inp, budget)
+    vals, secs, rows, threads = [], 0.0, 0, 1
+    for _ in range(args.steps):
+        v, t, r, threads = time_cpu_prefill(inp, budget)
+        vals.append(v)
+        secs += t
+        rows += r
+    value = sum(vals) / len(vals)
+    sample = f"{rows} one-row prompts cut from the workload over {args.steps} steps, C float64 oracle"
+    return {
+        "impl": "reference",
+        "metric": "pa_prefill causal attention TFLOP/s (4*D flops per query row, head and visible token)",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": prefill_config(args.workload, inp, "n/a (CPU)"),
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=6000)
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", choices=["tiny", "mha", "gqa", "prefix", "longctx"], default="gqa")
+    ap.add_argument("--workload", choices=["tiny", "mha", "gqa", "prefix", "longctx", "prefill", "prefill_hist"],
+                    default="gqa")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -486,7 +666,12 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if args.impl == "reference":
+        line = run_reference(args)
+    elif args.workload.startswith("prefill"):
+        line = run_prefill_gpu(args)
+    else:
+        line = run_gpu(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 

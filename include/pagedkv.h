@@ -245,6 +245,33 @@ PA_API pa_status pa_decode_shared(void *out, const void *q, const void *k_cache,
                                   const int32_t *plan_dev, void *workspace,
                                   size_t workspace_bytes, int *debug_err, void *stream);
 
+/*
+ * Prompt (prefill) attention through the block table.  Sequence s owns the
+ * query rows q_start[s] .. q_start[s+1]-1 of q / out ([T][num_heads][head_dim],
+ * T = q_start[num_seqs]); they are the last n = q_start[s+1] - q_start[s]
+ * positions of its context, whose length context_lens[s] counts them, and
+ * their K/V are already in the cache (pa_write_kv).  The row at position p
+ * attends over tokens 0 .. p: the whole cached history, then the prompt up
+ * to itself.  The prompt's tokens enter blocks as the request arrives
+ * (cf-1.com news/5879632, section 3.2) and each attends to all history
+ * before it (aiqz.cc, section "显存痛点"); the causal mask is the textbook
+ * definition.  fp16 / bf16 with block_size a multiple of 16 only (else
+ * PA_ERR_UNSUPPORTED); head_dim 64 or 128.
+ *   q_start     device int32 [num_seqs + 1], q_start[0] = 0, non-decreasing;
+ *               a sequence with n > context_lens[s] sets PA_DEVERR_CONTEXT
+ *               and is skipped.
+ *   max_q_len   host bound of n over the sequences (sizes the grid).
+ * One launch on `stream`: one CTA per (sequence, kv head, 64 query rows);
+ * fp32 arithmetic on the tensor cores, out rounded to nearest even.
+ * Allocates nothing; no workspace.
+ */
+PA_API pa_status pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, const int32_t *q_start, int num_seqs,
+                            int max_q_len, int num_heads, int num_kv_heads, int head_dim,
+                            int block_size, int64_t num_blocks, float scale, pa_dtype dtype,
+                            int *debug_err, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "pa_decode_shared.cuh"
+#include "pa_prefill.cuh"
 #include "pa_sched.cuh"
 
 namespace pagedkv {
@@ -20,6 +21,9 @@ pa_status launch_decode_shared(const SharedArgs &a, const CUtensorMap &mk, const
                                cudaStream_t stream);
 template <typename T, int D>
 pa_status launch_merge_shared(const MergeArgs &a, cudaStream_t stream);
+template <typename T, int D>
+pa_status launch_prefill(const PrefillArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t ring_bytes,
+                         dim3 grid, cudaStream_t stream);
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -416,4 +420,67 @@ extern "C" pa_status pa_decode_shared(void *out, const void *q, const void *k_ca
   if (st != PA_OK) return st;
   // 3. merge
   return dtype == PA_BF16 ? merge_step<__nv_bfloat16>(ma, head_dim, s) : merge_step<__half>(ma, head_dim, s);
+}
+
+// ------------------------------------------------------------------ prefill
+namespace pagedkv {
+
+template <typename T>
+static pa_status prefill_dispatch(const PrefillArgs &pa_args, const void *k_cache, const void *v_cache,
+                                  pa_dtype dtype, int D, size_t ring, dim3 grid, cudaStream_t st) {
+  CUtensorMap mk, mv;
+  PrefillArgs b = pa_args;
+  if (!encode_pool_maps(k_cache, v_cache, dtype, b.num_blocks, b.Hkv, b.B, D, &mk, &mv, &b.nops)) return PA_ERR_CUDA;
+  return D == 64 ? launch_prefill<T, 64>(b, mk, mv, ring, grid, st) : launch_prefill<T, 128>(b, mk, mv, ring, grid, st);
+}
+
+}  // namespace pagedkv
+
+extern "C" pa_status pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                                const int32_t *q_start, int num_seqs, int max_q_len, int num_heads,
+                                int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, float scale,
+                                pa_dtype dtype, int *debug_err, void *stream) {
+  if (num_seqs < 0 || max_q_len < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
+    return PA_ERR_INVALID_ARG;
+  if (block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || !isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (dtype != PA_F32 && dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+  if (dtype == PA_F32 || block_size % 16 != 0 || block_size > kMaxBlockSize) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if ((long long)max_blocks_per_seq * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  if (num_blocks * num_kv_heads * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  if (tensor_map_encoder() == nullptr) return PA_ERR_UNSUPPORTED;
+  const long long tiles = ((long long)max_q_len * (num_heads / num_kv_heads) + kPrefillRows - 1) / kPrefillRows;
+  if (num_seqs == 0 || tiles == 0) return PA_OK;
+  if (tiles > 0x7fffffffLL || num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !q_start) return PA_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+
+  PrefillArgs a;
+  a.out = out;
+  a.q = q;
+  a.tables = block_tables;
+  a.lens = context_lens;
+  a.q_start = q_start;
+  a.num_blocks = num_blocks;
+  a.max_blocks = max_blocks_per_seq;
+  a.S = num_seqs;
+  a.Hq = num_heads;
+  a.Hkv = num_kv_heads;
+  a.B = block_size;
+  a.qscale = scale * kLog2e;
+  a.err = debug_err;
+  const size_t tile_bytes = size_t(block_size) * head_dim * dtype_bytes(dtype);
+  a.tile_stride = uint32_t((tile_bytes + 1023) / 1024 * 1024);  // the swizzled tiles repeat every 1024 bytes
+  a.slot_stride = 2 * a.tile_stride;
+  a.nstage = int(kRingBytesPrefill / a.slot_stride);
+  if (a.nstage > kMaxStages) a.nstage = kMaxStages;
+  if (a.nstage < 1) return PA_ERR_UNSUPPORTED;
+  a.pg = a.nstage < 4 ? a.nstage : 4;
+  a.nops = 1;
+  const size_t ring = size_t(a.nstage) * a.slot_stride;
+  const dim3 grid{unsigned(tiles), unsigned(num_seqs), unsigned(num_kv_heads)};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return dtype == PA_BF16 ? prefill_dispatch<__nv_bfloat16>(a, k_cache, v_cache, dtype, head_dim, ring, grid, s)
+                          : prefill_dispatch<__half>(a, k_cache, v_cache, dtype, head_dim, ring, grid, s);
 }

@@ -6,4 +6,5 @@ namespace pagedkv {
 PAGEDKV_INSTANTIATE_SIMT(__nv_bfloat16)
 PAGEDKV_INSTANTIATE_MMA(__nv_bfloat16)
 PAGEDKV_INSTANTIATE_SHARED(__nv_bfloat16)
+PAGEDKV_INSTANTIATE_PREFILL(__nv_bfloat16)
 }  // namespace pagedkv

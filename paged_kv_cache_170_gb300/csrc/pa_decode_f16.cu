@@ -6,4 +6,5 @@ namespace pagedkv {
 PAGEDKV_INSTANTIATE_SIMT(__half)
 PAGEDKV_INSTANTIATE_MMA(__half)
 PAGEDKV_INSTANTIATE_SHARED(__half)
+PAGEDKV_INSTANTIATE_PREFILL(__half)
 }  // namespace pagedkv

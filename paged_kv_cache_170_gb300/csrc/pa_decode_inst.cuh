@@ -6,6 +6,7 @@
 #include "pa_decode_mma.cuh"
 #include "pa_decode_shared.cuh"
 #include "pa_decode_simt.cuh"
+#include "pa_prefill.cuh"
 
 namespace pagedkv {
 
@@ -57,6 +58,22 @@ pa_status launch_merge_shared(const MergeArgs &a, cudaStream_t stream) {
   merge_shared_kernel<T, D><<<unsigned((rows + kMergeWarps - 1) / kMergeWarps), kMergeWarps * 32, 0, stream>>>(a);
   return launch_status();
 }
+
+template <typename T, int D>
+pa_status launch_prefill(const PrefillArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t ring_bytes,
+                         dim3 grid, cudaStream_t stream) {
+  static int configured[64] = {0};
+  auto kern = prefill_mma_kernel<T, D>;
+  if (!configure_once(kern, kRingBytesPrefill + 1024, configured)) return PA_ERR_CUDA;
+  kern<<<grid, kPrefillThreads, ring_bytes + 1024, stream>>>(a, mk, mv);
+  return launch_status();
+}
+
+#define PAGEDKV_INSTANTIATE_PREFILL(T)                                                                      \
+  template pa_status launch_prefill<T, 64>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &,    \
+                                           size_t, dim3, cudaStream_t);                                      \
+  template pa_status launch_prefill<T, 128>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &,   \
+                                            size_t, dim3, cudaStream_t);
 
 #define PAGEDKV_INSTANTIATE_SHARED(T)                                                                         \
   template pa_status launch_decode_shared<T, 64>(const SharedArgs &, const CUtensorMap &, const CUtensorMap &, \

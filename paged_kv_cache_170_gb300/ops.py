@@ -44,6 +44,7 @@ def _load() -> ctypes.CDLL:
         "pa_share_plan": [vp, i32, vp, i32, i32, i32, i32, i32, vp, sz, ctypes.POINTER(sz)],
         "pa_decode_shared": [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp, vp, sz,
                              vp, vp],
+        "pa_prefill": [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -305,6 +306,32 @@ def pa_decode_shared(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
                                 D, B, NB, float(scale), _DTYPES[q.dtype], plan_host.data_ptr(), plan_dev.data_ptr(),
                                 workspace.data_ptr(), workspace.numel(), _ptr(err), _stream(q.device)),
            "pa_decode_shared")
+    return out
+
+
+def pa_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+               context_lens: torch.Tensor, q_start: torch.Tensor, max_q_len: int, scale: float,
+               out: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Prompt attention: q [T][Hq][D], the query rows of sequence s being
+    q[q_start[s]:q_start[s+1]] (the last positions of its context)."""
+    NB, Hkv, B, D = _cache_shape(k_cache, v_cache)
+    dev = k_cache.device
+    _need(q, "q", k_cache.dtype, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    _need(q_start, "q_start", torch.int32, 1, dev)
+    S = context_lens.numel()
+    if block_tables.shape[0] != S or q_start.numel() != S + 1 or q.shape[2] != D:
+        raise ValueError("q [T][Hq][D], block_tables [S][*], context_lens [S], q_start [S+1] disagree")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, 3, dev)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    _check(lib.pa_prefill(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                          block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), q_start.data_ptr(),
+                          S, int(max_q_len), q.shape[1], Hkv, D, B, NB, float(scale), _DTYPES[q.dtype], _ptr(err),
+                          _stream(dev)), "pa_prefill")
     return out
 
 

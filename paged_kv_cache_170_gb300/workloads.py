@@ -36,6 +36,8 @@ class Workload:
     fixed_lens: tuple = field(default=())   # explicit context lengths (overrides the draw)
     note: str = ""
     placement: str = "random"  # physical ids of a row: "random" permutation, or "contiguous" runs
+    prompt_min: int = 0        # prefill workloads: prompt tokens per sequence drawn in [prompt_min, prompt_max]
+    prompt_max: int = 0        # (the last positions of the context)
 
 
 TINY = Workload("tiny", 4, 4, 2, 2, 64, torch.float32, 16, 4, 1, 16, fixed_lens=(10, 3, 16, 1),
@@ -51,7 +53,15 @@ PREFIX = Workload("prefix", 128, 16, 32, 8, 128, torch.bfloat16, 8192, 128, 16, 
 LONGCTX = Workload("longctx", 32, 32, 64, 8, 128, torch.bfloat16, 10000, 1040, 1, 512,
                    note="8 prompts x 4 branches; 32768-token prompt; branch suffix U[1, 512]")
 
-WORKLOADS = {w.name: w for w in (TINY, MHA, GQA, PREFIX, LONGCTX)}
+# Prompt (prefill) steps of the GQA layer: the K/V of every context position,
+# prompt included, already in the pools.
+PREFILL = Workload("prefill", 8, 16, 32, 8, 128, torch.bfloat16, 1100, 128, 2048, 2048,
+                   note="8 prompts of 2048 tokens, no history", prompt_min=2048, prompt_max=2048)
+PREFILL_HIST = Workload("prefill_hist", 8, 16, 32, 8, 128, torch.bfloat16, 2100, 256, 4096, 4096,
+                        note="8 sequences of 4096 tokens, the last 1024 are the prompt", prompt_min=1024,
+                        prompt_max=1024)
+
+WORKLOADS = {w.name: w for w in (TINY, MHA, GQA, PREFIX, LONGCTX, PREFILL, PREFILL_HIST)}
 
 
 def scaled(w: Workload, **changes) -> Workload:
@@ -155,4 +165,42 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu") -> DecodeInputs:
     inp = DecodeInputs(w, q, k_cache, v_cache, tables, lens, new_key[keep], new_value[keep],
                        new_seq[keep], new_pos[keep], torch.zeros((0, 2), dtype=torch.int64),
                        float(D) ** -0.5)
+    return inp.to(device)
+
+
+@dataclass
+class PrefillInputs:
+    """One prompt step (K/V of the history and the prompt already in the pools)."""
+
+    workload: Workload
+    q: torch.Tensor               # [T][Hq][D] query rows of all prompts
+    k_cache: torch.Tensor         # [NB][Hkv][B][D]
+    v_cache: torch.Tensor
+    block_tables: torch.Tensor    # int32 [S][max_blocks]
+    context_lens: torch.Tensor    # int32 [S], prompts included
+    q_start: torch.Tensor         # int32 [S + 1]: rows of sequence s are q_start[s] .. q_start[s+1]-1
+    max_q_len: int
+    scale: float
+
+    def to(self, device) -> "PrefillInputs":
+        mv = lambda t: t.to(device)  # noqa: E731
+        return PrefillInputs(self.workload, mv(self.q), mv(self.k_cache), mv(self.v_cache), mv(self.block_tables),
+                             mv(self.context_lens), mv(self.q_start), self.max_q_len, self.scale)
+
+
+def make_prefill_inputs(w: Workload, seed: int = 0, device="cpu") -> PrefillInputs:
+    """Inputs of a prompt step: context lengths as drawn, prompt lengths drawn in
+    [prompt_min, prompt_max] (at most the context), random placement."""
+    gen = cpu_generator(seed)
+    lens = draw_lengths(w, gen)
+    tables = draw_full_tables(w, gen)
+    n = torch.randint(w.prompt_min, w.prompt_max + 1, (w.num_seqs,), generator=gen, dtype=torch.int64)
+    n = torch.minimum(n, lens.to(torch.int64))
+    q_start = torch.zeros(w.num_seqs + 1, dtype=torch.int64)
+    q_start[1:] = torch.cumsum(n, 0)
+    T = int(q_start[-1])
+    q = randn((T, w.num_heads, w.head_dim), w.dtype, gen)
+    k_cache, v_cache = draw_pools(w, gen, device, seed)
+    inp = PrefillInputs(w, q, k_cache, v_cache, tables, lens, q_start.to(torch.int32), int(n.max()) if len(n) else 0,
+                        float(w.head_dim) ** -0.5)
     return inp.to(device)

@@ -13,7 +13,7 @@ def test_library_builds_loads_and_exports_header_symbols():
     names = ops.header_functions()
     expected = {"pa_status_string", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks", "pa_decode_workspace_size",
                 "pa_decode", "pa_decode_grid_size", "pa_decode_noalloc", "pa_share_plan",
-                "pa_decode_shared_workspace_size", "pa_decode_shared"}
+                "pa_decode_shared_workspace_size", "pa_decode_shared", "pa_prefill"}
     assert expected <= set(names), sorted(expected - set(names))
     for name in names:
         assert hasattr(lib, name), f"{name} declared in include/pagedkv.h but not exported"
