@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 
 NOMINAL_HBM_GBS = 8000.0
 KERNEL_SOURCES = ["paged_kv_cache_170_gb300/csrc/pa_decode_mma.cuh", "paged_kv_cache_170_gb300/csrc/pa_sched.cuh",
+                  "paged_kv_cache_170_gb300/csrc/pa_mma_tile.cuh",
                   "paged_kv_cache_170_gb300/csrc/pa_common.cuh"]  # the tensor-core decode kernel
 
 
