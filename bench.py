@@ -521,7 +521,7 @@ def run_prefill_gpu(args) -> dict:
         "config": prefill_config(args.workload, inp, l2),
         "tokens_per_s": round(sum_over_ranks(float(inp.q.shape[0]), dist) / (step_ms * 1e-3), 0),
         "prefill_kernel_us": round(step_ms * 1e3, 2),
-        "roofline": {"kernel": "prefill_mma_kernel", "bound": "tensor", "achieved": round(tflops / world, 2),
+        "roofline": {"kernel": "prefill_tc_kernel", "bound": "tensor", "achieved": round(tflops / world, 2),
                      "peak": bf16, "unit": "TFLOP/s", "frac": round(tflops / world / bf16, 4),
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops, cuBLAS bf16 GEMM burst)",
                      "algorithmic_flops_per_launch": flops, "traffic": None},

@@ -255,14 +255,16 @@ PA_API pa_status pa_decode_shared(void *out, const void *q, const void *k_cache,
  * to itself.  The prompt's tokens enter blocks as the request arrives
  * (cf-1.com news/5879632, section 3.2) and each attends to all history
  * before it (aiqz.cc, section "显存痛点"); the causal mask is the textbook
- * definition.  fp16 / bf16 with block_size a multiple of 16 only (else
+ * definition.  fp16 / bf16 with block_size 16, 32 or 64 only (else
  * PA_ERR_UNSUPPORTED); head_dim 64 or 128.
  *   q_start     device int32 [num_seqs + 1], q_start[0] = 0, non-decreasing;
  *               a sequence with n > context_lens[s] sets PA_DEVERR_CONTEXT
  *               and is skipped.
  *   max_q_len   host bound of n over the sequences (sizes the grid).
- * One launch on `stream`: one CTA per (sequence, kv head, 64 query rows);
- * fp32 arithmetic on the tensor cores, out rounded to nearest even.
+ * One launch on `stream`: one CTA per (sequence, kv head, 128 query rows),
+ * tcgen05 MMAs with fp32 accumulators in tensor memory; the probabilities
+ * enter the P.V product as two fp16 / bf16 terms (hi + lo), so the result
+ * carries fp32-level error; out rounded to nearest even.
  * Allocates nothing; no workspace.
  */
 PA_API pa_status pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,

@@ -254,6 +254,7 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 template <typename T> struct Mma;
 
 template <> struct Mma<__nv_bfloat16> {
+  static constexpr bool kIsBf16 = true;
   // d += A(16x16, row) * B(16x8, col), fp32 accumulate
   static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -274,6 +275,7 @@ template <> struct Mma<__nv_bfloat16> {
 };
 
 template <> struct Mma<__half> {
+  static constexpr bool kIsBf16 = false;
   static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "

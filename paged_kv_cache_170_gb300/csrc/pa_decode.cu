@@ -7,6 +7,7 @@
 
 #include "pa_decode_shared.cuh"
 #include "pa_prefill.cuh"
+#include "pa_prefill_tc.cuh"
 #include "pa_sched.cuh"
 
 namespace pagedkv {
@@ -24,6 +25,9 @@ pa_status launch_merge_shared(const MergeArgs &a, cudaStream_t stream);
 template <typename T, int D>
 pa_status launch_prefill(const PrefillArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t ring_bytes,
                          dim3 grid, cudaStream_t stream);
+template <typename T, int D>
+pa_status launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t smem_bytes,
+                            dim3 grid, cudaStream_t stream);
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -427,11 +431,15 @@ namespace pagedkv {
 
 template <typename T>
 static pa_status prefill_dispatch(const PrefillArgs &pa_args, const void *k_cache, const void *v_cache,
-                                  pa_dtype dtype, int D, size_t ring, dim3 grid, cudaStream_t st) {
+                                  pa_dtype dtype, int D, size_t smem, dim3 grid, cudaStream_t st) {
   CUtensorMap mk, mv;
   PrefillArgs b = pa_args;
-  if (!encode_pool_maps(k_cache, v_cache, dtype, b.num_blocks, b.Hkv, b.B, D, &mk, &mv, &b.nops)) return PA_ERR_CUDA;
-  return D == 64 ? launch_prefill<T, 64>(b, mk, mv, ring, grid, st) : launch_prefill<T, 128>(b, mk, mv, ring, grid, st);
+  // one 2-D box (B rows x 64 columns) per block and half
+  if (!encode_pool_map(&mk, k_cache, dtype, b.num_blocks, b.Hkv, b.B, D, false) ||
+      !encode_pool_map(&mv, v_cache, dtype, b.num_blocks, b.Hkv, b.B, D, false))
+    return PA_ERR_CUDA;
+  return D == 64 ? launch_prefill_tc<T, 64>(b, mk, mv, smem, grid, st)
+                 : launch_prefill_tc<T, 128>(b, mk, mv, smem, grid, st);
 }
 
 }  // namespace pagedkv
@@ -445,14 +453,15 @@ extern "C" pa_status pa_prefill(void *out, const void *q, const void *k_cache, c
     return PA_ERR_INVALID_ARG;
   if (block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || !isfinite(scale)) return PA_ERR_INVALID_ARG;
   if (dtype != PA_F32 && dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
-  if (dtype == PA_F32 || block_size % 16 != 0 || block_size > kMaxBlockSize) return PA_ERR_UNSUPPORTED;
+  // a block must be an MMA column group (16 tokens) and divide the 64-token softmax step
+  if (dtype == PA_F32 || block_size % 16 != 0 || kTcStepTokens % block_size != 0) return PA_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if ((long long)max_blocks_per_seq * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   if (num_blocks * num_kv_heads * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   if (tensor_map_encoder() == nullptr) return PA_ERR_UNSUPPORTED;
-  const long long tiles = ((long long)max_q_len * (num_heads / num_kv_heads) + kPrefillRows - 1) / kPrefillRows;
+  const long long tiles = ((long long)max_q_len * (num_heads / num_kv_heads) + kTcRows - 1) / kTcRows;
   if (num_seqs == 0 || tiles == 0) return PA_OK;
-  if (tiles > 0x7fffffffLL || num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  if (tiles * num_seqs * num_kv_heads > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !q_start) return PA_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
 
@@ -470,17 +479,17 @@ extern "C" pa_status pa_prefill(void *out, const void *q, const void *k_cache, c
   a.B = block_size;
   a.qscale = scale * kLog2e;
   a.err = debug_err;
-  const size_t tile_bytes = size_t(block_size) * head_dim * dtype_bytes(dtype);
-  a.tile_stride = uint32_t((tile_bytes + 1023) / 1024 * 1024);  // the swizzled tiles repeat every 1024 bytes
-  a.slot_stride = 2 * a.tile_stride;
-  a.nstage = int(kRingBytesPrefill / a.slot_stride);
-  if (a.nstage > kMaxStages) a.nstage = kMaxStages;
-  if (a.nstage < 1) return PA_ERR_UNSUPPORTED;
-  a.pg = a.nstage < 4 ? a.nstage : 4;
+  // each ring slot holds one step (64 tokens) of K or V as [head_dim / 64 halves][64 rows][128 B]
+  a.slot_stride = uint32_t(head_dim / 64) * kTcStepTokens * 128;
+  a.tile_stride = 0;
+  a.nstage = int(kTcRingBytes / 2 / a.slot_stride);
+  if (a.nstage > kTcMaxSlots) a.nstage = kTcMaxSlots;
+  a.pg = 1;
   a.nops = 1;
-  const size_t ring = size_t(a.nstage) * a.slot_stride;
-  const dim3 grid{unsigned(tiles), unsigned(num_seqs), unsigned(num_kv_heads)};
+  // dynamic shared memory: the Q tile (head_dim / 64 halves of 128 rows x 128 B), both rings, alignment slack
+  const size_t smem = size_t(head_dim / 64) * kTcRows * 128 + 2 * size_t(a.nstage) * a.slot_stride + 1024;
+  const dim3 grid{unsigned(tiles * num_seqs * num_kv_heads), 1u, 1u};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return dtype == PA_BF16 ? prefill_dispatch<__nv_bfloat16>(a, k_cache, v_cache, dtype, head_dim, ring, grid, s)
-                          : prefill_dispatch<__half>(a, k_cache, v_cache, dtype, head_dim, ring, grid, s);
+  return dtype == PA_BF16 ? prefill_dispatch<__nv_bfloat16>(a, k_cache, v_cache, dtype, head_dim, smem, grid, s)
+                          : prefill_dispatch<__half>(a, k_cache, v_cache, dtype, head_dim, smem, grid, s);
 }

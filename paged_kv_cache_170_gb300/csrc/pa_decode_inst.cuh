@@ -7,6 +7,7 @@
 #include "pa_decode_shared.cuh"
 #include "pa_decode_simt.cuh"
 #include "pa_prefill.cuh"
+#include "pa_prefill_tc.cuh"
 
 namespace pagedkv {
 
@@ -69,11 +70,25 @@ pa_status launch_prefill(const PrefillArgs &a, const CUtensorMap &mk, const CUte
   return launch_status();
 }
 
+template <typename T, int D>
+pa_status launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t smem_bytes,
+                            dim3 grid, cudaStream_t stream) {
+  static int configured[64] = {0};
+  auto kern = prefill_tc_kernel<T, D>;
+  if (!configure_once(kern, (D / 64) * kTcRows * 128 + kTcRingBytes + 1024, configured)) return PA_ERR_CUDA;
+  kern<<<grid, kTcThreads, smem_bytes, stream>>>(a, mk, mv);
+  return launch_status();
+}
+
 #define PAGEDKV_INSTANTIATE_PREFILL(T)                                                                      \
   template pa_status launch_prefill<T, 64>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &,    \
                                            size_t, dim3, cudaStream_t);                                      \
   template pa_status launch_prefill<T, 128>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &,   \
-                                            size_t, dim3, cudaStream_t);
+                                            size_t, dim3, cudaStream_t);                                     \
+  template pa_status launch_prefill_tc<T, 64>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &, \
+                                              size_t, dim3, cudaStream_t);                                   \
+  template pa_status launch_prefill_tc<T, 128>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &, \
+                                               size_t, dim3, cudaStream_t);
 
 #define PAGEDKV_INSTANTIATE_SHARED(T)                                                                         \
   template pa_status launch_decode_shared<T, 64>(const SharedArgs &, const CUtensorMap &, const CUtensorMap &, \

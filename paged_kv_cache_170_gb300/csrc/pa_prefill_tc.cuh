@@ -1,0 +1,478 @@
+// pa_prefill_tc.cuh -- prompt (prefill) attention on the 5th-generation tensor
+// cores: tcgen05.mma with operands in shared memory (TMA-loaded, 128-byte
+// swizzle) and accumulators in tensor memory (TMEM).
+//
+// One CTA takes one (sequence, kv head, tile of 128 query rows); a row is
+// (prompt position i, head hh of the kv head's group of G), position-major,
+// so all rows share every K/V tile.  The context is consumed in steps of 64
+// tokens (64 / B blocks).  Six warps:
+//   warps 0-3  softmax: thread t of warp w owns row 32w + t = TMEM lane
+//              32w + t; they stage the Q tile, turn each S into P and write
+//              the normalised output;
+//   warp 4     producer (one lane): streams each step's K blocks into the K
+//              ring and its V blocks into the V ring (TMA, one 2-D box per
+//              block and 64-column half), each ring slot holding one step as
+//              [half][64 tokens][128 B], so a step's keys are one operand;
+//   warp 5     MMA (one lane): allocates TMEM and issues every MMA.
+// Per step j:
+//   S_j = Q K_j^T  M = 128 rows, N = the step's tokens, K = D in 16-column
+//                  MMAs; A = Q (K-major), B = K (K-major) -> S buffer j % 2;
+//   softmax        each thread loads its row of S_j, masks tokens past its
+//                  position (only on steps that reach the diagonal or end
+//                  short), and forms p = 2^(s * scale * log2 e - m) against a
+//                  running maximum m that only moves when the row maximum
+//                  exceeds it by more than 8 (l and the row of O are then
+//                  rescaled), so most steps never touch O; p goes back into
+//                  the same TMEM columns as two fp16 / bf16 terms p_hi, p_lo;
+//   O += P_j V_j   M = 128, N = D, K = 16 tokens per MMA; A = P from TMEM,
+//                  B = V read MN-major (rows = tokens) -> O in TMEM.
+// The MMA lane issues QK(j + 1) before it waits for P_j, so the softmax of
+// one step runs while the tensor pipe does the previous step's PV and the
+// next step's QK.  Every mbarrier phase is waited in order by one role and
+// cannot run ahead of that wait (each phase's producer depends on the
+// waiter's previous signal).  Rows of a partly filled last block past the
+// context are zeroed in the V ring before the PV MMAs read them.  All waits
+// are bounded; TMEM is released on every path.
+#pragma once
+
+#include "pa_prefill.cuh"
+#include "pa_sched.cuh"
+
+namespace pagedkv {
+
+constexpr int kTcRows = 128;                 // query rows per CTA (= TMEM lanes)
+constexpr int kTcStepTokens = 64;            // tokens per softmax step
+constexpr int kTcThreads = 6 * 32;
+constexpr int kTcRingBytes = 64 * 1024;      // K ring + V ring
+constexpr int kTcMaxSlots = 4;               // step slots per ring
+constexpr int kTcCols = 256;                 // TMEM columns: O (D) | S/P buffer 0 (64) | S/P buffer 1 (64)
+
+// Shared memory matrix descriptor (tcgen05): 128-byte swizzle, version 1.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+  d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, A / B of type T,
+// A K-major, B K-major (b_mn = false) or MN-major (b_mn = true), M x N.
+template <typename T>
+__device__ __forceinline__ uint32_t umma_idesc(int M, int N, bool b_mn) {
+  const uint32_t ab = Mma<T>::kIsBf16 ? 1u : 0u;
+  return (1u << 4) | (ab << 7) | (ab << 10) | ((b_mn ? 1u : 0u) << 16) | (uint32_t(N >> 3) << 17) |
+         (uint32_t(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile("{.reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;}"
+               ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+               : "memory");
+}
+
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile("{.reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;}"
+               ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+               : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kTcThreads, 2)
+    prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap map_k,
+                      const __grid_constant__ CUtensorMap map_v) {
+  constexpr int HALVES = D / 64;
+  constexpr uint32_t QHALF = kTcRows * 128;        // one 64-column half of the Q tile
+  constexpr uint32_t SHALF = kTcStepTokens * 128;  // one 64-column half of a step slot
+  static_assert(D + 2 * kTcStepTokens <= kTcCols, "TMEM budget");
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t k_full[kTcMaxSlots], k_empty[kTcMaxSlots];
+  __shared__ __align__(8) uint64_t v_full[kTcMaxSlots], v_empty[kTcMaxSlots];
+  __shared__ __align__(8) uint64_t s_full[2], p_full, o_done, mma_done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int sh_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // heaviest tiles first over all (sequence, kv head) pairs
+  const int pairs = a.S * a.Hkv;
+  const int pair = int(blockIdx.x % unsigned(pairs));
+  const int qt = int(gridDim.x / unsigned(pairs)) - 1 - int(blockIdx.x / unsigned(pairs));
+  const int s = pair / a.Hkv, kvh = pair % a.Hkv;
+  const int G = a.Hq / a.Hkv;
+  const int B = a.B;
+  const int q0 = a.q_start[s];
+  const int n = a.q_start[s + 1] - q0;
+  const long long cap = (long long)a.max_blocks * B;
+  long long Lr = a.lens[s];
+  Lr = Lr < 0 ? 0 : (Lr > cap ? cap : Lr);
+  const int L = int(Lr);
+  if (n < 0 || n > L) {
+    if (threadIdx.x == 0 && qt == 0 && kvh == 0) raise_error(a.err, PA_DEVERR_CONTEXT);
+    return;
+  }
+  const int rows = n * G;
+  const int r0 = qt * kTcRows;
+  if (r0 >= rows) return;
+  const int pos0 = L - n;
+  const int p_last = pos0 + (min(rows, r0 + kTcRows) - 1) / G;
+  const int ntile = p_last / B + 1;
+  const int bps = kTcStepTokens / B;  // blocks per step
+  const int nstep = (ntile + bps - 1) / bps;
+  const int nsl = a.nstage;           // step slots per ring
+  const uint32_t SS = a.slot_stride;  // bytes per step slot (HALVES * SHALF)
+
+  // shared memory: Q tile (1024-aligned), K ring, V ring
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  unsigned char *qs = smem_raw + pad;
+  unsigned char *kring = qs + HALVES * QHALF;
+  unsigned char *vring = kring + size_t(nsl) * SS;
+  const uint32_t q_addr = raw + pad;
+  const uint32_t kring_addr = q_addr + HALVES * QHALF, vring_addr = kring_addr + uint32_t(nsl) * SS;
+  volatile int *abort_flag = &sh_abort;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nsl; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(&p_full, 4);
+    mbar_init(&o_done, 1);
+    mbar_init(&mma_done, 1);
+    sh_abort = 0;
+    fence_barrier_init();
+  }
+  // ---- the Q tile: rows r0 .. r0 + 127, K-major halves [128 rows][128 B], swizzled
+  if (warp < 4) {
+    const int t = threadIdx.x;  // 0..127
+    for (int i = t; i < kTcRows * D / 8; i += 128) {
+      const int r = i / (D / 8), c = i % (D / 8);  // row, 16-byte chunk
+      const int gr = r0 + r;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (gr < rows)
+        v = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.q) +
+                                             ((long long)(q0 + gr / G) * a.Hq + kvh * G + gr % G) * D + c * 8);
+      *reinterpret_cast<uint4 *>(qs + (c >> 3) * QHALF + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+    }
+    fence_proxy_async_shared();
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_base)),
+                 "n"(kTcCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_k)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_v)) : "memory");
+      const int32_t *trow = a.tables + (long long)s * a.max_blocks;
+      const uint32_t tile_bytes = uint32_t(B) * D * 2;
+      // one step's blocks into a step slot: [half][64 tokens][128 B]
+      auto load_step = [&](unsigned char *dst, uint64_t *bar, const CUtensorMap *map, int j) {
+        const int b0 = j * bps, nb = min(bps, ntile - b0);
+        uint32_t valid = 0;
+        for (int i = 0; i < nb; ++i) {
+          const int pid = trow[b0 + i];
+          valid += (pid >= 0 && pid < a.num_blocks) ? 1u : 0u;
+        }
+        mbar_arrive_expect_tx(bar, valid * tile_bytes);
+        for (int i = 0; i < nb; ++i) {
+          const int pid = trow[b0 + i];
+          if (pid < 0 || pid >= a.num_blocks) {
+            raise_error(a.err, PA_DEVERR_BLOCK_ID);
+            continue;
+          }
+          const int y = (pid * a.Hkv + kvh) * B;
+#pragma unroll
+          for (int hh = 0; hh < HALVES; ++hh) tma_load_2d(dst + hh * SHALF + i * B * 128, map, 64 * hh, y, bar);
+        }
+      };
+      int kj = 0, vj = 0;
+      long long t_last = clock64();
+      while (kj < nstep || vj < nstep) {
+        bool prog = false;
+        if (kj < nstep) {
+          const int slot = kj % nsl;
+          const uint32_t use = uint32_t(kj / nsl);
+          if (use == 0 || mbar_try_wait(&k_empty[slot], (use - 1) & 1u)) {
+            load_step(kring + size_t(slot) * SS, &k_full[slot], &map_k, kj);
+            ++kj;
+            prog = true;
+          }
+        }
+        if (vj < kj) {  // a step's values after its keys
+          const int slot = vj % nsl;
+          const uint32_t use = uint32_t(vj / nsl);
+          if (use == 0 || mbar_try_wait(&v_empty[slot], (use - 1) & 1u)) {
+            load_step(vring + size_t(slot) * SS, &v_full[slot], &map_v, vj);
+            ++vj;
+            prog = true;
+          }
+        }
+        if (prog) {
+          t_last = clock64();
+        } else if (*abort_flag) {
+          break;
+        } else if (clock64() - t_last > kWaitLimitCycles) {
+          *abort_flag = 1;
+          raise_error(a.err, PA_DEVERR_TIMEOUT);
+          break;
+        }
+      }
+      // no copy into this CTA's shared memory may still be in flight at the end
+      int never = 0;
+      for (int slot = 0; slot < nsl; ++slot) {
+        if (kj > slot) mbar_wait(&k_full[slot], uint32_t((kj - 1 - slot) / nsl) & 1u, &never);
+        if (vj > slot) mbar_wait(&v_full[slot], uint32_t((vj - 1 - slot) / nsl) & 1u, &never);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      const uint32_t id_pv = umma_idesc<T>(kTcRows, D, true);
+      bool ok = true;
+      for (int j = 0; j <= nstep && ok; ++j) {
+        if (j < nstep) {  // S_j = Q K_j^T into buffer j % 2
+          const int nb = min(bps, ntile - j * bps);
+          const int slot = j % nsl;
+          if (!mbar_wait(&k_full[slot], uint32_t(j / nsl) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kb = kring_addr + uint32_t(slot) * SS;
+          const uint32_t id_qk = umma_idesc<T>(kTcRows, nb * B, false);
+          const uint32_t sb = tmem + uint32_t(D + kTcStepTokens * (j & 1));
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint64_t ad = umma_desc_sw128(q_addr + (ks >> 2) * QHALF + (ks & 3) * 32, 16, 1024);
+            const uint64_t bd = umma_desc_sw128(kb + (ks >> 2) * SHALF + (ks & 3) * 32, 16, 1024);
+            umma_ss(sb, ad, bd, id_qk, ks > 0);
+          }
+          umma_commit(&k_empty[slot]);
+          umma_commit(&s_full[j & 1]);
+        }
+        if (j >= 1) {  // O += P_i V_i once the softmax warps stored P_i
+          const int i = j - 1;
+          const int nb = min(bps, ntile - i * bps);
+          const int slot = i % nsl;
+          if (!mbar_wait(&p_full, uint32_t(i) & 1u, abort_flag) ||
+              !mbar_wait(&v_full[slot], uint32_t(i / nsl) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vb = vring_addr + uint32_t(slot) * SS;
+          const uint32_t pb = tmem + uint32_t(D + kTcStepTokens * (i & 1));
+          for (int kk = 0; kk < nb * B / 16; ++kk) {
+            const uint64_t bd = umma_desc_sw128(vb + kk * 16 * 128, SHALF, 1024);
+            umma_ts(tmem, pb + kk * 8, bd, id_pv, (i > 0 || kk > 0) ? 1u : 0u);
+            umma_ts(tmem, pb + 32 + kk * 8, bd, id_pv, 1u);
+          }
+          umma_commit(&v_empty[slot]);
+          umma_commit(&o_done);
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        raise_error(a.err, PA_DEVERR_TIMEOUT);
+      }
+      // every MMA this thread issued has finished before TMEM is released
+      umma_commit(&mma_done);
+      int never = 0;
+      mbar_wait(&mma_done, 0u, &never);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- softmax
+    const int row = warp * 32 + lane;  // TMEM lane
+    const int gr = r0 + row;
+    const int pos = pos0 + gr / G;
+    const int pos_first = pos0 + r0 / G;
+    const uint32_t tl = tmem + (uint32_t(warp * 32) << 16);
+    const float qscale = a.qscale;
+    const bool up = qscale >= 0.f;  // the largest score is the largest scaled score
+    const float init = up ? -CUDART_INF_F : CUDART_INF_F;
+    float m = -CUDART_INF_F, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nstep; ++j) {
+      const int t0 = j * kTcStepTokens;
+      const int nb = min(bps, ntile - j * bps);
+      ok = ok && !*abort_flag && mbar_wait(&s_full[j & 1], uint32_t(j >> 1) & 1u, abort_flag);
+      ok = __all_sync(kFullMask, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t sb = tl + uint32_t(D + kTcStepTokens * (j & 1));
+      // a partly filled last block: zero its V rows past the context before the PV MMAs read them
+      if (j == nstep - 1 && L < ntile * B) {
+        const int slot = j % nsl;
+        ok = mbar_wait(&v_full[slot], uint32_t(j / nsl) & 1u, abort_flag);
+        ok = __all_sync(kFullMask, ok);
+        if (!ok) break;
+        unsigned char *vs = vring + size_t(slot) * SS;
+        const int zfrom = L - (ntile - 1) * B;
+        const int rbase = (ntile - 1 - j * bps) * B;
+        for (int i = threadIdx.x; i < (B - zfrom) * HALVES * 8; i += 128) {
+          const int r = rbase + zfrom + i / (HALVES * 8);
+          const int hc = i % (HALVES * 8);
+          *reinterpret_cast<uint4 *>(vs + (hc >> 3) * SHALF + r * 128 + (hc & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_shared();
+      }
+      uint32_t s0[32], s1[32];
+      tmem_ld32(sb, s0);
+      tmem_ld32(sb + 32, s1);
+      const bool need_mask = t0 + kTcStepTokens - 1 > pos_first || nb * B < kTcStepTokens;
+      uint64_t vis = ~0ull;
+      if (need_mask) {
+        const int nv = min(nb * B, pos - t0 + 1);  // visible columns 0 .. nv - 1
+        vis = nv <= 0 ? 0ull : (nv >= 64 ? ~0ull : ((1ull << nv) - 1ull));
+      }
+      float best = init;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float x0 = __uint_as_float(s0[c]), x1 = __uint_as_float(s1[c]);
+        const bool v0 = (vis >> c) & 1ull, v1 = (vis >> (32 + c)) & 1ull;
+        if (up) {
+          best = fmaxf(best, v0 ? x0 : init);
+          best = fmaxf(best, v1 ? x1 : init);
+        } else {
+          best = fminf(best, v0 ? x0 : init);
+          best = fminf(best, v1 ? x1 : init);
+        }
+      }
+      // move the running maximum only when the row's maximum exceeds it by more than 8
+      const float cand = best == init ? -CUDART_INF_F : best * qscale;
+      const bool grow = cand > m + 8.f || (m == -CUDART_INF_F && cand > -CUDART_INF_F);
+      const float mnew = grow ? cand : m;
+      const float alpha = (grow && m > -CUDART_INF_F) ? fast_exp2(m - mnew) : 1.f;
+      const float neg_m = mnew == -CUDART_INF_F ? -CUDART_INF_F : -mnew;
+      uint32_t ph[32], pl[32];
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        // column 2c + e of the step lives in s0 for c < 16, in s1 above
+        const int c0 = 2 * c, c1 = 2 * c + 1;
+        const float x0 = __uint_as_float(c0 < 32 ? s0[c0 & 31] : s1[c0 & 31]);
+        const float x1 = __uint_as_float(c1 < 32 ? s0[c1 & 31] : s1[c1 & 31]);
+        const float p0 = ((vis >> c0) & 1ull) ? fast_exp2(fmaf(x0, qscale, neg_m)) : 0.f;
+        const float p1 = ((vis >> c1) & 1ull) ? fast_exp2(fmaf(x1, qscale, neg_m)) : 0.f;
+        lsum += p0 + p1;
+        ph[c] = Mma<T>::pack(p0, p1);
+        const float2 f = Mma<T>::unpack(ph[c]);
+        pl[c] = Mma<T>::pack(p0 - f.x, p1 - f.y);
+      }
+      l = l * alpha + lsum;
+      m = mnew;
+      // the previous step's PV must be done before O is rescaled
+      if (j > 0) {
+        ok = mbar_wait(&o_done, uint32_t(j - 1) & 1u, abort_flag);
+        ok = __all_sync(kFullMask, ok);
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(kFullMask, alpha != 1.f)) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t ov[32];
+            tmem_ld32(tl + c0, ov);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+            tmem_st32(tl + c0, ov);
+          }
+        }
+      }
+      tmem_st32(sb, ph);
+      tmem_st32(sb + 32, pl);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full);
+    }
+    // ---- the output row: O / l
+    if (ok) {
+      ok = mbar_wait(&o_done, uint32_t(nstep - 1) & 1u, abort_flag);
+      ok = __all_sync(kFullMask, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      T *orow = static_cast<T *>(a.out) + ((long long)(q0 + gr / G) * a.Hq + kvh * G + gr % G) * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t ov[32];
+        tmem_ld32(tl + c0, ov);
+        if (gr < rows) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[c] = Mma<T>::pack(__uint_as_float(ov[2 * c]) * inv, __uint_as_float(ov[2 * c + 1]) * inv);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4 *>(orow + c0 + 8 * c) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                                                                       pk[4 * c + 3]);
+        }
+      }
+    } else if (lane == 0) {
+      *abort_flag = 1;
+      raise_error(a.err, PA_DEVERR_TIMEOUT);
+    }
+  }
+
+  // ---- every role is done with TMEM (the MMA lane waited for its last MMA)
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTcCols));
+  }
+}
+
+}  // namespace pagedkv

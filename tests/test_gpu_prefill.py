@@ -1,7 +1,7 @@
 """pa_prefill (prompt attention through the block table) against the float64
 oracle: ragged prompts with and without cached history, one-token prompts,
 empty prompts, partly filled last blocks, head groups of 1, 4 and 8, head
-dims 64 and 128, block sizes 16 and 32, fp16 and bf16; the full-size prompt
+dims 64 and 128, block sizes 16, 32 and 64, fp16 and bf16; the full-size prompt
 workloads on sampled sequences; invariance under block relabelling."""
 import math
 
@@ -77,6 +77,8 @@ CASES = {
     "g8_b32_d64": ([513, 40, 1], [200, 40, 1], 16, 2, 64, 32),
     "long_prompt": ([700], [700], 8, 2, 128, 16),
     "empty_prompts": ([50, 0, 80], [0, 0, 30], 8, 4, 64, 16),
+    "b64_partial_last_block": ([200, 64, 130], [130, 64, 3], 8, 8, 128, 64),
+    "g1_many_tiles": ([1100], [1000], 2, 2, 64, 16),
 }
 
 
@@ -132,6 +134,9 @@ def test_prefill_full_size_sampled(ops, name, sample):
 
 def test_prefill_rejects_fp32_and_reports_overlong_prompts(ops):
     q, k, v, tables, L, qs = _case([40], [10], 4, 2, 64, 16, torch.float32)
+    with pytest.raises(ops.PagedKVError, match="UNSUPPORTED"):
+        _run(ops, q, k, v, tables, L, qs, 0.1)
+    q, k, v, tables, L, qs = _case([100], [10], 4, 2, 64, 48, torch.bfloat16)  # 48 does not divide 64
     with pytest.raises(ops.PagedKVError, match="UNSUPPORTED"):
         _run(ops, q, k, v, tables, L, qs, 0.1)
     q, k, v, tables, L, qs = _case([40, 30], [10, 5], 4, 2, 64, 16, torch.bfloat16)
