@@ -89,7 +89,35 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive 32-bit TMEM columns of this thread's lane.
+// 32 consecutive 32-bit TMEM columns of this thread's lane; tmem_ld32_async
+// leaves the wait to tmem_wait_ld.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r0)[32], uint32_t (&r1)[32]) {
+  // every destination register of both loads is an operand, so no use of one
+  // can be scheduled before the wait
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r0[0]), "+r"(r0[1]), "+r"(r0[2]), "+r"(r0[3]), "+r"(r0[4]), "+r"(r0[5]), "+r"(r0[6]), "+r"(r0[7]),
+        "+r"(r0[8]), "+r"(r0[9]), "+r"(r0[10]), "+r"(r0[11]), "+r"(r0[12]), "+r"(r0[13]), "+r"(r0[14]), "+r"(r0[15]),
+        "+r"(r0[16]), "+r"(r0[17]), "+r"(r0[18]), "+r"(r0[19]), "+r"(r0[20]), "+r"(r0[21]), "+r"(r0[22]), "+r"(r0[23]),
+        "+r"(r0[24]), "+r"(r0[25]), "+r"(r0[26]), "+r"(r0[27]), "+r"(r0[28]), "+r"(r0[29]), "+r"(r0[30]), "+r"(r0[31]),
+        "+r"(r1[0]), "+r"(r1[1]), "+r"(r1[2]), "+r"(r1[3]), "+r"(r1[4]), "+r"(r1[5]), "+r"(r1[6]), "+r"(r1[7]),
+        "+r"(r1[8]), "+r"(r1[9]), "+r"(r1[10]), "+r"(r1[11]), "+r"(r1[12]), "+r"(r1[13]), "+r"(r1[14]), "+r"(r1[15]),
+        "+r"(r1[16]), "+r"(r1[17]), "+r"(r1[18]), "+r"(r1[19]), "+r"(r1[20]), "+r"(r1[21]), "+r"(r1[22]), "+r"(r1[23]),
+        "+r"(r1[24]), "+r"(r1[25]), "+r"(r1[26]), "+r"(r1[27]), "+r"(r1[28]), "+r"(r1[29]), "+r"(r1[30]), "+r"(r1[31])
+               :
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
@@ -113,6 +141,94 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// p = p_hi + p_lo in two 16-bit terms per value, packed in pairs.  bf16: p_hi
+// is p with its low 16 bits cleared (exact), p_lo = p - p_hi rounded, so the
+// pair carries p to about 2^-16 relative.  fp16: p_hi rounded, then the rest.
+template <typename T>
+struct PSplit {
+  static __device__ __forceinline__ void run(float p0, float p1, uint32_t &hi, uint32_t &lo) {
+    hi = Mma<T>::pack(p0, p1);
+    const float2 f = Mma<T>::unpack(hi);
+    lo = Mma<T>::pack(p0 - f.x, p1 - f.y);
+  }
+};
+template <>
+struct PSplit<__nv_bfloat16> {
+  static __device__ __forceinline__ void run(float p0, float p1, uint32_t &hi, uint32_t &lo) {
+    const uint32_t b0 = __float_as_uint(p0) & 0xFFFF0000u, b1 = __float_as_uint(p1) & 0xFFFF0000u;
+    hi = __byte_perm(b0, b1, 0x7632);
+    lo = Mma<__nv_bfloat16>::pack(p0 - __uint_as_float(b0), p1 - __uint_as_float(b1));
+  }
+};
+
+// One row's step of the online softmax.  Scores s0 (columns 0..31) and s1
+// (32..63); with kMask only columns 0 .. nv - 1 are visible.  Moves the
+// running maximum m (scaled, base 2) only when the step's maximum exceeds it
+// by more than 8; returns the sum of the new p and sets alpha (the factor
+// for the old l and O) and the packed p_hi / p_lo.
+template <typename T, bool kMask>
+__device__ __forceinline__ float softmax_step(const uint32_t (&s0)[32], const uint32_t (&s1)[32], int nv,
+                                              float qscale, float &m, float &alpha, uint32_t (&ph)[32],
+                                              uint32_t (&pl)[32]) {
+  float b0 = -CUDART_INF_F, b1 = -CUDART_INF_F;
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    float x0 = __uint_as_float(s0[c]), x1 = __uint_as_float(s0[c + 1]);
+    float y0 = __uint_as_float(s1[c]), y1 = __uint_as_float(s1[c + 1]);
+    if (kMask) {
+      x0 = c < nv ? x0 : -CUDART_INF_F;
+      x1 = c + 1 < nv ? x1 : -CUDART_INF_F;
+      y0 = c + 32 < nv ? y0 : -CUDART_INF_F;
+      y1 = c + 33 < nv ? y1 : -CUDART_INF_F;
+    }
+    b0 = fmax3(b0, x0, x1);
+    b1 = fmax3(b1, y0, y1);
+  }
+  const float best = fmaxf(b0, b1);
+  const float cand = best == -CUDART_INF_F ? -CUDART_INF_F : best * qscale;
+  const bool grow = cand > m + 8.f || (m == -CUDART_INF_F && cand > -CUDART_INF_F);
+  const float mnew = grow ? cand : m;
+  alpha = (grow && m > -CUDART_INF_F) ? fast_exp2(m - mnew) : 1.f;
+  m = mnew;
+  const float neg_m = mnew == -CUDART_INF_F ? -CUDART_INF_F : -mnew;
+  float lsum0 = 0.f, lsum1 = 0.f;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    // the pair (2c, 2c + 1) of the step's columns
+    const int c0 = 2 * c, c1 = 2 * c + 1;
+    const float x0 = __uint_as_float(c0 < 32 ? s0[c0 & 31] : s1[c0 & 31]);
+    const float x1 = __uint_as_float(c1 < 32 ? s0[c1 & 31] : s1[c1 & 31]);
+    float p0 = fast_exp2(fmaf(x0, qscale, neg_m));
+    float p1 = fast_exp2(fmaf(x1, qscale, neg_m));
+    if (kMask) {
+      p0 = c0 < nv ? p0 : 0.f;
+      p1 = c1 < nv ? p1 : 0.f;
+    }
+    lsum0 += p0;
+    lsum1 += p1;
+    PSplit<T>::run(p0, p1, ph[c], pl[c]);
+  }
+  return lsum0 + lsum1;
+}
+
+// Per-step SM clock stamps of one CTA (PA_TRACE builds only).
+#ifdef PA_TRACE
+#define TC_TRACE(j, f)                                                 \
+  do {                                                                 \
+    if (PA_TRACE_CTA(blockIdx.x) && (j) < 64) tc_tr[(j)][(f)] = clock64(); \
+  } while (0)
+#else
+#define TC_TRACE(j, f) \
+  do {                 \
+  } while (0)
+#endif
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 2)
     prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap map_k,
@@ -127,6 +243,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   __shared__ __align__(8) uint64_t s_full[2], p_full, o_done, mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ int sh_abort;
+#ifdef PA_TRACE
+  __shared__ long long tc_tr[64][16];
+#endif
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -193,6 +312,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       if (gr < rows)
         v = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.q) +
                                              ((long long)(q0 + gr / G) * a.Hq + kvh * G + gr % G) * D + c * 8);
+      if (a.qscale < 0.f) {  // S of -q with |scale|: the softmax only ever looks for the largest score
+        v.x ^= 0x80008000u;
+        v.y ^= 0x80008000u;
+        v.z ^= 0x80008000u;
+        v.w ^= 0x80008000u;
+      }
       *reinterpret_cast<uint4 *>(qs + (c >> 3) * QHALF + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
     }
     fence_proxy_async_shared();
@@ -206,67 +331,98 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
+  if (threadIdx.x == 0) TC_TRACE(0, 11);
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
+    // The whole warp runs the loop; lane 0 polls the barriers and issues the
+    // copies.  Each stream (K, V) holds the table entries of its current 32
+    // blocks in the lanes' registers, the next 32 already requested.
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_k)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_v)) : "memory");
-      const int32_t *trow = a.tables + (long long)s * a.max_blocks;
-      const uint32_t tile_bytes = uint32_t(B) * D * 2;
-      // one step's blocks into a step slot: [half][64 tokens][128 B]
-      auto load_step = [&](unsigned char *dst, uint64_t *bar, const CUtensorMap *map, int j) {
-        const int b0 = j * bps, nb = min(bps, ntile - b0);
-        uint32_t valid = 0;
-        for (int i = 0; i < nb; ++i) {
-          const int pid = trow[b0 + i];
-          valid += (pid >= 0 && pid < a.num_blocks) ? 1u : 0u;
-        }
+    }
+    const int32_t *trow = a.tables + (long long)s * a.max_blocks;
+    const uint32_t tile_bytes = uint32_t(B) * D * 2;
+    auto entry = [&](int b) { return b < ntile ? trow[b] : -1; };
+    struct Window {
+      int cur, nxt, chunk;
+    };
+    Window wk{entry(lane), entry(32 + lane), 0}, wv = wk;
+    // one step's blocks into a step slot: [half][64 tokens][128 B]; a step's
+    // blocks lie in one 32-block chunk (the blocks per step divide 32)
+    auto load_step = [&](Window &w, unsigned char *dst, uint64_t *bar, const CUtensorMap *map, int j) {
+      const int b0 = j * bps, nb = min(bps, ntile - b0);
+      if (b0 >> 5 != w.chunk) {
+        w.cur = w.nxt;
+        w.chunk = b0 >> 5;
+        w.nxt = entry(((w.chunk + 1) << 5) + lane);
+      }
+      int pid[4];
+      uint32_t valid = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        pid[i] = __shfl_sync(kFullMask, w.cur, (b0 + i) & 31);
+        if (i < nb && pid[i] >= 0 && pid[i] < a.num_blocks) ++valid;
+      }
+      if (lane == 0) {
         mbar_arrive_expect_tx(bar, valid * tile_bytes);
-        for (int i = 0; i < nb; ++i) {
-          const int pid = trow[b0 + i];
-          if (pid < 0 || pid >= a.num_blocks) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (i >= nb) break;
+          if (pid[i] < 0 || pid[i] >= a.num_blocks) {
             raise_error(a.err, PA_DEVERR_BLOCK_ID);
             continue;
           }
-          const int y = (pid * a.Hkv + kvh) * B;
+          const int y = (pid[i] * a.Hkv + kvh) * B;
 #pragma unroll
           for (int hh = 0; hh < HALVES; ++hh) tma_load_2d(dst + hh * SHALF + i * B * 128, map, 64 * hh, y, bar);
         }
-      };
-      int kj = 0, vj = 0;
-      long long t_last = clock64();
-      while (kj < nstep || vj < nstep) {
-        bool prog = false;
-        if (kj < nstep) {
-          const int slot = kj % nsl;
-          const uint32_t use = uint32_t(kj / nsl);
-          if (use == 0 || mbar_try_wait(&k_empty[slot], (use - 1) & 1u)) {
-            load_step(kring + size_t(slot) * SS, &k_full[slot], &map_k, kj);
-            ++kj;
-            prog = true;
-          }
-        }
-        if (vj < kj) {  // a step's values after its keys
-          const int slot = vj % nsl;
-          const uint32_t use = uint32_t(vj / nsl);
-          if (use == 0 || mbar_try_wait(&v_empty[slot], (use - 1) & 1u)) {
-            load_step(vring + size_t(slot) * SS, &v_full[slot], &map_v, vj);
-            ++vj;
-            prog = true;
-          }
-        }
-        if (prog) {
-          t_last = clock64();
-        } else if (*abort_flag) {
-          break;
-        } else if (clock64() - t_last > kWaitLimitCycles) {
-          *abort_flag = 1;
-          raise_error(a.err, PA_DEVERR_TIMEOUT);
-          break;
+      }
+    };
+    int kj = 0, vj = 0;
+    long long t_last = clock64();
+    while (kj < nstep || vj < nstep) {
+      bool prog = false;
+      if (kj < nstep) {
+        const int slot = kj % nsl;
+        const uint32_t use = uint32_t(kj / nsl);
+        const bool free_slot = __shfl_sync(kFullMask, use == 0 || (lane == 0 && mbar_test_wait(&k_empty[slot], (use - 1) & 1u)), 0);
+        if (free_slot) {
+          if (lane == 0) TC_TRACE(kj, 12);
+          load_step(wk, kring + size_t(slot) * SS, &k_full[slot], &map_k, kj);
+          if (lane == 0) TC_TRACE(kj, 9);
+          ++kj;
+          prog = true;
         }
       }
-      // no copy into this CTA's shared memory may still be in flight at the end
+      if (vj < kj) {  // a step's values after its keys
+        const int slot = vj % nsl;
+        const uint32_t use = uint32_t(vj / nsl);
+        const bool free_slot = __shfl_sync(kFullMask, use == 0 || (lane == 0 && mbar_test_wait(&v_empty[slot], (use - 1) & 1u)), 0);
+        if (free_slot) {
+          if (lane == 0) TC_TRACE(vj, 13);
+          load_step(wv, vring + size_t(slot) * SS, &v_full[slot], &map_v, vj);
+          if (lane == 0) TC_TRACE(vj, 10);
+          ++vj;
+          prog = true;
+        }
+      }
+      if (prog) {
+        t_last = clock64();
+        continue;
+      }
+      const bool stop = __shfl_sync(kFullMask, *abort_flag != 0 || clock64() - t_last > kWaitLimitCycles, 0);
+      if (stop) {
+        if (lane == 0 && !*abort_flag) {
+          *abort_flag = 1;
+          raise_error(a.err, PA_DEVERR_TIMEOUT);
+        }
+        break;
+      }
+    }
+    // no copy into this CTA's shared memory may still be in flight at the end
+    if (lane == 0) {
       int never = 0;
       for (int slot = 0; slot < nsl; ++slot) {
         if (kj > slot) mbar_wait(&k_full[slot], uint32_t((kj - 1 - slot) / nsl) & 1u, &never);
@@ -287,6 +443,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             ok = false;
             break;
           }
+          TC_TRACE(j, 4);
           tc_fence_after();
           const uint32_t kb = kring_addr + uint32_t(slot) * SS;
           const uint32_t id_qk = umma_idesc<T>(kTcRows, nb * B, false);
@@ -297,18 +454,25 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const uint64_t bd = umma_desc_sw128(kb + (ks >> 2) * SHALF + (ks & 3) * 32, 16, 1024);
             umma_ss(sb, ad, bd, id_qk, ks > 0);
           }
+          TC_TRACE(j, 14);
           umma_commit(&k_empty[slot]);
           umma_commit(&s_full[j & 1]);
+          TC_TRACE(j, 5);
         }
         if (j >= 1) {  // O += P_i V_i once the softmax warps stored P_i
           const int i = j - 1;
           const int nb = min(bps, ntile - i * bps);
           const int slot = i % nsl;
-          if (!mbar_wait(&p_full, uint32_t(i) & 1u, abort_flag) ||
-              !mbar_wait(&v_full[slot], uint32_t(i / nsl) & 1u, abort_flag)) {
+          if (!mbar_wait(&p_full, uint32_t(i) & 1u, abort_flag)) {
             ok = false;
             break;
           }
+          TC_TRACE(i, 6);
+          if (!mbar_wait(&v_full[slot], uint32_t(i / nsl) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          TC_TRACE(i, 7);
           tc_fence_after();
           const uint32_t vb = vring_addr + uint32_t(slot) * SS;
           const uint32_t pb = tmem + uint32_t(D + kTcStepTokens * (i & 1));
@@ -317,8 +481,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             umma_ts(tmem, pb + kk * 8, bd, id_pv, (i > 0 || kk > 0) ? 1u : 0u);
             umma_ts(tmem, pb + 32 + kk * 8, bd, id_pv, 1u);
           }
+          TC_TRACE(i, 15);
           umma_commit(&v_empty[slot]);
           umma_commit(&o_done);
+          TC_TRACE(i, 8);
         }
       }
       if (!ok) {
@@ -338,9 +504,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const int pos = pos0 + gr / G;
     const int pos_first = pos0 + r0 / G;
     const uint32_t tl = tmem + (uint32_t(warp * 32) << 16);
-    const float qscale = a.qscale;
-    const bool up = qscale >= 0.f;  // the largest score is the largest scaled score
-    const float init = up ? -CUDART_INF_F : CUDART_INF_F;
+    const float qscale = fabsf(a.qscale);  // Q was negated for a negative scale
     float m = -CUDART_INF_F, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nstep; ++j) {
@@ -349,6 +513,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       ok = ok && !*abort_flag && mbar_wait(&s_full[j & 1], uint32_t(j >> 1) & 1u, abort_flag);
       ok = __all_sync(kFullMask, ok);
       if (!ok) break;
+      if (threadIdx.x == 0) TC_TRACE(j, 0);
       tc_fence_after();
       const uint32_t sb = tl + uint32_t(D + kTcStepTokens * (j & 1));
       // a partly filled last block: zero its V rows past the context before the PV MMAs read them
@@ -368,50 +533,20 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         fence_proxy_async_shared();
       }
       uint32_t s0[32], s1[32];
-      tmem_ld32(sb, s0);
-      tmem_ld32(sb + 32, s1);
+      tmem_ld32_async(sb, s0);
+      tmem_ld32_async(sb + 32, s1);
+      tmem_wait_ld(s0, s1);
+      // only steps that reach the diagonal or end short need a mask; the
+      // visible columns of a row are then a prefix 0 .. nv - 1
       const bool need_mask = t0 + kTcStepTokens - 1 > pos_first || nb * B < kTcStepTokens;
-      uint64_t vis = ~0ull;
-      if (need_mask) {
-        const int nv = min(nb * B, pos - t0 + 1);  // visible columns 0 .. nv - 1
-        vis = nv <= 0 ? 0ull : (nv >= 64 ? ~0ull : ((1ull << nv) - 1ull));
-      }
-      float best = init;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float x0 = __uint_as_float(s0[c]), x1 = __uint_as_float(s1[c]);
-        const bool v0 = (vis >> c) & 1ull, v1 = (vis >> (32 + c)) & 1ull;
-        if (up) {
-          best = fmaxf(best, v0 ? x0 : init);
-          best = fmaxf(best, v1 ? x1 : init);
-        } else {
-          best = fminf(best, v0 ? x0 : init);
-          best = fminf(best, v1 ? x1 : init);
-        }
-      }
-      // move the running maximum only when the row's maximum exceeds it by more than 8
-      const float cand = best == init ? -CUDART_INF_F : best * qscale;
-      const bool grow = cand > m + 8.f || (m == -CUDART_INF_F && cand > -CUDART_INF_F);
-      const float mnew = grow ? cand : m;
-      const float alpha = (grow && m > -CUDART_INF_F) ? fast_exp2(m - mnew) : 1.f;
-      const float neg_m = mnew == -CUDART_INF_F ? -CUDART_INF_F : -mnew;
       uint32_t ph[32], pl[32];
-      float lsum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        // column 2c + e of the step lives in s0 for c < 16, in s1 above
-        const int c0 = 2 * c, c1 = 2 * c + 1;
-        const float x0 = __uint_as_float(c0 < 32 ? s0[c0 & 31] : s1[c0 & 31]);
-        const float x1 = __uint_as_float(c1 < 32 ? s0[c1 & 31] : s1[c1 & 31]);
-        const float p0 = ((vis >> c0) & 1ull) ? fast_exp2(fmaf(x0, qscale, neg_m)) : 0.f;
-        const float p1 = ((vis >> c1) & 1ull) ? fast_exp2(fmaf(x1, qscale, neg_m)) : 0.f;
-        lsum += p0 + p1;
-        ph[c] = Mma<T>::pack(p0, p1);
-        const float2 f = Mma<T>::unpack(ph[c]);
-        pl[c] = Mma<T>::pack(p0 - f.x, p1 - f.y);
-      }
+      float alpha, lsum;
+      if (need_mask)
+        lsum = softmax_step<T, true>(s0, s1, min(nb * B, pos - t0 + 1), qscale, m, alpha, ph, pl);
+      else
+        lsum = softmax_step<T, false>(s0, s1, kTcStepTokens, qscale, m, alpha, ph, pl);
       l = l * alpha + lsum;
-      m = mnew;
+      if (threadIdx.x == 0) TC_TRACE(j, 1);
       // the previous step's PV must be done before O is rescaled
       if (j > 0) {
         ok = mbar_wait(&o_done, uint32_t(j - 1) & 1u, abort_flag);
@@ -429,12 +564,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           }
         }
       }
+      if (threadIdx.x == 0) TC_TRACE(j, 2);
       tmem_st32(sb, ph);
       tmem_st32(sb + 32, pl);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full);
+      if (threadIdx.x == 0) TC_TRACE(j, 3);
     }
     // ---- the output row: O / l
     if (ok) {
@@ -473,6 +610,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTcCols));
   }
+#ifdef PA_TRACE
+  if (threadIdx.x == 0 && PA_TRACE_CTA(blockIdx.x)) {
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    const long long t0 = tc_tr[0][11];
+    for (int j = 0; j < nstep && j < 64; ++j) {
+      const long long *t = tc_tr[j];
+      printf("trp %d %u %d %lld %lld %lld %lld %lld %lld %lld %lld %lld %lld %lld %lld %lld %lld %lld\n",
+             int(blockIdx.x), smid, j, t[0] - t0, t[1] - t0, t[2] - t0, t[3] - t0, t[4] - t0, t[5] - t0, t[6] - t0,
+             t[7] - t0, t[8] - t0, t[9] - t0, t[10] - t0, t[12] - t0, t[13] - t0, t[14] - t0, t[15] - t0);
+    }
+  }
+#endif
 }
 
 }  // namespace pagedkv

@@ -94,6 +94,15 @@ def test_prefill_matches_oracle(ops, name, dtype):
     assert_prefill_close(out, ref)
 
 
+@pytest.mark.parametrize("scale", [-0.07, 0.0])
+def test_prefill_negative_and_zero_scale(ops, scale):
+    lens, prompts = [300, 90], [200, 90]
+    q, k, v, tables, L, qs = _case(lens, prompts, 8, 2, 128, 16, torch.bfloat16, seed=11)
+    out, err = _run(ops, q, k, v, tables, L, qs, scale)
+    assert err == 0, ops.error_names(err)
+    assert_prefill_close(out, native.prefill(q, k, v, tables.numpy(), L.numpy(), qs.numpy(), scale))
+
+
 def test_prefill_invariant_under_block_relabelling_and_deterministic(ops):
     lens, prompts = [300, 129], [100, 129]
     q, k, v, tables, L, qs = _case(lens, prompts, 16, 4, 128, 16, torch.bfloat16, seed=5)
