@@ -434,9 +434,10 @@ static pa_status prefill_dispatch(const PrefillArgs &pa_args, const void *k_cach
                                   pa_dtype dtype, int D, size_t smem, dim3 grid, cudaStream_t st) {
   CUtensorMap mk, mv;
   PrefillArgs b = pa_args;
-  // one 2-D box (B rows x 64 columns) per block and half
+  // K: one 2-D box (B rows x 64 columns) per block and half; V: one box per
+  // block (a 3-D box over both halves when head_dim is 128)
   if (!encode_pool_map(&mk, k_cache, dtype, b.num_blocks, b.Hkv, b.B, D, false) ||
-      !encode_pool_map(&mv, v_cache, dtype, b.num_blocks, b.Hkv, b.B, D, false))
+      !encode_pool_map(&mv, v_cache, dtype, b.num_blocks, b.Hkv, b.B, D, D == 128))
     return PA_ERR_CUDA;
   return D == 64 ? launch_prefill_tc<T, 64>(b, mk, mv, smem, grid, st)
                  : launch_prefill_tc<T, 128>(b, mk, mv, smem, grid, st);

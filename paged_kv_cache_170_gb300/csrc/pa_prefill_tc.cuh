@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t k_full[kTcMaxSlots], k_empty[kTcMaxSlots];
   __shared__ __align__(8) uint64_t v_full[kTcMaxSlots], v_empty[kTcMaxSlots];
-  __shared__ __align__(8) uint64_t s_full[2], p_full, o_done, mma_done;
+  __shared__ __align__(8) uint64_t s_full[2], p_full[2], o_done[2], mma_done;  // [2]: by step parity
   __shared__ uint32_t tmem_base;
   __shared__ int sh_abort;
 #ifdef PA_TRACE
@@ -249,6 +249,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+#ifdef PA_TRACE
+  unsigned long long tc_g0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tc_g0));
+#endif
   // heaviest tiles first over all (sequence, kv head) pairs
   const int pairs = a.S * a.Hkv;
   const int pair = int(blockIdx.x % unsigned(pairs));
@@ -296,29 +300,39 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(&p_full, 4);
-    mbar_init(&o_done, 1);
+    mbar_init(&p_full[0], 4);
+    mbar_init(&p_full[1], 4);
+    mbar_init(&o_done[0], 1);
+    mbar_init(&o_done[1], 1);
     mbar_init(&mma_done, 1);
     sh_abort = 0;
     fence_barrier_init();
   }
-  // ---- the Q tile: rows r0 .. r0 + 127, K-major halves [128 rows][128 B], swizzled
+  __syncthreads();  // the barriers are initialised; the producer starts at once
+  if (threadIdx.x == 0) TC_TRACE(0, 11);
   if (warp < 4) {
-    const int t = threadIdx.x;  // 0..127
-    for (int i = t; i < kTcRows * D / 8; i += 128) {
+    // ---- the Q tile: rows r0 .. r0 + 127, K-major halves [128 rows][128 B],
+    // swizzled; every load is issued before the first store
+    constexpr int kPer = kTcRows * D / 8 / 128;  // 16-byte chunks per thread
+    const int t = threadIdx.x;                    // 0..127
+    uint4 v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = t + 128 * k;
       const int r = i / (D / 8), c = i % (D / 8);  // row, 16-byte chunk
       const int gr = r0 + r;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      v[k] = make_uint4(0u, 0u, 0u, 0u);
       if (gr < rows)
-        v = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.q) +
-                                             ((long long)(q0 + gr / G) * a.Hq + kvh * G + gr % G) * D + c * 8);
-      if (a.qscale < 0.f) {  // S of -q with |scale|: the softmax only ever looks for the largest score
-        v.x ^= 0x80008000u;
-        v.y ^= 0x80008000u;
-        v.z ^= 0x80008000u;
-        v.w ^= 0x80008000u;
-      }
-      *reinterpret_cast<uint4 *>(qs + (c >> 3) * QHALF + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+        v[k] = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.q) +
+                                                ((long long)(q0 + gr / G) * a.Hq + kvh * G + gr % G) * D + c * 8);
+    }
+    const uint32_t flip = a.qscale < 0.f ? 0x80008000u : 0u;  // S of -q with |scale|: the softmax only looks for maxima
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = t + 128 * k;
+      const int r = i / (D / 8), c = i % (D / 8);
+      const uint4 w = make_uint4(v[k].x ^ flip, v[k].y ^ flip, v[k].z ^ flip, v[k].w ^ flip);
+      *reinterpret_cast<uint4 *>(qs + (c >> 3) * QHALF + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = w;
     }
     fence_proxy_async_shared();
   }
@@ -327,11 +341,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                  "n"(kTcCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_base;
-  if (threadIdx.x == 0) TC_TRACE(0, 11);
+  // the softmax and MMA warps meet once the Q tile is staged and TMEM allocated
+  if (warp != 4) {
+    tc_fence_before();
+    named_barrier_sync(1, 5 * 32);
+    tc_fence_after();
+  }
+  const uint32_t tmem = warp != 4 ? tmem_base : 0u;  // the producer never touches TMEM
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
@@ -349,34 +365,42 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       int cur, nxt, chunk;
     };
     Window wk{entry(lane), entry(32 + lane), 0}, wv = wk;
-    // one step's blocks into a step slot: [half][64 tokens][128 B]; a step's
-    // blocks lie in one 32-block chunk (the blocks per step divide 32)
-    auto load_step = [&](Window &w, unsigned char *dst, uint64_t *bar, const CUtensorMap *map, int j) {
+    // A step's K blocks go to a K slot as [half][64 tokens][128 B] (one 2-D
+    // box per block and half, so a step's keys are one MMA operand); its V
+    // blocks to a V slot as [block][half][B tokens][128 B] (one box per
+    // block).  A step's blocks lie in one 32-block chunk (the blocks per
+    // step divide 32).  A table entry outside the pool raises the error and
+    // loads block 0 in its place, so the byte count is always nb tiles.
+    auto load_step = [&](Window &w, const bool is_v, unsigned char *dst, uint64_t *bar, int j) {
       const int b0 = j * bps, nb = min(bps, ntile - b0);
       if (b0 >> 5 != w.chunk) {
         w.cur = w.nxt;
         w.chunk = b0 >> 5;
         w.nxt = entry(((w.chunk + 1) << 5) + lane);
       }
-      int pid[4];
-      uint32_t valid = 0;
+      int y[4];
+      bool bad = false;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        pid[i] = __shfl_sync(kFullMask, w.cur, (b0 + i) & 31);
-        if (i < nb && pid[i] >= 0 && pid[i] < a.num_blocks) ++valid;
+        const int pid = __shfl_sync(kFullMask, w.cur, (b0 + i) & 31);
+        const bool in_pool = pid >= 0 && pid < a.num_blocks;
+        bad = bad || (i < nb && !in_pool);
+        y[i] = ((in_pool ? pid : 0) * a.Hkv + kvh) * B;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar, valid * tile_bytes);
+        if (bad) raise_error(a.err, PA_DEVERR_BLOCK_ID);
+        mbar_arrive_expect_tx(bar, uint32_t(nb) * tile_bytes);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           if (i >= nb) break;
-          if (pid[i] < 0 || pid[i] >= a.num_blocks) {
-            raise_error(a.err, PA_DEVERR_BLOCK_ID);
-            continue;
-          }
-          const int y = (pid[i] * a.Hkv + kvh) * B;
+          if (!is_v) {
 #pragma unroll
-          for (int hh = 0; hh < HALVES; ++hh) tma_load_2d(dst + hh * SHALF + i * B * 128, map, 64 * hh, y, bar);
+            for (int hh = 0; hh < HALVES; ++hh) tma_load_2d(dst + hh * SHALF + i * B * 128, &map_k, 64 * hh, y[i], bar);
+          } else if (HALVES == 2) {
+            tma_load_3d(dst + i * 2 * B * 128, &map_v, 0, y[i], 0, bar);
+          } else {
+            tma_load_2d(dst + i * B * 128, &map_v, 0, y[i], bar);
+          }
         }
       }
     };
@@ -390,7 +414,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const bool free_slot = __shfl_sync(kFullMask, use == 0 || (lane == 0 && mbar_test_wait(&k_empty[slot], (use - 1) & 1u)), 0);
         if (free_slot) {
           if (lane == 0) TC_TRACE(kj, 12);
-          load_step(wk, kring + size_t(slot) * SS, &k_full[slot], &map_k, kj);
+          load_step(wk, false, kring + size_t(slot) * SS, &k_full[slot], kj);
           if (lane == 0) TC_TRACE(kj, 9);
           ++kj;
           prog = true;
@@ -402,7 +426,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const bool free_slot = __shfl_sync(kFullMask, use == 0 || (lane == 0 && mbar_test_wait(&v_empty[slot], (use - 1) & 1u)), 0);
         if (free_slot) {
           if (lane == 0) TC_TRACE(vj, 13);
-          load_step(wv, vring + size_t(slot) * SS, &v_full[slot], &map_v, vj);
+          load_step(wv, true, vring + size_t(slot) * SS, &v_full[slot], vj);
           if (lane == 0) TC_TRACE(vj, 10);
           ++vj;
           prog = true;
@@ -434,60 +458,76 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
       const uint32_t id_pv = umma_idesc<T>(kTcRows, D, true);
+      // descriptors are built once; the address field counts 16-byte units,
+      // so an offset inside shared memory is added to it directly
+      const uint64_t qd0 = umma_desc_sw128(q_addr, 16, 1024);
+      const uint64_t kd0 = umma_desc_sw128(kring_addr, 16, 1024);
+      const uint64_t vd0 = umma_desc_sw128(vring_addr, uint32_t(B) * 128, 1024);  // LBO: the halves of a V block
+      uint32_t vofs[4];  // the step's 16-token k-steps in a V slot ([block][half][B][128 B])
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const int t = kk * 16;
+        vofs[kk] = uint32_t((t / B) * HALVES * B * 128 + (t % B) * 128) >> 4;
+      }
+      // Issue PV(i) once P_i and V_i are in, and QK(j) once K_j is in and
+      // PV(j - 2) has been issued (QK(j) overwrites the buffer P_{j-2} is
+      // read from; MMAs of one thread run in issue order).
       bool ok = true;
-      for (int j = 0; j <= nstep && ok; ++j) {
-        if (j < nstep) {  // S_j = Q K_j^T into buffer j % 2
+      int nq = 0, np = 0;  // QKs and PVs issued
+      long long t_last = clock64();
+      while (np < nstep) {
+        bool prog = false;
+        if (np < nq && mbar_test_wait(&p_full[np & 1], uint32_t(np >> 1) & 1u) &&
+            mbar_test_wait(&v_full[np % nsl], uint32_t(np / nsl) & 1u)) {  // O += P_i V_i
+          const int i = np;
+          const int nkk = min(bps, ntile - i * bps) * B / 16;
+          const int slot = i % nsl;
+          TC_TRACE(i, 7);
+          tc_fence_after();
+          const uint64_t vd = vd0 + ((uint32_t(slot) * SS) >> 4);
+          const uint32_t pb = tmem + uint32_t(D + kTcStepTokens * (i & 1));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            if (kk < nkk) {
+              umma_ts(tmem, pb + kk * 8, vd + vofs[kk], id_pv, (i > 0 || kk > 0) ? 1u : 0u);
+              umma_ts(tmem, pb + 32 + kk * 8, vd + vofs[kk], id_pv, 1u);
+            }
+          }
+          TC_TRACE(i, 15);
+          umma_commit(&v_empty[slot]);
+          umma_commit(&o_done[i & 1]);
+          TC_TRACE(i, 8);
+          ++np;
+          prog = true;
+        }
+        if (nq < nstep && nq <= np + 1 && mbar_test_wait(&k_full[nq % nsl], uint32_t(nq / nsl) & 1u)) {
+          const int j = nq;  // S_j = Q K_j^T into buffer j % 2
           const int nb = min(bps, ntile - j * bps);
           const int slot = j % nsl;
-          if (!mbar_wait(&k_full[slot], uint32_t(j / nsl) & 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
           TC_TRACE(j, 4);
           tc_fence_after();
-          const uint32_t kb = kring_addr + uint32_t(slot) * SS;
+          const uint64_t kd = kd0 + ((uint32_t(slot) * SS) >> 4);
           const uint32_t id_qk = umma_idesc<T>(kTcRows, nb * B, false);
           const uint32_t sb = tmem + uint32_t(D + kTcStepTokens * (j & 1));
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t ad = umma_desc_sw128(q_addr + (ks >> 2) * QHALF + (ks & 3) * 32, 16, 1024);
-            const uint64_t bd = umma_desc_sw128(kb + (ks >> 2) * SHALF + (ks & 3) * 32, 16, 1024);
-            umma_ss(sb, ad, bd, id_qk, ks > 0);
-          }
+          for (int ks = 0; ks < D / 16; ++ks)
+            umma_ss(sb, qd0 + uint32_t(((ks >> 2) * QHALF + (ks & 3) * 32) >> 4),
+                    kd + uint32_t(((ks >> 2) * SHALF + (ks & 3) * 32) >> 4), id_qk, ks > 0 ? 1u : 0u);
           TC_TRACE(j, 14);
           umma_commit(&k_empty[slot]);
           umma_commit(&s_full[j & 1]);
           TC_TRACE(j, 5);
+          ++nq;
+          prog = true;
         }
-        if (j >= 1) {  // O += P_i V_i once the softmax warps stored P_i
-          const int i = j - 1;
-          const int nb = min(bps, ntile - i * bps);
-          const int slot = i % nsl;
-          if (!mbar_wait(&p_full, uint32_t(i) & 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          TC_TRACE(i, 6);
-          if (!mbar_wait(&v_full[slot], uint32_t(i / nsl) & 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          TC_TRACE(i, 7);
-          tc_fence_after();
-          const uint32_t vb = vring_addr + uint32_t(slot) * SS;
-          const uint32_t pb = tmem + uint32_t(D + kTcStepTokens * (i & 1));
-          for (int kk = 0; kk < nb * B / 16; ++kk) {
-            const uint64_t bd = umma_desc_sw128(vb + kk * 16 * 128, SHALF, 1024);
-            umma_ts(tmem, pb + kk * 8, bd, id_pv, (i > 0 || kk > 0) ? 1u : 0u);
-            umma_ts(tmem, pb + 32 + kk * 8, bd, id_pv, 1u);
-          }
-          TC_TRACE(i, 15);
-          umma_commit(&v_empty[slot]);
-          umma_commit(&o_done);
-          TC_TRACE(i, 8);
+        if (prog) {
+          t_last = clock64();
+        } else if (*abort_flag || clock64() - t_last > kWaitLimitCycles) {
+          ok = false;
+          break;
         }
       }
-      if (!ok) {
+      if (!ok && !*abort_flag) {
         *abort_flag = 1;
         raise_error(a.err, PA_DEVERR_TIMEOUT);
       }
@@ -522,13 +562,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         ok = mbar_wait(&v_full[slot], uint32_t(j / nsl) & 1u, abort_flag);
         ok = __all_sync(kFullMask, ok);
         if (!ok) break;
-        unsigned char *vs = vring + size_t(slot) * SS;
+        // the last block of the slot ([block][half][B][128 B]); its rows zfrom .. B - 1
+        unsigned char *vs = vring + size_t(slot) * SS + size_t(ntile - 1 - j * bps) * HALVES * B * 128;
         const int zfrom = L - (ntile - 1) * B;
-        const int rbase = (ntile - 1 - j * bps) * B;
         for (int i = threadIdx.x; i < (B - zfrom) * HALVES * 8; i += 128) {
-          const int r = rbase + zfrom + i / (HALVES * 8);
+          const int r = zfrom + i / (HALVES * 8);
           const int hc = i % (HALVES * 8);
-          *reinterpret_cast<uint4 *>(vs + (hc >> 3) * SHALF + r * 128 + (hc & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4 *>(vs + (hc >> 3) * B * 128 + r * 128 + (hc & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_shared();
       }
@@ -547,21 +587,21 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         lsum = softmax_step<T, false>(s0, s1, kTcStepTokens, qscale, m, alpha, ph, pl);
       l = l * alpha + lsum;
       if (threadIdx.x == 0) TC_TRACE(j, 1);
-      // the previous step's PV must be done before O is rescaled
-      if (j > 0) {
-        ok = mbar_wait(&o_done, uint32_t(j - 1) & 1u, abort_flag);
+      // a rescale of O waits for the previous step's PV (PV(j) waits for
+      // this warp's P_j); P_j itself goes to the other buffer, so a step
+      // that keeps its maximum does not wait for the tensor pipe
+      if (j > 0 && __any_sync(kFullMask, alpha != 1.f)) {
+        ok = mbar_wait(&o_done[(j - 1) & 1], uint32_t((j - 1) >> 1) & 1u, abort_flag);
         ok = __all_sync(kFullMask, ok);
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(kFullMask, alpha != 1.f)) {
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t ov[32];
-            tmem_ld32(tl + c0, ov);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tl + c0, ov);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-            tmem_st32(tl + c0, ov);
-          }
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+          tmem_st32(tl + c0, ov);
         }
       }
       if (threadIdx.x == 0) TC_TRACE(j, 2);
@@ -570,12 +610,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full);
+      if (lane == 0) mbar_arrive(&p_full[j & 1]);
       if (threadIdx.x == 0) TC_TRACE(j, 3);
     }
     // ---- the output row: O / l
     if (ok) {
-      ok = mbar_wait(&o_done, uint32_t(nstep - 1) & 1u, abort_flag);
+      ok = mbar_wait(&o_done[(nstep - 1) & 1], uint32_t((nstep - 1) >> 1) & 1u, abort_flag);
       ok = __all_sync(kFullMask, ok);
     }
     if (ok) {
@@ -611,6 +651,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTcCols));
   }
 #ifdef PA_TRACE
+  if (threadIdx.x == 0) {  // every CTA: its SM, start and end (global ns timer), steps
+    unsigned long long g1;
+    unsigned sm;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(g1));
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+    printf("tpc %d %u %llu %llu %d\n", int(blockIdx.x), sm, tc_g0, g1, nstep);
+  }
   if (threadIdx.x == 0 && PA_TRACE_CTA(blockIdx.x)) {
     unsigned smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
