@@ -65,6 +65,7 @@ typedef enum {
 #define PA_DEVERR_CONTEXT 4u   /* context_len < 0 or > max_blocks_per_seq * B */
 #define PA_DEVERR_TIMEOUT 8u   /* an internal pipeline wait gave up (~1.5 s)  */
 #define PA_DEVERR_POSITION 16u /* a token position outside its block table    */
+#define PA_DEVERR_LAYOUT 32u   /* shared memory not 1024-byte aligned (internal; the launch did no work) */
 
 /* Human-readable name of a status code (static string). */
 PA_API const char *pa_status_string(pa_status status);

@@ -7,7 +7,6 @@
 
 #include "pa_decode_shared.cuh"
 #include "pa_prefill.cuh"
-#include "pa_prefill_tc.cuh"
 #include "pa_sched.cuh"
 
 namespace pagedkv {
@@ -23,10 +22,7 @@ pa_status launch_decode_shared(const SharedArgs &a, const CUtensorMap &mk, const
 template <typename T, int D>
 pa_status launch_merge_shared(const MergeArgs &a, cudaStream_t stream);
 template <typename T, int D>
-pa_status launch_prefill(const PrefillArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t ring_bytes,
-                         dim3 grid, cudaStream_t stream);
-template <typename T, int D>
-pa_status launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t smem_bytes,
+pa_status launch_prefill(const PrefillArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t smem_bytes,
                             dim3 grid, cudaStream_t stream);
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -439,8 +435,8 @@ static pa_status prefill_dispatch(const PrefillArgs &pa_args, const void *k_cach
   if (!encode_pool_map(&mk, k_cache, dtype, b.num_blocks, b.Hkv, b.B, D, false) ||
       !encode_pool_map(&mv, v_cache, dtype, b.num_blocks, b.Hkv, b.B, D, D == 128))
     return PA_ERR_CUDA;
-  return D == 64 ? launch_prefill_tc<T, 64>(b, mk, mv, smem, grid, st)
-                 : launch_prefill_tc<T, 128>(b, mk, mv, smem, grid, st);
+  return D == 64 ? launch_prefill<T, 64>(b, mk, mv, smem, grid, st)
+                 : launch_prefill<T, 128>(b, mk, mv, smem, grid, st);
 }
 
 }  // namespace pagedkv
@@ -480,15 +476,9 @@ extern "C" pa_status pa_prefill(void *out, const void *q, const void *k_cache, c
   a.B = block_size;
   a.qscale = scale * kLog2e;
   a.err = debug_err;
-  // each ring slot holds one step (64 tokens) of K or V as [head_dim / 64 halves][64 rows][128 B]
-  a.slot_stride = uint32_t(head_dim / 64) * kTcStepTokens * 128;
-  a.tile_stride = 0;
-  a.nstage = int(kTcRingBytes / 2 / a.slot_stride);
-  if (a.nstage > kTcMaxSlots) a.nstage = kTcMaxSlots;
-  a.pg = 1;
-  a.nops = 1;
-  // dynamic shared memory: the Q tile (head_dim / 64 halves of 128 rows x 128 B), both rings, alignment slack
-  const size_t smem = size_t(head_dim / 64) * kTcRows * 128 + 2 * size_t(a.nstage) * a.slot_stride + 1024;
+  // dynamic shared memory: the Q tile and the K and V rings, no slack (the
+  // kernel checks the 1024-byte alignment its swizzled tiles need)
+  const size_t smem = size_t(tc_smem_bytes(head_dim));
   const dim3 grid{unsigned(tiles * num_seqs * num_kv_heads), 1u, 1u};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return dtype == PA_BF16 ? prefill_dispatch<__nv_bfloat16>(a, k_cache, v_cache, dtype, head_dim, smem, grid, s)

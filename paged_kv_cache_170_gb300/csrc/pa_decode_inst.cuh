@@ -7,7 +7,6 @@
 #include "pa_decode_shared.cuh"
 #include "pa_decode_simt.cuh"
 #include "pa_prefill.cuh"
-#include "pa_prefill_tc.cuh"
 
 namespace pagedkv {
 
@@ -61,33 +60,19 @@ pa_status launch_merge_shared(const MergeArgs &a, cudaStream_t stream) {
 }
 
 template <typename T, int D>
-pa_status launch_prefill(const PrefillArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t ring_bytes,
-                         dim3 grid, cudaStream_t stream) {
-  static int configured[64] = {0};
-  auto kern = prefill_mma_kernel<T, D>;
-  if (!configure_once(kern, kRingBytesPrefill + 1024, configured)) return PA_ERR_CUDA;
-  kern<<<grid, kPrefillThreads, ring_bytes + 1024, stream>>>(a, mk, mv);
-  return launch_status();
-}
-
-template <typename T, int D>
-pa_status launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t smem_bytes,
+pa_status launch_prefill(const PrefillArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t smem_bytes,
                             dim3 grid, cudaStream_t stream) {
   static int configured[64] = {0};
   auto kern = prefill_tc_kernel<T, D>;
-  if (!configure_once(kern, (D / 64) * kTcRows * 128 + kTcRingBytes + 1024, configured)) return PA_ERR_CUDA;
+  if (!configure_once(kern, tc_smem_bytes(D), configured)) return PA_ERR_CUDA;
   kern<<<grid, kTcThreads, smem_bytes, stream>>>(a, mk, mv);
   return launch_status();
 }
 
 #define PAGEDKV_INSTANTIATE_PREFILL(T)                                                                      \
-  template pa_status launch_prefill<T, 64>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &,    \
-                                           size_t, dim3, cudaStream_t);                                      \
-  template pa_status launch_prefill<T, 128>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &,   \
-                                            size_t, dim3, cudaStream_t);                                     \
-  template pa_status launch_prefill_tc<T, 64>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &, \
+  template pa_status launch_prefill<T, 64>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &, \
                                               size_t, dim3, cudaStream_t);                                   \
-  template pa_status launch_prefill_tc<T, 128>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &, \
+  template pa_status launch_prefill<T, 128>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &, \
                                                size_t, dim3, cudaStream_t);
 
 #define PAGEDKV_INSTANTIATE_SHARED(T)                                                                         \

@@ -22,7 +22,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "pagedkv.h")
 
 PA_OK = 0
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
-DEVERR_BITS = {1: "BLOCK_ID", 2: "SLOT", 4: "CONTEXT", 8: "TIMEOUT", 16: "POSITION",
+DEVERR_BITS = {1: "BLOCK_ID", 2: "SLOT", 4: "CONTEXT", 8: "TIMEOUT", 16: "POSITION", 32: "LAYOUT",
                256: "DEBUG_SMEM_RANGE", 512: "DEBUG_TMA_BOX", 1024: "DEBUG_GLOBAL_RANGE", 2048: "DEBUG_BARRIER_PHASE"}
 
 
