@@ -557,7 +557,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           for (int ks = 0; ks < D / 16; ++ks)
             umma_ss(sb, qd0 + uint32_t(((ks >> 2) * QHALF + (ks & 3) * 32) >> 4),
                     kd + uint32_t(((ks >> 2) * SHALF + (ks & 3) * 32) >> 4), id_qk, ks > 0 ? 1u : 0u);
-          TC_TRACE(j, 14);
           umma_commit(&s_full[j & 1]);
           TC_TRACE(j, 5);
           ++nq;
@@ -568,8 +567,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         } else if (*abort_flag || clock64() - t_last > kWaitLimitCycles) {
           ok = false;
           break;
+        } else if (np < nq) {
+          // nothing ready: suspend on the likeliest next event (the softmax
+          // warps' P_i) instead of spinning on the issue slots they share
+          mbar_try_wait(&p_full[np & 1], uint32_t(np >> 1) & 1u);
         } else {
-          __nanosleep(20);  // nothing ready: leave the issue slots to the softmax warps for a moment
+          mbar_try_wait(&k_full[nq % NKS], uint32_t(nq / NKS) & 1u);
         }
       }
       if (!ok && !*abort_flag) {
@@ -599,12 +602,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       ok = __all_sync(kFullMask, ok);
       if (!ok) break;
       if (threadIdx.x == 0) TC_TRACE(j, 0);
-      if (lane == 0 && j + NKS < nstep) {  // QK(j) is done: its K slot takes K(j + NKS)
-        k_issue(j + NKS, kpid_next);
-        ++kissued;
-        kpid_next = k_entry(j + NKS + 1);
-        if (warp == 0) TC_TRACE(j + NKS, 9);
-      }
       tc_fence_after();
       const uint32_t sb = tl + uint32_t(D + kTcStepTokens * (j & 1));
       // a partly filled last block: zero its V rows past the context before the PV MMAs read them
@@ -662,7 +659,20 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[j & 1]);
-      if (threadIdx.x == 0) TC_TRACE(j, 3);
+      if (lane == 0) {  // trace: each softmax warp's release of P_j (warp 0: field 3; warps 1-3: 6, 12, 14)
+        if (warp == 0) TC_TRACE(j, 3);
+        else if (warp == 1) TC_TRACE(j, 6);
+        else if (warp == 2) TC_TRACE(j, 12);
+        else TC_TRACE(j, 14);
+      }
+      // QK(j) is done (S_j was read): its K slot takes K(j + NKS); issued
+      // once P_j is out, off the path from S_j to P_j
+      if (lane == 0 && j + NKS < nstep) {
+        k_issue(j + NKS, kpid_next);
+        ++kissued;
+        kpid_next = k_entry(j + NKS + 1);
+        if (warp == 0) TC_TRACE(j + NKS, 9);
+      }
     }
     // ---- the output row: O / l
     if (ok) {
