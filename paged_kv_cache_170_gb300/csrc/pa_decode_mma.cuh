@@ -177,9 +177,9 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     if (!phase_range(plan, ph, &from, &to)) continue;
     Walk wk;
     if (ph == 0)
-      wk.start(a, plan.sA, plan.rA, from);
+      wk.start(a, plan.sA, plan.rA, from, plan.cA);
     else
-      wk.start(a, plan.s0, plan.r0, from);
+      wk.start(a, plan.s0, plan.r0, from, plan.c0);
     while (wk.w < to) {
       const int n = wk.seg_len(to);
       const bool complete = (wk.b == 0 && n == wk.nb);

@@ -4,8 +4,10 @@
 // logical block b), pc = kv head * HC + head chunk, where a head chunk is GT
 // of the G query heads that share one kv head and a tile is one physical
 // block of K plus the same block of V for that kv head.  The W tiles are cut
-// into N equal contiguous ranges, one per CTA (N = one full wave, 2 CTAs per
-// SM): every CTA streams the same number of bytes whatever the length mix.
+// into N contiguous ranges of equal cost, one per CTA (N = one full wave, 2
+// CTAs per SM), a tile costing 1 and each (s, pc) segment kSegCost more: every
+// CTA streams about the same number of bytes, fewer when its range holds many
+// short segments, whatever the length mix.
 // A CTA finishes any (s, pc) whose tiles all fall in its range and writes
 // `out`; a (s, pc) cut by a range boundary leaves a partial (acc, m, l) for
 // the pair's last contributor to merge: slot 0 for the CTA's first segment,
@@ -133,86 +135,147 @@ __device__ __forceinline__ int blocks_of(const DecodeArgs &a, int s) {
   return (eff_len(a, s) + a.B - 1) / a.B;
 }
 
-// Sequence holding flattened tile x, and x's offset inside that sequence's
-// tiles.  Run by one whole warp; x must be < W.
-__device__ __forceinline__ void locate_tile(const DecodeArgs &a, int PC, int lane, long long x, int *s_out,
-                                            long long *r_out) {
+// The step's tiles are flattened in (s, pc, block) order; a segment is the nb
+// tiles of one (s, pc).  CTAs split the step by cost, not by tiles: a segment
+// costs kSegCost + nb, so that CTAs whose range holds many short segments
+// (their hand-offs and merges, about 2.6k SM cycles each, measured) get fewer
+// tiles.  Tile b of a segment whose cost range starts at Cp sits at cost
+// position Cp + kSegCost + b; CTA c owns the tiles at positions
+// [ceil(c Wc / N), ceil((c + 1) Wc / N)), i.e. the tile at position P
+// belongs to CTA floor(P N / Wc).
+constexpr int kSegCost = 4;
+
+__device__ __forceinline__ long long seg_cost(int nb) { return nb > 0 ? (long long)nb + kSegCost : 0; }
+
+// Where a key falls: by tile index (by_cost false) or by cost position.  Run
+// by one whole warp; the key must be < W (resp. < Wc).  Returns the
+// sequence, the tile offset inside it (for a cost position inside a
+// segment's fixed cost: that segment's first tile), the tiles and the cost
+// before the sequence.
+__device__ __forceinline__ void locate(const DecodeArgs &a, int PC, int lane, long long key, bool by_cost,
+                                       int *s_out, long long *r_out, long long *texcl_out, long long *cexcl_out) {
   int sx = a.S;
-  long long rx = 0, run = 0;
+  long long rx = 0, tx = 0, cx = 0, run = 0, crun = 0;
   for (int base = 0; base < a.S && sx == a.S; base += 32) {
     const int s = base + lane;
-    const long long n = s < a.S ? (long long)blocks_of(a, s) * PC : 0;
-    long long incl = n;
+    const int nb = s < a.S ? blocks_of(a, s) : 0;
+    const long long n = (long long)nb * PC, c = seg_cost(nb) * PC;
+    long long incl = n, cincl = c;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const long long y = __shfl_up_sync(kFullMask, incl, off);
-      if (lane >= off) incl += y;
+      const long long cy = __shfl_up_sync(kFullMask, cincl, off);
+      if (lane >= off) {
+        incl += y;
+        cincl += cy;
+      }
     }
-    const long long excl = run + incl - n;
-    const unsigned m = __ballot_sync(kFullMask, n > 0 && excl <= x && x < run + incl);
+    const long long excl = run + incl - n, cexcl = crun + cincl - c;
+    const bool hit = by_cost ? (c > 0 && cexcl <= key && key < crun + cincl) : (n > 0 && excl <= key && key < run + incl);
+    const unsigned m = __ballot_sync(kFullMask, hit);
     if (m) {
       const int leader = __ffs(m) - 1;
+      long long r = key - excl;
+      if (by_cost && hit) {
+        const long long rc = key - cexcl, sc = seg_cost(nb);
+        const long long o = rc % sc - kSegCost;
+        r = (rc / sc) * nb + (o > 0 ? o : 0);
+      }
       sx = __shfl_sync(kFullMask, s, leader);
-      rx = __shfl_sync(kFullMask, x - excl, leader);
+      rx = __shfl_sync(kFullMask, r, leader);
+      tx = __shfl_sync(kFullMask, excl, leader);
+      cx = __shfl_sync(kFullMask, cexcl, leader);
     }
     run += __shfl_sync(kFullMask, incl, 31);
+    crun += __shfl_sync(kFullMask, cincl, 31);
   }
   *s_out = sx;
   *r_out = rx;
+  *texcl_out = tx;
+  *cexcl_out = cx;
 }
 
-// The CTA's plan.  W = total tiles of the step; the CTA owns [w0, w1).  It
-// processes its range rotated: first [Ls, w1), the segment that ends the
-// range (usually the head of a (s, pc) cut by the range end), then
-// [w0, Ls).  Both ends of a cut (s, pc) are then worked on early by the two
-// CTAs that share it, so their merge overlaps with streaming instead of
-// piling up at the end of the kernel.  (sA, rA) / (s0, r0) locate Ls / w0.
+// The CTA's plan.  W = total tiles of the step, Wc their total cost; the CTA
+// owns the tiles [w0, w1).  It processes its range rotated: first [Ls, w1),
+// the segment that ends the range (usually the head of a (s, pc) cut by the
+// range end), then [w0, Ls).  Both ends of a cut (s, pc) are then worked on
+// early by the two CTAs that share it, so their merge overlaps with
+// streaming instead of piling up at the end of the kernel.  (sA, rA, cA) /
+// (s0, r0, c0) locate Ls / w0: sequence, tile offset inside it, cost position
+// where the segment holding that tile starts.
 struct Plan {
-  long long W, w0, w1, Ls;
+  long long W, Wc, w0, w1, Ls;
   int sA, s0;
-  long long rA, r0;
+  long long rA, r0, cA, c0;
 };
+
+// First tile at cost position >= t.
+__device__ __forceinline__ long long tile_at_cost(const DecodeArgs &a, int PC, int lane, long long t, long long W,
+                                                  long long Wc) {
+  if (t >= Wc) return W;
+  int s;
+  long long r, te, ce;
+  locate(a, PC, lane, t, true, &s, &r, &te, &ce);
+  return te + r;
+}
+
+// CTA that owns the tile at cost position P, and whether CTA c owns any tile.
+__device__ __forceinline__ int cta_at_cost(long long P, long long Wc, int N) { return int(P * N / Wc); }
+__device__ __forceinline__ long long cost_start(int c, long long Wc, int N) { return ((long long)c * Wc + N - 1) / N; }
 
 __device__ __forceinline__ void schedule_scan(const DecodeArgs &a, int PC, int lane, Plan *plan) {
   const int cap = a.max_blocks * a.B;
-  long long run = 0;
+  long long run = 0, crun = 0;
   for (int base = 0; base < a.S; base += 32) {
     const int s = base + lane;
-    long long n = 0;
+    long long n = 0, c = 0;
     if (s < a.S) {
       const int L = a.lens[s];
       if ((L < 0 || L > cap) && blockIdx.x == 0) raise_error(a.err, PA_DEVERR_CONTEXT);
-      n = (long long)blocks_of(a, s) * PC;
+      const int nb = blocks_of(a, s);
+      n = (long long)nb * PC;
+      c = seg_cost(nb) * PC;
     }
-    long long incl = n;
+    long long incl = n, cincl = c;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const long long y = __shfl_up_sync(kFullMask, incl, off);
-      if (lane >= off) incl += y;
+      const long long cy = __shfl_up_sync(kFullMask, cincl, off);
+      if (lane >= off) {
+        incl += y;
+        cincl += cy;
+      }
     }
     run += __shfl_sync(kFullMask, incl, 31);
+    crun += __shfl_sync(kFullMask, cincl, 31);
   }
   Plan p;
   p.W = run;
-  p.w0 = (long long)blockIdx.x * p.W / a.nctas;
-  p.w1 = (long long)(blockIdx.x + 1) * p.W / a.nctas;
+  p.Wc = crun;
+  p.w0 = tile_at_cost(a, PC, lane, cost_start(blockIdx.x, p.Wc, a.nctas), p.W, p.Wc);
+  p.w1 = tile_at_cost(a, PC, lane, cost_start(blockIdx.x + 1, p.Wc, a.nctas), p.W, p.Wc);
   p.Ls = p.w0;
   p.sA = p.s0 = a.S;
-  p.rA = p.r0 = 0;
+  p.rA = p.r0 = p.cA = p.c0 = 0;
   if (p.w0 < p.w1) {
-    locate_tile(a, PC, lane, p.w0, &p.s0, &p.r0);
+    long long te, ce;
+    locate(a, PC, lane, p.w0, false, &p.s0, &p.r0, &te, &ce);
+    const int nb0 = blocks_of(a, p.s0);
+    p.c0 = ce + (p.r0 / nb0) * seg_cost(nb0);
     int sl;
     long long rl;
-    locate_tile(a, PC, lane, p.w1 - 1, &sl, &rl);
+    locate(a, PC, lane, p.w1 - 1, false, &sl, &rl, &te, &ce);
     const int nb = blocks_of(a, sl);
     const long long pair_start = (p.w1 - 1) - rl % nb;
     if (pair_start > p.w0) {
       p.Ls = pair_start;
       p.sA = sl;
       p.rA = rl - rl % nb;
+      p.cA = ce + (rl / nb) * seg_cost(nb);
     } else {
       p.sA = p.s0;
       p.rA = p.r0;
+      p.cA = p.c0;
     }
   }
   *plan = p;
@@ -231,7 +294,8 @@ struct Walk {
   int s, pc, b, nb, L;  // L: tokens of s this call reads (eff_len, read once per sequence)
   int fb;               // first_block(s): table index of this call's block 0
   long long w;
-  __device__ __forceinline__ void start(const DecodeArgs &a, int s0, long long r0, long long w0) {
+  long long cp;         // cost position where the current segment starts
+  __device__ __forceinline__ void start(const DecodeArgs &a, int s0, long long r0, long long w0, long long c0) {
     s = s0;
     L = eff_len(a, s);
     fb = first_block(a, s);
@@ -239,6 +303,7 @@ struct Walk {
     pc = int(r0 / nb);
     b = int(r0 % nb);
     w = w0;
+    cp = c0;
   }
   __device__ __forceinline__ int seg_len(long long w1) const {
     return int((long long)(nb - b) < w1 - w ? (long long)(nb - b) : w1 - w);
@@ -248,6 +313,7 @@ struct Walk {
     b += n;
     if (b == nb) {
       b = 0;
+      cp += seg_cost(nb);
       if (++pc == PC) {
         pc = 0;
         do {
@@ -289,9 +355,9 @@ __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, con
     if (!phase_range(plan, ph, &from, &to)) continue;
     Walk wk;
     if (ph == 0)
-      wk.start(a, plan.sA, plan.rA, from);
+      wk.start(a, plan.sA, plan.rA, from, plan.cA);
     else
-      wk.start(a, plan.s0, plan.r0, from);
+      wk.start(a, plan.s0, plan.r0, from, plan.c0);
     while (wk.w < to && !aborted) {
       const int n = wk.seg_len(to);
       const int kvh = wk.pc / HC;
@@ -363,13 +429,6 @@ __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, con
   }
 }
 
-// CTA whose tile range [c*W/N, (c+1)*W/N) holds tile x.
-__device__ __forceinline__ int cta_of(long long x, long long W, int N) {
-  return int(((x + 1) * N + W - 1) / W - 1);
-}
-
-__device__ __forceinline__ long long range_start(int c, long long W, int N) { return (long long)c * W / N; }
-
 // Consumer warps that take at least one tile of the segment [j, j + n) of a
 // CTA's processing order (tile j goes to warp j % ncw), as a bit mask.
 __device__ __forceinline__ unsigned participants(long long j, int n, int ncw) {
@@ -424,7 +483,7 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
   static_assert(kConsumerWarps == 4 && (8 * C4) % 32 == 0, "lane = 4 * head + warp below");
   const int GT = a.GT;
   const int N = a.nctas;
-  const long long W = plan.W;
+  const long long Wc = plan.Wc;
   const int lh = lane >> 2, lq = lane & 3;  // the (head, warp) whose weight this lane forms
   float *sh_m = sh_w, *sh_l = sh_w + kMergeRecords * 8;
   int *sh_rec = reinterpret_cast<int *>(sh_w + 2 * kMergeRecords * 8);  // contributors of a cut pair
@@ -439,9 +498,9 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
     if (!phase_range(plan, ph, &from, &to)) continue;
     Walk wk;
     if (ph == 0)
-      wk.start(a, plan.sA, plan.rA, from);
+      wk.start(a, plan.sA, plan.rA, from, plan.cA);
     else
-      wk.start(a, plan.s0, plan.r0, from);
+      wk.start(a, plan.s0, plan.r0, from, plan.c0);
     while (wk.w < to) {
       const int n = wk.seg_len(to);
       const bool complete = (wk.b == 0 && n == wk.nb);
@@ -533,21 +592,24 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
         // ---- count this CTA in; the last of the pair's CTAs merges
         __threadfence();  // publish this CTA's record before it is counted
         __syncwarp();
-        const long long P0 = wk.w - wk.b;
+        // the pair's tiles sit at cost positions Cp + kSegCost + b, b < nb
+        const long long Cp = wk.cp;
         const int nb = wk.nb;
-        const int cf = cta_of(P0, W, N);
-        const int cl = cta_of(P0 + nb - 1, W, N);
-        // the pair's contributors: the CTAs of [cf, cl] with a non-empty range
-        // (all of them when W >= N), found 32 at a time; the first
-        // kMergeRecords are listed in sh_rec
+        const int cf = cta_at_cost(Cp + kSegCost, Wc, N);
+        const int cl = cta_at_cost(Cp + kSegCost + nb - 1, Wc, N);
+        // a CTA strictly between cf and cl owns tiles of the pair iff its cost
+        // range holds a position (always when Wc >= N)
+        auto owns = [&](int c) { return c == cf || c == cl || cost_start(c, Wc, N) < cost_start(c + 1, Wc, N); };
+        // the pair's contributors: the CTAs of [cf, cl] that own tiles of it,
+        // found 32 at a time; the first kMergeRecords are listed in sh_rec
         int kc = 0;
-        if (W >= N) {
+        if (Wc >= N) {
           kc = cl - cf + 1;
           for (int r = lane; r < min(kc, kMergeRecords); r += 32) sh_rec[r] = cf + r;
         } else {
           for (int base = cf; base <= cl; base += 32) {
             const int c = base + lane;
-            const bool has = c <= cl && range_start(c, W, N) < range_start(c + 1, W, N);
+            const bool has = c <= cl && owns(c);
             const unsigned mk = __ballot_sync(kFullMask, has);
             const int pos = kc + __popc(mk & ((1u << lane) - 1u));
             if (has && pos < kMergeRecords) sh_rec[pos] = c;
@@ -567,7 +629,8 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
         }
         last = __shfl_sync(kFullMask, last, 0);
         if (last) {
-          const bool cf_last_seg = range_start(cf, W, N) < P0;
+          // the pair is cf's last segment iff cf also owns the tile before it (at Cp - 1)
+          const bool cf_last_seg = Cp > 0 && cta_at_cost(Cp - 1, Wc, N) == cf;
           auto rec_of = [&](int c) {
             const int slot = (c == cf && cf_last_seg) ? 1 : 0;
             return a.partials + ((long long)c * 2 + slot) * 8 * R;
@@ -631,12 +694,12 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
               const int d = idx - h * D;
               float Mr = -CUDART_INF_F;
               for (int c = cf; c <= cl; ++c) {
-                if (W < N && range_start(c, W, N) == range_start(c + 1, W, N)) continue;
+                if (!owns(c)) continue;
                 Mr = fmaxf(Mr, __ldcg(rec_of(c) + h * R + D));
               }
               float num = 0.f, dr = 0.f;
               for (int c = cf; c <= cl; ++c) {
-                if (W < N && range_start(c, W, N) == range_start(c + 1, W, N)) continue;
+                if (!owns(c)) continue;
                 const float *rr = rec_of(c) + h * R;
                 const float fr = fast_exp2(__ldcg(rr + D) - Mr);
                 num += fr * __ldcg(rr + d);
