@@ -37,11 +37,13 @@ NOMINAL_HBM_GBS = 8000.0
 KERNEL_SOURCES = ["paged_kv_cache_170_gb300/csrc/pa_decode_mma.cuh", "paged_kv_cache_170_gb300/csrc/pa_sched.cuh",
                   "paged_kv_cache_170_gb300/csrc/pa_mma_tile.cuh",
                   "paged_kv_cache_170_gb300/csrc/pa_common.cuh"]  # the tensor-core decode kernel
+PREFILL_SOURCES = ["paged_kv_cache_170_gb300/csrc/pa_prefill.cuh", "paged_kv_cache_170_gb300/csrc/pa_sched.cuh",
+                   "paged_kv_cache_170_gb300/csrc/pa_common.cuh"]  # the tcgen05 prefill kernel
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -57,16 +59,16 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per decode-partition launch from the committed ncu summary,
-    if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", f"decode_partition_{workload}.md")
+def profiled_traffic(workload: str, kernel: str = "decode_partition", sources=KERNEL_SOURCES):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path, encoding="utf-8").read()
     m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(sources):
         return None
     return float(m_bytes.group(1))
 
@@ -524,7 +526,8 @@ def run_prefill_gpu(args) -> dict:
         "roofline": {"kernel": "prefill_tc_kernel", "bound": "tensor", "achieved": round(tflops / world, 2),
                      "peak": bf16, "unit": "TFLOP/s", "frac": round(tflops / world / bf16, 4),
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops, cuBLAS bf16 GEMM burst)",
-                     "algorithmic_flops_per_launch": flops, "traffic": None},
+                     "algorithmic_flops_per_launch": flops,
+                     "traffic": profiled_traffic(args.workload, "prefill_tc", PREFILL_SOURCES)},
         "e2e": {"value": round(total_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
