@@ -160,6 +160,31 @@ def test_many_short_sequences(ops):
     assert_attention_close(out, ref, strict=False)
 
 
+@pytest.mark.parametrize("case", ["long_among_short", "one_tile_segments_few_ctas"])
+def test_cost_weighted_split(ops, case):
+    """CTA ranges split tiles + a fixed cost per (sequence, head) segment:
+    long sequences among many one-to-three-block ones (boundaries shift with
+    the short segments; long pairs are cut among several CTAs), and one-tile
+    segments whose total cost is below the CTA count (some CTAs own only
+    fixed-cost positions, i.e. no tile)."""
+    g = torch.Generator().manual_seed(21)
+    if case == "long_among_short":
+        lens = torch.randint(1, 48, (300,), generator=g).tolist()
+        for i in range(0, 300, 37):
+            lens[i] = int(torch.randint(2000, 6000, (1,), generator=g))
+        Hq = Hkv = 16
+    else:
+        lens = [1] * 10 + [0, 3]
+        Hq, Hkv = 8, 4
+    q, kc, vc, tables, lens_t = random_case(lens, Hq, Hkv, 128, 16, torch.float16, seed=22, pad_tables=True)
+    err = ops.new_error_word(DEV)
+    out = ops.pa_decode(q.to(DEV), kc.to(DEV), vc.to(DEV), tables.to(DEV), lens_t.to(DEV), 0.09, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, ops.error_names(int(err.item()))
+    ref = native.decode(q, kc, vc, tables.numpy(), lens_t.numpy(), 0.09)
+    assert_attention_close(out, ref, strict=False)
+
+
 def test_relabelled_blocks_give_bit_identical_output(ops):
     q, kc, vc, tables, lens = random_case([300, 4096, 17, 1000], 32, 8, 128, 16, torch.bfloat16, seed=1)
     args = [t.to(DEV) for t in (q, kc, vc, tables, lens)]
