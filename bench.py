@@ -298,8 +298,11 @@ def run_gpu(args) -> dict:
     inp = workload_inputs(args.workload, args.seed + rank, dev, args.num_seqs, args.placement)
     S, Hq, D = inp.q.shape
     stream = torch.cuda.current_stream(dev)
-    from paged_kv_cache_170_gb300.step import DecodeStep
+    from paged_kv_cache_170_gb300.step import DecodeStep, PackedInputs
 
+    # the per-step inputs live in one device buffer with a pinned host mirror
+    # (one host-to-device copy per step in the end-to-end loop below)
+    packed = PackedInputs(inp)
     runner = DecodeStep(inp, graphs=not args.no_graph, shared=args.shared)
     out, err = runner.out, runner.err
     step = runner.run
@@ -340,17 +343,13 @@ def run_gpu(args) -> dict:
     step_ms_max = max_over_ranks(step_ms, dist)
 
     # -- end to end through the public API: pinned host inputs in, output out
-    host = {n: getattr(inp, n).cpu().pin_memory() for n in
-            ("q", "new_key", "new_value", "new_seq", "new_pos", "block_tables", "context_lens", "copy_pairs")}
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     plan_host = runner.plan.pin_memory() if args.shared else None  # the plan travels with the tables
-    h2d = sum(t.numel() * t.element_size() for t in host.values()) + \
-        (plan_host.numel() * plan_host.element_size() if args.shared else 0)
+    h2d = packed.nbytes + (plan_host.numel() * plan_host.element_size() if args.shared else 0)
     d2h = out_host.numel() * out_host.element_size()
 
     def e2e_step():
-        for n, t in host.items():
-            getattr(inp, n).copy_(t, non_blocking=True)
+        packed.upload()  # q, new K/V and their slots, tables, lengths, copy pairs: one copy
         if args.shared:
             runner.plan_dev.copy_(plan_host, non_blocking=True)
         step()
@@ -455,6 +454,9 @@ def run_prefill_gpu(args) -> dict:
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     inp = workloads.make_prefill_inputs(workloads.WORKLOADS[args.workload], args.seed + rank, device=dev)
+    # the prompt's inputs in one device buffer with a pinned host mirror (one upload per step)
+    from paged_kv_cache_170_gb300.step import PackedInputs
+    packed = PackedInputs(inp, names=("q", "block_tables", "context_lens", "q_start"))
     out = torch.empty_like(inp.q)
     err = ops.new_error_word(dev)
     stream = torch.cuda.current_stream(dev)
@@ -494,9 +496,8 @@ def run_prefill_gpu(args) -> dict:
     peaks = measured_peaks()
     tflops = total_flops / (step_ms * 1e-3) / 1e12
     # end to end: the prompts' queries in from pinned host memory, the outputs back
-    host = {n: getattr(inp, n).cpu().pin_memory() for n in ("q", "block_tables", "context_lens", "q_start")}
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = packed.nbytes
     d2h = out_host.numel() * out_host.element_size()
     e2e_steps = max(1, min(args.steps, 200))
     for _ in range(3):
@@ -505,8 +506,7 @@ def run_prefill_gpu(args) -> dict:
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        for n, t in host.items():
-            getattr(inp, n).copy_(t, non_blocking=True)
+        packed.upload()
         step()
         out_host.copy_(out, non_blocking=True)
     e1.record(stream)
