@@ -298,11 +298,8 @@ def run_gpu(args) -> dict:
     inp = workload_inputs(args.workload, args.seed + rank, dev, args.num_seqs, args.placement)
     S, Hq, D = inp.q.shape
     stream = torch.cuda.current_stream(dev)
-    from paged_kv_cache_170_gb300.step import DecodeStep, PackedInputs
+    from paged_kv_cache_170_gb300.step import DecodeStep, StepPipeline
 
-    # the per-step inputs live in one device buffer with a pinned host mirror
-    # (one host-to-device copy per step in the end-to-end loop below)
-    packed = PackedInputs(inp)
     runner = DecodeStep(inp, graphs=not args.no_graph, shared=args.shared)
     out, err = runner.out, runner.err
     step = runner.run
@@ -342,31 +339,27 @@ def run_gpu(args) -> dict:
     kernel_ms = sum(kernel_times) / args.steps
     step_ms_max = max_over_ranks(step_ms, dist)
 
-    # -- end to end through the public API: pinned host inputs in, output out
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    plan_host = runner.plan.pin_memory() if args.shared else None  # the plan travels with the tables
-    h2d = packed.nbytes + (plan_host.numel() * plan_host.element_size() if args.shared else 0)
-    d2h = out_host.numel() * out_host.element_size()
-
-    def e2e_step():
-        packed.upload()  # q, new K/V and their slots, tables, lengths, copy pairs: one copy
-        if args.shared:
-            runner.plan_dev.copy_(plan_host, non_blocking=True)
-        step()
-        out_host.copy_(out, non_blocking=True)
-
+    # -- end to end through the public API: pinned host inputs in, output out,
+    # every step; two step slots pipelined so that one slot's copies overlap
+    # the other slot's kernels
+    pipe = StepPipeline(inp, graphs=not args.no_graph, shared=args.shared)
+    h2d, d2h = pipe.h2d_bytes, pipe.d2h_bytes
     e2e_steps = max(1, min(args.steps, 2000))
     for _ in range(3):
-        e2e_step()
+        pipe.step()
+    pipe.drain()
     torch.cuda.synchronize(dev)
     barrier(dist)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        e2e_step()
+        pipe.step()
+    pipe.drain()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist)
+    for sl in pipe.slots:
+        assert int(sl.runner.err.item()) == 0, ops.error_names(int(sl.runner.err.item()))
     assert int(err.item()) == 0, ops.error_names(int(err.item()))
 
     kvb = kv_bytes(inp)

@@ -16,6 +16,8 @@ needs a new ``DecodeStep``.
 """
 from __future__ import annotations
 
+import copy
+from types import SimpleNamespace
 from typing import Optional
 
 import torch
@@ -153,3 +155,71 @@ class DecodeStep:
         if ev_decode_end is not None:
             ev_decode_end.record(stream)
         return self.out
+
+
+class StepPipeline:
+    """Decode steps through host memory as a two-deep pipeline.
+
+    Two step slots over the same K/V pools, each with its own packed inputs,
+    output, pinned output mirror and graphs.  Step k runs in slot k mod 2: its
+    inputs are uploaded on an upload stream once the slot's previous step has
+    consumed them; the step runs on the caller's stream once that upload is in
+    and the slot's previous output has been read back; its output is copied to
+    the slot's pinned ``out_host`` on a download stream.  The uploads and
+    downloads of one slot thus overlap the other slot's kernels, while the
+    pools are written in step order on the one compute stream.  The caller
+    writes the next step's inputs into ``slot.packed.host_views`` before
+    ``step()`` and reads ``slot.out_host`` after ``slot.ev_down``.
+    """
+
+    def __init__(self, inp, graphs: bool = True, shared: bool = False):
+        dev = inp.q.device
+        self.device = dev
+        self.slots = []
+        for _ in range(2):
+            si = copy.copy(inp)  # shares the pools; its per-step inputs are packed anew
+            packed = PackedInputs(si)
+            runner = DecodeStep(si, graphs=graphs, shared=shared)
+            out_host = torch.empty(runner.out.shape, dtype=runner.out.dtype).pin_memory()
+            plan_host = runner.plan.pin_memory() if shared else None
+            self.slots.append(SimpleNamespace(inp=si, packed=packed, runner=runner, out_host=out_host,
+                                              plan_host=plan_host, ev_up=torch.cuda.Event(),
+                                              ev_done=torch.cuda.Event(), ev_down=torch.cuda.Event()))
+        self.up_stream = torch.cuda.Stream(dev)
+        self.down_stream = torch.cuda.Stream(dev)
+        comp = torch.cuda.current_stream(dev)
+        for sl in self.slots:  # nothing to wait for before the first two steps
+            sl.ev_done.record(comp)
+            sl.ev_down.record(comp)
+        sl = self.slots[0]
+        self.h2d_bytes = sl.packed.nbytes + (sl.plan_host.numel() * sl.plan_host.element_size() if shared else 0)
+        self.d2h_bytes = sl.out_host.numel() * sl.out_host.element_size()
+        self.k = 0
+
+    def step(self):
+        """Enqueue the next step; returns its slot."""
+        sl = self.slots[self.k % 2]
+        comp = torch.cuda.current_stream(self.device)
+        self.up_stream.wait_event(sl.ev_done)  # the slot's previous step has read its inputs
+        with torch.cuda.stream(self.up_stream):
+            sl.packed.upload()
+            if sl.plan_host is not None:
+                sl.runner.plan_dev.copy_(sl.plan_host, non_blocking=True)
+            sl.ev_up.record(self.up_stream)
+        comp.wait_event(sl.ev_up)
+        comp.wait_event(sl.ev_down)  # the slot's previous output has been read back
+        sl.runner.run()
+        sl.ev_done.record(comp)
+        self.down_stream.wait_event(sl.ev_done)
+        with torch.cuda.stream(self.down_stream):
+            sl.out_host.copy_(sl.runner.out, non_blocking=True)
+            sl.ev_down.record(self.down_stream)
+        self.k += 1
+        return sl
+
+    def drain(self) -> None:
+        """Make the caller's stream wait for every download enqueued so far."""
+        comp = torch.cuda.current_stream(self.device)
+        for sl in self.slots:
+            comp.wait_event(sl.ev_down)
+

@@ -87,3 +87,37 @@ def test_graph_step_with_shared_decode(step_mod, name):
     torch.cuda.synchronize()
     assert int(runner.err.item()) == 0
     assert_attention_close(out, ref, strict=True)
+
+
+def test_step_pipeline_outputs_follow_host_inputs(step_mod):
+    """StepPipeline: new queries written into each step's host buffer (after
+    that slot's previous upload) come back, step by step, as exactly what
+    pa_decode gives on them."""
+    from paged_kv_cache_170_gb300 import ops
+
+    inp_cpu = _case("gqa", seed=5)
+    dev_in = inp_cpu.to("cuda")
+    pipe = step_mod.StepPipeline(dev_in, graphs=True)
+    g = torch.Generator(device="cpu").manual_seed(12)
+    qs, outs, pending = [], [], None
+    for k in range(6):
+        sl = pipe.slots[k % 2]
+        sl.ev_up.synchronize()  # the slot's previous upload has read its host buffer
+        q = torch.randn(dev_in.q.shape, generator=g).to(dev_in.q.dtype)
+        sl.packed.host_views["q"].copy_(q)
+        qs.append(q)
+        pipe.step()
+        if pending is not None:  # the previous step's output, read before its slot is reused
+            pending.ev_down.synchronize()
+            outs.append(pending.out_host.clone())
+        pending = sl
+    pending.ev_down.synchronize()
+    outs.append(pending.out_host.clone())
+    torch.cuda.synchronize()
+    for sl in pipe.slots:
+        assert int(sl.runner.err.item()) == 0
+    for q, out in zip(qs, outs):
+        ref = ops.pa_decode(q.to("cuda"), dev_in.k_cache, dev_in.v_cache, dev_in.block_tables, dev_in.context_lens,
+                            dev_in.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref.cpu())
