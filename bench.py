@@ -42,10 +42,15 @@ PREFILL_SOURCES = ["paged_kv_cache_170_gb300/csrc/pa_prefill.cuh", "paged_kv_cac
 
 
 def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
+    """Hash of the kernel's code with comments and blank space removed: an
+    edit of comments alone leaves a profiled kernel the same kernel."""
     h = hashlib.sha256()
     for rel in sources:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(line.strip() for line in text.splitlines() if line.strip()).encode())
     return h.hexdigest()[:16]
 
 

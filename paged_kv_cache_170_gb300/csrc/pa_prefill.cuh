@@ -11,13 +11,17 @@
 // in steps of 64 tokens (64 / B blocks).  Six warps:
 //   warps 0-3  softmax: thread t of warp w owns row 32w + t = TMEM lane
 //              32w + t; they stage the Q tile, turn each S into P and write
-//              the normalised output;
-//   warp 4     producer: streams each step's K blocks into the K ring as
-//              [half][64 tokens][128 B] (one 2-D box per block and 64-column
-//              half, so a step's keys form one MMA operand) and its V blocks
-//              into the V ring as [block][half][B tokens][128 B] (one box per
-//              block); the lanes hold the block table 32 entries at a time;
+//              the normalised output.  They also load the keys: each warp
+//              its share of a step's K blocks into the K ring as [half][64
+//              tokens][128 B] (one 2-D box per block and 64-column half, so a
+//              step's keys form one MMA operand), K(j + NKS) into the slot of
+//              K(j) once it has seen S_j (QK(j) done);
+//   warp 4     producer: streams each step's V blocks into the V ring as
+//              [block][half][B tokens][128 B] (one box per block); the lanes
+//              hold the block table 32 entries at a time;
 //   warp 5     MMA: allocates TMEM and, from one lane, issues every MMA.
+// With head_dim 128 the rings hold 2 K and 3 V steps: a K slot is free once
+// its QK is done, early in a step, a V slot only once its PV is done.
 // Per step j:
 //   S_j = Q K_j^T  M = 128 rows, N = the step's tokens, K = D in 16-column
 //                  MMAs; A = Q (K-major), B = K (K-major) -> S buffer j % 2;
