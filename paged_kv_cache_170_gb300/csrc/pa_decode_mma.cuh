@@ -44,13 +44,16 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   __shared__ Plan sh_plan;
   __shared__ uint32_t issued[kMaxStages];
   __shared__ int sh_abort;
-  __shared__ __align__(8) uint64_t st_full[kConsumerWarps], st_free[kConsumerWarps];  // hand-off of mrg[w]
+  // hand-off of a warp's state: two buffers (head slots 0-3 and 4-7 of mrg[w])
+  // when GT <= 4, so a warp may run one segment ahead of the merger
+  __shared__ __align__(8) uint64_t st_full[kConsumerWarps][2], st_free[kConsumerWarps][2];
   __shared__ float sh_mw[kMergeScratch];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = a.Hq / a.Hkv;
   const int GT = a.GT;
+  const int nbuf = GT <= 4 ? 2 : 1;  // state buffers per consumer warp in mrg
   const int HC = G / GT;
   const int PC = a.Hkv * HC;
   const int B = a.B;
@@ -72,8 +75,10 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
       issued[i] = 0;
     }
     for (int w = 0; w < kConsumerWarps; ++w) {
-      mbar_init(&st_full[w], 1);
-      mbar_init(&st_free[w], 1);
+      mbar_init(&st_full[w][0], 1);
+      mbar_init(&st_free[w][0], 1);
+      mbar_init(&st_full[w][1], 1);
+      mbar_init(&st_free[w][1], 1);
     }
     sh_abort = 0;
     fence_barrier_init();
@@ -147,7 +152,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
 
   if (warp == kMergerWarp) {
     // -------------------------------------------------------------- merger
-    run_merger<T, D, true>(a, plan, PC, HC, G, lane, &mrg[0][0][0], 8 * state_row(D), st_full, st_free, sh_mw,
+    run_merger<T, D, true>(a, plan, PC, HC, G, lane, &mrg[0][0][0], 8 * state_row(D), nbuf, &st_full[0][0],
+                           &st_free[0][0], sh_mw,
                            abort_flag);
     zero_empty_rows<T>(a, D, lane, 32);
 #ifdef PA_TRACE
@@ -298,26 +304,29 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
             if (h1 < GT) store_lse(a, row0 + h1, m1, l1);
           }
         } else {
-          deposit_state(a, dep, lane, &st_full[warp], &st_free[warp], abort_flag, [&]() {
+          const int b = nbuf == 2 ? int(dep & 1) : 0;
+          const long long use = nbuf == 2 ? (dep >> 1) : dep;
+          deposit_state(a, use, lane, &st_full[warp][b], &st_free[warp][b], abort_flag, [&]() {
+            float(*buf)[state_row(D)] = &mrg[warp][4 * b];
             if (g == 0) {
               if (h0 < GT) {
-                mrg[warp][h0][D] = m0;
-                mrg[warp][h0][D + 1] = l0;
+                buf[h0][D] = m0;
+                buf[h0][D + 1] = l0;
               }
               if (h1 < GT) {
-                mrg[warp][h1][D] = m1;
-                mrg[warp][h1][D + 1] = l1;
+                buf[h1][D] = m1;
+                buf[h1][D + 1] = l1;
               }
             }
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
               if (h0 < GT) {
-                mrg[warp][h0][16 * mt + g] = o[mt][0];
-                mrg[warp][h0][16 * mt + g + 8] = o[mt][2];
+                buf[h0][16 * mt + g] = o[mt][0];
+                buf[h0][16 * mt + g + 8] = o[mt][2];
               }
               if (h1 < GT) {
-                mrg[warp][h1][16 * mt + g] = o[mt][1];
-                mrg[warp][h1][16 * mt + g + 8] = o[mt][3];
+                buf[h1][16 * mt + g] = o[mt][1];
+                buf[h1][16 * mt + g + 8] = o[mt][3];
               }
             }
           });

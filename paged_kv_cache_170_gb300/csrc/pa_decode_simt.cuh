@@ -98,7 +98,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
   __shared__ Plan sh_plan;
   __shared__ uint32_t issued[kMaxStages];
   __shared__ int sh_abort;
-  __shared__ __align__(8) uint64_t st_full[kConsumerWarps], st_free[kConsumerWarps];  // hand-off of mrg[w]
+  // hand-off of mrg[w] (one buffer here; the [2] layout is the merger's)
+  __shared__ __align__(8) uint64_t st_full[kConsumerWarps][2], st_free[kConsumerWarps][2];
   __shared__ float sh_mw[kMergeScratch];
 
   const int warp = threadIdx.x >> 5;
@@ -120,8 +121,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
       issued[i] = 0;
     }
     for (int w = 0; w < kConsumerWarps; ++w) {
-      mbar_init(&st_full[w], 1);
-      mbar_init(&st_free[w], 1);
+      mbar_init(&st_full[w][0], 1);
+      mbar_init(&st_free[w][0], 1);
     }
     sh_abort = 0;
     fence_barrier_init();
@@ -165,7 +166,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
 
   if (warp == kMergerWarp) {
     // -------------------------------------------------------------- merger
-    run_merger<T, D, false>(a, plan, PC, HC, G, lane, &mrg[0][0][0], GT * state_row(D), st_full, st_free, sh_mw,
+    run_merger<T, D, false>(a, plan, PC, HC, G, lane, &mrg[0][0][0], GT * state_row(D), 1, &st_full[0][0],
+                            &st_free[0][0], sh_mw,
                             abort_flag);
     zero_empty_rows<T>(a, D, lane, 32);
 #ifdef PA_TRACE
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
         float lsum = l_mine;
 #pragma unroll
         for (int off = GT; off < 32; off <<= 1) lsum += __shfl_xor_sync(kFullMask, lsum, off);
-        deposit_state(a, dep, lane, &st_full[warp], &st_free[warp], abort_flag, [&]() {
+        deposit_state(a, dep, lane, &st_full[warp][0], &st_free[warp][0], abort_flag, [&]() {
           if (lane < GT) {
             mrg[warp][lane][D] = m_mine;
             mrg[warp][lane][D + 1] = lsum;

@@ -475,8 +475,8 @@ __host__ __device__ constexpr int state_row(int D) { return D + 4; }
 // a merge costs one L2 round trip per record rather than one per element.
 template <typename T, int D, bool kSoloWrites>
 __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan, int PC, int HC, int G, int lane,
-                                           const float *mrg, int warp_stride, uint64_t *st_full, uint64_t *st_free,
-                                           float *sh_w, volatile int *abort_flag) {
+                                           const float *mrg, int warp_stride, int nbuf, uint64_t *st_full,
+                                           uint64_t *st_free, float *sh_w, volatile int *abort_flag) {
   constexpr int R = state_row(D);
   constexpr int C4 = D / 4;            // 16-byte chunks per head row
   constexpr int kIters = 8 * C4 / 32;  // chunks per lane for 8 heads
@@ -518,7 +518,8 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
       }
 #pragma unroll
       for (int q = 0; q < kConsumerWarps; ++q) {
-        if (((pm >> q) & 1u) && !mbar_wait(&st_full[q], taken[q] & 1u, abort_flag)) {
+        const uint32_t bq = nbuf == 2 ? (taken[q] & 1u) : 0u, uq = nbuf == 2 ? (taken[q] >> 1) : taken[q];
+        if (((pm >> q) & 1u) && !mbar_wait(&st_full[2 * q + bq], uq & 1u, abort_flag)) {
           if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
           *abort_flag = 1;
         }
@@ -529,10 +530,15 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
       __syncwarp();
       // ---- combine the participants' states: weights per (warp, head) ...
       const bool mine = lh < GT && ((pm >> lq) & 1u);
+      // the buffer each warp's state of this segment is in (head slots 4 b ..)
+      int boff[kConsumerWarps];
+#pragma unroll
+      for (int q = 0; q < kConsumerWarps; ++q) boff[q] = nbuf == 2 ? int(taken[q] & 1u) * 4 * R : 0;
+      const int boff_l = lq == 0 ? boff[0] : lq == 1 ? boff[1] : lq == 2 ? boff[2] : boff[3];
       float m = -CUDART_INF_F, l = 0.f;
       if (mine) {
-        m = mrg[lq * warp_stride + lh * R + D];
-        l = mrg[lq * warp_stride + lh * R + D + 1];
+        m = mrg[lq * warp_stride + boff_l + lh * R + D];
+        l = mrg[lq * warp_stride + boff_l + lh * R + D + 1];
       }
       float M = fmaxf(m, __shfl_xor_sync(kFullMask, m, 1));
       M = fmaxf(M, __shfl_xor_sync(kFullMask, M, 2));
@@ -565,7 +571,7 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
 #pragma unroll
           for (int q = 0; q < kConsumerWarps; ++q) {
             if (!((pm >> q) & 1u)) continue;  // a buffer that got no state this segment
-            const float4 v = *reinterpret_cast<const float4 *>(mrg + q * warp_stride + h * R + d);
+            const float4 v = *reinterpret_cast<const float4 *>(mrg + q * warp_stride + boff[q] + h * R + d);
             acc.x += w[q] * v.x;
             acc.y += w[q] * v.y;
             acc.z += w[q] * v.z;
@@ -584,7 +590,7 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
 #pragma unroll
       for (int q = 0; q < kConsumerWarps; ++q) {
         if ((pm >> q) & 1u) {
-          if (lane == 0) mbar_arrive(&st_free[q]);  // warp q may overwrite its buffer now
+          if (lane == 0) mbar_arrive(&st_free[2 * q + (nbuf == 2 ? (taken[q] & 1u) : 0u)]);  // warp q may reuse it now
           ++taken[q];
         }
       }
@@ -728,9 +734,10 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
 // is exact), then let `write` store the state into the warp's buffer and
 // announce it (its st_full).
 template <class Write>
-__device__ __forceinline__ void deposit_state(const DecodeArgs &a, long long dep, int lane, uint64_t *st_full,
+__device__ __forceinline__ void deposit_state(const DecodeArgs &a, long long use, int lane, uint64_t *st_full,
                                               uint64_t *st_free, volatile int *abort_flag, Write write) {
-  if (dep > 0 && !mbar_wait(st_free, uint32_t(dep - 1) & 1u, abort_flag)) {
+  // `use`: how many states this warp has put in this buffer before
+  if (use > 0 && !mbar_wait(st_free, uint32_t(use - 1) & 1u, abort_flag)) {
     if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
     *abort_flag = 1;
   }
