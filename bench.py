@@ -11,7 +11,7 @@ copied from pinned host memory and the output copied back inside the timed
 region.  The step reads 1 GiB of K/V on the default workload, far more than
 the 129 MB L2, so no L2 flush is needed between steps; a workload whose
 distinct K/V is under 4x the L2 (the shared-prefix one) gets a 512 MiB buffer
-written between steps, outside the timed intervals.
+written and read back between steps, outside the timed intervals.
 """
 from __future__ import annotations
 
@@ -126,6 +126,16 @@ L2_BYTES = 129 * 1024 * 1024
 FLUSH_BYTES = 512 * 1024 * 1024  # written between timed steps when a step's distinct K/V would sit in L2
 
 
+def flush_l2(buf: torch.Tensor, k: int) -> None:
+    """Evict the step's K/V from L2 between timed steps: write ``buf`` (4x
+    the L2), then read it back.  The read leaves L2 holding clean lines of
+    the flush buffer; after the write alone up to 129 MB of dirty flush lines
+    stay in L2, and the next decode would pay for writing them back to DRAM
+    (traffic of the harness, not of the kernel)."""
+    buf.fill_(k & 255)
+    torch.amax(buf.view(torch.int32))
+
+
 def needs_l2_flush(inp, mode: str = "auto") -> bool:
     """auto: flush when a step's distinct K/V is under 4x the L2; "flush" /
     "warm" force it on / off ("warm" numbers are for analysis, not the line's
@@ -133,6 +143,16 @@ def needs_l2_flush(inp, mode: str = "auto") -> bool:
     if mode != "auto":
         return mode == "flush"
     return unique_kv_bytes(inp) < 4 * L2_BYTES
+
+
+def decode_kernel_name(inp, shared: bool) -> str:
+    """The kernel(s) the decode launch runs: the tensor-core kernel takes
+    fp16 / bf16 caches whose block size is a multiple of 16."""
+    if shared:
+        return "decode_shared_mma_kernel + decode_partition_mma_kernel + merge_shared_kernel"
+    if inp.k_cache.dtype != torch.float32 and inp.k_cache.shape[2] % 16 == 0:
+        return "decode_partition_mma_kernel"
+    return "decode_partition_kernel"
 
 
 def algorithmic_bytes(inp) -> int:
@@ -163,8 +183,8 @@ def workload_config(name: str, inp, l2_mode: str = "auto") -> dict:
         l2 = "warm: no flush between steps (forced for analysis; the step's distinct K/V is %.2f GB)" % (
             unique_kv_bytes(inp) / 1e9)
     elif needs_l2_flush(inp, l2_mode):
-        l2 = ("flush: %d MiB written between timed steps (outside the timed intervals); the step's distinct "
-              "K/V is %.2f GB" % (FLUSH_BYTES >> 20, unique_kv_bytes(inp) / 1e9))
+        l2 = ("flush: %d MiB written then read between timed steps (outside the timed intervals); the step's "
+              "distinct K/V is %.2f GB" % (FLUSH_BYTES >> 20, unique_kv_bytes(inp) / 1e9))
     else:
         l2 = "no flush: each step reads %.2f GB of distinct K/V, larger than the 129 MB L2" % (
             unique_kv_bytes(inp) / 1e9)
@@ -305,7 +325,7 @@ def run_gpu(args) -> dict:
     stream = torch.cuda.current_stream(dev)
     from paged_kv_cache_170_gb300.step import DecodeStep, StepPipeline
 
-    runner = DecodeStep(inp, graphs=not args.no_graph, shared=args.shared)
+    runner = DecodeStep(inp, graphs=not args.no_graph, shared=args.shared, fused=not args.unfused)
     out, err = runner.out, runner.err
     step = runner.run
     launches_per_step = runner.launches_per_step
@@ -328,7 +348,7 @@ def run_gpu(args) -> dict:
         start.record(stream)
         for k in range(args.steps):
             if flush:
-                flush_buf.fill_(k & 255)
+                flush_l2(flush_buf, k)
                 sev[k][0].record(stream)
             step(*kev[k])
             if flush:
@@ -347,7 +367,7 @@ def run_gpu(args) -> dict:
     # -- end to end through the public API: pinned host inputs in, output out,
     # every step; two step slots pipelined so that one slot's copies overlap
     # the other slot's kernels
-    pipe = StepPipeline(inp, graphs=not args.no_graph, shared=args.shared)
+    pipe = StepPipeline(inp, graphs=not args.no_graph, shared=args.shared, fused=not args.unfused)
     h2d, d2h = pipe.h2d_bytes, pipe.d2h_bytes
     e2e_steps = max(1, min(args.steps, 2000))
     for _ in range(3):
@@ -388,8 +408,12 @@ def run_gpu(args) -> dict:
         "dtype": {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}[inp.q.dtype],
         "data": "synthetic: seeded N(0,1) q/K/V, random physical placement",
         "config": dict(workload_config(args.workload, inp, args.l2),
-                       step_launch="eager, kernel by kernel" if args.no_graph
-                       else "CUDA graphs: pre (copies, slots, write) then decode",
+                       step_launch="%s: %s%s (%d launch%s per step)" % (
+                           "eager, kernel by kernel" if args.no_graph else "CUDA graphs",
+                           "copy-on-write copies, then " if inp.copy_pairs.numel() else "",
+                           "slot lookup + K/V write + decode in one pa_write_decode call" if runner.fused
+                           else "slot lookup, K/V write, then decode", runner.launches_per_step,
+                           "" if runner.launches_per_step == 1 else "es"),
                        decode="pa_decode_shared (plan: %d groups, %d pieces)" % (
                            runner.plan_info["num_groups"], runner.plan_info["num_pieces"]) if args.shared
                        else "pa_decode"),
@@ -398,7 +422,7 @@ def run_gpu(args) -> dict:
         "pct_of_measured_hbm": round(100 * value / world / peaks["hbm_gbs"], 2),
         "decode_kernel_us": round(kernel_ms * 1e3, 2),
         "decode_kernel_us_median": round(statistics.median(kernel_times) * 1e3, 2),
-        "roofline": {"kernel": "decode_partition_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+        "roofline": {"kernel": decode_kernel_name(inp, args.shared), "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
                      "frac_of_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4),
@@ -474,7 +498,8 @@ def run_prefill_gpu(args) -> dict:
     _, Hkv, _, D = inp.k_cache.shape
     distinct = int(inp.context_lens.to(torch.int64).sum()) * Hkv * D * inp.k_cache.element_size() * 2
     flush = args.l2 == "flush" or (args.l2 == "auto" and distinct < 4 * L2_BYTES)
-    l2 = ("flush: %d MiB written between timed steps (outside the timed intervals); the step's K/V is %.3f GB"
+    l2 = ("flush: %d MiB written then read between timed steps (outside the timed intervals); the step's K/V "
+          "is %.3f GB"
           % (FLUSH_BYTES >> 20, distinct / 1e9)) if flush else "no flush (%s)" % args.l2
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -483,7 +508,7 @@ def run_prefill_gpu(args) -> dict:
     with ClockSampler(local) as clocks:
         for k in range(args.steps):
             if flush:
-                flush_buf.fill_(k & 255)
+                flush_l2(flush_buf, k)
             step(*kev[k])
         torch.cuda.synchronize(dev)
     barrier(dist)
@@ -658,6 +683,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-seqs", type=int, default=None, help="fewer sequences (profiling captures only)")
     ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one")
+    ap.add_argument("--unfused", action="store_true",
+                    help="slot lookup and K/V write as their own kernels before the decode (default: one "
+                         "pa_write_decode call when every sequence appends one token)")
     ap.add_argument("--l2", choices=["auto", "flush", "warm"], default="auto",
                     help="L2 between timed steps: auto (flush when the distinct K/V is under 4x L2), "
                          "flush, or warm (no flush; analysis only)")

@@ -155,6 +155,37 @@ PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache,
                     pa_dtype dtype, void *workspace, size_t workspace_bytes,
                     int *debug_err, void *stream);
 
+/*
+ * a1 + a2 + a4 + a5 in one call: the decode step's K/V write and its decode
+ * attention.  Each sequence s with context_lens[s] >= 1 appends one token at
+ * position t = context_lens[s] - 1 (the token the step decodes; every new
+ * token attends to the whole history including itself, aiqz.cc, section
+ * "显存痛点"), so the result is exactly that of
+ *     pa_write_kv(new_key[s], new_value[s]) into slot
+ *         block_tables[s][t / B] * B + t % B          (for every s), then
+ *     pa_decode(...)                                  (same arguments).
+ * new_key, new_value: device [num_seqs][num_kv_heads][head_dim], dtype of
+ * the pools, 16-byte aligned.  k_cache / v_cache are written (the new rows
+ * only).  Sequences with context_len 0 write nothing.  Block ids and
+ * positions are range-checked as in pa_slot_mapping (PA_DEVERR bits).
+ *
+ * For fp16 / bf16 pools with block_size % 16 == 0 this is ONE kernel launch:
+ * the decode kernel's warp that takes the block holding position t puts the
+ * token's rows into its staged copy of the block and stores them to the pool
+ * (the lookup and write happen inside the decode).  Other shapes take two
+ * launches (the write, then the decode).  The pool rows at the new positions
+ * are overwritten while the kernel reads the blocks that hold them; their
+ * previous contents are never used.  Workspace rules as for pa_decode.
+ */
+PA_API pa_status pa_write_decode(void *out, const void *q, const void *new_key,
+                                 const void *new_value, void *k_cache, void *v_cache,
+                                 const int32_t *block_tables, int max_blocks_per_seq,
+                                 const int32_t *context_lens, int num_seqs, int num_heads,
+                                 int num_kv_heads, int head_dim, int block_size,
+                                 int64_t num_blocks, float scale, pa_dtype dtype,
+                                 void *workspace, size_t workspace_bytes, int *debug_err,
+                                 void *stream);
+
 /* Number of CTAs the decode kernel launches on the current device. */
 PA_API int pa_decode_grid_size(void);
 

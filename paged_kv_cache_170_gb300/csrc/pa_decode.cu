@@ -25,6 +25,10 @@ template <typename T, int D>
 pa_status launch_prefill(const PrefillArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t smem_bytes,
                             dim3 grid, cudaStream_t stream);
 
+pa_status launch_append_last(const void *key, const void *value, void *k_cache, void *v_cache,
+                             const int32_t *tables, int max_blocks, const int32_t *lens, int S, int Hkv, int D,
+                             int B, int64_t num_blocks, pa_dtype dtype, int *err, cudaStream_t stream);
+
 constexpr float kLog2e = 1.4426950408889634f;
 
 static int decode_grid() { return device_sm_count() * kCtasPerSm; }
@@ -209,12 +213,15 @@ extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_
 namespace pagedkv {
 
 // pa_decode, optionally over each sequence's blocks from start_block[s] on,
-// with fp32 output rows (out_f32) and their log2-sum-exp (lse).
+// with fp32 output rows (out_f32) and their log2-sum-exp (lse), or (new_key
+// non-null, pa_write_decode) with each sequence's token at position
+// context_lens[s] - 1 written first.
 static pa_status decode_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
                              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
                              int64_t num_blocks, float scale, pa_dtype dtype, void *workspace, size_t workspace_bytes,
-                             int *debug_err, void *stream, const int32_t *start_block, float *out_f32, float *lse) {
+                             int *debug_err, void *stream, const int32_t *start_block, float *out_f32, float *lse,
+                             const void *new_key = nullptr, const void *new_value = nullptr) {
   DecodeShape sh;
   pa_status st = check_decode_args(max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                                    num_blocks, dtype, &sh);
@@ -226,6 +233,9 @@ static pa_status decode_impl(void *out, const void *q, const void *k_cache, cons
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace))
     return PA_ERR_INVALID_ARG;
   if (workspace_bytes < workspace_bytes_for(num_seqs, num_heads, head_dim, sh.nctas)) return PA_ERR_WORKSPACE;
+  if (new_key != nullptr && (new_value == nullptr || !aligned16(new_key) || !aligned16(new_value) ||
+                             start_block != nullptr))
+    return PA_ERR_INVALID_ARG;
 
   DecodeArgs a;
   a.out = out;
@@ -257,7 +267,25 @@ static pa_status decode_impl(void *out, const void *q, const void *k_cache, cons
   a.start_block = start_block;
   a.out_f32 = out_f32;
   a.lse = lse;
+  a.new_k = nullptr;
+  a.new_v = nullptr;
+  a.k_store = nullptr;
+  a.v_store = nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (new_key != nullptr) {
+    if (sh.mma) {  // the decode kernel writes the tokens itself
+      a.new_k = new_key;
+      a.new_v = new_value;
+      a.k_store = static_cast<char *>(const_cast<void *>(k_cache));
+      a.v_store = static_cast<char *>(const_cast<void *>(v_cache));
+    } else {  // CUDA-core kernel: one write launch before the decode
+      const pa_status w = launch_append_last(new_key, new_value, const_cast<void *>(k_cache),
+                                             const_cast<void *>(v_cache), block_tables, max_blocks_per_seq,
+                                             context_lens, num_seqs, num_kv_heads, head_dim, block_size, num_blocks,
+                                             dtype, debug_err, s);
+      if (w != PA_OK) return w;
+    }
+  }
   if (sh.mma) {
     return dtype == PA_BF16
                ? dispatch_mma<__nv_bfloat16>(a, k_cache, v_cache, dtype, head_dim, sh.ring_bytes, s)
@@ -281,6 +309,18 @@ extern "C" pa_status pa_decode(void *out, const void *q, const void *k_cache, co
   return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_heads,
                      num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace, workspace_bytes,
                      debug_err, stream, nullptr, nullptr, nullptr);
+}
+
+extern "C" pa_status pa_write_decode(void *out, const void *q, const void *new_key, const void *new_value,
+                                     void *k_cache, void *v_cache, const int32_t *block_tables,
+                                     int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                     int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                     int64_t num_blocks, float scale, pa_dtype dtype, void *workspace,
+                                     size_t workspace_bytes, int *debug_err, void *stream) {
+  if (num_seqs > 0 && (new_key == nullptr || new_value == nullptr)) return PA_ERR_INVALID_ARG;
+  return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_heads,
+                     num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace, workspace_bytes,
+                     debug_err, stream, nullptr, nullptr, nullptr, new_key, new_value);
 }
 
 // ------------------------------------------------------ shared-block decode

@@ -1,7 +1,8 @@
-// pa_kv.cu -- slot lookup, KV write and copy-on-write block copy kernels, plus
-// the library's shared host helpers.
+// pa_kv.cu -- slot lookup, KV write and copy-on-write block copy kernels, the
+// write of pa_write_decode's CUDA-core path, plus the library's shared host
+// helpers.
 //
-// All three kernels are plain bandwidth kernels: 16-byte vector loads and
+// All four kernels are plain bandwidth kernels: 16-byte vector loads and
 // stores, one thread per 16-byte chunk, grid-stride loops over a grid sized
 // in multiples of the SM count.
 
@@ -110,6 +111,56 @@ __global__ void copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restric
       vd[c] = b;
     }
   }
+}
+
+// ------------------------------------------------- a2 for pa_write_decode
+// The step's token of each sequence, at position lens[s] - 1, into its slot
+// (the lookup of a1 and the write of a2 in one pass): pa_write_decode's write
+// when the decode runs on the CUDA-core kernel.  key / value: [S][Hkv][D];
+// one thread per 16-byte chunk.
+__global__ void append_last_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                                   uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                                   const int32_t *__restrict__ tables, int max_blocks,
+                                   const int32_t *__restrict__ lens, int S, int Hkv, int row_chunks, int B,
+                                   int64_t num_blocks, int *err) {
+  const int64_t per_seq = int64_t(Hkv) * row_chunks;
+  const int64_t total = int64_t(S) * per_seq;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t s = i / per_seq;
+    const int64_t rem = i - s * per_seq;  // head * row_chunks + chunk
+    const int L = lens[s];
+    if (L <= 0) continue;
+    const int t = L - 1;
+    const int logical = t / B;
+    if (logical >= max_blocks) {
+      if (rem == 0) raise_error(err, PA_DEVERR_POSITION);
+      continue;
+    }
+    const int32_t pid = tables[s * max_blocks + logical];
+    if (pid < 0 || pid >= num_blocks) {
+      if (rem == 0) raise_error(err, PA_DEVERR_BLOCK_ID);
+      continue;
+    }
+    const int64_t head = rem / row_chunks;
+    const int64_t chunk = rem - head * row_chunks;
+    const int64_t dst = ((int64_t(pid) * Hkv + head) * B + (t - logical * B)) * row_chunks + chunk;
+    k_cache[dst] = key[i];
+    v_cache[dst] = value[i];
+  }
+}
+
+pa_status launch_append_last(const void *key, const void *value, void *k_cache, void *v_cache,
+                             const int32_t *tables, int max_blocks, const int32_t *lens, int S, int Hkv, int D,
+                             int B, int64_t num_blocks, pa_dtype dtype, int *err, cudaStream_t stream) {
+  const int row_chunks = static_cast<int>(D * dtype_bytes(dtype) / 16);
+  const int64_t work = int64_t(S) * Hkv * row_chunks;
+  if (work == 0) return PA_OK;
+  const int threads = 256;
+  append_last_kernel<<<stride_grid(work, threads), threads, 0, stream>>>(
+      static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), static_cast<uint4 *>(k_cache),
+      static_cast<uint4 *>(v_cache), tables, max_blocks, lens, S, Hkv, row_chunks, B, num_blocks, err);
+  return launch_status();
 }
 
 }  // namespace pagedkv

@@ -67,6 +67,15 @@ struct DecodeArgs {
   const int32_t *start_block;  // [S] first block of each sequence to read (earlier ones are shared, done elsewhere)
   float *out_f32;              // [S][Hq][D] fp32 output rows, written instead of `out`
   float *lse;                  // [S][Hq] log2-sum-exp of each row, m + log2(l); -inf for a row with no tokens
+  // Set only by pa_write_decode on the tensor-core kernel (null otherwise):
+  // the step's token of each sequence, at position lens[s] - 1, not yet in
+  // the pools.  The warp that takes the tile holding it puts the token's rows
+  // into its staged copy of the tile, and the warp of head chunk 0 also stores
+  // them to the pools.
+  const void *new_k;  // [S][Hkv][D]
+  const void *new_v;  // [S][Hkv][D]
+  char *k_store;      // the K pool, writable
+  char *v_store;      // the V pool, writable
 };
 
 // Output row `row` (= s * Hq + hq), dims d .. d+3, to `out` (or `out_f32`).

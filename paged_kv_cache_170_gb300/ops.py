@@ -41,6 +41,8 @@ def _load() -> ctypes.CDLL:
         "pa_copy_blocks": [vp, vp, vp, i64, i32, i32, i32, i64, i32, vp, vp],
         "pa_decode": [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, sz, vp, vp],
         "pa_decode_noalloc": [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp],
+        "pa_write_decode": [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, sz,
+                            vp, vp],
         "pa_share_plan": [vp, i32, vp, i32, i32, i32, i32, i32, vp, sz, ctypes.POINTER(sz)],
         "pa_decode_shared": [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp, vp, sz,
                              vp, vp],
@@ -210,6 +212,31 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, blo
                          NB, float(scale), _DTYPES[q.dtype], ws.data_ptr(), ws.numel(), _ptr(err),
                          _stream(q.device)), "pa_decode")
     return out
+
+
+def pa_write_decode(q: torch.Tensor, new_key: torch.Tensor, new_value: torch.Tensor, k_cache: torch.Tensor,
+                    v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                    out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                    err: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Each sequence's new token (new_key / new_value [S][Hkv][D], at position
+    context_lens[s] - 1) written into its slot, then decode attention; one
+    launch on the tensor-core path."""
+    NB, Hkv, B, D, S, Hq, out, ws = _decode_args(q, k_cache, v_cache, block_tables, context_lens, out, workspace)
+    for name, t in (("new_key", new_key), ("new_value", new_value)):
+        _need(t, name, k_cache.dtype, 3, k_cache.device)
+        if tuple(t.shape) != (S, Hkv, D):
+            raise ValueError(f"{name} must be [num_seqs][num_kv_heads][head_dim]")
+    _check(lib.pa_write_decode(out.data_ptr(), q.data_ptr(), new_key.data_ptr(), new_value.data_ptr(),
+                               k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
+                               context_lens.data_ptr(), S, Hq, Hkv, D, B, NB, float(scale), _DTYPES[q.dtype],
+                               ws.data_ptr(), ws.numel(), _ptr(err), _stream(q.device)), "pa_write_decode")
+    return out
+
+
+def write_decode_is_one_launch(k_cache: torch.Tensor) -> bool:
+    """pa_write_decode runs as one kernel for fp16 / bf16 pools whose block
+    size is a multiple of 16 (the tensor-core decode); else as two."""
+    return k_cache.dtype in (torch.float16, torch.bfloat16) and k_cache.shape[2] % 16 == 0
 
 
 def pa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,

@@ -2,7 +2,8 @@
 
 One step is: copy-on-write block copies (when the step has any), slot lookup of
 the new tokens, their K/V write, then split-context decode attention over every
-sequence.  Launched one by one from Python, each call pays host-side argument
+sequence (the last three in one kernel when each sequence appends one token,
+see ``DecodeStep``).  Launched one by one from Python, each call pays host-side argument
 checks and a launch, and the GPU idles whenever the host falls behind; small
 batches are then launch-bound.  Here the step's kernels are captured into two
 CUDA graphs on first use: ``pre`` (copies, slots, write) and ``decode``.  A
@@ -70,6 +71,18 @@ class PackedInputs:
         self.device.copy_(self.host, non_blocking=True)
 
 
+def one_token_per_sequence(inp) -> bool:
+    """True when the step appends one token to every sequence, at position
+    context_lens - 1 (what pa_write_decode writes)."""
+    S = inp.q.shape[0]
+    if inp.new_seq.numel() != S or S == 0:
+        return False
+    seq = inp.new_seq.cpu().to(torch.int64)
+    pos = inp.new_pos.cpu().to(torch.int64)
+    lens = inp.context_lens.cpu().to(torch.int64)
+    return bool(torch.equal(seq, torch.arange(S)) and torch.equal(pos, lens - 1) and (lens >= 1).all())
+
+
 class DecodeStep:
     """The decode step of one set of resident inputs, as CUDA graphs.
 
@@ -79,15 +92,23 @@ class DecodeStep:
     one instead (same results, for comparison).  ``shared=True`` decodes with
     pa_decode_shared, reading each block that several sequences share once
     per group (the plan is built here from the tables).
+
+    When every sequence appends exactly one token, at its last context
+    position (``new_seq`` = 0 .. S-1, ``new_pos`` = context_lens - 1: a plain
+    decode step), the write and the decode run as one call, pa_write_decode
+    (one kernel on the tensor-core path); ``fused=False`` keeps the separate
+    slot lookup and write.  The step's shape is checked here, at
+    construction: later steps must keep it.
     """
 
-    def __init__(self, inp, graphs: bool = True, shared: bool = False):
+    def __init__(self, inp, graphs: bool = True, shared: bool = False, fused: bool = True):
         self.inp = inp
         dev = inp.q.device
         S, Hq, D = inp.q.shape
         Hkv, B = inp.k_cache.shape[1], inp.k_cache.shape[2]
         self.out = torch.empty_like(inp.q)
         self.shared = shared
+        self.fused = fused and not shared and one_token_per_sequence(inp)
         decode_launches = 1
         if shared:
             # the plan follows the tables as the decode sees them; this step
@@ -102,9 +123,13 @@ class DecodeStep:
             self.workspace = ops.new_workspace(S, Hq, Hkv, D, dev)
         self.slots = torch.empty(inp.new_seq.numel(), dtype=torch.int64, device=dev)
         self.err = ops.new_error_word(dev)
-        self.launches_per_step = (1 if inp.copy_pairs.numel() else 0) + (2 if inp.new_seq.numel() else 0) + \
-            decode_launches
+        writes = 0 if self.fused else (2 if inp.new_seq.numel() else 0)
+        if self.fused and not ops.write_decode_is_one_launch(inp.k_cache):
+            decode_launches = 2
+        self.launches_per_step = (1 if inp.copy_pairs.numel() else 0) + writes + decode_launches
         self.graphs = graphs
+        # kernels before the decode: copy-on-write copies; slot lookup and write unless fused
+        self.has_pre = bool(inp.copy_pairs.numel()) or (bool(inp.new_seq.numel()) and not self.fused)
         self._pre: Optional[torch.cuda.CUDAGraph] = None
         self._dec: Optional[torch.cuda.CUDAGraph] = None
         if graphs:
@@ -113,9 +138,10 @@ class DecodeStep:
             self._run_pre()
             self._run_decode()
             torch.cuda.synchronize(dev)
-            self._pre = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(self._pre):
-                self._run_pre()
+            if self.has_pre:
+                self._pre = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(self._pre):
+                    self._run_pre()
             self._dec = torch.cuda.CUDAGraph()
             with torch.cuda.graph(self._dec):
                 self._run_decode()
@@ -124,7 +150,7 @@ class DecodeStep:
         inp = self.inp
         if inp.copy_pairs.numel():
             ops.pa_copy_blocks(inp.k_cache, inp.v_cache, inp.copy_pairs, self.err)
-        if inp.new_seq.numel():
+        if inp.new_seq.numel() and not self.fused:
             ops.pa_slot_mapping(inp.block_tables, inp.new_seq, inp.new_pos, inp.k_cache.shape[2],
                                 inp.k_cache.shape[0], self.slots, self.err)
             ops.pa_write_kv(inp.new_key, inp.new_value, inp.k_cache, inp.v_cache, self.slots, self.err)
@@ -134,6 +160,9 @@ class DecodeStep:
         if self.shared:
             ops.pa_decode_shared(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale,
                                  self.plan, self.plan_dev, self.out, self.workspace, self.err)
+        elif self.fused:
+            ops.pa_write_decode(inp.q, inp.new_key, inp.new_value, inp.k_cache, inp.v_cache, inp.block_tables,
+                                inp.context_lens, inp.scale, self.out, self.workspace, self.err)
         else:
             ops.pa_decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale, self.out,
                           self.workspace, self.err)
@@ -144,7 +173,7 @@ class DecodeStep:
         stream = torch.cuda.current_stream(self.inp.q.device)
         if self._pre is not None:
             self._pre.replay()
-        else:
+        elif self.has_pre:
             self._run_pre()
         if ev_decode_start is not None:
             ev_decode_start.record(stream)
@@ -172,14 +201,14 @@ class StepPipeline:
     ``step()`` and reads ``slot.out_host`` after ``slot.ev_down``.
     """
 
-    def __init__(self, inp, graphs: bool = True, shared: bool = False):
+    def __init__(self, inp, graphs: bool = True, shared: bool = False, fused: bool = True):
         dev = inp.q.device
         self.device = dev
         self.slots = []
         for _ in range(2):
             si = copy.copy(inp)  # shares the pools; its per-step inputs are packed anew
             packed = PackedInputs(si)
-            runner = DecodeStep(si, graphs=graphs, shared=shared)
+            runner = DecodeStep(si, graphs=graphs, shared=shared, fused=fused)
             out_host = torch.empty(runner.out.shape, dtype=runner.out.dtype).pin_memory()
             plan_host = runner.plan.pin_memory() if shared else None
             self.slots.append(SimpleNamespace(inp=si, packed=packed, runner=runner, out_host=out_host,
