@@ -145,23 +145,29 @@ def needs_l2_flush(inp, mode: str = "auto") -> bool:
     return unique_kv_bytes(inp) < 4 * L2_BYTES
 
 
-def decode_kernel_name(inp, shared: bool) -> str:
-    """The kernel(s) the decode launch runs: the tensor-core kernel takes
-    fp16 / bf16 caches whose block size is a multiple of 16."""
+def decode_kernel_name(inp, shared: bool, fused: bool = False) -> str:
+    """The kernel(s) the timed decode call runs: the tensor-core kernel takes
+    fp16 / bf16 caches whose block size is a multiple of 16; pa_write_decode
+    runs the write kernel first."""
     if shared:
         return "decode_shared_mma_kernel + decode_partition_mma_kernel + merge_shared_kernel"
-    if inp.k_cache.dtype != torch.float32 and inp.k_cache.shape[2] % 16 == 0:
-        return "decode_partition_mma_kernel"
-    return "decode_partition_kernel"
+    name = "decode_partition_mma_kernel" if inp.k_cache.dtype != torch.float32 and inp.k_cache.shape[2] % 16 == 0 \
+        else "decode_partition_kernel"
+    return "append_last_kernel + " + name + " (pa_write_decode, timed as one call)" if fused else name
 
 
-def algorithmic_bytes(inp) -> int:
-    """Bytes the decode kernel must move: K/V + q + out + the table entries it reads + lengths."""
+def algorithmic_bytes(inp, with_write: bool = False) -> int:
+    """Bytes the decode kernel must move: K/V + q + out + the table entries it
+    reads + lengths; with_write (pa_write_decode, timed as one call) adds its
+    write kernel's: the new K/V rows read and stored, one table entry and one
+    length per sequence."""
     B = inp.k_cache.shape[2]
     lens = inp.context_lens.to(torch.int64)
     entries = int(((lens + B - 1) // B).sum().item())
     Hkv = inp.k_cache.shape[1]
-    return kv_bytes(inp) + 2 * inp.q.numel() * inp.q.element_size() + entries * 4 * Hkv + lens.numel() * 4
+    write = 2 * (inp.new_key.numel() + inp.new_value.numel()) * inp.new_key.element_size() + 8 * lens.numel() \
+        if with_write else 0
+    return kv_bytes(inp) + 2 * inp.q.numel() * inp.q.element_size() + entries * 4 * Hkv + lens.numel() * 4 + write
 
 
 def memory_report(inp) -> dict:
@@ -389,7 +395,7 @@ def run_gpu(args) -> dict:
 
     kvb = kv_bytes(inp)
     total_kv = sum_over_ranks(float(kvb), dist)
-    alg = algorithmic_bytes(inp)
+    alg = algorithmic_bytes(inp, with_write=runner.fused)
     uniq = unique_kv_bytes(inp) + (alg - kvb)
     peaks = measured_peaks()
     achieved = alg / (kernel_ms * 1e-3) / 1e9
@@ -411,7 +417,8 @@ def run_gpu(args) -> dict:
                        step_launch="%s: %s%s (%d launch%s per step)" % (
                            "eager, kernel by kernel" if args.no_graph else "CUDA graphs",
                            "copy-on-write copies, then " if inp.copy_pairs.numel() else "",
-                           "slot lookup + K/V write + decode in one pa_write_decode call" if runner.fused
+                           "pa_write_decode: slot lookup + K/V write in one kernel, the decode launched early "
+                           "(programmatic dependent launch)" if runner.fused
                            else "slot lookup, K/V write, then decode", runner.launches_per_step,
                            "" if runner.launches_per_step == 1 else "es"),
                        decode="pa_decode_shared (plan: %d groups, %d pieces)" % (
@@ -422,7 +429,7 @@ def run_gpu(args) -> dict:
         "pct_of_measured_hbm": round(100 * value / world / peaks["hbm_gbs"], 2),
         "decode_kernel_us": round(kernel_ms * 1e3, 2),
         "decode_kernel_us_median": round(statistics.median(kernel_times) * 1e3, 2),
-        "roofline": {"kernel": decode_kernel_name(inp, args.shared), "bound": "hbm", "achieved": round(achieved, 1),
+        "roofline": {"kernel": decode_kernel_name(inp, args.shared, runner.fused), "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
                      "frac_of_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4),

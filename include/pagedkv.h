@@ -169,13 +169,12 @@ PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache,
  * only).  Sequences with context_len 0 write nothing.  Block ids and
  * positions are range-checked as in pa_slot_mapping (PA_DEVERR bits).
  *
- * For fp16 / bf16 pools with block_size % 16 == 0 this is ONE kernel launch:
- * the decode kernel's warp that takes the block holding position t puts the
- * token's rows into its staged copy of the block and stores them to the pool
- * (the lookup and write happen inside the decode).  Other shapes take two
- * launches (the write, then the decode).  The pool rows at the new positions
- * are overwritten while the kernel reads the blocks that hold them; their
- * previous contents are never used.  Workspace rules as for pa_decode.
+ * Two launches: one kernel looks up every slot and writes the rows (16-byte
+ * chunks), then the decode.  On the tensor-core path (fp16 / bf16 pools,
+ * block_size % 16 == 0) the decode is launched as a programmatic dependent
+ * of the write: it starts while the write runs, sets up its schedule and
+ * barriers, and waits for the write to finish before its first read of the
+ * pools.  Workspace rules as for pa_decode.
  */
 PA_API pa_status pa_write_decode(void *out, const void *q, const void *new_key,
                                  const void *new_value, void *k_cache, void *v_cache,

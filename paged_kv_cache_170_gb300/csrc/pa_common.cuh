@@ -241,6 +241,13 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
       : "memory");
 }
 
+// Programmatic dependent launch.  grid_dependency_wait: block until the grids
+// this one depends on have completed and their writes are visible (returns at
+// once when the launch did not allow an early start).  launch_dependents:
+// let a dependent grid that allows it start launching now.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (bulk copy) accesses of the same bytes.
 __device__ __forceinline__ void fence_proxy_async_shared() {

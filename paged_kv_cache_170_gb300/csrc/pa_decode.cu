@@ -15,7 +15,7 @@ template <typename T, int D, int GT>
 pa_status launch_decode_simt(const DecodeArgs &a, size_t ring_bytes, cudaStream_t stream);
 template <typename T, int D>
 pa_status launch_decode_mma(const DecodeArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t ring_bytes,
-                            cudaStream_t stream);
+                            cudaStream_t stream, bool early);
 template <typename T, int D>
 pa_status launch_decode_shared(const SharedArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t ring_bytes,
                                cudaStream_t stream);
@@ -189,11 +189,12 @@ static bool encode_pool_maps(const void *k_cache, const void *v_cache, pa_dtype 
 
 template <typename T>
 static pa_status dispatch_mma(const DecodeArgs &a, const void *k_cache, const void *v_cache, pa_dtype dtype, int D,
-                              size_t ring, cudaStream_t st) {
+                              size_t ring, cudaStream_t st, bool early = false) {
   CUtensorMap mk, mv;
   DecodeArgs b = a;
   if (!encode_pool_maps(k_cache, v_cache, dtype, a.num_blocks, a.Hkv, a.B, D, &mk, &mv, &b.nops)) return PA_ERR_CUDA;
-  return D == 64 ? launch_decode_mma<T, 64>(b, mk, mv, ring, st) : launch_decode_mma<T, 128>(b, mk, mv, ring, st);
+  return D == 64 ? launch_decode_mma<T, 64>(b, mk, mv, ring, st, early)
+                 : launch_decode_mma<T, 128>(b, mk, mv, ring, st, early);
 }
 
 }  // namespace pagedkv
@@ -267,29 +268,20 @@ static pa_status decode_impl(void *out, const void *q, const void *k_cache, cons
   a.start_block = start_block;
   a.out_f32 = out_f32;
   a.lse = lse;
-  a.new_k = nullptr;
-  a.new_v = nullptr;
-  a.k_store = nullptr;
-  a.v_store = nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool early = false;  // the decode may start launching while the write kernel runs
   if (new_key != nullptr) {
-    if (sh.mma) {  // the decode kernel writes the tokens itself
-      a.new_k = new_key;
-      a.new_v = new_value;
-      a.k_store = static_cast<char *>(const_cast<void *>(k_cache));
-      a.v_store = static_cast<char *>(const_cast<void *>(v_cache));
-    } else {  // CUDA-core kernel: one write launch before the decode
-      const pa_status w = launch_append_last(new_key, new_value, const_cast<void *>(k_cache),
-                                             const_cast<void *>(v_cache), block_tables, max_blocks_per_seq,
-                                             context_lens, num_seqs, num_kv_heads, head_dim, block_size, num_blocks,
-                                             dtype, debug_err, s);
-      if (w != PA_OK) return w;
-    }
+    const pa_status w = launch_append_last(new_key, new_value, const_cast<void *>(k_cache),
+                                           const_cast<void *>(v_cache), block_tables, max_blocks_per_seq,
+                                           context_lens, num_seqs, num_kv_heads, head_dim, block_size, num_blocks,
+                                           dtype, debug_err, s);
+    if (w != PA_OK) return w;
+    early = sh.mma;
   }
   if (sh.mma) {
     return dtype == PA_BF16
-               ? dispatch_mma<__nv_bfloat16>(a, k_cache, v_cache, dtype, head_dim, sh.ring_bytes, s)
-               : dispatch_mma<__half>(a, k_cache, v_cache, dtype, head_dim, sh.ring_bytes, s);
+               ? dispatch_mma<__nv_bfloat16>(a, k_cache, v_cache, dtype, head_dim, sh.ring_bytes, s, early)
+               : dispatch_mma<__half>(a, k_cache, v_cache, dtype, head_dim, sh.ring_bytes, s, early);
   }
   switch (dtype) {
     case PA_F32: return dispatch_simt<float>(a, head_dim, sh.GT, sh.ring_bytes, s);

@@ -31,13 +31,33 @@ pa_status launch_decode_simt(const DecodeArgs &a, size_t ring_bytes, cudaStream_
   return launch_status();
 }
 
+// early: allow the launch to start while the previous kernel in the stream
+// is still running (programmatic dependent launch); the kernel's producer
+// waits for that kernel before its first copy from the pools.
 template <typename T, int D>
 pa_status launch_decode_mma(const DecodeArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t ring_bytes,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool early) {
   static int configured[64] = {0};
   auto kern = decode_partition_mma_kernel<T, D>;
   if (!configure_once(kern, kRingBytesMma + 1024, configured)) return PA_ERR_CUDA;
-  kern<<<a.nctas, kDecodeThreads, ring_bytes + 1024, stream>>>(a, mk, mv);
+  if (!early) {
+    kern<<<a.nctas, kDecodeThreads, ring_bytes + 1024, stream>>>(a, mk, mv);
+    return launch_status();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.nctas);
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = ring_bytes + 1024;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, a, mk, mv) != cudaSuccess) {
+    cudaGetLastError();
+    return PA_ERR_CUDA;
+  }
   return launch_status();
 }
 
@@ -95,8 +115,8 @@ pa_status launch_prefill(const PrefillArgs &a, const CUtensorMap &mk, const CUte
 
 #define PAGEDKV_INSTANTIATE_MMA(T)                                                                          \
   template pa_status launch_decode_mma<T, 64>(const DecodeArgs &, const CUtensorMap &, const CUtensorMap &, \
-                                              size_t, cudaStream_t);                                        \
+                                              size_t, cudaStream_t, bool);                                  \
   template pa_status launch_decode_mma<T, 128>(const DecodeArgs &, const CUtensorMap &, const CUtensorMap &, \
-                                               size_t, cudaStream_t);
+                                               size_t, cudaStream_t, bool);
 
 }  // namespace pagedkv

@@ -265,34 +265,6 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
             fence_proxy_async_shared();
             __syncwarp();
           }
-          if (a.new_k != nullptr && (bb + 1) * B >= L) {
-            // fused write: the step's token (position L - 1, row nv - 1 of this
-            // tile) is not in the pool yet.  Its K and V rows go into the staged
-            // tile (swizzled: chunk c of row r sits at chunk c ^ (r & 7)); head
-            // chunk 0 of the kv head also stores them to the pool, for later
-            // steps.  Lanes 0 .. D/8-1 move K, the next D/8 move V, 16 bytes each.
-            constexpr int CPR = D / 8;  // 16-byte chunks per row
-            const int r = nv - 1;
-            if (lane < 2 * CPR) {
-              const int which = lane / CPR, hc = lane % CPR;
-              const long long src = ((long long)wk.s * a.Hkv + kvh) * D + hc * 8;
-              const uint4 val =
-                  *reinterpret_cast<const uint4 *>(static_cast<const T *>(which ? a.new_v : a.new_k) + src);
-              size_t so = (size_t)slot * a.slot_stride + (which ? a.tile_stride : 0u) + (hc >> 3) * B * 128 + r * 128 +
-                          ((hc & 7) ^ (r & 7)) * 16;
-              PA_DBG_FIX(so + 16 <= (size_t)a.nstage * a.slot_stride, kDbgSmem, so = 0);
-              *reinterpret_cast<uint4 *>(ring + so) = val;
-              if (wk.pc % HC == 0) {
-                const int pid = a.tables[(long long)wk.s * a.max_blocks + bb];
-                if (pid >= 0 && pid < a.num_blocks) {
-                  char *pool = which ? a.v_store : a.k_store;
-                  *reinterpret_cast<uint4 *>(pool + ((((long long)pid * a.Hkv + kvh) * B + r) * D + hc * 8) * sizeof(T)) = val;
-                }
-              }
-            }
-            fence_proxy_async_shared();  // generic writes to the slot before its next TMA fill
-            __syncwarp();
-          }
           mma_tile<T, D>(a, kt, vt, B, nv, qf, a.qscale, m0, m1, l0, l1, o, lane, ring_addr,
                          ring_addr + uint32_t(a.nstage) * a.slot_stride);
           __syncwarp();

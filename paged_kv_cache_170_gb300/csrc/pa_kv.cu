@@ -1,6 +1,5 @@
 // pa_kv.cu -- slot lookup, KV write and copy-on-write block copy kernels, the
-// write of pa_write_decode's CUDA-core path, plus the library's shared host
-// helpers.
+// write of pa_write_decode, plus the library's shared host helpers.
 //
 // All four kernels are plain bandwidth kernels: 16-byte vector loads and
 // stores, one thread per 16-byte chunk, grid-stride loops over a grid sized
@@ -115,14 +114,16 @@ __global__ void copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restric
 
 // ------------------------------------------------- a2 for pa_write_decode
 // The step's token of each sequence, at position lens[s] - 1, into its slot
-// (the lookup of a1 and the write of a2 in one pass): pa_write_decode's write
-// when the decode runs on the CUDA-core kernel.  key / value: [S][Hkv][D];
-// one thread per 16-byte chunk.
+// (the lookup of a1 and the write of a2 in one pass): pa_write_decode's write,
+// before its decode.  key / value: [S][Hkv][D]; one thread per 16-byte chunk.
 __global__ void append_last_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
                                    uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                                    const int32_t *__restrict__ tables, int max_blocks,
                                    const int32_t *__restrict__ lens, int S, int Hkv, int row_chunks, int B,
                                    int64_t num_blocks, int *err) {
+  // the decode that follows in pa_write_decode may start launching now: it
+  // sets itself up meanwhile and waits for this grid before reading the pools
+  launch_dependents();
   const int64_t per_seq = int64_t(Hkv) * row_chunks;
   const int64_t total = int64_t(S) * per_seq;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;

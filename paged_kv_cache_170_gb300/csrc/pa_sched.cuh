@@ -67,15 +67,6 @@ struct DecodeArgs {
   const int32_t *start_block;  // [S] first block of each sequence to read (earlier ones are shared, done elsewhere)
   float *out_f32;              // [S][Hq][D] fp32 output rows, written instead of `out`
   float *lse;                  // [S][Hq] log2-sum-exp of each row, m + log2(l); -inf for a row with no tokens
-  // Set only by pa_write_decode on the tensor-core kernel (null otherwise):
-  // the step's token of each sequence, at position lens[s] - 1, not yet in
-  // the pools.  The warp that takes the tile holding it puts the token's rows
-  // into its staged copy of the tile, and the warp of head chunk 0 also stores
-  // them to the pools.
-  const void *new_k;  // [S][Hkv][D]
-  const void *new_v;  // [S][Hkv][D]
-  char *k_store;      // the K pool, writable
-  char *v_store;      // the V pool, writable
 };
 
 // Output row `row` (= s * Hq + hq), dims d .. d+3, to `out` (or `out_f32`).
@@ -350,10 +341,16 @@ struct Walk {
 // (the q rows) with those entries only.  issued[slot] keeps the last use
 // issued into each slot so the producer can wait for every copy still in
 // flight before it leaves (after an abort too).
+//
+// The producer's copies are the kernel's first reads of the pools, so it is
+// where the kernel waits for the grid it depends on (griddepcontrol.wait: a
+// no-op unless the launch allowed an early start, as pa_write_decode's does,
+// so that the plan and the barriers are set up while the write kernel runs).
 template <class Issue>
 __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, const Plan &plan, int lane,
                                         uint64_t *full_bar, uint64_t *empty_bar, uint32_t *issued,
                                         volatile int *abort_flag, Issue issue) {
+  grid_dependency_wait();
   long long e = 0;
   bool aborted = false;
 #ifdef PA_TRACE
@@ -373,6 +370,8 @@ __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, con
       const int L = wk.L;
       const int32_t *trow = a.tables + (long long)wk.s * a.max_blocks + wk.fb + wk.b;
       int pid_next = lane < n ? trow[lane] : -1;
+
+
 #ifdef PA_TRACE
       {
         const long long t = clock64();
@@ -388,6 +387,8 @@ __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, con
         for (int k = 0; k < cnt; k += a.pg) {
           const int t = k + lane;
           const int p = __shfl_sync(kFullMask, pid_cur, t < 32 ? t : 31);
+
+
           bool fail = false;
           if (lane < a.pg && t < cnt) {
             const uint32_t me = uint32_t(e) + uint32_t(lane);  // a CTA's entry count fits 32 bits

@@ -219,8 +219,8 @@ def pa_write_decode(q: torch.Tensor, new_key: torch.Tensor, new_value: torch.Ten
                     out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                     err: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Each sequence's new token (new_key / new_value [S][Hkv][D], at position
-    context_lens[s] - 1) written into its slot, then decode attention; one
-    launch on the tensor-core path."""
+    context_lens[s] - 1) written into its slot, then decode attention: two
+    launches, the decode allowed to start while the write runs."""
     NB, Hkv, B, D, S, Hq, out, ws = _decode_args(q, k_cache, v_cache, block_tables, context_lens, out, workspace)
     for name, t in (("new_key", new_key), ("new_value", new_value)):
         _need(t, name, k_cache.dtype, 3, k_cache.device)
@@ -231,12 +231,6 @@ def pa_write_decode(q: torch.Tensor, new_key: torch.Tensor, new_value: torch.Ten
                                context_lens.data_ptr(), S, Hq, Hkv, D, B, NB, float(scale), _DTYPES[q.dtype],
                                ws.data_ptr(), ws.numel(), _ptr(err), _stream(q.device)), "pa_write_decode")
     return out
-
-
-def write_decode_is_one_launch(k_cache: torch.Tensor) -> bool:
-    """pa_write_decode runs as one kernel for fp16 / bf16 pools whose block
-    size is a multiple of 16 (the tensor-core decode); else as two."""
-    return k_cache.dtype in (torch.float16, torch.bfloat16) and k_cache.shape[2] % 16 == 0
 
 
 def pa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,

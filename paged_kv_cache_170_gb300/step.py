@@ -2,7 +2,7 @@
 
 One step is: copy-on-write block copies (when the step has any), slot lookup of
 the new tokens, their K/V write, then split-context decode attention over every
-sequence (the last three in one kernel when each sequence appends one token,
+sequence (the last three in one call when each sequence appends one token,
 see ``DecodeStep``).  Launched one by one from Python, each call pays host-side argument
 checks and a launch, and the GPU idles whenever the host falls behind; small
 batches are then launch-bound.  Here the step's kernels are captured into two
@@ -96,9 +96,10 @@ class DecodeStep:
     When every sequence appends exactly one token, at its last context
     position (``new_seq`` = 0 .. S-1, ``new_pos`` = context_lens - 1: a plain
     decode step), the write and the decode run as one call, pa_write_decode
-    (one kernel on the tensor-core path); ``fused=False`` keeps the separate
-    slot lookup and write.  The step's shape is checked here, at
-    construction: later steps must keep it.
+    (slot lookup and write in one kernel; the decode starts launching while it
+    runs); ``fused=False`` keeps the separate slot lookup, write and decode.
+    The step's shape is checked here, at construction: later steps must keep
+    it.
     """
 
     def __init__(self, inp, graphs: bool = True, shared: bool = False, fused: bool = True):
@@ -123,9 +124,7 @@ class DecodeStep:
             self.workspace = ops.new_workspace(S, Hq, Hkv, D, dev)
         self.slots = torch.empty(inp.new_seq.numel(), dtype=torch.int64, device=dev)
         self.err = ops.new_error_word(dev)
-        writes = 0 if self.fused else (2 if inp.new_seq.numel() else 0)
-        if self.fused and not ops.write_decode_is_one_launch(inp.k_cache):
-            decode_launches = 2
+        writes = 1 if self.fused else (2 if inp.new_seq.numel() else 0)
         self.launches_per_step = (1 if inp.copy_pairs.numel() else 0) + writes + decode_launches
         self.graphs = graphs
         # kernels before the decode: copy-on-write copies; slot lookup and write unless fused

@@ -1,6 +1,6 @@
 """Parity of pa_write_decode (each sequence's new token written at position
-context_len - 1, then decode attention, one launch on the tensor-core path)
-with the CPU oracle's write followed by its decode, through the C ABI.
+context_len - 1, then decode attention, the decode launched while the write
+runs) with the CPU oracle's write followed by its decode, through the C ABI.
 
 The pools after the call must equal the oracle's pools bit for bit; the
 output is held to the decode tolerances (fp16/bf16 max abs 2e-3 and max rel
@@ -76,13 +76,13 @@ CASES = {
     # name: (lens, Hq, Hkv, D, B, dtype, pad_tables)
     # empty sequences, tails of one token, full last blocks
     "zero_one_full_tails": ([0, 1, 0, 2, 16, 17, 32, 33], 8, 2, 128, 16, torch.bfloat16, True),
-    # two head chunks per kv head (G = 16): both stage the token, one stores it
+    # two head chunks per kv head (G = 16)
     "group16_two_chunks": ([300, 45, 1, 4096], 32, 2, 128, 32, torch.bfloat16, True),
     # long sequences cut among several CTAs next to short ones
     "cut_pairs": ([20000, 5, 9000, 16, 12345], 8, 8, 128, 16, torch.float16, True),
     "d64_b64": ([64, 65, 1, 700], 8, 4, 64, 64, torch.bfloat16, True),
     "gqa3_b48": ([47, 48, 49, 1000], 6, 2, 128, 48, torch.float16, False),
-    # CUDA-core paths: a write launch, then the decode
+    # CUDA-core decode paths
     "fp32": ([3, 130, 64, 0, 9], 4, 2, 128, 8, torch.float32, True),
     "block8_bf16": ([7, 8, 9, 300], 8, 2, 64, 8, torch.bfloat16, True),
 }
@@ -133,7 +133,7 @@ def test_fused_step_graphs_match_eager_and_oracle(ops):
     cpu = small_case("gqa_small", seed=5)
     eager_in, graph_in = cpu.to(DEV), cpu.to(DEV)
     eager = step_mod.DecodeStep(eager_in, graphs=False)
-    assert eager.fused and eager.launches_per_step == 1 and not eager.has_pre
+    assert eager.fused and eager.launches_per_step == 2 and not eager.has_pre
     a = eager.run().clone()
     runner = step_mod.DecodeStep(graph_in, graphs=True)
     for _ in range(3):
