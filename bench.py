@@ -37,6 +37,8 @@ NOMINAL_HBM_GBS = 8000.0
 KERNEL_SOURCES = ["paged_kv_cache_170_gb300/csrc/pa_decode_mma.cuh", "paged_kv_cache_170_gb300/csrc/pa_sched.cuh",
                   "paged_kv_cache_170_gb300/csrc/pa_mma_tile.cuh",
                   "paged_kv_cache_170_gb300/csrc/pa_common.cuh"]  # the tensor-core decode kernel
+SHARED_SOURCES = KERNEL_SOURCES + ["paged_kv_cache_170_gb300/csrc/pa_decode_shared.cuh",
+                                   "paged_kv_cache_170_gb300/csrc/pa_share.cu"]  # the shared-block decode's three kernels
 PREFILL_SOURCES = ["paged_kv_cache_170_gb300/csrc/pa_prefill.cuh", "paged_kv_cache_170_gb300/csrc/pa_sched.cuh",
                    "paged_kv_cache_170_gb300/csrc/pa_common.cuh"]  # the tcgen05 prefill kernel
 
@@ -436,7 +438,8 @@ def run_gpu(args) -> dict:
                      "algorithmic_bytes_per_launch": alg,
                      "distinct_bytes_per_launch": uniq,
                      "frac_distinct": round(uniq / (kernel_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                     "traffic": profiled_traffic(args.workload)},
+                     "traffic": profiled_traffic(args.workload, "decode_shared", SHARED_SOURCES) if args.shared
+                     else profiled_traffic(args.workload)},
         "e2e": {"value": round(total_kv / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
