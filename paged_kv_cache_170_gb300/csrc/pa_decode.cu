@@ -216,13 +216,17 @@ namespace pagedkv {
 // pa_decode, optionally over each sequence's blocks from start_block[s] on,
 // with fp32 output rows (out_f32) and their log2-sum-exp (lse), or (new_key
 // non-null, pa_write_decode) with each sequence's token at position
-// context_lens[s] - 1 written first.
+// context_lens[s] - 1 written first.  early_launch: the previous kernel in the
+// stream lets this one start launching before it ends (it triggers
+// griddepcontrol.launch_dependents); the decode's producer waits for it
+// before its first copy.
 static pa_status decode_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
                              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
                              int64_t num_blocks, float scale, pa_dtype dtype, void *workspace, size_t workspace_bytes,
                              int *debug_err, void *stream, const int32_t *start_block, float *out_f32, float *lse,
-                             const void *new_key = nullptr, const void *new_value = nullptr) {
+                             const void *new_key = nullptr, const void *new_value = nullptr,
+                             bool early_launch = false) {
   DecodeShape sh;
   pa_status st = check_decode_args(max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                                    num_blocks, dtype, &sh);
@@ -269,7 +273,7 @@ static pa_status decode_impl(void *out, const void *q, const void *k_cache, cons
   a.out_f32 = out_f32;
   a.lse = lse;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  bool early = false;  // the decode may start launching while the write kernel runs
+  bool early = early_launch && sh.mma;  // the decode may start launching while the previous kernel runs
   if (new_key != nullptr) {
     const pa_status w = launch_append_last(new_key, new_value, const_cast<void *>(k_cache),
                                            const_cast<void *>(v_cache), block_tables, max_blocks_per_seq,
@@ -445,10 +449,13 @@ extern "C" pa_status pa_decode_shared(void *out, const void *q, const void *k_ca
                           : shared_step<__half>(sa, k_cache, v_cache, dtype, head_dim, ring, s);
     if (st != PA_OK) return st;
   }
-  // 2. each sequence's own blocks: fp32 rows and their log2-sum-exp
+  // 2. each sequence's own blocks: fp32 rows and their log2-sum-exp; launched
+  // as a programmatic dependent of step 1, so its CTAs set up while step 1's
+  // last CTAs finish (it needs nothing from step 1, and waits for it anyway
+  // before its first copy, so step 3 after it sees both)
   st = decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_heads,
                    num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace, w.out_f32, debug_err,
-                   stream, plan_dev + h->s_start, out_f32, lse);
+                   stream, plan_dev + h->s_start, out_f32, lse, nullptr, nullptr, h->num_pieces > 0);
   if (st != PA_OK) return st;
   // 3. merge
   return dtype == PA_BF16 ? merge_step<__nv_bfloat16>(ma, head_dim, s) : merge_step<__half>(ma, head_dim, s);

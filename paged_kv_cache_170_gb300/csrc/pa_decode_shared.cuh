@@ -61,6 +61,9 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
   __shared__ int sh_abort;
   __shared__ __align__(16) float st[kConsumerWarps][8][R];  // tile-lane states of a piece's rows
 
+  // the own-block decode that follows may start launching now (it waits for
+  // this grid before its first copy)
+  launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int32_t *P = a.plan;
