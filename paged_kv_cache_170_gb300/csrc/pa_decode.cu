@@ -451,11 +451,14 @@ extern "C" pa_status pa_decode_shared(void *out, const void *q, const void *k_ca
   }
   // 2. each sequence's own blocks: fp32 rows and their log2-sum-exp; launched
   // as a programmatic dependent of step 1, so its CTAs set up while step 1's
-  // last CTAs finish (it needs nothing from step 1, and waits for it anyway
-  // before its first copy, so step 3 after it sees both)
+  // last CTAs finish.  It needs nothing from step 1, but every CTA with tiles
+  // waits for step 1 before its first copy, so step 2 ends after step 1 and
+  // step 3 sees both; with no own tiles at all no CTA would wait, so then it
+  // is launched normally.
   st = decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_heads,
                    num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace, w.out_f32, debug_err,
-                   stream, plan_dev + h->s_start, out_f32, lse, nullptr, nullptr, h->num_pieces > 0);
+                   stream, plan_dev + h->s_start, out_f32, lse, nullptr, nullptr,
+                   h->num_pieces > 0 && h->own_tiles != 0);
   if (st != PA_OK) return st;
   // 3. merge
   return dtype == PA_BF16 ? merge_step<__nv_bfloat16>(ma, head_dim, s) : merge_step<__half>(ma, head_dim, s);

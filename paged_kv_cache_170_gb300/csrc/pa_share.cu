@@ -254,6 +254,12 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
   if (plan == nullptr) return PA_OK;  // size query
   if (plan_capacity < size_t(off)) return PA_ERR_WORKSPACE;
 
+  h.own_tiles = 0;
+  for (int s = 0; s < S; ++s) {
+    long long L = context_lens[s];
+    L = L < 0 ? 0 : (L > cap ? cap : L);
+    if (L > (long long)start[s] * B) h.own_tiles = 1;
+  }
   memcpy(plan, &h, sizeof(h));
   auto put = [&](int32_t at, const int32_t *src, long long n) {
     if (n > 0) memcpy(plan + at, src, size_t(n) * sizeof(int32_t));

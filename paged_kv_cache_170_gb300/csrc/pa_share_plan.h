@@ -30,7 +30,7 @@ struct SharePlanHeader {
   int32_t u_group, u_kvh, u_pass, u_poff;
   int32_t p_unit, p_t0, p_t1, c_poff;
   int32_t s_start, s_moff, s_mgroup, s_midx;
-  int32_t reserved[1];
+  int32_t own_tiles;  // 1 when some sequence has tokens past its shared blocks (the own-block decode has work)
 };
 
 constexpr int kSharePlanHeaderInts = int(sizeof(SharePlanHeader) / sizeof(int32_t));

@@ -104,7 +104,8 @@ def _random_pool(S, Hq, Hkv, D, B, NB, dtype, seed):
 def test_shared_decode_edge_cases(ops, dtype):
     """Identical tables with a partial tail, an empty sequence, a sequence
     shorter than one block, a sequence whose blocks are all shared, and a
-    sequence outside every group; head_dim 64 and 128."""
+    sequence outside every group; then sequences with no blocks of their own
+    at all; head_dim 64 and 128."""
     for D in (64, 128):
         S, Hq, Hkv, B, NB = 6, 8, 2, 16, 64
         q, kc, vc = _random_pool(S, Hq, Hkv, D, B, NB, dtype, seed=D)
@@ -118,6 +119,13 @@ def test_shared_decode_edge_cases(ops, dtype):
         ref = native.decode(q, kc, vc, tables.numpy(), lens.numpy(), scale)
         assert_attention_close(out, ref, strict=False)
         assert torch.count_nonzero(out[2]) == 0  # empty sequence: zero row
+        # every sequence's blocks all shared and full: the own-block step has no tiles
+        full = torch.tensor([row] * 4, dtype=torch.int32)
+        lens_full = torch.full((4,), 144, dtype=torch.int32)
+        out, f = _shared(ops, q[:4].to(DEV), args[1], args[2], full.to(DEV), lens_full.to(DEV), scale)
+        assert f["num_groups"] == 1 and f["own_tiles"] == 0
+        ref = native.decode(q[:4], kc, vc, full.numpy(), lens_full.numpy(), scale)
+        assert_attention_close(out, ref, strict=False)
 
 
 def test_shared_decode_deterministic_reusable_workspace_and_no_group_plan(ops):

@@ -216,6 +216,7 @@ def test_plan_of_unshared_tables_has_no_groups(ops):
     f = ops.plan_fields(plan)
     assert f["num_groups"] == 0 and f["num_pieces"] == 0
     assert list(f["s_start_arr"]) == [0] * 4
+    assert f["own_tiles"] == 1
     _check_structure(f, inp.block_tables.numpy(), inp.context_lens.numpy(), 16, 32, 8)
 
 
@@ -230,6 +231,7 @@ def test_plan_edge_cases(ops):
     assert f["num_groups"] == 1
     assert list(f["g_members_arr"]) == [0, 1] and (f["g_b0_arr"][0], f["g_b1_arr"][0]) == (0, 9)
     assert list(f["s_start_arr"]) == [9, 9, 0, 0]
+    assert f["own_tiles"] == 1
     _check_structure(f, tables.numpy(), lens.numpy(), B, 4, 2)
     # 40 members x 4 heads = 160 rows: 5 passes per kv head
     tables = torch.tensor([row] * 40, dtype=torch.int32)
@@ -237,6 +239,7 @@ def test_plan_edge_cases(ops):
     f = ops.plan_fields(ops.share_plan(tables, lens, B, 8, 2, nctas=9))
     assert f["num_groups"] == 1 and f["g_passes_arr"][0] == 5 and f["num_units"] == 10
     assert list(f["s_start_arr"]) == [4] * 40  # every block shared: nothing of their own
+    assert f["own_tiles"] == 0  # so the own-block decode is not launched early (no CTA of it would wait)
 
 
 def test_plan_rejects_bad_arguments_and_small_buffers(ops):
