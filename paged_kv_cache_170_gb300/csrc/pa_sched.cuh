@@ -344,8 +344,9 @@ struct Walk {
 //
 // The producer's copies are the kernel's first reads of the pools, so it is
 // where the kernel waits for the grid it depends on (griddepcontrol.wait: a
-// no-op unless the launch allowed an early start, as pa_write_decode's does,
-// so that the plan and the barriers are set up while the write kernel runs).
+// no-op unless the launch allowed an early start, as pa_write_decode's and
+// the shared-block decode's own-block step do, so that the plan and the
+// barriers are set up while the previous kernel runs).
 template <class Issue>
 __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, const Plan &plan, int lane,
                                         uint64_t *full_bar, uint64_t *empty_bar, uint32_t *issued,
@@ -370,8 +371,6 @@ __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, con
       const int L = wk.L;
       const int32_t *trow = a.tables + (long long)wk.s * a.max_blocks + wk.fb + wk.b;
       int pid_next = lane < n ? trow[lane] : -1;
-
-
 #ifdef PA_TRACE
       {
         const long long t = clock64();
@@ -387,8 +386,6 @@ __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, con
         for (int k = 0; k < cnt; k += a.pg) {
           const int t = k + lane;
           const int p = __shfl_sync(kFullMask, pid_cur, t < 32 ? t : 31);
-
-
           bool fail = false;
           if (lane < a.pg && t < cnt) {
             const uint32_t me = uint32_t(e) + uint32_t(lane);  // a CTA's entry count fits 32 bits
