@@ -205,11 +205,15 @@ def workload_config(name: str, inp, l2_mode: str = "auto") -> dict:
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed loop runs."""
+    """nvidia-smi clock / throttle sampling while the loaded phase and the timed
+    loop run (the caller keeps the GPU busy for ``LOAD_SECONDS`` first, so
+    that the record covers the workload's own clocks, not an idle GPU)."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,utilization.gpu")
+    LOAD_SECONDS = 1.2
+    BUSY_PCT = 50.0  # a sample counts as under load at this GPU utilisation or more
 
     def __init__(self, index: int):
         self.index = index
@@ -237,25 +241,49 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
 
     def summary(self) -> dict:
-        sm, mx, reasons = [], None, set()
+        """Median SM clock over the samples taken under load (GPU utilisation
+        >= BUSY_PCT; the upper half of all samples if none reports it), the
+        throttle reasons seen in any sample, and the sample counts."""
+        sm, loaded, mx, reasons = [], [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
+                mhz = float(f[1])
                 mx = float(f[2])
             except ValueError:
                 continue
+            sm.append(mhz)
+            try:
+                if len(f) > 9 and float(f[9]) >= self.BUSY_PCT:
+                    loaded.append(mhz)
+            except ValueError:
+                pass
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        busy = sorted(sm)[len(sm) // 2:]  # the loaded half of the samples
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0,
+                    "samples_under_load": 0}
+        busy = loaded if loaded else sorted(sm)[len(sm) // 2:]
         return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "samples_under_load": len(loaded)}
+
+
+def keep_busy(step, seconds: float, device, flush=None) -> int:
+    """Replay ``step`` (and the L2 flush between steps, when given) untimed
+    for about ``seconds``; returns the steps run."""
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(64):
+            if flush is not None:
+                flush(n)
+            step()
+            n += 1
+        torch.cuda.synchronize(device)
+    return n
 
 
 def time_cpu_oracle(inp_cpu, max_seconds: float, nthreads: int = 0):
@@ -353,6 +381,10 @@ def run_gpu(args) -> dict:
     barrier(dist)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
+        # the same step, untimed, so that the clock record covers this load
+        load_steps = keep_busy(step, ClockSampler.LOAD_SECONDS, dev,
+                               (lambda k: flush_l2(flush_buf, k)) if flush else None)
+        torch.cuda.synchronize(dev)
         start.record(stream)
         for k in range(args.steps):
             if flush:
@@ -383,9 +415,14 @@ def run_gpu(args) -> dict:
     pipe.drain()
     torch.cuda.synchronize(dev)
     barrier(dist)
+    # each step's inputs are staged anew on the host (written into the pinned
+    # buffer the step uploads from), as a serving loop hands over a new batch
+    host_src = {n: getattr(inp, n).cpu() for n in pipe.slots[0].packed.host_views}
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
+        for n, v in pipe.next_host_views().items():
+            v.copy_(host_src[n])
         pipe.step()
     pipe.drain()
     e1.record(stream)
@@ -441,9 +478,13 @@ def run_gpu(args) -> dict:
                      "traffic": profiled_traffic(args.workload, "decode_shared", SHARED_SOURCES) if args.shared
                      else profiled_traffic(args.workload)},
         "e2e": {"value": round(total_kv / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "host_staging": "each step's inputs written into the pinned upload buffer by the host, one upload, "
+                                "the output read back; two steps in flight"},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks.summary(),
+        "clocks": dict(clocks.summary(), untimed_load_steps=load_steps,
+                       load_note="the same step replayed untimed for %.1f s inside the sampling window before the "
+                                 "timed loop" % ClockSampler.LOAD_SECONDS),
     }
     if rank == 0 and not args.no_cpu_baseline:
         cpu = inp.to("cpu")
@@ -516,6 +557,8 @@ def run_prefill_gpu(args) -> dict:
     barrier(dist)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
+        load_steps = keep_busy(step, ClockSampler.LOAD_SECONDS, dev,
+                               (lambda k: flush_l2(flush_buf, k)) if flush else None)
         for k in range(args.steps):
             if flush:
                 flush_l2(flush_buf, k)
@@ -564,7 +607,7 @@ def run_prefill_gpu(args) -> dict:
         "e2e": {"value": round(total_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
-        "clocks": clocks.summary(),
+        "clocks": dict(clocks.summary(), untimed_load_steps=load_steps),
     }
     if rank == 0 and not args.no_cpu_baseline:
         cpu = inp.to("cpu")

@@ -1,6 +1,11 @@
 """Build libpagedkv.so in-tree for sm_103a (nvcc, one translation unit per job).
 
-    python -m paged_kv_cache_170_gb300.build [--force] [--verbose]
+    python -m paged_kv_cache_170_gb300.build [--force] [--verbose] [--variant faulttest]
+
+The ``faulttest`` variant (its own folder, ``_build_faulttest/``) is for the
+test of the kernels' bounded waits only: the decode's producer never issues the
+first ring entry of the CTA that owns the step's first tile, and the waits
+give up after about half a second instead of 1.5 s.  Nothing but that test loads it.
 """
 from __future__ import annotations
 
@@ -41,19 +46,33 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    os.makedirs(OUT_DIR, exist_ok=True)
-    stamp = os.path.join(OUT_DIR, "flags.txt")
-    flags_now = " ".join(ARCH + FLAGS)
+VARIANTS = {
+    "": [],
+    # one lost arrival and a 1e9-cycle wait limit (see the module docstring)
+    "faulttest": ["-DPA_FAULT_WITHHOLD_FIRST_ENTRY", "-DPA_WAIT_LIMIT_CYCLES=1000000000LL"],
+}
+
+
+def lib_path(variant: str = "") -> str:
+    return LIB if not variant else os.path.join(PKG, f"_build_{variant}", "libpagedkv.so")
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False, variant: str = "") -> str:
+    out_dir = os.path.dirname(lib_path(variant))
+    lib = lib_path(variant)
+    flags = FLAGS + VARIANTS[variant]
+    os.makedirs(out_dir, exist_ok=True)
+    stamp = os.path.join(out_dir, "flags.txt")
+    flags_now = " ".join(ARCH + flags)
     same_flags = os.path.exists(stamp) and open(stamp).read() == flags_now
-    if not force and same_flags and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
-        return LIB
+    if not force and same_flags and os.path.exists(lib) and os.path.getmtime(lib) >= _deps_mtime():
+        return lib
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
 
     def compile_one(src: str) -> tuple[str, str]:
-        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
-        cmd = [cc, *ARCH, *FLAGS, *extra, "-I", os.path.join(ROOT, "include"), "-c", os.path.join(CSRC, src),
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
+        cmd = [cc, *ARCH, *flags, *extra, "-I", os.path.join(ROOT, "include"), "-c", os.path.join(CSRC, src),
                "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -66,14 +85,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
         for _, log in results:
             sys.stderr.write(log)
     objs = [o for o, _ in results]
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp, "w") as f:
         f.write(flags_now)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
@@ -81,5 +100,6 @@ if __name__ == "__main__":
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
     ap.add_argument("--ptxas", action="store_true", help="print ptxas register/smem usage")
+    ap.add_argument("--variant", choices=sorted(VARIANTS), default="")
     args = ap.parse_args()
-    print(build(force=args.force, verbose=args.verbose, ptxas_verbose=args.ptxas))
+    print(build(force=args.force, verbose=args.verbose, ptxas_verbose=args.ptxas, variant=args.variant))

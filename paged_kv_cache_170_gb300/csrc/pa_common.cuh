@@ -186,12 +186,16 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
-// after kWaitLimitCycles SM cycles (>= 1.4 s at the 2.07 GHz maximum clock),
+// after kWaitLimitCycles SM cycles (>= 1.4 s at the 2.07 GHz maximum clock;
+// a test build of the library may set a shorter limit with PA_WAIT_LIMIT_CYCLES),
 // or at once when *abort is set; returns false then.  The limit is counted on
 // the SM cycle counter, which only moves forward within a thread: the global
 // nanosecond timer is re-synchronised to host time and can jump forward by
 // more than a second, which would end healthy waits.
-constexpr long long kWaitLimitCycles = 3000000000LL;
+#ifndef PA_WAIT_LIMIT_CYCLES
+#define PA_WAIT_LIMIT_CYCLES 3000000000LL
+#endif
+constexpr long long kWaitLimitCycles = PA_WAIT_LIMIT_CYCLES;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
   // a phase that has already completed is seen by test_wait at a fraction of

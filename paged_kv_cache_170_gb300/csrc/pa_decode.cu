@@ -45,6 +45,14 @@ static size_t workspace_bytes_for(int num_seqs, int num_heads, int head_dim, int
   return partial_bytes(nctas, head_dim) + round256(size_t(num_seqs) * num_heads * sizeof(unsigned));
 }
 
+bool decode_counter_region(int num_seqs, int num_heads, int head_dim, size_t *offset, size_t *bytes) {
+  const int n = decode_grid();
+  if (n <= 0 || num_seqs < 0 || num_heads <= 0 || (head_dim != 64 && head_dim != 128)) return false;
+  *offset = partial_bytes(n, head_dim);
+  *bytes = size_t(num_seqs) * num_heads * sizeof(unsigned);
+  return true;
+}
+
 // ----------------------------------------------------------------- tensor maps
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -213,6 +221,28 @@ extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_
 
 namespace pagedkv {
 
+// The host-side checks of a decode call (everything but the workspace size):
+// PA_OK when pa_decode would go on to launch (or, for num_seqs == 0, return
+// PA_OK without work).
+pa_status check_decode_call(const void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                            int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                            int64_t num_blocks, float scale, pa_dtype dtype, const void *workspace,
+                            DecodeShape *shape) {
+  DecodeShape local;
+  DecodeShape &sh = shape != nullptr ? *shape : local;
+  const pa_status st = check_decode_args(max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, head_dim,
+                                         block_size, num_blocks, dtype, &sh);
+  if (st != PA_OK) return st;
+  if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace))
+    return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
 // pa_decode, optionally over each sequence's blocks from start_block[s] on,
 // with fp32 output rows (out_f32) and their log2-sum-exp (lse), or (new_key
 // non-null, pa_write_decode) with each sequence's token at position
@@ -228,15 +258,10 @@ static pa_status decode_impl(void *out, const void *q, const void *k_cache, cons
                              const void *new_key = nullptr, const void *new_value = nullptr,
                              bool early_launch = false) {
   DecodeShape sh;
-  pa_status st = check_decode_args(max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
-                                   num_blocks, dtype, &sh);
-  if (st != PA_OK) return st;
-  if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
-  if (num_seqs == 0) return PA_OK;
-  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
-    return PA_ERR_INVALID_ARG;
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace))
-    return PA_ERR_INVALID_ARG;
+  pa_status st = check_decode_call(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                   num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype,
+                                   workspace, &sh);
+  if (st != PA_OK || num_seqs == 0) return st;
   if (workspace_bytes < workspace_bytes_for(num_seqs, num_heads, head_dim, sh.nctas)) return PA_ERR_WORKSPACE;
   if (new_key != nullptr && (new_value == nullptr || !aligned16(new_key) || !aligned16(new_value) ||
                              start_block != nullptr))

@@ -400,8 +400,19 @@ __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, con
 #ifdef PA_TRACE
               if (lane == 0) tr_empty += clock64() - t;
 #endif
-              issue(slot, p, kvh, wk.b + base + t, L, wk.s, wk.pc, base + t < a.ncw);
-              issued[slot] = u + 1;
+#ifdef PA_FAULT_WITHHOLD_FIRST_ENTRY
+              // Test build only: the first entry of the CTA whose range starts
+              // at the step's first tile is never issued (no copy and no
+              // arrival), so the consumer that waits for it runs into its wait
+              // limit, as a lost arrival would make it.
+              const bool withhold = plan.w0 == 0 && me == 0;
+#else
+              constexpr bool withhold = false;
+#endif
+              if (!withhold) {
+                issue(slot, p, kvh, wk.b + base + t, L, wk.s, wk.pc, base + t < a.ncw);
+                issued[slot] = u + 1;
+              }
             }
           }
           if (__any_sync(kFullMask, fail)) {

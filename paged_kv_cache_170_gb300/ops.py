@@ -30,10 +30,11 @@ class PagedKVError(RuntimeError):
     pass
 
 
-def _load() -> ctypes.CDLL:
-    if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m paged_kv_cache_170_gb300.build`")
-    lib = ctypes.CDLL(LIB_PATH)
+def _load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """The library at ``path`` with every entry point's argument types set."""
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -m paged_kv_cache_170_gb300.build`")
+    lib = ctypes.CDLL(path)
     vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     sig = {
         "pa_slot_mapping": [vp, vp, i32, i32, vp, vp, i64, i32, i64, vp, vp],
@@ -183,7 +184,9 @@ def new_workspace(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: in
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
-def _decode_args(q, k_cache, v_cache, block_tables, context_lens, out, workspace):
+def _decode_args(q, k_cache, v_cache, block_tables, context_lens, out, workspace, with_workspace=True):
+    """Checks of a decode call's tensors; ``out`` and (with_workspace) the
+    workspace are allocated when not given."""
     NB, Hkv, B, D = _cache_shape(k_cache, v_cache)
     dev = k_cache.device
     _need(q, "q", k_cache.dtype, 3, dev)
@@ -197,9 +200,10 @@ def _decode_args(q, k_cache, v_cache, block_tables, context_lens, out, workspace
     _need(out, "out", q.dtype, 3, dev)
     if out.shape != q.shape:
         raise ValueError("out must have q's shape")
-    if workspace is None:
-        workspace = new_workspace(S, Hq, Hkv, D, dev)
-    _need(workspace, "workspace", torch.uint8, 1, dev)
+    if with_workspace:
+        if workspace is None:
+            workspace = new_workspace(S, Hq, Hkv, D, dev)
+        _need(workspace, "workspace", torch.uint8, 1, dev)
     return NB, Hkv, B, D, S, Hq, out, workspace
 
 
@@ -239,15 +243,9 @@ def pa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     """pa_decode without a workspace, for callers that cannot allocate device
     memory: the library keeps the scratch in a static 4 MiB device array.
     ``out`` is still the caller's (allocated here only when not given)."""
-    NB, Hkv, B, D = _cache_shape(k_cache, v_cache)
-    dev = k_cache.device
-    _need(q, "q", k_cache.dtype, 3, dev)
-    _need(block_tables, "block_tables", torch.int32, 2, dev)
-    _need(context_lens, "context_lens", torch.int32, 1, dev)
-    S, Hq, _ = q.shape
-    if out is None:
-        out = torch.empty_like(q)
-    _need(out, "out", q.dtype, 3, dev)
+    NB, Hkv, B, D, S, Hq, out, _ = _decode_args(q, k_cache, v_cache, block_tables, context_lens, out, None,
+                                                with_workspace=False)
+    dev = q.device
     _check(lib.pa_decode_noalloc(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                  block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), S, Hq, Hkv,
                                  D, B, NB, float(scale), _DTYPES[q.dtype], _ptr(err), _stream(dev)),

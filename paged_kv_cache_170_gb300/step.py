@@ -224,6 +224,15 @@ class StepPipeline:
         self.d2h_bytes = sl.out_host.numel() * sl.out_host.element_size()
         self.k = 0
 
+    def next_host_views(self) -> dict:
+        """The pinned host views of the next step's inputs (``PackedInputs.host_views``
+        of the slot ``step()`` uses next), once the upload of that slot's
+        previous step has read them: the caller writes the step's inputs there,
+        then calls ``step()``."""
+        sl = self.slots[self.k % 2]
+        sl.ev_up.synchronize()
+        return sl.packed.host_views
+
     def step(self):
         """Enqueue the next step; returns its slot."""
         sl = self.slots[self.k % 2]

@@ -46,3 +46,41 @@ def test_product_path_does_not_import_the_oracle():
                         assert not any(a.name.split(".")[0] == "oracle" for a in node.names), f
                     if isinstance(node, ast.ImportFrom) and node.module:
                         assert node.module.split(".")[0] != "oracle", f
+
+
+def _header_signatures():
+    """{name: [parameter declarations]} of every function include/pagedkv.h declares."""
+    import re
+
+    from paged_kv_cache_170_gb300 import ops
+
+    text = open(ops.HEADER_PATH, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    sigs = {}
+    for m in re.finditer(r"PA_API\s+[\w\s\*]*?\b(pa_\w+)\s*\(([^)]*)\)\s*;", text):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        sigs[m.group(1)] = params
+    return sigs
+
+
+def test_header_signatures_match_the_binding_and_the_recorded_boundary():
+    """Every declared function has the arity the ctypes binding passes, and the
+    calls of the decode step keep the parameter lists the design records
+    (pa_decode without a max_context_len, its workspace sized by the head
+    counts and head_dim, debug_err on the write and copy calls)."""
+    from paged_kv_cache_170_gb300 import ops
+
+    sigs = _header_signatures()
+    assert set(sigs) == set(ops.header_functions())
+    for name, params in sigs.items():
+        fn = getattr(ops.lib, name)
+        assert fn.argtypes is not None, f"{name}: the binding declares no argtypes"
+        assert len(fn.argtypes) == len(params), (name, len(fn.argtypes), params)
+    names = {n: [p.split()[-1].lstrip("*") for p in ps] for n, ps in sigs.items()}
+    assert names["pa_decode_workspace_size"] == ["num_seqs", "num_heads", "num_kv_heads", "head_dim"]
+    assert "max_context_len" not in names["pa_decode"]
+    assert names["pa_decode"][:3] == ["out", "q", "k_cache"]
+    assert names["pa_decode"][-3:] == ["workspace_bytes", "debug_err", "stream"]
+    assert names["pa_write_kv"][-2:] == ["debug_err", "stream"]
+    assert names["pa_copy_blocks"][-2:] == ["debug_err", "stream"]
+    assert len(sigs["pa_decode"]) == 19 and len(sigs["pa_write_kv"]) == 13 and len(sigs["pa_copy_blocks"]) == 11
