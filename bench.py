@@ -382,8 +382,7 @@ def run_gpu(args) -> dict:
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
         # the same step, untimed, so that the clock record covers this load
-        load_steps = keep_busy(step, ClockSampler.LOAD_SECONDS, dev,
-                               (lambda k: flush_l2(flush_buf, k)) if flush else None)
+        load_steps = keep_busy(step, args.load_seconds, dev, (lambda k: flush_l2(flush_buf, k)) if flush else None)
         torch.cuda.synchronize(dev)
         start.record(stream)
         for k in range(args.steps):
@@ -484,7 +483,7 @@ def run_gpu(args) -> dict:
         "gpu_launches": launches_per_step * args.steps,
         "clocks": dict(clocks.summary(), untimed_load_steps=load_steps,
                        load_note="the same step replayed untimed for %.1f s inside the sampling window before the "
-                                 "timed loop" % ClockSampler.LOAD_SECONDS),
+                                 "timed loop" % args.load_seconds),
     }
     if rank == 0 and not args.no_cpu_baseline:
         cpu = inp.to("cpu")
@@ -557,8 +556,7 @@ def run_prefill_gpu(args) -> dict:
     barrier(dist)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
-        load_steps = keep_busy(step, ClockSampler.LOAD_SECONDS, dev,
-                               (lambda k: flush_l2(flush_buf, k)) if flush else None)
+        load_steps = keep_busy(step, args.load_seconds, dev, (lambda k: flush_l2(flush_buf, k)) if flush else None)
         for k in range(args.steps):
             if flush:
                 flush_l2(flush_buf, k)
@@ -744,6 +742,8 @@ def main(argv=None):
                          "flush, or warm (no flush; analysis only)")
     ap.add_argument("--placement", choices=["random", "contiguous"], default="random",
                     help="physical placement of the plain workloads' blocks")
+    ap.add_argument("--load-seconds", type=float, default=ClockSampler.LOAD_SECONDS,
+                    help="untimed replay of the step inside the clock-sampling window before the timed loop")
     ap.add_argument("--shared", action="store_true",
                     help="decode with pa_decode_shared (each shared block read once per group of sharers)")
     args = ap.parse_args(argv)

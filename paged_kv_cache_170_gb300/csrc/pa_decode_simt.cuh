@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm) decode_partition_k
   const long long w0 = plan.w0, w1 = plan.w1;
   if (w0 >= w1) {  // fewer tiles than CTAs: nothing to stream, only empty rows to zero
     if (warp == kMergerWarp) zero_empty_rows<T>(a, D, lane, 32);
+    if (warp == kProducerWarp) grid_dependency_wait();  // never complete before the grid this one depends on
     return;
   }
   const size_t tile_elems = size_t(B) * D;
