@@ -38,7 +38,7 @@ KERNEL_SOURCES = ["paged_kv_cache_170_gb300/csrc/pa_decode_mma.cuh", "paged_kv_c
                   "paged_kv_cache_170_gb300/csrc/pa_mma_tile.cuh",
                   "paged_kv_cache_170_gb300/csrc/pa_common.cuh"]  # the tensor-core decode kernel
 SHARED_SOURCES = KERNEL_SOURCES + ["paged_kv_cache_170_gb300/csrc/pa_decode_shared.cuh",
-                                   "paged_kv_cache_170_gb300/csrc/pa_share.cu"]  # the shared-block decode's three kernels
+                                   "paged_kv_cache_170_gb300/csrc/pa_share.cu"]  # the shared-block decode's two kernels
 PREFILL_SOURCES = ["paged_kv_cache_170_gb300/csrc/pa_prefill.cuh", "paged_kv_cache_170_gb300/csrc/pa_sched.cuh",
                    "paged_kv_cache_170_gb300/csrc/pa_common.cuh"]  # the tcgen05 prefill kernel
 
@@ -152,7 +152,7 @@ def decode_kernel_name(inp, shared: bool, fused: bool = False) -> str:
     fp16 / bf16 caches whose block size is a multiple of 16; pa_write_decode
     runs the write kernel first."""
     if shared:
-        return "decode_shared_mma_kernel + decode_partition_mma_kernel + merge_shared_kernel"
+        return "decode_shared_mma_kernel + merge_shared_kernel"
     name = "decode_partition_mma_kernel" if inp.k_cache.dtype != torch.float32 and inp.k_cache.shape[2] % 16 == 0 \
         else "decode_partition_kernel"
     return "append_last_kernel + " + name + " (pa_write_decode, timed as one call)" if fused else name
@@ -459,8 +459,10 @@ def run_gpu(args) -> dict:
                            "(programmatic dependent launch)" if runner.fused
                            else "slot lookup, K/V write, then decode", runner.launches_per_step,
                            "" if runner.launches_per_step == 1 else "es"),
-                       decode="pa_decode_shared (plan: %d groups, %d pieces)" % (
-                           runner.plan_info["num_groups"], runner.plan_info["num_pieces"]) if args.shared
+                       decode="pa_decode_shared (plan: %d shared and %d own groups, %d pieces)" % (
+                           runner.plan_info["num_shared_groups"],
+                           runner.plan_info["num_groups"] - runner.plan_info["num_shared_groups"],
+                           runner.plan_info["num_pieces"]) if args.shared
                        else "pa_decode"),
         "tokens_per_s": round(sum_over_ranks(float(S), dist) / (step_ms_max * 1e-3), 0),
         "pct_of_nominal_8000_gbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),

@@ -225,7 +225,9 @@ PA_API pa_status pa_decode_noalloc(void *out, const void *q, const void *k_cache
  * 4.1) -- are found from the block tables: groups of two or more sequences
  * whose tables agree on a run of blocks that are full for every member.  The
  * pages read a shared block once per sharer; pa_decode_shared reads it once
- * per group.  The plan also splits the groups' work evenly over `nctas` CTAs
+ * per group.  Each sequence's blocks past its shared runs (its private blocks,
+ * the last one possibly partly filled) form a one-member own group, read by
+ * the same kernel.  The plan also splits the groups' work evenly over `nctas` CTAs
  * (pass pa_decode_grid_size()).
  *
  * block_tables, context_lens: HOST int32 arrays [num_seqs][max_blocks_per_seq]

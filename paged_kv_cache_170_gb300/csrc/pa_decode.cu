@@ -354,26 +354,19 @@ static const SharePlanHeader *check_plan(const int32_t *plan_host, int num_seqs,
   const SharePlanHeader *h = reinterpret_cast<const SharePlanHeader *>(plan_host);
   if (h->magic != kSharePlanMagic || h->num_seqs != num_seqs || num_kv_heads <= 0 ||
       h->group_size * num_kv_heads != num_heads || h->num_kv_heads != num_kv_heads || h->block_size != block_size ||
-      h->max_blocks != max_blocks_per_seq || h->nctas <= 0 || h->num_pieces < 0 || h->total_ints < kSharePlanHeaderInts)
+      h->max_blocks != max_blocks_per_seq || h->nctas <= 0 || h->num_pieces < 0 || h->total_ints < kSharePlanHeaderInts ||
+      h->num_shared_groups < 0 || h->num_shared_groups > h->num_groups || (h->p_desc & 3) != 0)
     return nullptr;
   return h;
 }
 
-// Workspace of the shared-block decode: the private-block decode's own
-// workspace (partials, counters), its fp32 rows and log2-sum-exp, then the
-// shared kernel's partial states [num_pieces][kSharePassRows][state_row(D)].
-struct SharedWorkspace {
-  size_t out_f32, lse, records, total;  // byte offsets of each part, and the total
-};
-
-static SharedWorkspace shared_workspace(const SharePlanHeader &h, int num_seqs, int num_heads, int head_dim,
-                                        int nctas) {
-  SharedWorkspace w;
-  w.out_f32 = round256(workspace_bytes_for(num_seqs, num_heads, head_dim, nctas));
-  w.lse = w.out_f32 + round256(size_t(num_seqs) * num_heads * head_dim * sizeof(float));
-  w.records = w.lse + round256(size_t(num_seqs) * num_heads * sizeof(float));
-  w.total = w.records + round256(size_t(h.num_pieces) * kSharePassRows * state_row(head_dim) * sizeof(float));
-  return w;
+// Workspace of the shared-block decode: the step-1 kernel's partial states
+// [num_pieces][kSharePassRows][state_row(D)]; for a plan with no shared group
+// (the call is then pa_decode), pa_decode's workspace.
+static size_t shared_workspace_bytes(const SharePlanHeader &h, int num_seqs, int num_heads, int head_dim,
+                                     int nctas) {
+  if (h.num_shared_groups == 0) return workspace_bytes_for(num_seqs, num_heads, head_dim, nctas);
+  return round256(size_t(h.num_pieces) * kSharePassRows * state_row(head_dim) * sizeof(float));
 }
 
 template <typename T>
@@ -401,7 +394,7 @@ extern "C" size_t pa_decode_shared_workspace_size(const int32_t *plan_host, int 
   if (h == nullptr || h->magic != kSharePlanMagic || h->num_seqs != num_seqs) return 0;
   const int n = decode_grid();
   if (n <= 0) return 0;
-  return shared_workspace(*h, num_seqs, num_heads, head_dim, n).total;
+  return shared_workspace_bytes(*h, num_seqs, num_heads, head_dim, n);
 }
 
 extern "C" pa_status pa_decode_shared(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -420,7 +413,7 @@ extern "C" pa_status pa_decode_shared(void *out, const void *q, const void *k_ca
       check_plan(plan_host, num_seqs, num_heads, num_kv_heads, block_size, max_blocks_per_seq);
   if (h == nullptr) return PA_ERR_INVALID_ARG;
   if (num_seqs == 0) return PA_OK;
-  if (h->num_groups == 0)  // nothing shared: the plain decode
+  if (h->num_shared_groups == 0)  // nothing shared: the plain decode
     return pa_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_heads,
                      num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace, workspace_bytes,
                      debug_err, stream);
@@ -429,18 +422,16 @@ extern "C" pa_status pa_decode_shared(void *out, const void *q, const void *k_ca
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace) ||
       !aligned16(plan_dev))
     return PA_ERR_INVALID_ARG;
-  const SharedWorkspace w = shared_workspace(*h, num_seqs, num_heads, head_dim, sh.nctas);
-  if (workspace_bytes < w.total) return PA_ERR_WORKSPACE;
-  char *ws = static_cast<char *>(workspace);
-  float *out_f32 = reinterpret_cast<float *>(ws + w.out_f32);
-  float *lse = reinterpret_cast<float *>(ws + w.lse);
-  float *records = reinterpret_cast<float *>(ws + w.records);
+  if (workspace_bytes < shared_workspace_bytes(*h, num_seqs, num_heads, head_dim, sh.nctas)) return PA_ERR_WORKSPACE;
+  float *records = static_cast<float *>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  // 1. shared blocks, once per group of sharers
+  // 1. every group's blocks: the shared runs once per group of sharers, and
+  // each sequence's own blocks
   SharedArgs sa;
   sa.q = q;
   sa.tables = block_tables;
+  sa.lens = context_lens;
   sa.plan = plan_dev;
   sa.h = *h;
   sa.num_blocks = num_blocks;
@@ -462,8 +453,6 @@ extern "C" pa_status pa_decode_shared(void *out, const void *q, const void *k_ca
   const size_t ring = size_t(sa.nstage) * sa.slot_stride;
   MergeArgs ma;
   ma.out = out;
-  ma.out_f32 = out_f32;
-  ma.lse = lse;
   ma.records = records;
   ma.plan = plan_dev;
   ma.h = *h;
@@ -474,18 +463,7 @@ extern "C" pa_status pa_decode_shared(void *out, const void *q, const void *k_ca
                           : shared_step<__half>(sa, k_cache, v_cache, dtype, head_dim, ring, s);
     if (st != PA_OK) return st;
   }
-  // 2. each sequence's own blocks: fp32 rows and their log2-sum-exp; launched
-  // as a programmatic dependent of step 1, so its CTAs set up while step 1's
-  // last CTAs finish.  It needs nothing from step 1, but every CTA with tiles
-  // waits for step 1 before its first copy, so step 2 ends after step 1 and
-  // step 3 sees both; with no own tiles at all no CTA would wait, so then it
-  // is launched normally.
-  st = decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_heads,
-                   num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace, w.out_f32, debug_err,
-                   stream, plan_dev + h->s_start, out_f32, lse, nullptr, nullptr,
-                   h->num_pieces > 0 && h->own_tiles != 0);
-  if (st != PA_OK) return st;
-  // 3. merge
+  // 2. merge
   return dtype == PA_BF16 ? merge_step<__nv_bfloat16>(ma, head_dim, s) : merge_step<__half>(ma, head_dim, s);
 }
 

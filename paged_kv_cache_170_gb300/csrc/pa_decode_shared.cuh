@@ -1,24 +1,23 @@
 // pa_decode_shared.cuh -- the two kernels of the shared-block decode:
 //
-// decode_shared_mma_kernel (step 1): every group's shared blocks against the
-//   query rows of all its members.  A CTA walks its pieces (plan: c_poff) in
-//   order; one producer warp streams each piece's K and V tiles into a ring by
-//   TMA.  The four consumer warps take the unit's pass of up to 32 query rows
-//   (row = member * G + head) as wr row-warps of 8 rows times 4 / wr
-//   tile-lanes: with 32 rows all four warps work on every tile, so a tile read
-//   once serves 32 rows of up to 32 sequences; with 8 rows each warp takes
-//   every fourth tile, and the tile-lanes' states are combined in shared
-//   memory at the piece's end.  Each piece leaves one partial state (acc, m,
-//   l) per row of its pass in `records`.
+// decode_shared_mma_kernel (step 1): every group's blocks against the query
+//   rows of all its members: the shared groups' runs of full blocks, and each
+//   sequence's own group (its private blocks, the last one partly filled).  A
+//   CTA walks its pieces (plan: c_poff) in order; one producer warp streams
+//   each piece's K and V tiles into a ring by TMA.  The four consumer warps
+//   take the unit's pass of up to 32 query rows (row = member * G + head) as
+//   wr row-warps of 8 rows times 4 / wr tile-lanes: with 32 rows all four
+//   warps work on every tile, so a tile read once serves 32 rows of up to 32
+//   sequences; with 8 rows (every own group) each warp takes every fourth
+//   tile, and the tile-lanes' states are combined in shared memory at the
+//   piece's end.  Each piece leaves one partial state (acc, m, l) per row of
+//   its pass in `records`.
 //   Every consumer waits for every entry in order, so the ring's mbarrier
 //   parity waits are exact (no warp can lag a full ring behind another).
 //
-// merge_shared_kernel (step 3): per output row (s, h), the row the
-//   split-context decode computed over the sequence's own blocks (fp32 o and
-//   its log2-sum-exp) and the partial states of every piece of every group s
-//   belongs to, merged with a running maximum:
-//     M = max_i m_i;  out = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i,
-//   where the own-block row enters as acc = o, m = lse, l = 1.
+// merge_shared_kernel (step 2): per output row (s, h), the partial states of
+//   every piece of every group s belongs to, merged with a running maximum:
+//     M = max_i m_i;  out = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i.
 #pragma once
 
 #include "pa_mma_tile.cuh"
@@ -30,6 +29,7 @@ namespace pagedkv {
 struct SharedArgs {
   const void *q;
   const int32_t *tables;
+  const int32_t *lens;  // context lengths (the own groups' last blocks may be partly filled)
   const int32_t *plan;  // device copy of the plan
   SharePlanHeader h;    // its header
   int64_t num_blocks;
@@ -47,6 +47,33 @@ constexpr int kSharedThreads = (kConsumerWarps + 1) * 32;
 __host__ __device__ __forceinline__ int share_row_warps(int rows) { return rows <= 8 ? 1 : (rows <= 16 ? 2 : 4); }
 constexpr int kRingBytesShared = 88 * 1024;  // ring of K + V tile pairs
 
+// A piece's descriptor (three 16-byte loads through the read-only path).
+__device__ __forceinline__ PieceDesc load_piece(const int32_t *plan, int desc_off, int p) {
+  const int4 *d = reinterpret_cast<const int4 *>(plan + desc_off) + 3 * p;
+  const int4 x = __ldg(d), y = __ldg(d + 1), z = __ldg(d + 2);
+  PieceDesc r;
+  r.unit = x.x; r.t0 = x.y; r.t1 = x.z; r.group = x.w;
+  r.kvh = y.x; r.pass = y.y; r.leader = y.z; r.blk0 = y.w;
+  r.moff = z.x; r.rows = z.y; r.prows = z.z; r.own = z.w;
+  return r;
+}
+
+// The CTA's pieces in the order it works them: those of own units (short,
+// their start latency overlaps the ring filling up), then those of shared units.
+struct PieceList {
+  int o0, no, s0, n;
+  __device__ __forceinline__ int at(int k) const { return k < no ? o0 + k : s0 + (k - no); }
+};
+
+__device__ __forceinline__ PieceList cta_pieces(const int32_t *P, const SharePlanHeader &h) {
+  PieceList l;
+  l.o0 = P[h.c_opoff + blockIdx.x];
+  l.no = P[h.c_opoff + blockIdx.x + 1] - l.o0;
+  l.s0 = P[h.c_poff + blockIdx.x];
+  l.n = l.no + P[h.c_poff + blockIdx.x + 1] - l.s0;
+  return l;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
     decode_shared_mma_kernel(const SharedArgs a, const __grid_constant__ CUtensorMap map_k,
@@ -61,9 +88,6 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
   __shared__ int sh_abort;
   __shared__ __align__(16) float st[kConsumerWarps][8][R];  // tile-lane states of a piece's rows
 
-  // the own-block decode that follows may start launching now (it waits for
-  // this grid before its first copy)
-  launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int32_t *P = a.plan;
@@ -88,7 +112,7 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
   }
   __syncthreads();
 
-  const int p0 = P[h.c_poff + blockIdx.x], p1 = P[h.c_poff + blockIdx.x + 1];
+  const PieceList pl = cta_pieces(P, h);
   const uint32_t tile_bytes = uint32_t(B) * D * 2;
 
   if (warp == kConsumerWarps) {
@@ -99,19 +123,17 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
     }
     uint32_t e = 0;
     bool aborted = false;
-    for (int p = p0; p < p1 && !aborted; ++p) {
-      const int u = P[h.p_unit + p];
-      const int t0 = P[h.p_t0 + p], t1 = P[h.p_t1 + p];
-      const int g = P[h.u_group + u];
-      const int kvh = P[h.u_kvh + u];
-      const int leader = P[h.g_members + P[h.g_moff + g]];
-      const int32_t *trow = a.tables + (long long)leader * a.max_blocks + P[h.g_b0 + g] + t0;
-      const int n = t1 - t0;
+    PieceDesc nxt = pl.n > 0 ? load_piece(P, h.p_desc, pl.at(0)) : PieceDesc{};
+    for (int k = 0; k < pl.n && !aborted; ++k) {
+      const PieceDesc d = nxt;
+      if (k + 1 < pl.n) nxt = load_piece(P, h.p_desc, pl.at(k + 1));  // the next piece's, while this one streams
+      const int32_t *trow = a.tables + (long long)d.leader * a.max_blocks + d.blk0;
+      const int n = d.t1 - d.t0;
       for (int base = 0; base < n && !aborted; base += 32) {
         const int cnt = min(32, n - base);
         const int pid_cur = lane < cnt ? trow[base + lane] : -1;
-        for (int k = 0; k < cnt; k += a.pg) {
-          const int t = k + lane;
+        for (int kk = 0; kk < cnt; kk += a.pg) {
+          const int t = kk + lane;
           const int pid = __shfl_sync(kFullMask, pid_cur, t < 32 ? t : 31);
           bool fail = false;
           if (lane < a.pg && t < cnt) {
@@ -127,7 +149,7 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
             } else {
               mbar_arrive_expect_tx(&full_bar[slot], 2 * tile_bytes);
               unsigned char *dst = ring + size_t(slot) * a.slot_stride;
-              const int y = (pid * a.Hkv + kvh) * B;
+              const int y = (pid * a.Hkv + d.kvh) * B;
               if (HALVES == 2 && a.nops == 1) {
                 tma_load_3d(dst, &map_k, 0, y, 0, &full_bar[slot]);
                 tma_load_3d(dst + a.tile_stride, &map_v, 0, y, 0, &full_bar[slot]);
@@ -149,7 +171,7 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
             }
             break;
           }
-          e += uint32_t(min(a.pg, cnt - k));
+          e += uint32_t(min(a.pg, cnt - kk));
         }
       }
     }
@@ -176,30 +198,36 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
 #ifdef PA_TRACE
   long long tr_c0 = clock64(), tr_setup = 0, tr_wait = 0, tr_math = 0, tr_end = 0, tr_tiles = 0;
 #endif
-  for (int p = p0; p < p1; ++p) {
+  PieceDesc nxt = pl.n > 0 ? load_piece(P, h.p_desc, pl.at(0)) : PieceDesc{};
+  for (int k = 0; k < pl.n; ++k) {
 #ifdef PA_TRACE
     const long long tr_p0 = clock64();
 #endif
-    const int u = P[h.p_unit + p];
-    const int t0 = P[h.p_t0 + p];
-    const int n = P[h.p_t1 + p] - t0;
-    const int g = P[h.u_group + u];
-    const int kvh = P[h.u_kvh + u];
-    const int moff = P[h.g_moff + g];
-    const int rows = (P[h.g_moff + g + 1] - moff) * Gq;
+    const PieceDesc d = nxt;
+    const int p = pl.at(k);
+    if (k + 1 < pl.n) nxt = load_piece(P, h.p_desc, pl.at(k + 1));  // the next piece's, while this one runs
+    const int n = d.t1 - d.t0;
     // wr row-warps cover the pass's rows (8 each); the 4 / wr tile-lanes take
     // every (4 / wr)-th tile, so a pass of few rows still keeps all warps busy
-    const int prow = P[h.u_pass + u] * kSharePassRows;
-    const int wr = share_row_warps(rows - prow);
+    const int prow = d.pass * d.prows;
+    const int wr = share_row_warps(min(d.prows, d.rows - prow));
     const int rw = warp % wr, tl = warp / wr, nl = kConsumerWarps / wr;
     const int rb = prow + rw * 8;  // this warp's first row
-    const int myrows = tl < nl ? max(0, min(8, rows - rb)) : 0;
+    const int myrows = tl < nl ? max(0, min(8, d.rows - rb)) : 0;
+    // an own group's last block may be partly filled: its tokens end at L
+    // (its pass has at most 8 rows, so one warp computes each of its tiles)
+    int L = 0;
+    if (d.own) {
+      const int cap = a.max_blocks * B;
+      L = a.lens[d.leader];
+      L = L < 0 ? 0 : (L > cap ? cap : L);
+    }
 
     uint32_t qf[KS][2];
     if (g8 < myrows) {
       const int r = rb + g8;
-      const int seq = P[h.g_members + moff + r / Gq];
-      const T *qrow = static_cast<const T *>(a.q) + ((long long)seq * a.Hq + kvh * Gq + r % Gq) * D;
+      const int seq = d.own ? d.leader : P[h.g_members + d.moff + r / Gq];
+      const T *qrow = static_cast<const T *>(a.q) + ((long long)seq * a.Hq + d.kvh * Gq + r % Gq) * D;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         qf[ks][0] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c4);
@@ -235,8 +263,24 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
       const long long tr_m0 = clock64();
       tr_wait += tr_m0 - tr_w0;
 #endif
-      if (ok && myrows > 0 && t % nl == tl) {  // shared blocks are full: B valid rows
-        mma_tile<T, D>(a, kt, kt + a.tile_stride, B, B, qf, a.qscale, m0, m1, l0, l1, o, lane, ring_addr,
+      if (ok && myrows > 0 && t % nl == tl) {
+        // shared blocks are full; an own group's last block holds L - blk * B tokens
+        const int nv = d.own ? min(B, L - (d.blk0 + t) * B) : B;
+        const int padded = ((nv + 15) >> 4) * 16;
+        if (nv < padded) {
+          // rows past the context in the last 16-row group: zero them so a zero
+          // weight never meets stale data (then order these writes before the
+          // slot's next bulk copy)
+          for (int i = lane; i < (padded - nv) * HALVES * 8; i += 32) {
+            const int r = nv + i / (HALVES * 8), hc = i % (HALVES * 8);
+            const uint32_t zo = uint32_t(slot) * a.slot_stride + a.tile_stride + uint32_t((hc >> 3) * B * 128 +
+                                                                                       r * 128 + (hc & 7) * 16);
+            *reinterpret_cast<uint4 *>(ring + zo) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_shared();
+          __syncwarp();
+        }
+        mma_tile<T, D>(a, kt, kt + a.tile_stride, B, nv, qf, a.qscale, m0, m1, l0, l1, o, lane, ring_addr,
                        ring_end);
 #ifdef PA_TRACE
         o[0][0] = __shfl_sync(kFullMask, o[0][0], lane);
@@ -338,14 +382,12 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
 #ifdef PA_TRACE
   if (lane == 0 && PA_TRACE_CTA(blockIdx.x))
     printf("trace shared cta %d warp %d: pieces %d tiles %lld cycles %lld setup %lld wait %lld math %lld end %lld\n",
-           blockIdx.x, warp, p1 - p0, tr_tiles, clock64() - tr_c0, tr_setup, tr_wait, tr_math, tr_end);
+           blockIdx.x, warp, pl.n, tr_tiles, clock64() - tr_c0, tr_setup, tr_wait, tr_math, tr_end);
 #endif
 }
 
 struct MergeArgs {
   void *out;             // [S][Hq][D], element type T
-  const float *out_f32;  // [S][Hq][D] the own-block rows, normalised
-  const float *lse;      // [S][Hq] their log2-sum-exp (-inf: no own tokens)
   const float *records;  // step 1's partial states
   const int32_t *plan;
   SharePlanHeader h;
@@ -369,18 +411,17 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_shared_kernel(const Me
   const int Gq = h.group_size;
   const int kvh = hq / Gq, hh = hq % Gq;
 
-  float M = a.lse[row];
-  const bool own = M > -CUDART_INF_F;
-  float den = own ? 1.f : 0.f;
+  float M = -CUDART_INF_F, den = 0.f;
   float num[V];
 #pragma unroll
-  for (int v = 0; v < V; ++v) num[v] = own ? a.out_f32[row * D + lane * V + v] : 0.f;
+  for (int v = 0; v < V; ++v) num[v] = 0.f;
   for (int k = P[h.s_moff + s]; k < P[h.s_moff + s + 1]; ++k) {
     const int g = P[h.s_mgroup + k];
     const int r = P[h.s_midx + k] * Gq + hh;
-    const int u = P[h.g_ubase + g] + kvh * P[h.g_passes + g] + r / kSharePassRows;
+    const int prows = P[h.g_prows + g];
+    const int u = P[h.g_ubase + g] + kvh * P[h.g_passes + g] + r / prows;
     for (int p = P[h.u_poff + u]; p < P[h.u_poff + u + 1]; ++p) {
-      const float *rec = a.records + ((long long)p * kSharePassRows + r % kSharePassRows) * R;
+      const float *rec = a.records + ((long long)p * kSharePassRows + r % prows) * R;
       const float m = __ldcg(rec + D), l = __ldcg(rec + D + 1);
       float acc[V];
 #pragma unroll

@@ -15,12 +15,13 @@
 // copy-on-write makes it private before it is written anyway).  The group
 // then splits again at the index where its members' ids diverge.  A sequence
 // leaves the trie at its private start block: blocks from there on are its
-// own, and the split-context decode reads them.
+// own.  They form the sequence's own group (one member, its blocks from the
+// private start to the last, partly filled one), read by the same kernel.
 //
 // The group work is laid out for the shared kernel: a unit is (group, kv
-// head, pass), a pass being up to 32 query rows of the group (rows are
-// member-major: row = member * G + head in the kv head's group of G); a
-// unit's tiles are the group's blocks.  All units' tiles are cut into nctas
+// head, pass), a pass being up to 32 query rows of a shared group, or 8 of
+// an own group (rows are member-major: row = member * G + head in the kv
+// head's group of G); a unit's tiles are the group's blocks.  All units' tiles are cut into nctas
 // contiguous ranges of equal cost (a tile costs its unit's row-warps), one
 // per CTA, and a piece is the part of one unit inside one CTA's range.  Each
 // piece leaves one partial state per row.
@@ -41,6 +42,7 @@ using pagedkv::SharePlanHeader;
 struct Group {
   std::vector<int32_t> members;  // sequence ids, increasing
   int b0, b1;                    // logical blocks [b0, b1) shared by all members
+  bool own = false;              // one sequence's private blocks (the last may be partly filled)
 };
 
 }  // namespace
@@ -115,15 +117,31 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
   std::sort(groups.begin(), groups.end(), [](const Group &x, const Group &y) {
     return x.members[0] != y.members[0] ? x.members[0] < y.members[0] : x.b0 < y.b0;
   });
+  const int num_shared = int(groups.size());
+  // own groups: each sequence's blocks past its private start, in sequence order
+  for (int s = 0; s < S; ++s) {
+    long long L = context_lens[s];
+    L = L < 0 ? 0 : (L > cap ? cap : L);
+    const int nb = int((L + B - 1) / B);
+    if (nb > start[s]) {
+      Group g;
+      g.members.push_back(s);
+      g.b0 = start[s];
+      g.b1 = nb;
+      g.own = true;
+      groups.push_back(std::move(g));
+    }
+  }
 
   // ---- units and pieces
   const int G = int(groups.size());
   long long total_members = 0;
-  std::vector<int32_t> ubase(G), passes(G);
+  std::vector<int32_t> ubase(G), passes(G), prows(G);
   int U = 0;
   for (int g = 0; g < G; ++g) {
     total_members += groups[g].members.size();
-    passes[g] = int((groups[g].members.size() * Gq + kSharePassRows - 1) / kSharePassRows);
+    prows[g] = groups[g].own ? kOwnPassRows : kSharePassRows;
+    passes[g] = int((groups[g].members.size() * Gq + prows[g] - 1) / prows[g]);
     ubase[g] = U;
     U += Hkv * passes[g];
   }
@@ -142,49 +160,57 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
   // 32-row tile, but take separate tiles of an 8-row unit, while every warp
   // still steps through every tile of the CTA.  Measured on a GB300, a 32-row
   // tile takes about 1.7x the CTA time of an 8-row one; the weights below
-  // (5, 4, 3 for 32, 16, 8 rows) follow that.  CTA ranges split the total
-  // cost evenly, at tile boundaries.
-  std::vector<long long> ucost(U), wpos(U + 1, 0);
+  // (5, 4, 3 for 32, 16, 8 rows) follow that.  A unit also costs kUnitCost
+  // once (its q rows and plan entries are loaded, its states handed over).
+  std::vector<long long> ucost(U);
   for (int u = 0; u < U; ++u) {
     const int g = ugroup[u];
-    const long long rows = (long long)groups[g].members.size() * Gq - (long long)upass[u] * kSharePassRows;
+    const long long rows = std::min<long long>(prows[g], (long long)groups[g].members.size() * Gq -
+                                                             (long long)upass[u] * prows[g]);  // rows of this pass
     ucost[u] = rows <= 8 ? 3 : (rows <= 16 ? 4 : 5);
     utile0[u + 1] = utile0[u] + (groups[g].b1 - groups[g].b0);
-    wpos[u + 1] = wpos[u] + (utile0[u + 1] - utile0[u]) * ucost[u];
   }
-  const long long W = utile0[U], Wc = wpos[U];
-  // first tile (flattened) of CTA c: the first tile whose cost starts at or
-  // after c * Wc / nctas
-  std::vector<long long> cstart(nctas + 1, W);
-  {
-    int u = 0;
+  // Two cost lines, each cut evenly over the CTAs at tile boundaries: the
+  // shared groups' units, then the own groups' units (so that every CTA gets
+  // its share of the many short own units, not a few CTAs all of them).  A
+  // piece is the part of one unit inside one CTA's range of one line; the
+  // pieces of a unit are consecutive.
+  std::vector<int32_t> punit, pt0, pt1, cpoff(nctas + 1, 0), copoff(nctas + 1, 0), upoff(U + 1, 0);
+  auto split = [&](int ua, int ub, std::vector<int32_t> &coff) {
+    std::vector<long long> wp(size_t(ub - ua) + 1, 0);  // cost before each unit of the line
+    for (int u = ua; u < ub; ++u)
+      wp[u - ua + 1] = wp[u - ua] + kUnitCost + (utile0[u + 1] - utile0[u]) * ucost[u];
+    const long long Wc = wp[ub - ua];
+    std::vector<long long> cs(nctas + 1, utile0[ub]);  // first (flattened) tile of each CTA
+    int i = 0;
     for (int c = 0; c < nctas; ++c) {
       const long long target = (long long)c * Wc / nctas;
-      while (u < U && wpos[u + 1] <= target) ++u;
-      if (u == U) break;
-      const long long t = (target - wpos[u] + ucost[u] - 1) / ucost[u];
-      cstart[c] = utile0[u] + std::min(t, utile0[u + 1] - utile0[u]);
+      while (ua + i < ub && wp[i + 1] <= target) ++i;
+      if (ua + i == ub) break;
+      const int u = ua + i;
+      const long long rel = target - wp[i] - kUnitCost;
+      const long long t = rel <= 0 ? 0 : (rel + ucost[u] - 1) / ucost[u];
+      cs[c] = utile0[u] + std::min(t, utile0[u + 1] - utile0[u]);
     }
-    for (int c = nctas - 1; c >= 0; --c) cstart[c] = std::min(cstart[c], cstart[c + 1]);
-  }
-  std::vector<int32_t> punit, pt0, pt1, cpoff(nctas + 1, 0), upoff(U + 1, 0);
-  {
-    int u = 0;
+    for (int c = nctas - 1; c >= 0; --c) cs[c] = std::min(cs[c], cs[c + 1]);
+    int u = ua;
     for (int c = 0; c < nctas; ++c) {
-      cpoff[c] = int(punit.size());
-      const long long w0 = cstart[c], w1 = cstart[c + 1];
-      long long w = w0;
-      while (w < w1) {
+      coff[c] = int(punit.size());
+      long long w = cs[c];
+      while (w < cs[c + 1]) {
         while (utile0[u + 1] <= w) ++u;
-        const long long e = std::min(w1, utile0[u + 1]);
+        const long long e = std::min(cs[c + 1], utile0[u + 1]);
         punit.push_back(u);
         pt0.push_back(int32_t(w - utile0[u]));
         pt1.push_back(int32_t(e - utile0[u]));
         w = e;
       }
     }
-    cpoff[nctas] = int(punit.size());
-  }
+    coff[nctas] = int(punit.size());
+  };
+  const int Us = num_shared < G ? ubase[num_shared] : U;  // the own groups' units follow the shared ones
+  split(0, Us, cpoff);
+  split(Us, U, copoff);
   const int P = int(punit.size());
   for (int p = 0; p < P; ++p) upoff[punit[p] + 1] = p + 1;  // pieces of a unit are consecutive
   for (int u = 0; u < U; ++u) upoff[u + 1] = std::max(upoff[u + 1], upoff[u]);
@@ -248,18 +274,18 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
   place(h.s_moff, S + 1);
   place(h.s_mgroup, TMS);
   place(h.s_midx, TMS);
+  place(h.g_prows, G);
+  place(h.c_opoff, nctas + 1);
+  off = (off + 3) / 4 * 4;  // the descriptors are read as 16-byte vectors
+  place(h.p_desc, (long long)P * kPieceDescInts);
   if (off > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   h.total_ints = int32_t(off);
   *plan_ints = size_t(off);
   if (plan == nullptr) return PA_OK;  // size query
   if (plan_capacity < size_t(off)) return PA_ERR_WORKSPACE;
 
-  h.own_tiles = 0;
-  for (int s = 0; s < S; ++s) {
-    long long L = context_lens[s];
-    L = L < 0 ? 0 : (L > cap ? cap : L);
-    if (L > (long long)start[s] * B) h.own_tiles = 1;
-  }
+  h.num_shared_groups = num_shared;
+  h.own_tiles = G > num_shared ? 1 : 0;
   memcpy(plan, &h, sizeof(h));
   auto put = [&](int32_t at, const int32_t *src, long long n) {
     if (n > 0) memcpy(plan + at, src, size_t(n) * sizeof(int32_t));
@@ -292,5 +318,35 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
   put(h.s_moff, smoff.data(), S + 1);
   put(h.s_mgroup, smgroup.data(), TMS);
   put(h.s_midx, smidx.data(), TMS);
+  put(h.g_prows, prows.data(), G);
+  put(h.c_opoff, copoff.data(), nctas + 1);
+  {
+    // one descriptor per piece: what the kernel needs at a piece's start, in
+    // three 16-byte loads (see PieceDesc)
+    std::vector<int32_t> gm(G);  // each group's first member in g_members (as g_moff)
+    long long mo = 0;
+    for (int g = 0; g < G; ++g) {
+      gm[g] = int32_t(mo);
+      mo += groups[g].members.size();
+    }
+    std::vector<int32_t> d(size_t(P) * kPieceDescInts, 0);
+    for (int p = 0; p < P; ++p) {
+      const int u = punit[p], g = ugroup[u];
+      int32_t *e = &d[size_t(p) * kPieceDescInts];
+      e[0] = u;
+      e[1] = pt0[p];
+      e[2] = pt1[p];
+      e[3] = g;
+      e[4] = ukvh[u];
+      e[5] = upass[u];
+      e[6] = groups[g].members[0];
+      e[7] = groups[g].b0 + pt0[p];
+      e[8] = gm[g];
+      e[9] = int32_t(groups[g].members.size()) * Gq;
+      e[10] = prows[g];
+      e[11] = groups[g].own ? 1 : 0;
+    }
+    put(h.p_desc, d.data(), (long long)d.size());
+  }
   return PA_OK;
 }

@@ -4,12 +4,17 @@
 // field below holds the array's offset in ints from the start of the plan).
 //   groups    g_moff[G+1], g_members[total_members] (sequence ids), logical
 //             block run g_b0[G] .. g_b1[G] (exclusive), g_ubase[G] (first
-//             unit), g_passes[G] (passes of up to 32 rows per kv head); a
-//             group has two or more members and shares only full blocks
+//             unit), g_passes[G] (passes per kv head), g_prows[G] (query rows
+//             of a pass).  The first num_shared_groups groups are shared: two
+//             or more members, full blocks only, 32-row passes.  The rest are
+//             own groups: one sequence's blocks from its private start to its
+//             last (partly filled) block, 8-row passes
 //   units     u_group[U], u_kvh[U], u_pass[U], u_poff[U+1] (its pieces);
 //             unit = g_ubase[g] + kv_head * g_passes[g] + pass
 //   pieces    p_unit[P], p_t0[P], p_t1[P] (tiles of the unit's run),
-//             c_poff[nctas+1] (pieces of each CTA)
+//             c_poff[nctas+1] (each CTA's pieces of shared units),
+//             c_opoff[nctas+1] (its pieces of own units), p_desc[P] (one
+//             PieceDesc per piece, 16-byte aligned)
 //   sequences s_start[S] (first private block), s_moff[S+1], s_mgroup[...],
 //             s_midx[...] (each membership: group, index among its members)
 #pragma once
@@ -19,7 +24,23 @@
 namespace pagedkv {
 
 constexpr int32_t kSharePlanMagic = 0x50534b50;  // "PKSP"
-constexpr int kSharePassRows = 32;               // query rows of one pass: 4 warps x 8
+constexpr int kSharePassRows = 32;               // query rows of a shared group's pass: 4 warps x 8
+constexpr int kOwnPassRows = 8;                  // query rows of an own group's pass: one warp
+constexpr int kUnitCost = 8;                     // fixed cost of a unit in the CTA split (tile costs are 3..5)
+
+// What a CTA needs at the start of a piece, in one record of the plan.
+struct PieceDesc {
+  int32_t unit, t0, t1;      // tiles [t0, t1) of the unit's run
+  int32_t group, kvh, pass;  // the unit
+  int32_t leader;            // the group's first member (its table row holds the run)
+  int32_t blk0;              // logical block of tile t0
+  int32_t moff;              // the group's first member in g_members
+  int32_t rows;              // the group's query rows: members * G
+  int32_t prows;             // rows of a pass
+  int32_t own;               // 1 for an own group (its last block may be partly filled)
+};
+constexpr int kPieceDescInts = int(sizeof(PieceDesc) / sizeof(int32_t));
+static_assert(sizeof(PieceDesc) == 48, "three 16-byte loads");
 
 struct SharePlanHeader {
   int32_t magic, total_ints;
@@ -30,7 +51,10 @@ struct SharePlanHeader {
   int32_t u_group, u_kvh, u_pass, u_poff;
   int32_t p_unit, p_t0, p_t1, c_poff;
   int32_t s_start, s_moff, s_mgroup, s_midx;
-  int32_t own_tiles;  // 1 when some sequence has tokens past its shared blocks (the own-block decode has work)
+  int32_t own_tiles;          // 1 when some sequence has tokens past its shared blocks (an own group exists)
+  int32_t num_shared_groups;  // groups 0 .. num_shared_groups-1 are shared, the rest own
+  int32_t g_prows;            // offset of g_prows[G]
+  int32_t c_opoff, p_desc;    // offsets of c_opoff[nctas+1] and p_desc[P]
 };
 
 constexpr int kSharePlanHeaderInts = int(sizeof(SharePlanHeader) / sizeof(int32_t));
@@ -39,6 +63,9 @@ static_assert(sizeof(SharePlanHeader) % sizeof(int32_t) == 0, "int32 fields only
 }  // namespace pagedkv
 
 // The unqualified names the planner uses.
+using pagedkv::kOwnPassRows;
+using pagedkv::kPieceDescInts;
+using pagedkv::kUnitCost;
 using pagedkv::kSharePassRows;
 using pagedkv::kSharePlanHeaderInts;
 using pagedkv::kSharePlanMagic;

@@ -258,7 +258,8 @@ def pa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
 PLAN_FIELDS = ["magic", "total_ints", "num_seqs", "num_groups", "num_units", "num_pieces", "nctas", "group_size",
                "num_kv_heads", "block_size", "max_blocks", "total_members", "total_memberships", "g_moff",
                "g_members", "g_b0", "g_b1", "g_ubase", "g_passes", "u_group", "u_kvh", "u_pass", "u_poff", "p_unit",
-               "p_t0", "p_t1", "c_poff", "s_start", "s_moff", "s_mgroup", "s_midx", "own_tiles"]
+               "p_t0", "p_t1", "c_poff", "s_start", "s_moff", "s_mgroup", "s_midx", "own_tiles", "num_shared_groups",
+               "g_prows", "c_opoff", "p_desc"]
 
 
 def share_plan(block_tables: torch.Tensor, context_lens: torch.Tensor, block_size: int, num_heads: int,
@@ -289,7 +290,8 @@ def plan_fields(plan: torch.Tensor) -> dict:
          "u_group": hdr["num_units"], "u_kvh": hdr["num_units"], "u_pass": hdr["num_units"],
          "u_poff": hdr["num_units"] + 1, "p_unit": hdr["num_pieces"], "p_t0": hdr["num_pieces"],
          "p_t1": hdr["num_pieces"], "c_poff": hdr["nctas"] + 1, "s_start": hdr["num_seqs"],
-         "s_moff": hdr["num_seqs"] + 1, "s_mgroup": hdr["total_memberships"], "s_midx": hdr["total_memberships"]}
+         "s_moff": hdr["num_seqs"] + 1, "s_mgroup": hdr["total_memberships"], "s_midx": hdr["total_memberships"],
+         "g_prows": hdr["num_groups"], "c_opoff": hdr["nctas"] + 1, "p_desc": hdr["num_pieces"] * 12}
     out = dict(hdr)
     for k, cnt in n.items():
         out[k + "_arr"] = p[hdr[k]:hdr[k] + cnt]

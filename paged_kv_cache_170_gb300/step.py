@@ -118,8 +118,8 @@ class DecodeStep:
             self.plan_dev = self.plan.to(dev)
             self.plan_info = {k: v for k, v in ops.plan_fields(self.plan).items() if not k.endswith("_arr")}
             self.workspace = ops.new_shared_workspace(self.plan, S, Hq, Hkv, D, dev)
-            if self.plan_info["num_groups"] > 0:
-                decode_launches = 3  # shared blocks, own blocks, merge
+            if self.plan_info["num_shared_groups"] > 0:
+                decode_launches = 2  # every group's blocks, then the merge
         else:
             self.workspace = ops.new_workspace(S, Hq, Hkv, D, dev)
         self.slots = torch.empty(inp.new_seq.numel(), dtype=torch.int64, device=dev)

@@ -128,6 +128,23 @@ def test_shared_decode_edge_cases(ops, dtype):
         assert_attention_close(out, ref, strict=False)
 
 
+@pytest.mark.parametrize("B", [16, 32])
+def test_shared_decode_own_groups_of_two_passes(ops, B):
+    """16 query heads per kv head: a sequence's own blocks are read in two
+    8-row passes; partly filled last blocks of every length mod B."""
+    S, Hq, Hkv, D = 6, 32, 2, 128
+    NB = 80
+    q, kc, vc = _random_pool(S, Hq, Hkv, D, B, NB, torch.bfloat16, seed=B)
+    shared = list(range(4))
+    tables = torch.tensor([shared + list(range(10 + 8 * i, 18 + 8 * i)) for i in range(S)], dtype=torch.int32)
+    lens = torch.tensor([4 * B + 1, 4 * B + B - 1, 6 * B, 5 * B + 7, 4 * B, 2 * B + 3], dtype=torch.int32)
+    scale = 1.0 / math.sqrt(D)
+    out, f = _shared(ops, *[x.to(DEV) for x in (q, kc, vc, tables, lens)], scale)
+    assert f["num_shared_groups"] >= 1 and f["num_groups"] > f["num_shared_groups"]
+    ref = native.decode(q, kc, vc, tables.numpy(), lens.numpy(), scale)
+    assert_attention_close(out, ref, strict=False)
+
+
 def test_shared_decode_deterministic_reusable_workspace_and_no_group_plan(ops):
     cpu = _small("prefix", seed=1)
     inp = cpu.to(DEV)
@@ -144,7 +161,7 @@ def test_shared_decode_deterministic_reusable_workspace_and_no_group_plan(ops):
     # tables without sharing: the plan has no groups and the call is pa_decode
     g = W.make_inputs(W.scaled(W.GQA, num_seqs=3, num_blocks=3 * 256 + 5), 0).to(DEV)
     out, f = _shared(ops, g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale)
-    assert f["num_groups"] == 0
+    assert f["num_shared_groups"] == 0
     plain = ops.pa_decode(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale)
     torch.cuda.synchronize()
     assert torch.equal(out, plain)

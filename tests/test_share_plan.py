@@ -2,9 +2,10 @@
 
 Structural checks of the plan against the block tables it was built from,
 and a float64 numpy walk through the plan -- partial states per piece and
-row, the private part per sequence, then the merge -- that must reproduce
-the oracle's decode: the plan's split of the work is complete and does not
-overlap.  (The GPU tests then check the kernels that follow the plan.)
+row (shared groups, and each sequence's own group of private blocks), then
+the merge -- that must reproduce the oracle's decode: the plan's split of the
+work is complete and does not overlap.  (The GPU tests then check the
+kernels that follow the plan.)
 """
 import math
 
@@ -17,7 +18,8 @@ from paged_kv_cache_170_gb300 import build, scenarios
 from paged_kv_cache_170_gb300 import workloads as W
 from paged_kv_cache_170_gb300.block_manager import BlockManager
 
-PASS_ROWS = 32
+PASS_ROWS = 32  # query rows of a shared group's pass
+OWN_PASS_ROWS = 8  # of an own group's pass
 
 
 @pytest.fixture(scope="module")
@@ -80,10 +82,20 @@ def _check_structure(f, tables, lens, B, Hq, Hkv):
     moff, mem = f["g_moff_arr"], f["g_members_arr"]
     b0, b1 = f["g_b0_arr"], f["g_b1_arr"]
     start = f["s_start_arr"]
+    nsg = f["num_shared_groups"]
+    own_of = {}
     for g in range(f["num_groups"]):
         members = mem[moff[g]:moff[g + 1]]
-        assert len(members) >= 2 and list(members) == sorted(set(members))
         assert 0 <= b0[g] < b1[g]
+        if g >= nsg:  # own group: one sequence's private blocks, to its last (partial) block
+            assert len(members) == 1 and members[0] not in own_of
+            s = members[0]
+            own_of[s] = g
+            assert (b0[g], b1[g]) == (start[s], nb[s])
+            assert f["g_prows_arr"][g] == OWN_PASS_ROWS
+            assert f["g_passes_arr"][g] == -(-Gq // OWN_PASS_ROWS)
+            continue
+        assert len(members) >= 2 and list(members) == sorted(set(members))
         for s in members:
             assert full[s] >= b1[g], "a group block must be full for every member"
             assert np.array_equal(tables[s, b0[g]:b1[g]], tables[members[0], b0[g]:b1[g]])
@@ -91,8 +103,12 @@ def _check_structure(f, tables, lens, B, Hq, Hkv):
         e = b1[g]
         extendable = all(full[s] > e for s in members) and len({int(tables[s, e]) for s in members}) == 1
         assert not extendable, f"group {g} could extend past block {e}"
+        assert f["g_prows_arr"][g] == PASS_ROWS
         assert f["g_passes_arr"][g] == -(-len(members) * Gq // PASS_ROWS)
-    # memberships of each sequence chain from block 0 to its private start
+    # every sequence with tokens past its shared blocks has its own group
+    assert set(own_of) == {s for s in range(S) if nb[s] > start[s]}
+    assert f["own_tiles"] == int(bool(own_of))
+    # memberships of each sequence chain from block 0 to its last block
     for s in range(S):
         ks = range(f["s_moff_arr"][s], f["s_moff_arr"][s + 1])
         runs = sorted((b0[f["s_mgroup_arr"][k]], b1[f["s_mgroup_arr"][k]]) for k in ks)
@@ -100,7 +116,7 @@ def _check_structure(f, tables, lens, B, Hq, Hkv):
         for x, y in runs:
             assert x == at
             at = y
-        assert at == start[s] <= full[s] <= nb[s]
+        assert at == nb[s] and start[s] <= full[s] <= nb[s]
         for k in ks:  # member index points back at s
             g, i = f["s_mgroup_arr"][k], f["s_midx_arr"][k]
             assert mem[moff[g] + i] == s
@@ -127,20 +143,40 @@ def _check_structure(f, tables, lens, B, Hq, Hkv):
             t = f["p_t1_arr"][p]
         assert t == b1[g] - b0[g]
         assert u == f["g_ubase_arr"][g] + f["u_kvh_arr"][u] * f["g_passes_arr"][g] + f["u_pass_arr"][u]
-    # CTA ranges: contiguous, covering all tiles, balanced in cost (a tile of a
-    # unit whose pass has <= 8, <= 16 or more rows costs 3, 4 or 5), to within
-    # one tile of the dearest unit
+    # CTA ranges, one set per cost line (shared units, then own units):
+    # contiguous, covering every tile of the line, balanced in cost (a tile of
+    # a unit whose pass has <= 8, <= 16 or more rows costs 3, 4 or 5, and a
+    # unit UNIT_COST once), to within one tile and one unit start
+    UNIT_COST = 8
+
     def cost(u):
         g = f["u_group_arr"][u]
-        rows = (moff[g + 1] - moff[g]) * Gq - f["u_pass_arr"][u] * PASS_ROWS
+        pr = f["g_prows_arr"][g]
+        rows = min(pr, (moff[g + 1] - moff[g]) * Gq - f["u_pass_arr"][u] * pr)
         return 3 if rows <= 8 else (4 if rows <= 16 else 5)
 
-    per_cta = [sum((f["p_t1_arr"][p] - f["p_t0_arr"][p]) * cost(f["p_unit_arr"][p])
-                   for p in range(f["c_poff_arr"][c], f["c_poff_arr"][c + 1])) for c in range(N)]
-    total = sum((b1[f["u_group_arr"][u]] - b0[f["u_group_arr"][u]]) * cost(u) for u in range(U))
-    assert f["c_poff_arr"][N] == P and sum(per_cta) == total
-    if U:
-        assert max(per_cta) - total / N <= max(cost(u) for u in range(U))
+    shared_units = [u for u in range(U) if f["u_group_arr"][u] < nsg]
+    own_units = [u for u in range(U) if f["u_group_arr"][u] >= nsg]
+    assert shared_units == list(range(len(shared_units)))  # the own units follow
+    assert f["c_poff_arr"][N] == f["c_opoff_arr"][0] and f["c_opoff_arr"][N] == P
+    for units, coff in ((shared_units, f["c_poff_arr"]), (own_units, f["c_opoff_arr"])):
+        per_cta = [sum((f["p_t1_arr"][p] - f["p_t0_arr"][p]) * cost(f["p_unit_arr"][p]) +
+                       (UNIT_COST if f["p_t0_arr"][p] == 0 else 0)
+                       for p in range(coff[c], coff[c + 1])) for c in range(N)]
+        total = sum((b1[f["u_group_arr"][u]] - b0[f["u_group_arr"][u]]) * cost(u) + UNIT_COST for u in units)
+        assert sum(per_cta) == total
+        assert all(f["p_unit_arr"][p] in units for p in range(coff[0], coff[N]))
+        if units:
+            assert max(per_cta) - total / N <= UNIT_COST + max(cost(u) for u in units)
+    # the packed descriptors repeat the piece's unit, tiles and group fields
+    desc = f["p_desc_arr"].reshape(P, 12)
+    for p in range(P):
+        u = f["p_unit_arr"][p]
+        g = f["u_group_arr"][u]
+        assert list(desc[p]) == [u, f["p_t0_arr"][p], f["p_t1_arr"][p], g, f["u_kvh_arr"][u], f["u_pass_arr"][u],
+                                 mem[moff[g]], b0[g] + f["p_t0_arr"][p], moff[g], (moff[g + 1] - moff[g]) * Gq,
+                                 f["g_prows_arr"][g], int(g >= nsg)]
+    assert f["p_desc"] % 4 == 0  # 16-byte aligned in the plan
 
 
 def _softmax_state(qv, keys, vals):
@@ -152,7 +188,7 @@ def _softmax_state(qv, keys, vals):
 
 
 def _emulate(f, q, kc, vc, tables, lens, scale):
-    """The three steps of the shared decode, in float64, driven by the plan."""
+    """The two steps of the shared decode, in float64, driven by the plan."""
     q, K, V = (x.double().numpy() for x in (q, kc, vc))
     tables, lens = tables.numpy(), lens.numpy()
     S, Hq, D = q.shape
@@ -169,26 +205,22 @@ def _emulate(f, q, kc, vc, tables, lens, scale):
         ntok = min(len(blocks) * B, int(lens[members[0]]) - first * B)  # a last block may be partly filled
         keys = np.concatenate([K[b, kvh] for b in blocks])[:ntok]
         vals = np.concatenate([V[b, kvh] for b in blocks])[:ntok]
-        for r in range(ps * PASS_ROWS, min(ps * PASS_ROWS + PASS_ROWS, len(members) * Gq)):
+        pr = f["g_prows_arr"][g]
+        for r in range(ps * pr, min(ps * pr + pr, len(members) * Gq)):
             s, hh = members[r // Gq], r % Gq
-            records[(p, r % PASS_ROWS)] = _softmax_state(q[s, kvh * Gq + hh] * scale, keys, vals)
+            records[(p, r % pr)] = _softmax_state(q[s, kvh * Gq + hh] * scale, keys, vals)
     out = np.zeros_like(q)
     for s in range(S):
-        L, st = int(lens[s]), int(f["s_start_arr"][s])
         for h in range(Hq):
             kvh, hh = h // Gq, h % Gq
             states = []
-            if L > st * B:  # the sequence's own tokens st*B .. L-1
-                toks = range(st * B, L)
-                keys = np.stack([K[tables[s, t // B], kvh, t % B] for t in toks])
-                vals = np.stack([V[tables[s, t // B], kvh, t % B] for t in toks])
-                states.append(_softmax_state(q[s, h] * scale, keys, vals))
             for k in range(f["s_moff_arr"][s], f["s_moff_arr"][s + 1]):
                 g, mi = f["s_mgroup_arr"][k], f["s_midx_arr"][k]
                 r = mi * Gq + hh
-                u = f["g_ubase_arr"][g] + kvh * f["g_passes_arr"][g] + r // PASS_ROWS
+                pr = f["g_prows_arr"][g]
+                u = f["g_ubase_arr"][g] + kvh * f["g_passes_arr"][g] + r // pr
                 for p in range(f["u_poff_arr"][u], f["u_poff_arr"][u + 1]):
-                    states.append(records[(p, r % PASS_ROWS)])
+                    states.append(records[(p, r % pr)])
             if states:
                 M = max(m for _, m, _ in states)
                 num = sum(a * np.exp(m - M) for a, m, _ in states)
@@ -214,7 +246,7 @@ def test_plan_of_unshared_tables_has_no_groups(ops):
     inp = W.make_inputs(W.scaled(W.GQA, num_seqs=4, num_blocks=4 * 256 + 3), 0)
     plan = ops.share_plan(inp.block_tables, inp.context_lens, 16, 32, 8, nctas=11)
     f = ops.plan_fields(plan)
-    assert f["num_groups"] == 0 and f["num_pieces"] == 0
+    assert f["num_shared_groups"] == 0 and f["num_groups"] == 4  # each sequence's own group only
     assert list(f["s_start_arr"]) == [0] * 4
     assert f["own_tiles"] == 1
     _check_structure(f, inp.block_tables.numpy(), inp.context_lens.numpy(), 16, 32, 8)
@@ -228,8 +260,9 @@ def test_plan_edge_cases(ops):
     tables = torch.tensor([row, row, row, row], dtype=torch.int32)
     lens = torch.tensor([150, 150, 0, 7], dtype=torch.int32)  # 9 full blocks + 6 tokens
     f = ops.plan_fields(ops.share_plan(tables, lens, B, 4, 2, nctas=3))
-    assert f["num_groups"] == 1
-    assert list(f["g_members_arr"]) == [0, 1] and (f["g_b0_arr"][0], f["g_b1_arr"][0]) == (0, 9)
+    assert f["num_shared_groups"] == 1 and f["num_groups"] == 4  # one shared, three own groups
+    assert list(f["g_members_arr"][:2]) == [0, 1] and (f["g_b0_arr"][0], f["g_b1_arr"][0]) == (0, 9)
+    assert list(f["g_members_arr"][2:]) == [0, 1, 3]  # the partial tails, and the one-token sequence
     assert list(f["s_start_arr"]) == [9, 9, 0, 0]
     assert f["own_tiles"] == 1
     _check_structure(f, tables.numpy(), lens.numpy(), B, 4, 2)
@@ -239,7 +272,7 @@ def test_plan_edge_cases(ops):
     f = ops.plan_fields(ops.share_plan(tables, lens, B, 8, 2, nctas=9))
     assert f["num_groups"] == 1 and f["g_passes_arr"][0] == 5 and f["num_units"] == 10
     assert list(f["s_start_arr"]) == [4] * 40  # every block shared: nothing of their own
-    assert f["own_tiles"] == 0  # so the own-block decode is not launched early (no CTA of it would wait)
+    assert f["own_tiles"] == 0 and f["num_shared_groups"] == 1  # no own group
 
 
 def test_plan_rejects_bad_arguments_and_small_buffers(ops):
