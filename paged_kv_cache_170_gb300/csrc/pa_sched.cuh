@@ -576,9 +576,11 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
           rec[lh * R + D + 1] = den;
         }
       }
-      // ... then the rows, 4 floats per lane and step
+      // ... then the rows, 4 floats per lane and step, over the chunks of the
+      // GT heads only (one step per head at D = 128: one step on an MHA layer)
 #pragma unroll
       for (int i = 0; i < kIters; ++i) {
+        if (32 * i >= GT * C4) break;
         const int c = lane + 32 * i;
         const int h = c / C4, d = (c % C4) * 4;
         float w[kConsumerWarps];
