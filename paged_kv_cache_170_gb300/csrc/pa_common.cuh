@@ -245,6 +245,18 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
       : "memory");
 }
 
+// Atomic add at GPU scope with acquire-release semantics: what this thread
+// wrote before it -- and what its warp wrote before a preceding __syncwarp --
+// is visible to a thread that reads the counter afterwards with acquire
+// semantics, and what other threads released before their own increments is
+// visible to this thread's later reads.  One such atomic replaces a full
+// (sequentially consistent) fence of every lane followed by a relaxed atomic.
+__device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned *p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Programmatic dependent launch.  grid_dependency_wait: block until the grids
 // this one depends on have completed and their writes are visible (returns at
 // once when the launch did not allow an early start).  launch_dependents:

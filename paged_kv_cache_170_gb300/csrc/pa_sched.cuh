@@ -509,7 +509,7 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
   long long j = 0;  // tiles before the current segment, in processing order
   uint32_t taken[kConsumerWarps] = {0u, 0u, 0u, 0u};  // deposits taken from each warp
 #ifdef PA_TRACE
-  long long tr_t0 = clock64(), tr_wait = 0;
+  long long tr_t0 = clock64(), tr_wait = 0, tr_comb = 0, tr_cut = 0, tr_adv = 0, tr_solo = 0, tr_c = 0;
 #endif
   for (int ph = 0; ph < 2; ++ph) {
     long long from, to;
@@ -532,6 +532,9 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
       if (kSoloWrites && complete && __popc(pm) == 1) {  // the warp wrote the rows itself
         j += n;
         wk.advance(a, n, PC);
+#ifdef PA_TRACE
+        tr_solo += clock64() - tr_w0;
+#endif
         continue;
       }
 #pragma unroll
@@ -544,6 +547,7 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
       }
 #ifdef PA_TRACE
       tr_wait += clock64() - tr_w0;
+      tr_c = clock64();
 #endif
       __syncwarp();
       // ---- combine the participants' states: weights per (warp, head) ...
@@ -614,10 +618,13 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
           ++taken[q];
         }
       }
+#ifdef PA_TRACE
+      tr_comb += clock64() - tr_c;
+      tr_c = clock64();
+#endif
       if (!complete) {
         // ---- count this CTA in; the last of the pair's CTAs merges
-        __threadfence();  // publish this CTA's record before it is counted
-        __syncwarp();
+        __syncwarp();  // every lane's record writes come before lane 0's release below
         // the pair's tiles sit at cost positions Cp + kSegCost + b, b < nb
         const long long Cp = wk.cp;
         const int nb = wk.nb;
@@ -645,15 +652,15 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
         __syncwarp();
         int last = 0;
         if (lane == 0) {
+          // release this CTA's record; the last contributor also acquires the
+          // records the others released before their counts
           unsigned *ctr = a.counters + (long long)s * PC + pc;
-          const unsigned seen = atomicAdd(ctr, 1u) + 1u;
+          const unsigned seen = atomic_add_acq_rel_gpu(ctr, 1u) + 1u;
           last = seen == unsigned(kc);
-          if (last) {
-            *ctr = 0u;        // ready for the next call
-            __threadfence();  // the other records were published before their counts
-          }
+          if (last) *ctr = 0u;  // ready for the next call
         }
         last = __shfl_sync(kFullMask, last, 0);
+        __syncwarp();  // the other lanes' record reads come after lane 0's acquire
         if (last) {
           // the pair is cf's last segment iff cf also owns the tile before it (at Cp - 1)
           const bool cf_last_seg = Cp > 0 && cta_at_cost(Cp - 1, Wc, N) == cf;
@@ -662,7 +669,51 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
             return a.partials + ((long long)c * 2 + slot) * 8 * R;
           };
           const int nrec = kc;
-          if (nrec <= kMergeRecords) {
+          if (nrec <= 2) {
+            // the common cut: a pair split between two CTAs.  Both records'
+            // rows (GT heads) and their (m, l) in one batch of L2 reads, then
+            // the weights and the combine in registers.
+            const float *ra = rec_of(sh_rec[0]);
+            const float *rb = nrec == 2 ? rec_of(sh_rec[1]) : ra;
+            float4 va[kIters], vb[kIters];
+#pragma unroll
+            for (int i = 0; i < kIters; ++i) {
+              va[i] = vb[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+              const int c = lane + 32 * i;
+              const int h = c / C4, d = (c % C4) * 4;
+              if (32 * i < GT * C4 && h < GT) {
+                va[i] = __ldcg(reinterpret_cast<const float4 *>(ra + h * R + d));
+                if (nrec == 2) vb[i] = __ldcg(reinterpret_cast<const float4 *>(rb + h * R + d));
+              }
+            }
+            // lane hh + 8 rs holds (m, l) of record rs for head hh
+            const int hh = lane & 7, rs = lane >> 3;
+            const bool has = hh < GT && rs < nrec;
+            const float *rr = (rs == 0 ? ra : rb) + hh * R;
+            const float mv = has ? __ldcg(rr + D) : -CUDART_INF_F;
+            const float lv = has ? __ldcg(rr + D + 1) : 0.f;
+            const float Mh = fmaxf(mv, __shfl_xor_sync(kFullMask, mv, 8));
+            const float fv = has ? fast_exp2(mv - Mh) : 0.f;
+            float den = fv * lv;
+            den += __shfl_xor_sync(kFullMask, den, 8);
+            const float wv = has ? fv / den : 0.f;  // weight of record rs for head hh
+            if (rs == 0 && hh < GT) store_lse(a, (long long)s * a.Hq + hq0 + hh, Mh, den);
+#pragma unroll
+            for (int i = 0; i < kIters; ++i) {
+              if (32 * i >= GT * C4) break;
+              const int c = lane + 32 * i;
+              const int h = c / C4, d = (c % C4) * 4;
+              const float wa = __shfl_sync(kFullMask, wv, h & 7), wb = __shfl_sync(kFullMask, wv, 8 + (h & 7));
+              if (h < GT) {
+                float4 o;
+                o.x = wa * va[i].x + wb * vb[i].x;
+                o.y = wa * va[i].y + wb * vb[i].y;
+                o.z = wa * va[i].z + wb * vb[i].z;
+                o.w = wa * va[i].w + wb * vb[i].w;
+                store_out4<T>(a, (long long)s * a.Hq + hq0 + h, d, D, o);
+              }
+            }
+          } else if (nrec <= kMergeRecords) {
             // every record's (m, l) per head at once, then the weights
             //     2^(m_r - M) / sum_r 2^(m_r - M) l_r   (in place of m_r)
             for (int i = lane; i < nrec * GT; i += 32) {
@@ -737,14 +788,22 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
           }
         }
       }
+#ifdef PA_TRACE
+      tr_cut += clock64() - tr_c;
+      tr_c = clock64();
+#endif
       ++k;
       j += n;
       wk.advance(a, n, PC);
+#ifdef PA_TRACE
+      tr_adv += clock64() - tr_c;
+#endif
     }
   }
 #ifdef PA_TRACE
   if (lane == 0 && PA_TRACE_CTA(blockIdx.x))
-    printf("trace cta %d merger: segments %lld cycles %lld waiting %lld\n", blockIdx.x, k, clock64() - tr_t0, tr_wait);
+    printf("trace cta %d merger: segments %lld cycles %lld waiting %lld combine %lld cut %lld advance %lld solo %lld\n",
+           blockIdx.x, k, clock64() - tr_t0, tr_wait, tr_comb, tr_cut, tr_adv, tr_solo);
 #endif
 }
 
