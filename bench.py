@@ -414,14 +414,14 @@ def run_gpu(args) -> dict:
     pipe.drain()
     torch.cuda.synchronize(dev)
     barrier(dist)
-    # each step's inputs are staged anew on the host (written into the pinned
-    # buffer the step uploads from), as a serving loop hands over a new batch
-    host_src = {n: getattr(inp, n).cpu() for n in pipe.slots[0].packed.host_views}
+    # each step's inputs are staged anew on the host: written (one copy, in
+    # the packed layout) into the pinned buffer the step uploads from, as a
+    # serving loop hands over a new batch
+    host_src = pipe.slots[0].packed.host.clone()  # pageable memory, the same layout
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        for n, v in pipe.next_host_views().items():
-            v.copy_(host_src[n])
+        pipe.next_host_buffer().copy_(host_src)
         pipe.step()
     pipe.drain()
     e1.record(stream)
@@ -480,8 +480,8 @@ def run_gpu(args) -> dict:
                      else profiled_traffic(args.workload)},
         "e2e": {"value": round(total_kv / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "host_staging": "each step's inputs written into the pinned upload buffer by the host, one upload, "
-                                "the output read back; two steps in flight"},
+                "host_staging": "each step's inputs written into the pinned upload buffer by the host (one copy "
+                                "of the packed inputs), one upload, the output read back; two steps in flight"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": dict(clocks.summary(), untimed_load_steps=load_steps,
                        load_note="the same step replayed untimed for %.1f s inside the sampling window before the "

@@ -233,6 +233,14 @@ class StepPipeline:
         sl.ev_up.synchronize()
         return sl.packed.host_views
 
+    def next_host_buffer(self) -> torch.Tensor:
+        """The same as one pinned uint8 buffer (every input in the packed
+        layout of ``PackedInputs``): a caller that lays out a step's inputs
+        itself writes them with one copy."""
+        sl = self.slots[self.k % 2]
+        sl.ev_up.synchronize()
+        return sl.packed.host
+
     def step(self):
         """Enqueue the next step; returns its slot."""
         sl = self.slots[self.k % 2]
