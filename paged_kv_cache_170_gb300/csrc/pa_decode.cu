@@ -35,8 +35,13 @@ static int decode_grid() { return device_sm_count() * kCtasPerSm; }
 
 static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Two partial records per CTA, sized for the largest head_dim whatever the
+// call's: the counters that follow then start at the same offset for every
+// call on this device, so calls of any shapes can share one workspace
+// without one call's records landing on another call's counters.
 static size_t partial_bytes(int nctas, int head_dim) {
-  return round256(size_t(nctas) * 2 * 8 * state_row(head_dim) * sizeof(float));
+  (void)head_dim;
+  return round256(size_t(nctas) * 2 * 8 * state_row(128) * sizeof(float));
 }
 
 // partial records, then one counter per (sequence, query head) (an upper

@@ -238,6 +238,30 @@ def test_decode_is_deterministic_and_workspace_reusable(ops):
     assert torch.equal(outs[0], outs[2])
 
 
+def test_one_workspace_serves_calls_of_any_shape(ops):
+    """Calls of different head dims, group sizes, dtypes and block sizes share
+    one workspace and each gives the bits a fresh workspace gives: the
+    counters sit at the same offset for every shape, and every call leaves
+    them at zero."""
+    shapes = [  # (D, Hq, Hkv, B, dtype)
+        (64, 8, 1, 16, torch.float16),
+        (128, 32, 8, 16, torch.bfloat16),
+        (64, 16, 2, 32, torch.bfloat16),
+        (128, 16, 2, 8, torch.float16),  # block size not a multiple of 16: the CUDA-core kernel
+        (128, 8, 8, 16, torch.float16),
+        (64, 8, 1, 16, torch.float16),
+    ]
+    ws = ops.new_workspace(64, 32, 1, 128, DEV)
+    for i, (D, Hq, Hkv, B, dtype) in enumerate(shapes):
+        q, kc, vc, tables, lens = random_case([700, 33, 1500, 0, 260, 4000, 17], Hq, Hkv, D, B, dtype, seed=i)
+        args = [x.to(DEV) for x in (q, kc, vc, tables, lens)]
+        got = ops.pa_decode(*args, 0.08, workspace=ws)
+        fresh = ops.pa_decode(*args, 0.08)
+        torch.cuda.synchronize()
+        assert torch.equal(got, fresh), (D, Hq, Hkv, B, dtype)
+        assert torch.count_nonzero(ws[-(64 * 32 * 4):]) == 0
+
+
 def test_device_bounds_checks_raise_error_bits(ops):
     q, kc, vc, tables, lens = random_case([40, 20], 4, 2, 128, 16, torch.bfloat16, seed=5, pad_tables=True)
     NB = kc.shape[0]
