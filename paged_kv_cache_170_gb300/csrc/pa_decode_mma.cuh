@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
 #ifdef PA_TRACE
     const long long tr_t0 = clock64();
 #endif
+    const uint64_t kv_policy = l2_evict_first_policy();  // each K/V tile is read once per step
     produce(a, PC, HC, plan, lane, full_bar, empty_bar, issued, abort_flag,
             [&](int slot, int p, int kvh, int bb, int L, int s, int pc, bool lead) {
               (void)bb;
@@ -134,13 +135,13 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
                              (smem_addr(dst) & 1023u) == 0,
                          kDbgSmem, dst = ring);
               if (HALVES == 2 && a.nops == 1) {
-                tma_load_3d(dst, &map_k, 0, y, 0, &full_bar[slot]);
-                tma_load_3d(dst + a.tile_stride, &map_v, 0, y, 0, &full_bar[slot]);
+                tma_load_3d_hint(dst, &map_k, 0, y, 0, &full_bar[slot], kv_policy);
+                tma_load_3d_hint(dst + a.tile_stride, &map_v, 0, y, 0, &full_bar[slot], kv_policy);
               } else {
 #pragma unroll
                 for (int h = 0; h < HALVES; ++h) {
-                  tma_load_2d(dst + h * B * 128, &map_k, 64 * h, y, &full_bar[slot]);
-                  tma_load_2d(dst + a.tile_stride + h * B * 128, &map_v, 64 * h, y, &full_bar[slot]);
+                  tma_load_2d_hint(dst + h * B * 128, &map_k, 64 * h, y, &full_bar[slot], kv_policy);
+                  tma_load_2d_hint(dst + a.tile_stride + h * B * 128, &map_v, 64 * h, y, &full_bar[slot], kv_policy);
                 }
               }
             });

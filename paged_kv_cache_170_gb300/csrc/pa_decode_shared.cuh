@@ -123,10 +123,15 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
     }
     uint32_t e = 0;
     bool aborted = false;
+    // a group read in one pass reads each of its tiles once per step: let
+    // those lines go first from L2; a group of several passes reads its tiles
+    // once per pass, so they keep the default policy
+    const uint64_t pol_once = l2_evict_first_policy(), pol_again = l2_evict_normal_policy();
     PieceDesc nxt = pl.n > 0 ? load_piece(P, h.p_desc, pl.at(0)) : PieceDesc{};
     for (int k = 0; k < pl.n && !aborted; ++k) {
       const PieceDesc d = nxt;
       if (k + 1 < pl.n) nxt = load_piece(P, h.p_desc, pl.at(k + 1));  // the next piece's, while this one streams
+      const uint64_t pol = d.rows <= d.prows ? pol_once : pol_again;
       const int32_t *trow = a.tables + (long long)d.leader * a.max_blocks + d.blk0;
       const int n = d.t1 - d.t0;
       for (int base = 0; base < n && !aborted; base += 32) {
@@ -151,13 +156,13 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
               unsigned char *dst = ring + size_t(slot) * a.slot_stride;
               const int y = (pid * a.Hkv + d.kvh) * B;
               if (HALVES == 2 && a.nops == 1) {
-                tma_load_3d(dst, &map_k, 0, y, 0, &full_bar[slot]);
-                tma_load_3d(dst + a.tile_stride, &map_v, 0, y, 0, &full_bar[slot]);
+                tma_load_3d_hint(dst, &map_k, 0, y, 0, &full_bar[slot], pol);
+                tma_load_3d_hint(dst + a.tile_stride, &map_v, 0, y, 0, &full_bar[slot], pol);
               } else {
 #pragma unroll
                 for (int hh = 0; hh < HALVES; ++hh) {
-                  tma_load_2d(dst + hh * B * 128, &map_k, 64 * hh, y, &full_bar[slot]);
-                  tma_load_2d(dst + a.tile_stride + hh * B * 128, &map_v, 64 * hh, y, &full_bar[slot]);
+                  tma_load_2d_hint(dst + hh * B * 128, &map_k, 64 * hh, y, &full_bar[slot], pol);
+                  tma_load_2d_hint(dst + a.tile_stride + hh * B * 128, &map_v, 64 * hh, y, &full_bar[slot], pol);
                 }
               }
               issued[slot] = use + 1;
