@@ -18,10 +18,10 @@ pa_status launch_decode_mma(const DecodeArgs &a, const CUtensorMap &mk, const CU
                             cudaStream_t stream, bool early);
 template <typename T, int D>
 pa_status launch_decode_shared(const SharedArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t ring_bytes,
-                               cudaStream_t stream);
+                               cudaStream_t stream, bool early);
 template <typename T, int D>
 pa_status launch_merge_shared(const MergeArgs &a, cudaStream_t stream);
-template <typename T, int D>
+template <typename T, int D, bool kGroups>
 pa_status launch_prefill(const PrefillArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t smem_bytes,
                             dim3 grid, cudaStream_t stream);
 
@@ -360,7 +360,10 @@ static const SharePlanHeader *check_plan(const int32_t *plan_host, int num_seqs,
   if (h->magic != kSharePlanMagic || h->num_seqs != num_seqs || num_kv_heads <= 0 ||
       h->group_size * num_kv_heads != num_heads || h->num_kv_heads != num_kv_heads || h->block_size != block_size ||
       h->max_blocks != max_blocks_per_seq || h->nctas <= 0 || h->num_pieces < 0 || h->total_ints < kSharePlanHeaderInts ||
-      h->num_shared_groups < 0 || h->num_shared_groups > h->num_groups || (h->p_desc & 3) != 0)
+      h->num_shared_groups < 0 || h->num_shared_groups > h->num_groups || (h->p_desc & 3) != 0 ||
+      h->num_tc_items < 0 || (h->t_items & 3) != 0 ||
+      (long long)h->t_items + (long long)h->num_tc_items * kTcItemInts > h->total_ints ||
+      (long long)h->r_off + (long long)num_seqs * num_heads + 1 > h->total_ints || h->r_rec > h->total_ints)
     return nullptr;
   return h;
 }
@@ -376,12 +379,27 @@ static size_t shared_workspace_bytes(const SharePlanHeader &h, int num_seqs, int
 
 template <typename T>
 static pa_status shared_step(const SharedArgs &sa, const void *k_cache, const void *v_cache, pa_dtype dtype, int D,
-                             size_t ring, cudaStream_t st) {
+                             size_t ring, cudaStream_t st, bool early) {
   CUtensorMap mk, mv;
   SharedArgs b = sa;
   if (!encode_pool_maps(k_cache, v_cache, dtype, sa.num_blocks, sa.Hkv, sa.B, D, &mk, &mv, &b.nops))
     return PA_ERR_CUDA;
-  return D == 64 ? launch_decode_shared<T, 64>(b, mk, mv, ring, st) : launch_decode_shared<T, 128>(b, mk, mv, ring, st);
+  return D == 64 ? launch_decode_shared<T, 64>(b, mk, mv, ring, st, early)
+                 : launch_decode_shared<T, 128>(b, mk, mv, ring, st, early);
+}
+
+template <typename T, bool kGroups = false>
+static pa_status prefill_dispatch(const PrefillArgs &pa_args, const void *k_cache, const void *v_cache,
+                                  pa_dtype dtype, int D, size_t smem, dim3 grid, cudaStream_t st) {
+  CUtensorMap mk, mv;
+  PrefillArgs b = pa_args;
+  // K: one 2-D box (B rows x 64 columns) per block and half; V: one box per
+  // block (a 3-D box over both halves when head_dim is 128)
+  if (!encode_pool_map(&mk, k_cache, dtype, b.num_blocks, b.Hkv, b.B, D, false) ||
+      !encode_pool_map(&mv, v_cache, dtype, b.num_blocks, b.Hkv, b.B, D, D == 128))
+    return PA_ERR_CUDA;
+  return D == 64 ? launch_prefill<T, 64, kGroups>(b, mk, mv, smem, grid, st)
+                 : launch_prefill<T, 128, kGroups>(b, mk, mv, smem, grid, st);
 }
 
 template <typename T>
@@ -463,9 +481,41 @@ extern "C" pa_status pa_decode_shared(void *out, const void *q, const void *k_ca
   ma.h = *h;
   ma.S = num_seqs;
   ma.Hq = num_heads;
-  if (h->num_pieces > 0) {
-    st = dtype == PA_BF16 ? shared_step<__nv_bfloat16>(sa, k_cache, v_cache, dtype, head_dim, ring, s)
-                          : shared_step<__half>(sa, k_cache, v_cache, dtype, head_dim, ring, s);
+  // 1a. the groups with many sharers, on the tensor cores (one CTA per item)
+  if (h->num_tc_items > 0) {
+    if (block_size % 16 != 0 || kTcStepTokens % block_size != 0) return PA_ERR_INVALID_ARG;  // no such plan
+    PrefillArgs ta;
+    memset(&ta, 0, sizeof(ta));
+    ta.q = q;
+    ta.tables = block_tables;
+    ta.lens = context_lens;
+    ta.num_blocks = num_blocks;
+    ta.max_blocks = max_blocks_per_seq;
+    ta.S = num_seqs;
+    ta.Hq = num_heads;
+    ta.Hkv = num_kv_heads;
+    ta.B = block_size;
+    ta.qscale = scale * kLog2e;
+    ta.err = debug_err;
+    ta.records = records;
+    ta.plan = plan_dev;
+    ta.t_items = h->t_items;
+    ta.g_members = h->g_members;
+    const size_t smem = size_t(tc_smem_bytes(head_dim));
+    const dim3 grid{unsigned(h->num_tc_items), 1u, 1u};
+    st = dtype == PA_BF16 ? prefill_dispatch<__nv_bfloat16, true>(ta, k_cache, v_cache, dtype, head_dim, smem, grid, s)
+                          : prefill_dispatch<__half, true>(ta, k_cache, v_cache, dtype, head_dim, smem, grid, s);
+    if (st != PA_OK) return st;
+  }
+  // 1b. every other group's blocks, in the CTAs' pieces; launched early
+  // beside 1a (it reads nothing 1a writes), so its CTAs fill the SMs 1a
+  // leaves idle
+  const long long mma_pieces = (long long)plan_host[h->c_poff + h->nctas] - plan_host[h->c_poff] +
+                               plan_host[h->c_opoff + h->nctas] - plan_host[h->c_opoff];
+  if (mma_pieces > 0) {
+    const bool early = h->num_tc_items > 0;
+    st = dtype == PA_BF16 ? shared_step<__nv_bfloat16>(sa, k_cache, v_cache, dtype, head_dim, ring, s, early)
+                          : shared_step<__half>(sa, k_cache, v_cache, dtype, head_dim, ring, s, early);
     if (st != PA_OK) return st;
   }
   // 2. merge
@@ -473,23 +523,6 @@ extern "C" pa_status pa_decode_shared(void *out, const void *q, const void *k_ca
 }
 
 // ------------------------------------------------------------------ prefill
-namespace pagedkv {
-
-template <typename T>
-static pa_status prefill_dispatch(const PrefillArgs &pa_args, const void *k_cache, const void *v_cache,
-                                  pa_dtype dtype, int D, size_t smem, dim3 grid, cudaStream_t st) {
-  CUtensorMap mk, mv;
-  PrefillArgs b = pa_args;
-  // K: one 2-D box (B rows x 64 columns) per block and half; V: one box per
-  // block (a 3-D box over both halves when head_dim is 128)
-  if (!encode_pool_map(&mk, k_cache, dtype, b.num_blocks, b.Hkv, b.B, D, false) ||
-      !encode_pool_map(&mv, v_cache, dtype, b.num_blocks, b.Hkv, b.B, D, D == 128))
-    return PA_ERR_CUDA;
-  return D == 64 ? launch_prefill<T, 64>(b, mk, mv, smem, grid, st)
-                 : launch_prefill<T, 128>(b, mk, mv, smem, grid, st);
-}
-
-}  // namespace pagedkv
 
 extern "C" pa_status pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
                                 const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,

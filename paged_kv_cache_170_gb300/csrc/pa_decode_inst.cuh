@@ -61,13 +61,31 @@ pa_status launch_decode_mma(const DecodeArgs &a, const CUtensorMap &mk, const CU
   return launch_status();
 }
 
+// early: may start while the previous kernel (the tensor-core groups') runs.
 template <typename T, int D>
 pa_status launch_decode_shared(const SharedArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t ring_bytes,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, bool early) {
   static int configured[64] = {0};
   auto kern = decode_shared_mma_kernel<T, D>;
   if (!configure_once(kern, kRingBytesShared + 1024, configured)) return PA_ERR_CUDA;
-  kern<<<a.h.nctas, kSharedThreads, ring_bytes + 1024, stream>>>(a, mk, mv);
+  if (!early) {
+    kern<<<a.h.nctas, kSharedThreads, ring_bytes + 1024, stream>>>(a, mk, mv);
+    return launch_status();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.h.nctas);
+  cfg.blockDim = dim3(kSharedThreads);
+  cfg.dynamicSmemBytes = ring_bytes + 1024;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, a, mk, mv) != cudaSuccess) {
+    cudaGetLastError();
+    return PA_ERR_CUDA;
+  }
   return launch_status();
 }
 
@@ -79,27 +97,32 @@ pa_status launch_merge_shared(const MergeArgs &a, cudaStream_t stream) {
   return launch_status();
 }
 
-template <typename T, int D>
+// kGroups: the shared-block decode's dense groups (grid = the plan's items).
+template <typename T, int D, bool kGroups>
 pa_status launch_prefill(const PrefillArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, size_t smem_bytes,
                             dim3 grid, cudaStream_t stream) {
   static int configured[64] = {0};
-  auto kern = prefill_tc_kernel<T, D>;
+  auto kern = prefill_tc_kernel<T, D, kGroups>;
   if (!configure_once(kern, tc_smem_bytes(D), configured)) return PA_ERR_CUDA;
   kern<<<grid, kTcThreads, smem_bytes, stream>>>(a, mk, mv);
   return launch_status();
 }
 
-#define PAGEDKV_INSTANTIATE_PREFILL(T)                                                                      \
-  template pa_status launch_prefill<T, 64>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &, \
-                                              size_t, dim3, cudaStream_t);                                   \
-  template pa_status launch_prefill<T, 128>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &, \
-                                               size_t, dim3, cudaStream_t);
+#define PAGEDKV_INSTANTIATE_PREFILL(T)                                                                           \
+  template pa_status launch_prefill<T, 64, false>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &, \
+                                                  size_t, dim3, cudaStream_t);                                   \
+  template pa_status launch_prefill<T, 128, false>(const PrefillArgs &, const CUtensorMap &,                     \
+                                                   const CUtensorMap &, size_t, dim3, cudaStream_t);             \
+  template pa_status launch_prefill<T, 64, true>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &,  \
+                                                 size_t, dim3, cudaStream_t);                                    \
+  template pa_status launch_prefill<T, 128, true>(const PrefillArgs &, const CUtensorMap &, const CUtensorMap &, \
+                                                  size_t, dim3, cudaStream_t);
 
 #define PAGEDKV_INSTANTIATE_SHARED(T)                                                                         \
   template pa_status launch_decode_shared<T, 64>(const SharedArgs &, const CUtensorMap &, const CUtensorMap &, \
-                                                 size_t, cudaStream_t);                                        \
+                                                 size_t, cudaStream_t, bool);                                  \
   template pa_status launch_decode_shared<T, 128>(const SharedArgs &, const CUtensorMap &,                     \
-                                                  const CUtensorMap &, size_t, cudaStream_t);                  \
+                                                  const CUtensorMap &, size_t, cudaStream_t, bool);            \
   template pa_status launch_merge_shared<T, 64>(const MergeArgs &, cudaStream_t);                              \
   template pa_status launch_merge_shared<T, 128>(const MergeArgs &, cudaStream_t);
 

@@ -189,6 +189,10 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
         mbar_wait(&full_bar[slot], (issued[slot] - 1) & 1u, &never);
       }
     }
+    // launched early beside the tensor-core groups' kernel (whose records
+    // this kernel never reads): never complete before it, so that the merge
+    // after this kernel sees its records too (a no-op on a plain launch)
+    grid_dependency_wait();
     return;
   }
 
@@ -402,7 +406,12 @@ struct MergeArgs {
 constexpr int kMergeWarps = 8;
 
 // One warp per output row; lane i owns dims 4i .. 4i+3 (D = 128) or
-// 2i .. 2i+1 (D = 64).  A row with no state at all (empty sequence) is zero.
+// 2i .. 2i+1 (D = 64).  The row's records are listed in the plan (r_off,
+// r_rec); their (m, l) come in one batch of loads, one record per lane, so
+// the weights
+//     w_j = 2^(m_j - M) / sum_j 2^(m_j - M) l_j,   M = max_j m_j,
+// are formed before any row is read; the rows then load back to back.  A
+// row with no record at all (empty sequence) is zero.
 template <typename T, int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_shared_kernel(const MergeArgs a) {
   constexpr int R = state_row(D);
@@ -412,36 +421,50 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_shared_kernel(const Me
   if (row >= (long long)a.S * a.Hq) return;
   const int32_t *P = a.plan;
   const SharePlanHeader &h = a.h;
-  const int s = int(row / a.Hq), hq = int(row % a.Hq);
-  const int Gq = h.group_size;
-  const int kvh = hq / Gq, hh = hq % Gq;
+  const int k0 = P[h.r_off + row], k1 = P[h.r_off + row + 1];
 
-  float M = -CUDART_INF_F, den = 0.f;
+  // pass 1: M and the denominator over all records, 32 at a time
+  float M = -CUDART_INF_F;
+  for (int base = k0; base < k1; base += 32) {
+    const int k = base + lane;
+    const float m = k < k1 ? __ldcg(a.records + (long long)P[h.r_rec + k] * R + D) : -CUDART_INF_F;
+    M = fmaxf(M, m);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
   float num[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) num[v] = 0.f;
-  for (int k = P[h.s_moff + s]; k < P[h.s_moff + s + 1]; ++k) {
-    const int g = P[h.s_mgroup + k];
-    const int r = P[h.s_midx + k] * Gq + hh;
-    const int prows = P[h.g_prows + g];
-    const int u = P[h.g_ubase + g] + kvh * P[h.g_passes + g] + r / prows;
-    for (int p = P[h.u_poff + u]; p < P[h.u_poff + u + 1]; ++p) {
-      const float *rec = a.records + ((long long)p * kSharePassRows + r % prows) * R;
-      const float m = __ldcg(rec + D), l = __ldcg(rec + D + 1);
-      float acc[V];
+  float den = 0.f;
+  if (M > -CUDART_INF_F) {
+    // pass 2: each batch's weights by lane, then its rows
+    for (int base = k0; base < k1; base += 32) {
+      const int k = base + lane;
+      const long long rid = k < k1 ? (long long)P[h.r_rec + k] : 0;
+      const float *rl = a.records + rid * R;
+      const float m = k < k1 ? __ldcg(rl + D) : -CUDART_INF_F;
+      const float l = k < k1 ? __ldcg(rl + D + 1) : 0.f;
+      const float f = m > -CUDART_INF_F ? fast_exp2(m - M) : 0.f;
+      float dl = f * l;
 #pragma unroll
-      for (int v = 0; v < V; ++v) acc[v] = __ldcg(rec + lane * V + v);
-      if (m > M) {
-        const float sc = fast_exp2(M - m);  // 0 while M is still -inf
+      for (int off = 16; off > 0; off >>= 1) dl += __shfl_xor_sync(kFullMask, dl, off);
+      den += dl;
+      const int n = min(32, k1 - base);
+#pragma unroll 4
+      for (int j = 0; j < n; ++j) {
+        const float fj = __shfl_sync(kFullMask, f, j);
+        const long long rj = __shfl_sync(kFullMask, rid, j);
+        const float *rec = a.records + rj * R + lane * V;
+        if constexpr (V == 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4 *>(rec));
+          num[0] += fj * x.x;
+          num[1] += fj * x.y;
+          num[2] += fj * x.z;
+          num[3] += fj * x.w;
+        } else {
 #pragma unroll
-        for (int v = 0; v < V; ++v) num[v] = num[v] * sc + acc[v];
-        den = den * sc + l;
-        M = m;
-      } else if (m > -CUDART_INF_F) {
-        const float f = fast_exp2(m - M);
-#pragma unroll
-        for (int v = 0; v < V; ++v) num[v] += f * acc[v];
-        den += f * l;
+          for (int v = 0; v < V; ++v) num[v] += fj * __ldcg(rec + v);
+        }
       }
     }
   }

@@ -45,9 +45,18 @@
 // step parity.  Rows of a partly filled last block past the context are
 // zeroed in the V ring before the PV MMAs read them.  All waits are bounded;
 // TMEM is released on every path.
+//
+// The same kernel also serves the shared-block decode (kGroups): a shared
+// group with many sharers is the same contraction -- the query rows of all
+// its members (row = member * G + head) against the group's run of shared
+// blocks, which every row sees in full.  There a CTA takes one work item of
+// the plan (128 rows of one (group, kv head) against a chunk of the run), no
+// step is masked but a short last one, and each row leaves its partial state
+// (O unnormalised, m, l) in the record of its pass's piece for the merge.
 #pragma once
 
 #include "pa_sched.cuh"
+#include "pa_share_plan.h"
 
 namespace pagedkv {
 
@@ -61,6 +70,11 @@ struct PrefillArgs {
   int max_blocks, S, Hq, Hkv, B;
   float qscale;          // scale * log2(e)
   int *err;
+  // the shared-block decode's groups (kGroups)
+  float *records;        // [piece][kSharePassRows][state_row(D)] partial states
+  const int32_t *plan;   // device copy of the plan
+  int32_t t_items;       // offset of its TcItem array
+  int32_t g_members;     // offset of its member list
 };
 
 constexpr int kTcRows = 128;                 // query rows per CTA (= TMEM lanes)
@@ -263,7 +277,7 @@ __device__ unsigned long long pa_prefill_cta_trace[16384][3];
   } while (0)
 #endif
 
-template <typename T, int D>
+template <typename T, int D, bool kGroups>
 __global__ void __launch_bounds__(kTcThreads, 2)
     prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v) {
@@ -287,29 +301,61 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   unsigned long long tc_g0;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tc_g0));
 #endif
-  // heaviest tiles first over all (sequence, kv head) pairs
-  const int pairs = a.S * a.Hkv;
-  const int pair = int(blockIdx.x % unsigned(pairs));
-  const int qt = int(gridDim.x / unsigned(pairs)) - 1 - int(blockIdx.x / unsigned(pairs));
-  const int s = pair / a.Hkv, kvh = pair % a.Hkv;
+  // the shared-block decode's other step may start launching now: it reads
+  // nothing this kernel writes, and fills the SMs this one leaves idle
+  if constexpr (kGroups) launch_dependents();
   const int G = a.Hq / a.Hkv;
   const int B = a.B;
-  const int q0 = a.q_start[s];
-  const int n = a.q_start[s + 1] - q0;
-  const long long cap = (long long)a.max_blocks * B;
-  long long Lr = a.lens[s];
-  Lr = Lr < 0 ? 0 : (Lr > cap ? cap : Lr);
-  const int L = int(Lr);
-  if (n < 0 || n > L) {
-    if (threadIdx.x == 0 && qt == 0 && kvh == 0) raise_error(a.err, PA_DEVERR_CONTEXT);
-    return;
+  // the CTA's rows r0 .. r0 + 127 (of `rows`), its blocks (ntile, from the
+  // table entry trow0 on), the tokens they hold (L) and, for a prompt, the
+  // position of its first query row (pos0) and where its q rows start (q0)
+  int kvh, rows, r0, ntile, L, pos0 = 0, q0 = 0;
+  const int32_t *trow0;
+  const int32_t *members = nullptr;  // kGroups: the group's sequences
+  int piece[4] = {-1, -1, -1, -1};   // kGroups: the record piece of each pass (32 rows)
+  if constexpr (kGroups) {
+    const int4 *it = reinterpret_cast<const int4 *>(a.plan + a.t_items + (long long)blockIdx.x * kTcItemInts);
+    const int4 w0 = it[0], w1 = it[1], w2 = it[2];
+    kvh = w0.y;
+    r0 = w0.z;
+    rows = w0.w;
+    members = a.plan + a.g_members + w1.y;
+    trow0 = a.tables + (long long)w1.x * a.max_blocks + w1.z;
+    ntile = w1.w;
+    piece[0] = w2.x;
+    piece[1] = w2.y;
+    piece[2] = w2.z;
+    piece[3] = w2.w;
+    L = ntile * B;  // shared blocks are full
+    if (ntile <= 0 || r0 >= rows) {
+      if (threadIdx.x == 0) raise_error(a.err, PA_DEVERR_CONTEXT);  // not an item the planner makes
+      return;
+    }
+  } else {
+    // heaviest tiles first over all (sequence, kv head) pairs
+    const int pairs = a.S * a.Hkv;
+    const int pair = int(blockIdx.x % unsigned(pairs));
+    const int qt = int(gridDim.x / unsigned(pairs)) - 1 - int(blockIdx.x / unsigned(pairs));
+    const int s = pair / a.Hkv;
+    kvh = pair % a.Hkv;
+    q0 = a.q_start[s];
+    const int n = a.q_start[s + 1] - q0;
+    const long long cap = (long long)a.max_blocks * B;
+    long long Lr = a.lens[s];
+    Lr = Lr < 0 ? 0 : (Lr > cap ? cap : Lr);
+    L = int(Lr);
+    if (n < 0 || n > L) {
+      if (threadIdx.x == 0 && qt == 0 && kvh == 0) raise_error(a.err, PA_DEVERR_CONTEXT);
+      return;
+    }
+    rows = n * G;
+    r0 = qt * kTcRows;
+    if (r0 >= rows) return;
+    pos0 = L - n;
+    const int p_last = pos0 + (min(rows, r0 + kTcRows) - 1) / G;
+    ntile = p_last / B + 1;
+    trow0 = a.tables + (long long)s * a.max_blocks;
   }
-  const int rows = n * G;
-  const int r0 = qt * kTcRows;
-  if (r0 >= rows) return;
-  const int pos0 = L - n;
-  const int p_last = pos0 + (min(rows, r0 + kTcRows) - 1) / G;
-  const int ntile = p_last / B + 1;
   const int bps = kTcStepTokens / B;  // blocks per step
   const int nstep = (ntile + bps - 1) / bps;
 
@@ -351,7 +397,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   // box per block and 64-column half, into the step's K slot as [half][64
   // tokens][128 B]); a warp's boxes lie in one block.  K(j + NKS) goes into
   // the slot of K(j) as soon as the warp sees S_j, i.e. QK(j) done.
-  const int32_t *ktrow = a.tables + (long long)s * a.max_blocks;
+  const int32_t *ktrow = trow0;
   const int kbpw = (bps * HALVES + 3) >> 2;     // boxes per warp in a full step: 1 or 2
   const int kfirst = (warp & 3) * kbpw;          // this warp's first box
   auto k_entry = [&](int jj) {                   // the table entry of this warp's block of step jj
@@ -393,9 +439,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       const int r = i / (D / 8), c = i % (D / 8);  // row, 16-byte chunk
       const int gr = r0 + r;
       v[k] = make_uint4(0u, 0u, 0u, 0u);
-      if (gr < rows)
-        v[k] = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.q) +
-                                                ((long long)(q0 + gr / G) * a.Hq + kvh * G + gr % G) * D + c * 8);
+      if (gr < rows) {
+        const long long qrow = kGroups ? (long long)members[gr / G] : (long long)(q0 + gr / G);
+        v[k] = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.q) + (qrow * a.Hq + kvh * G + gr % G) * D +
+                                                c * 8);
+      }
     }
     if (lane == 0) {  // the first NKS steps' keys, while the Q loads are in flight
 #pragma unroll
@@ -432,7 +480,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // copies of the values.  The lanes hold the table entries of the current
     // 32 blocks, the next 32 already requested.
     if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_v)) : "memory");
-    const int32_t *trow = a.tables + (long long)s * a.max_blocks;
+    const int32_t *trow = trow0;
     const uint32_t tile_bytes = uint32_t(B) * D * 2;
     auto entry = [&](int b) { return b < ntile ? trow[b] : -1; };
     int cur = entry(lane), nxt = entry(32 + lane), chunk = 0;
@@ -629,12 +677,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       tmem_ld32_async(sb + 32, s1);
       tmem_wait_ld(s0, s1);
       // only steps that reach the diagonal or end short need a mask; the
-      // visible columns of a row are then a prefix 0 .. nv - 1
-      const bool need_mask = t0 + kTcStepTokens - 1 > pos_first || nb * B < kTcStepTokens;
+      // visible columns of a row are then a prefix 0 .. nv - 1 (a group's
+      // rows see every token: only a short last step is masked)
+      const bool need_mask =
+          kGroups ? nb * B < kTcStepTokens : (t0 + kTcStepTokens - 1 > pos_first || nb * B < kTcStepTokens);
       uint32_t ph[32], pl[32];
       float alpha, lsum;
       if (need_mask)
-        lsum = softmax_step<T, true>(s0, s1, min(nb * B, pos - t0 + 1), qscale, m, alpha, ph, pl);
+        lsum = softmax_step<T, true>(s0, s1, kGroups ? nb * B : min(nb * B, pos - t0 + 1), qscale, m, alpha, ph,
+                                     pl);
       else
         lsum = softmax_step<T, false>(s0, s1, kTcStepTokens, qscale, m, alpha, ph, pl);
       l = l * alpha + lsum;
@@ -683,7 +734,28 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       ok = mbar_wait(&o_done[(nstep - 1) & 1], uint32_t((nstep - 1) >> 1) & 1u, abort_flag);
       ok = __all_sync(kFullMask, ok);
     }
-    if (ok) {
+    if (ok && kGroups) {
+      // the row's partial state (O, m, l) in the record of its pass's piece:
+      // softmax warp w holds pass 4 * (r0 / 128) + w, row lane of it
+      tc_fence_after();
+      constexpr int R = state_row(D);
+      float *rec = gr < rows ? a.records + ((long long)piece[warp] * kSharePassRows + lane) * R : nullptr;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t ov[32];
+        tmem_ld32(tl + c0, ov);
+        if (rec != nullptr) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            *reinterpret_cast<float4 *>(rec + c0 + c) = make_float4(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1]),
+                                                                    __uint_as_float(ov[c + 2]), __uint_as_float(ov[c + 3]));
+        }
+      }
+      if (rec != nullptr) {
+        rec[D] = m;
+        rec[D + 1] = l;
+      }
+    } else if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       T *orow = static_cast<T *>(a.out) + ((long long)(q0 + gr / G) * a.Hq + kvh * G + gr % G) * D;

@@ -24,7 +24,10 @@
 // head's group of G); a unit's tiles are the group's blocks.  All units' tiles are cut into nctas
 // contiguous ranges of equal cost (a tile costs its unit's row-warps), one
 // per CTA, and a piece is the part of one unit inside one CTA's range.  Each
-// piece leaves one partial state per row.
+// piece leaves one partial state per row.  A shared group with at least 32
+// query rows per kv head is a dense contraction instead: its units' pieces
+// are chunks of its run, computed by the tensor-core kernel, 128 rows (four
+// passes) against one chunk per work item.
 #include <stdint.h>
 #include <string.h>
 
@@ -117,7 +120,15 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
   std::sort(groups.begin(), groups.end(), [](const Group &x, const Group &y) {
     return x.members[0] != y.members[0] ? x.members[0] < y.members[0] : x.b0 < y.b0;
   });
+  // Shared groups with many query rows per kv head go to the tensor-core
+  // kernel (a step of it is 64 tokens of whole blocks): they follow the
+  // other shared groups, so that each kind's units are one range
+  const bool tc_blocks = B == 16 || B == 32 || B == 64;
+  auto is_tc = [&](const Group &g) { return tc_blocks && (long long)g.members.size() * Gq >= kTcGroupMinRows; };
+  std::stable_partition(groups.begin(), groups.end(), [&](const Group &g) { return !is_tc(g); });
   const int num_shared = int(groups.size());
+  int num_mma_shared = 0;
+  while (num_mma_shared < num_shared && !is_tc(groups[num_mma_shared])) ++num_mma_shared;
   // own groups: each sequence's blocks past its private start, in sequence order
   for (int s = 0; s < S; ++s) {
     long long L = context_lens[s];
@@ -209,7 +220,43 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
     coff[nctas] = int(punit.size());
   };
   const int Us = num_shared < G ? ubase[num_shared] : U;  // the own groups' units follow the shared ones
-  split(0, Us, cpoff);
+  const int Ut = num_mma_shared < G ? ubase[num_mma_shared] : U;  // the tensor-core groups' units, [Ut, Us)
+  split(0, Ut, cpoff);
+  // the tensor-core groups' pieces: chunks of their runs, the same for every
+  // pass; a chunk is sp steps of 64 tokens.  The items run two per SM
+  // (nctas slots at a time): sp is the smallest length at which the items
+  // fill whole waves of slots, no wave holding a chunk longer than
+  // kTcItemMaxSteps, so that the last wave is not a few stragglers
+  const int bps = tc_blocks ? kTcStepTokens64 / B : 1;
+  std::vector<long long> tc_run_steps;  // steps of each (group, kv head, 128-row tile)'s run
+  long long tc_steps = 0;
+  for (int g = num_mma_shared; g < num_shared; ++g) {
+    const long long tiles = (long long)((groups[g].members.size() * Gq + kTcItemRows - 1) / kTcItemRows);
+    const long long st = (groups[g].b1 - groups[g].b0 + bps - 1) / bps;
+    for (long long i = 0; i < (long long)Hkv * tiles; ++i) tc_run_steps.push_back(st);
+    tc_steps += (long long)Hkv * tiles * st;
+  }
+  long long sp = kTcItemMinSteps;
+  if (tc_steps > 0) {
+    const long long slots = nctas;
+    const long long waves = std::max<long long>(1, (tc_steps + slots * kTcItemMaxSteps - 1) / (slots * kTcItemMaxSteps));
+    sp = std::max<long long>(kTcItemMinSteps, (tc_steps + waves * slots - 1) / (waves * slots));
+    auto items_of = [&](long long len) {
+      long long n = 0;
+      for (long long st : tc_run_steps) n += (st + len - 1) / len;
+      return n;
+    };
+    while (sp < kTcItemMaxSteps && items_of(sp) > waves * slots) ++sp;
+  }
+  const long long chunk_tiles = sp * bps;
+  for (int u = Ut; u < Us; ++u) {
+    const long long nb = utile0[u + 1] - utile0[u];
+    for (long long t = 0; t < nb; t += chunk_tiles) {
+      punit.push_back(u);
+      pt0.push_back(int32_t(t));
+      pt1.push_back(int32_t(std::min(nb, t + chunk_tiles)));
+    }
+  }
   split(Us, U, copoff);
   const int P = int(punit.size());
   for (int p = 0; p < P; ++p) upoff[punit[p] + 1] = p + 1;  // pieces of a unit are consecutive
@@ -278,6 +325,65 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
   place(h.c_opoff, nctas + 1);
   off = (off + 3) / 4 * 4;  // the descriptors are read as 16-byte vectors
   place(h.p_desc, (long long)P * kPieceDescInts);
+  // the tensor-core items: (group, kv head, 128-row tile, chunk), each
+  // naming the pieces (one per pass of its rows) whose records it writes
+  std::vector<int32_t> titems;
+  {
+    std::vector<int32_t> gm(G);
+    long long mo = 0;
+    for (int g = 0; g < G; ++g) {
+      gm[g] = int32_t(mo);
+      mo += groups[g].members.size();
+    }
+    std::vector<std::pair<int32_t, std::vector<int32_t>>> items;  // (tiles, item)
+    for (int g = num_mma_shared; g < num_shared; ++g) {
+      const int rows = int(groups[g].members.size()) * Gq;
+      const long long nb = groups[g].b1 - groups[g].b0;
+      for (int kv = 0; kv < Hkv; ++kv)
+        for (int r0 = 0; r0 < rows; r0 += kTcItemRows)
+          for (long long c = 0; c * chunk_tiles < nb; ++c) {
+            std::vector<int32_t> it(kTcItemInts, -1);
+            it[0] = g;
+            it[1] = kv;
+            it[2] = r0;
+            it[3] = rows;
+            it[4] = groups[g].members[0];
+            it[5] = gm[g];
+            it[6] = int32_t(groups[g].b0 + c * chunk_tiles);
+            it[7] = int32_t(std::min(nb, (c + 1) * chunk_tiles) - c * chunk_tiles);
+            for (int k = 0; k < kTcItemRows / kSharePassRows; ++k) {
+              const int pass = r0 / kSharePassRows + k;
+              if (pass < passes[g]) it[8 + k] = upoff[ubase[g] + kv * passes[g] + pass] + int32_t(c);
+            }
+            items.push_back({it[7], std::move(it)});
+          }
+    }
+    // the longest chunks first (the last chunk of a run may be short)
+    std::stable_sort(items.begin(), items.end(),
+                     [](const std::pair<int32_t, std::vector<int32_t>> &x,
+                        const std::pair<int32_t, std::vector<int32_t>> &y) { return x.first > y.first; });
+    for (auto &it : items) titems.insert(titems.end(), it.second.begin(), it.second.end());
+  }
+  const int NT = int(titems.size()) / kTcItemInts;
+  place(h.t_items, (long long)titems.size());
+  h.num_tc_items = NT;
+  // each output row's records: every membership of its sequence, the unit of
+  // the row's pass, that unit's pieces
+  const int Hq = num_heads;
+  std::vector<int32_t> roff(size_t(S) * Hq + 1, 0), rrec;
+  for (int s = 0; s < S; ++s)
+    for (int hq = 0; hq < Hq; ++hq) {
+      const int kv = hq / Gq, hh = hq % Gq;
+      for (int k = smoff[s]; k < smoff[s + 1]; ++k) {
+        const int g = smgroup[k];
+        const int r = smidx[k] * Gq + hh;
+        const int u = ubase[g] + kv * passes[g] + r / prows[g];
+        for (int p = upoff[u]; p < upoff[u + 1]; ++p) rrec.push_back(p * kSharePassRows + r % prows[g]);
+      }
+      roff[size_t(s) * Hq + hq + 1] = int32_t(rrec.size());
+    }
+  place(h.r_off, (long long)roff.size());
+  place(h.r_rec, (long long)rrec.size());
   if (off > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   h.total_ints = int32_t(off);
   *plan_ints = size_t(off);
@@ -348,5 +454,8 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
     }
     put(h.p_desc, d.data(), (long long)d.size());
   }
+  put(h.t_items, titems.data(), (long long)titems.size());
+  put(h.r_off, roff.data(), (long long)roff.size());
+  put(h.r_rec, rrec.data(), (long long)rrec.size());
   return PA_OK;
 }

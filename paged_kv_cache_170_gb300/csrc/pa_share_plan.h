@@ -17,6 +17,15 @@
 //             PieceDesc per piece, 16-byte aligned)
 //   sequences s_start[S] (first private block), s_moff[S+1], s_mgroup[...],
 //             s_midx[...] (each membership: group, index among its members)
+//   rows      r_off[S*Hq+1], r_rec[...]: the partial records of each output
+//             row (s, query head), as record indices piece * kSharePassRows
+//             + row of its pass, for the merge
+//   tc items  t_items[num_tc_items] (one TcItem each, 16-byte aligned): the
+//             work of the tensor-core kernel.  A shared group with at least
+//             kTcGroupMinRows query rows per kv head is a dense contraction
+//             (rows x the run's tokens): its units' pieces are token chunks,
+//             cut the same way for the four passes of each 128-row tile, and
+//             computed by that kernel, not by the CTAs of c_poff
 #pragma once
 
 #include <stdint.h>
@@ -27,6 +36,28 @@ constexpr int32_t kSharePlanMagic = 0x50534b50;  // "PKSP"
 constexpr int kSharePassRows = 32;               // query rows of a shared group's pass: 4 warps x 8
 constexpr int kOwnPassRows = 8;                  // query rows of an own group's pass: one warp
 constexpr int kUnitCost = 8;                     // fixed cost of a unit in the CTA split (tile costs are 3..5)
+constexpr int kTcGroupMinRows = 32;              // query rows per kv head from which a shared group takes the tensor cores
+constexpr int kTcItemRows = 128;                 // query rows of a tensor-core work item (one MMA tile, four passes)
+constexpr int kTcStepTokens64 = 64;              // tokens of a step of that kernel
+constexpr int kTcItemMinSteps = 4;               // a chunk's steps: at least this many ...
+constexpr int kTcItemMaxSteps = 32;              // ... and at most this many
+
+// One work item of the tensor-core kernel: the query rows row0 .. row0 + 127
+// (fewer at the group's end) of one (group, kv head) against a chunk of the
+// group's run, leaving each row's partial state in the record of the piece
+// of its pass.
+struct TcItem {
+  int32_t group, kvh;
+  int32_t row0;      // first row (a multiple of 128)
+  int32_t rows;      // the group's query rows: members * G
+  int32_t leader;    // the group's first member (its table row holds the run)
+  int32_t moff;      // the group's first member in g_members
+  int32_t blk0;      // logical block of the chunk's first tile
+  int32_t ntile;     // tiles (blocks) of the chunk
+  int32_t piece[4];  // piece of each of the four passes (-1 past the group's rows)
+};
+constexpr int kTcItemInts = int(sizeof(TcItem) / sizeof(int32_t));
+static_assert(sizeof(TcItem) == 48, "three 16-byte loads");
 
 // What a CTA needs at the start of a piece, in one record of the plan.
 struct PieceDesc {
@@ -55,6 +86,8 @@ struct SharePlanHeader {
   int32_t num_shared_groups;  // groups 0 .. num_shared_groups-1 are shared, the rest own
   int32_t g_prows;            // offset of g_prows[G]
   int32_t c_opoff, p_desc;    // offsets of c_opoff[nctas+1] and p_desc[P]
+  int32_t num_tc_items, t_items;  // the tensor-core kernel's work items and their offset
+  int32_t r_off, r_rec;           // offsets of r_off[S*Hq+1] and r_rec[...]
 };
 
 constexpr int kSharePlanHeaderInts = int(sizeof(SharePlanHeader) / sizeof(int32_t));
@@ -69,3 +102,9 @@ using pagedkv::kUnitCost;
 using pagedkv::kSharePassRows;
 using pagedkv::kSharePlanHeaderInts;
 using pagedkv::kSharePlanMagic;
+using pagedkv::kTcGroupMinRows;
+using pagedkv::kTcItemInts;
+using pagedkv::kTcItemMaxSteps;
+using pagedkv::kTcItemMinSteps;
+using pagedkv::kTcItemRows;
+using pagedkv::kTcStepTokens64;

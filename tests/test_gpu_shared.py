@@ -145,6 +145,46 @@ def test_shared_decode_own_groups_of_two_passes(ops, B):
     assert_attention_close(out, ref, strict=False)
 
 
+@pytest.mark.parametrize("B,D,dtype,members,Hq,Hkv,run", [
+    (16, 128, torch.bfloat16, 40, 8, 2, 37),   # 160 rows: two 128-row items, a short last step
+    (32, 64, torch.float16, 12, 16, 2, 21),    # 96 rows, two blocks per step
+    (64, 128, torch.bfloat16, 9, 32, 8, 7),    # 36 rows, one block per step
+    (16, 64, torch.bfloat16, 8, 32, 8, 64),    # exactly 32 rows, a run of 16 whole steps
+])
+def test_shared_decode_tensor_core_groups(ops, B, D, dtype, members, Hq, Hkv, run):
+    """Groups with 32 or more query rows per kv head are computed on the
+    tensor cores (the prompt kernel's pipeline over the group's rows): every
+    block size it takes, both head dims and dtypes, row counts that are not a
+    multiple of 128, runs that end in a short step; some members also have
+    blocks of their own with a partly filled last one."""
+    S = members + 2
+    own = [0, 3, 1, 0, 2] * ((S + 4) // 5)
+    NB = run + sum(own[:S]) + 2 * 5 + 4
+    q, kc, vc = _random_pool(S, Hq, Hkv, D, B, NB, dtype, seed=B + D + members)
+    tables = torch.full((S, run + 6), 0, dtype=torch.int32)
+    lens = torch.zeros(S, dtype=torch.int32)
+    nxt = run
+    for s in range(S):
+        if s < members:  # the shared run, then own blocks (the last one partly filled)
+            tables[s, :run] = torch.arange(run, dtype=torch.int32)
+            k = own[s]
+            tables[s, run:run + k] = torch.arange(nxt, nxt + k, dtype=torch.int32)
+            nxt += k
+            lens[s] = run * B + (k - 1) * B + 1 + s % B if k else run * B
+        else:  # two sequences outside every group
+            tables[s, :5] = torch.arange(nxt, nxt + 5, dtype=torch.int32)
+            nxt += 5
+            lens[s] = 4 * B + 3
+    scale = 1.0 / math.sqrt(D)
+    out, f = _shared(ops, *[x.to(DEV) for x in (q, kc, vc, tables, lens)], scale)
+    assert f["num_tc_items"] > 0
+    ref = native.decode(q, kc, vc, tables.numpy(), lens.numpy(), scale)
+    assert_attention_close(out, ref, strict=False)
+    plain = ops.pa_decode(*[x.to(DEV) for x in (q, kc, vc, tables, lens)], scale)
+    torch.cuda.synchronize()
+    assert (out.float() - plain.float()).abs().max().item() <= 4e-3
+
+
 def test_shared_decode_deterministic_reusable_workspace_and_no_group_plan(ops):
     cpu = _small("prefix", seed=1)
     inp = cpu.to(DEV)

@@ -20,6 +20,8 @@ from paged_kv_cache_170_gb300.block_manager import BlockManager
 
 PASS_ROWS = 32  # query rows of a shared group's pass
 OWN_PASS_ROWS = 8  # of an own group's pass
+TC_MIN_ROWS = 32  # query rows per kv head from which a shared group goes to the tensor-core kernel
+TC_ITEM_ROWS = 128  # rows of one of its work items
 
 
 @pytest.fixture(scope="module")
@@ -69,6 +71,10 @@ def _beam_like(seed=0):
 def _case(name):
     if name == "beam":
         return _beam_like()
+    if name == "longctx4":  # four branches x 8 heads = 32 rows per kv head: the tensor cores take the prompts
+        inp = scenarios.long_context_inputs(0, num_prompts=2, branches=4, prompt_tokens=2048, suffix_max=200,
+                                            w=W.scaled(W.LONGCTX, num_blocks=220, max_blocks_per_seq=80))
+        return inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale
     inp = _prefix_small() if name == "prefix" else _longctx_small()
     # the plan is built from the tables as the decode sees them (after the step's copies / writes)
     return inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale
@@ -130,6 +136,11 @@ def _check_structure(f, tables, lens, B, Hq, Hkv):
             g2 = {f["s_mgroup_arr"][j] for j in range(f["s_moff_arr"][s2], f["s_moff_arr"][s2 + 1])}
             covered = sum(b1[g] - b0[g] for g in g1 & g2)
             assert covered == k, (s1, s2, covered, k)
+    # shared groups on the tensor cores (many sharers, whole-block steps)
+    # follow the other shared groups
+    G = f["num_groups"]
+    is_tc = [g < nsg and B in (16, 32, 64) and (moff[g + 1] - moff[g]) * Gq >= TC_MIN_ROWS for g in range(G)]
+    assert is_tc[:nsg] == sorted(is_tc[:nsg])
     # pieces: each unit's tiles exactly once, in order; CTA ranges balanced
     U, P, N = f["num_units"], f["num_pieces"], f["nctas"]
     poff = f["u_poff_arr"]
@@ -155,10 +166,14 @@ def _check_structure(f, tables, lens, B, Hq, Hkv):
         rows = min(pr, (moff[g + 1] - moff[g]) * Gq - f["u_pass_arr"][u] * pr)
         return 3 if rows <= 8 else (4 if rows <= 16 else 5)
 
-    shared_units = [u for u in range(U) if f["u_group_arr"][u] < nsg]
+    shared_units = [u for u in range(U) if f["u_group_arr"][u] < nsg and not is_tc[f["u_group_arr"][u]]]
+    tc_units = [u for u in range(U) if is_tc[f["u_group_arr"][u]]]
     own_units = [u for u in range(U) if f["u_group_arr"][u] >= nsg]
-    assert shared_units == list(range(len(shared_units)))  # the own units follow
-    assert f["c_poff_arr"][N] == f["c_opoff_arr"][0] and f["c_opoff_arr"][N] == P
+    assert shared_units + tc_units + own_units == list(range(U))  # in this order
+    # the tensor-core pieces lie between the two CTA lines
+    tc_pieces = list(range(f["c_poff_arr"][N], f["c_opoff_arr"][0]))
+    assert f["c_poff_arr"][0] == 0 and f["c_opoff_arr"][N] == P
+    assert sorted(tc_pieces) == [p for u in tc_units for p in range(poff[u], poff[u + 1])]
     for units, coff in ((shared_units, f["c_poff_arr"]), (own_units, f["c_opoff_arr"])):
         per_cta = [sum((f["p_t1_arr"][p] - f["p_t0_arr"][p]) * cost(f["p_unit_arr"][p]) +
                        (UNIT_COST if f["p_t0_arr"][p] == 0 else 0)
@@ -168,6 +183,34 @@ def _check_structure(f, tables, lens, B, Hq, Hkv):
         assert all(f["p_unit_arr"][p] in units for p in range(coff[0], coff[N]))
         if units:
             assert max(per_cta) - total / N <= UNIT_COST + max(cost(u) for u in units)
+    # a tensor-core group's units are all cut into the same chunks; every
+    # tensor-core piece belongs to exactly one item, which names the pieces of
+    # the passes of its 128 rows against one chunk
+    for g in range(G):
+        if not is_tc[g]:
+            continue
+        us = [u for u in tc_units if f["u_group_arr"][u] == g]
+        cuts = {tuple((f["p_t0_arr"][p], f["p_t1_arr"][p]) for p in range(poff[u], poff[u + 1])) for u in us}
+        assert len(cuts) == 1
+    items = f["t_items_arr"].reshape(-1, 12)
+    assert len(items) == f["num_tc_items"] and f["t_items"] % 4 == 0
+    seen = []
+    for it in items:
+        g, kvh, row0, rows, leader, mo, blk0, ntile = (int(x) for x in it[:8])
+        assert is_tc[g] and row0 % TC_ITEM_ROWS == 0 and 0 <= row0 < rows == (moff[g + 1] - moff[g]) * Gq
+        assert leader == mem[moff[g]] and mo == moff[g] and ntile > 0
+        for k in range(4):
+            pas = row0 // PASS_ROWS + k
+            p = int(it[8 + k])
+            if pas >= f["g_passes_arr"][g]:
+                assert p == -1
+                continue
+            u = f["g_ubase_arr"][g] + kvh * f["g_passes_arr"][g] + pas
+            assert f["p_unit_arr"][p] == u
+            assert (b0[g] + f["p_t0_arr"][p], f["p_t1_arr"][p] - f["p_t0_arr"][p]) == (blk0, ntile)
+            seen.append(p)
+    assert sorted(seen) == tc_pieces
+    assert list(items[:, 7]) == sorted(items[:, 7], reverse=True)  # the longest chunks first
     # the packed descriptors repeat the piece's unit, tiles and group fields
     desc = f["p_desc_arr"].reshape(P, 12)
     for p in range(P):
@@ -210,17 +253,23 @@ def _emulate(f, q, kc, vc, tables, lens, scale):
             s, hh = members[r // Gq], r % Gq
             records[(p, r % pr)] = _softmax_state(q[s, kvh * Gq + hh] * scale, keys, vals)
     out = np.zeros_like(q)
+    roff, rrec = f["r_off_arr"], f["r_rec_arr"]
+    assert len(roff) == S * Hq + 1
     for s in range(S):
         for h in range(Hq):
             kvh, hh = h // Gq, h % Gq
-            states = []
+            want = []  # the row's records, from its memberships
             for k in range(f["s_moff_arr"][s], f["s_moff_arr"][s + 1]):
                 g, mi = f["s_mgroup_arr"][k], f["s_midx_arr"][k]
                 r = mi * Gq + hh
                 pr = f["g_prows_arr"][g]
                 u = f["g_ubase_arr"][g] + kvh * f["g_passes_arr"][g] + r // pr
                 for p in range(f["u_poff_arr"][u], f["u_poff_arr"][u + 1]):
-                    states.append(records[(p, r % pr)])
+                    want.append(p * PASS_ROWS + r % pr)
+            row = s * Hq + h
+            got = [int(x) for x in rrec[roff[row]:roff[row + 1]]]
+            assert got == want  # the merge's list of the row
+            states = [records[(x // PASS_ROWS, x % PASS_ROWS)] for x in got]
             if states:
                 M = max(m for _, m, _ in states)
                 num = sum(a * np.exp(m - M) for a, m, _ in states)
@@ -229,7 +278,7 @@ def _emulate(f, q, kc, vc, tables, lens, scale):
     return out
 
 
-@pytest.mark.parametrize("name,nctas", [("prefix", 7), ("prefix", 304), ("longctx", 5), ("beam", 3)])
+@pytest.mark.parametrize("name,nctas", [("prefix", 7), ("prefix", 304), ("longctx", 5), ("longctx4", 6), ("beam", 3)])
 def test_plan_structure_and_emulated_decode_match_oracle(ops, name, nctas):
     q, kc, vc, tables, lens, scale = _case(name)
     B, Hq, Hkv = kc.shape[2], q.shape[1], kc.shape[1]
@@ -273,6 +322,12 @@ def test_plan_edge_cases(ops):
     assert f["num_groups"] == 1 and f["g_passes_arr"][0] == 5 and f["num_units"] == 10
     assert list(f["s_start_arr"]) == [4] * 40  # every block shared: nothing of their own
     assert f["own_tiles"] == 0 and f["num_shared_groups"] == 1  # no own group
+    # 160 rows per kv head: the tensor cores take it, two 128-row items per kv head
+    assert f["num_tc_items"] == 4 and f["c_poff_arr"][-1] == 0
+    _check_structure(f, tables.numpy(), lens.numpy(), B, 8, 2)
+    # with a block size that does not divide a 64-token step it stays on the CUDA cores
+    f = ops.plan_fields(ops.share_plan(tables, lens, 48, 8, 2, nctas=9))
+    assert f["num_tc_items"] == 0
 
 
 def test_plan_rejects_bad_arguments_and_small_buffers(ops):
