@@ -43,8 +43,6 @@ struct SharedArgs {
 
 constexpr int kSharedThreads = (kConsumerWarps + 1) * 32;
 
-// Row-warps (8 rows each) a pass of `rows` query rows takes: 1, 2 or 4.
-__host__ __device__ __forceinline__ int share_row_warps(int rows) { return rows <= 8 ? 1 : (rows <= 16 ? 2 : 4); }
 constexpr int kRingBytesShared = 88 * 1024;  // ring of K + V tile pairs
 
 // A piece's descriptor (three 16-byte loads through the read-only path).
@@ -86,7 +84,6 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ uint32_t issued[kMaxStages];
   __shared__ int sh_abort;
-  __shared__ __align__(16) float st[kConsumerWarps][8][R];  // tile-lane states of a piece's rows
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -272,7 +269,7 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
       const long long tr_m0 = clock64();
       tr_wait += tr_m0 - tr_w0;
 #endif
-      if (ok && myrows > 0 && t % nl == tl) {
+      if (ok && myrows > 0 && (t + p) % nl == tl) {
         // shared blocks are full; an own group's last block holds L - blk * B tokens
         const int nv = d.own ? min(B, L - (d.blk0 + t) * B) : B;
         const int padded = ((nv + 15) >> 4) * 16;
@@ -308,17 +305,16 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
 #ifdef PA_TRACE
     const long long tr_e0 = clock64();
 #endif
-    // ---- the piece's partial state per row (acc, m, l): straight to the
-    // record (one tile-lane), or through shared memory, combining the
-    // tile-lanes of each row first
+    // ---- the piece's partial state per row (acc, m, l), straight to the
+    // record rows of this tile-lane (no wait for the other warps)
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l0 += __shfl_xor_sync(kFullMask, l0, off);
       l1 += __shfl_xor_sync(kFullMask, l1, off);
     }
     const int h0 = 2 * c4, h1 = 2 * c4 + 1;
-    float *dst = nl == 1 ? a.records + ((long long)p * kSharePassRows + rw * 8) * R : &st[warp][0][0];
-    if (myrows > 0) {
+    if (myrows > 0 && share_lane_has_tile(p, n, tl, nl)) {
+      float *dst = a.records + ((long long)p * kSharePassRows + tl * wr * 8 + rw * 8) * R;
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
         if (h0 < myrows) {
@@ -340,49 +336,6 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
           dst[h1 * R + D + 1] = l1;
         }
       }
-    }
-    if (nl > 1) {
-      named_barrier_sync(1, kConsumerWarps * 32);
-      if (tl == 0 && myrows > 0) {
-        // lane (j, hh) = (lane / 8, lane % 8): weight of tile-lane j for row hh
-        const int j = lane >> 3, hh = lane & 7;
-        const bool mine = j < nl && hh < myrows;
-        const float *sj = &st[j * wr + rw][0][0];
-        const float m = mine ? sj[hh * R + D] : -CUDART_INF_F;
-        const float lv = mine ? sj[hh * R + D + 1] : 0.f;
-        float M = fmaxf(m, __shfl_xor_sync(kFullMask, m, 8));
-        M = fmaxf(M, __shfl_xor_sync(kFullMask, M, 16));
-        const float f = (mine && M > -CUDART_INF_F) ? fast_exp2(m - M) : 0.f;
-        float den = f * lv;
-        den += __shfl_xor_sync(kFullMask, den, 8);
-        den += __shfl_xor_sync(kFullMask, den, 16);
-        float *rec = a.records + ((long long)p * kSharePassRows + rw * 8) * R;
-        if (j == 0 && hh < myrows) {
-          rec[hh * R + D] = M;
-          rec[hh * R + D + 1] = den;
-        }
-        constexpr int C4 = D / 4;
-#pragma unroll
-        for (int i = 0; i < 8 * C4 / 32; ++i) {
-          const int idx = lane + 32 * i;
-          const int row = idx / C4, d = (idx % C4) * 4;
-          float w[kConsumerWarps];
-#pragma unroll
-          for (int jj = 0; jj < kConsumerWarps; ++jj) w[jj] = __shfl_sync(kFullMask, f, jj * 8 + row);
-          if (row < myrows) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int jj = 0; jj < nl; ++jj) {
-              const float4 v = *reinterpret_cast<const float4 *>(&st[jj * wr + rw][row][d]);
-              acc.x += w[jj] * v.x;
-              acc.y += w[jj] * v.y;
-              acc.z += w[jj] * v.z;
-              acc.w += w[jj] * v.w;
-            }
-            *reinterpret_cast<float4 *>(rec + row * R + d) = acc;
-          }
-        }
-      }
-      named_barrier_sync(1, kConsumerWarps * 32);  // st is free for the next piece
     }
 #ifdef PA_TRACE
     tr_end += clock64() - tr_e0;
@@ -410,8 +363,9 @@ constexpr int kMergeWarps = 8;
 // r_rec); their (m, l) come in one batch of loads, one record per lane, so
 // the weights
 //     w_j = 2^(m_j - M) / sum_j 2^(m_j - M) l_j,   M = max_j m_j,
-// are formed before any row is read; the rows then load back to back.  A
-// row with no record at all (empty sequence) is zero.
+// are formed before any row is read; the rows then load eight at a time.  A
+// row with more than 32 records takes the weights in batches of 32, after a
+// first pass for M.  A row with no record at all (empty sequence) is zero.
 template <typename T, int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_shared_kernel(const MergeArgs a) {
   constexpr int R = state_row(D);
@@ -423,49 +377,60 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_shared_kernel(const Me
   const SharePlanHeader &h = a.h;
   const int k0 = P[h.r_off + row], k1 = P[h.r_off + row + 1];
 
-  // pass 1: M and the denominator over all records, 32 at a time
   float M = -CUDART_INF_F;
-  for (int base = k0; base < k1; base += 32) {
-    const int k = base + lane;
-    const float m = k < k1 ? __ldcg(a.records + (long long)P[h.r_rec + k] * R + D) : -CUDART_INF_F;
-    M = fmaxf(M, m);
+  if (k1 - k0 > 32) {  // pass 1 (long lists only): M over all records
+    for (int base = k0; base < k1; base += 32) {
+      const int k = base + lane;
+      M = fmaxf(M, k < k1 ? __ldcg(a.records + (long long)P[h.r_rec + k] * R + D) : -CUDART_INF_F);
+    }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
   float num[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) num[v] = 0.f;
   float den = 0.f;
-  if (M > -CUDART_INF_F) {
-    // pass 2: each batch's weights by lane, then its rows
-    for (int base = k0; base < k1; base += 32) {
-      const int k = base + lane;
-      const long long rid = k < k1 ? (long long)P[h.r_rec + k] : 0;
-      const float *rl = a.records + rid * R;
-      const float m = k < k1 ? __ldcg(rl + D) : -CUDART_INF_F;
-      const float l = k < k1 ? __ldcg(rl + D + 1) : 0.f;
-      const float f = m > -CUDART_INF_F ? fast_exp2(m - M) : 0.f;
-      float dl = f * l;
+  for (int base = k0; base < k1; base += 32) {
+    // this batch's records, one per lane, and their weights
+    const int k = base + lane;
+    const long long rid = k < k1 ? (long long)P[h.r_rec + k] : 0;
+    const float *rl = a.records + rid * R;
+    const float m = k < k1 ? __ldcg(rl + D) : -CUDART_INF_F;
+    const float l = k < k1 ? __ldcg(rl + D + 1) : 0.f;
+    if (k1 - k0 <= 32) {
+      M = m;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) dl += __shfl_xor_sync(kFullMask, dl, off);
-      den += dl;
-      const int n = min(32, k1 - base);
-#pragma unroll 4
-      for (int j = 0; j < n; ++j) {
-        const float fj = __shfl_sync(kFullMask, f, j);
-        const long long rj = __shfl_sync(kFullMask, rid, j);
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
+    }
+    const float f = m > -CUDART_INF_F ? fast_exp2(m - M) : 0.f;
+    float dl = f * l;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dl += __shfl_xor_sync(kFullMask, dl, off);
+    den += dl;
+    // the rows, eight records' loads in flight at a time
+    const int n = min(32, k1 - base);
+    for (int j0 = 0; j0 < n; j0 += 8) {
+      float x[8][V];
+      float w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int j = j0 + i;
+        const long long rj = __shfl_sync(kFullMask, rid, j & 31);
+        w[i] = j < n ? __shfl_sync(kFullMask, f, j & 31) : 0.f;
         const float *rec = a.records + rj * R + lane * V;
         if constexpr (V == 4) {
-          const float4 x = __ldcg(reinterpret_cast<const float4 *>(rec));
-          num[0] += fj * x.x;
-          num[1] += fj * x.y;
-          num[2] += fj * x.z;
-          num[3] += fj * x.w;
+          const float4 y = j < n ? __ldcg(reinterpret_cast<const float4 *>(rec)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          x[i][0] = y.x;
+          x[i][1] = y.y;
+          x[i][2] = y.z;
+          x[i][3] = y.w;
         } else {
 #pragma unroll
-          for (int v = 0; v < V; ++v) num[v] += fj * __ldcg(rec + v);
+          for (int v = 0; v < V; ++v) x[i][v] = j < n ? __ldcg(rec + v) : 0.f;
         }
       }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int v = 0; v < V; ++v) num[v] += w[i] * x[i][v];
     }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;

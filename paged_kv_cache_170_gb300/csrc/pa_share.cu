@@ -378,7 +378,19 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
         const int g = smgroup[k];
         const int r = smidx[k] * Gq + hh;
         const int u = ubase[g] + kv * passes[g] + r / prows[g];
-        for (int p = upoff[u]; p < upoff[u + 1]; ++p) rrec.push_back(p * kSharePassRows + r % prows[g]);
+        const int rin = r % prows[g];  // row of the pass
+        if (u >= Ut && u < Us) {  // the tensor-core kernel: one state per row and piece
+          for (int p = upoff[u]; p < upoff[u + 1]; ++p) rrec.push_back(p * kSharePassRows + rin);
+          continue;
+        }
+        // the CUDA-core kernel: one state per tile-lane that got a tile
+        const int prow = (r / prows[g]) * prows[g];
+        const int wr = pagedkv::share_row_warps(std::min(prows[g], int(groups[g].members.size()) * Gq - prow));
+        const int nl = 4 / wr;
+        for (int p = upoff[u]; p < upoff[u + 1]; ++p)
+          for (int tl = 0; tl < nl; ++tl)
+            if (pagedkv::share_lane_has_tile(p, pt1[p] - pt0[p], tl, nl))
+              rrec.push_back(p * kSharePassRows + tl * wr * 8 + rin);
       }
       roff[size_t(s) * Hq + hq + 1] = int32_t(rrec.size());
     }

@@ -40,7 +40,7 @@ constexpr int kTcGroupMinRows = 32;              // query rows per kv head from 
 constexpr int kTcItemRows = 128;                 // query rows of a tensor-core work item (one MMA tile, four passes)
 constexpr int kTcStepTokens64 = 64;              // tokens of a step of that kernel
 constexpr int kTcItemMinSteps = 4;               // a chunk's steps: at least this many ...
-constexpr int kTcItemMaxSteps = 32;              // ... and at most this many
+constexpr int kTcItemMaxSteps = 64;              // ... and at most this many
 
 // One work item of the tensor-core kernel: the query rows row0 .. row0 + 127
 // (fewer at the group's end) of one (group, kv head) against a chunk of the
@@ -58,6 +58,25 @@ struct TcItem {
 };
 constexpr int kTcItemInts = int(sizeof(TcItem) / sizeof(int32_t));
 static_assert(sizeof(TcItem) == 48, "three 16-byte loads");
+
+#ifdef __CUDACC__
+#define PA_SHARE_HD __host__ __device__
+#else
+#define PA_SHARE_HD
+#endif
+
+// Row-warps (8 rows each) the CUDA-core kernel gives a pass of `rows` query
+// rows: 1, 2 or 4.  Its four consumer warps form 4 / wr tile-lanes of wr
+// row-warps; tile t of piece p goes to tile-lane (t + p) mod (4 / wr), and
+// each tile-lane leaves its own partial states: row r of the pass in record
+// row tl * wr * 8 + r of the piece (the 32 record rows of a piece hold them
+// all, whatever wr).
+PA_SHARE_HD inline int share_row_warps(int rows) { return rows <= 8 ? 1 : (rows <= 16 ? 2 : 4); }
+
+// Whether tile-lane tl of nl got a tile of piece p, which has n tiles.
+PA_SHARE_HD inline bool share_lane_has_tile(int p, int n, int tl, int nl) {
+  return n >= nl || ((tl - p % nl + nl) % nl) < n;
+}
 
 // What a CTA needs at the start of a piece, in one record of the plan.
 struct PieceDesc {

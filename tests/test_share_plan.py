@@ -230,6 +230,34 @@ def _softmax_state(qv, keys, vals):
     return w @ vals, m, w.sum()
 
 
+def _row_warps(rows):
+    return 1 if rows <= 8 else (2 if rows <= 16 else 4)
+
+
+def _lanes(f, p, B, Gq):
+    """The partial states piece p leaves: (record row offset of the lane,
+    the piece's tiles it covers).  The tensor-core kernel leaves one state per
+    row over all the piece's tiles; the CUDA-core kernel one per tile-lane
+    that got a tile: tile t to lane (t + p) mod nl, lane tl's rows at record
+    row tl * wr * 8 + row of the pass."""
+    u = f["p_unit_arr"][p]
+    g, ps = f["u_group_arr"][u], f["u_pass_arr"][u]
+    moff = f["g_moff_arr"]
+    rows = (moff[g + 1] - moff[g]) * Gq
+    n = f["p_t1_arr"][p] - f["p_t0_arr"][p]
+    if g < f["num_shared_groups"] and B in (16, 32, 64) and rows >= TC_MIN_ROWS:
+        return [(0, list(range(n)))]
+    pr = f["g_prows_arr"][g]
+    wr = _row_warps(min(pr, rows - ps * pr))
+    nl = 4 // wr
+    out = []
+    for tl in range(nl):
+        ts = [t for t in range(n) if (t + p) % nl == tl]
+        if ts:
+            out.append((tl * wr * 8, ts))
+    return out
+
+
 def _emulate(f, q, kc, vc, tables, lens, scale):
     """The two steps of the shared decode, in float64, driven by the plan."""
     q, K, V = (x.double().numpy() for x in (q, kc, vc))
@@ -238,20 +266,24 @@ def _emulate(f, q, kc, vc, tables, lens, scale):
     Hkv, B = K.shape[1], K.shape[2]
     Gq = Hq // Hkv
     moff, mem = f["g_moff_arr"], f["g_members_arr"]
-    records = {}
+    records = {}  # record index (piece * 32 + record row) -> (acc, m, l)
     for p in range(f["num_pieces"]):
         u = f["p_unit_arr"][p]
         g, kvh, ps = f["u_group_arr"][u], f["u_kvh_arr"][u], f["u_pass_arr"][u]
         members = mem[moff[g]:moff[g + 1]]
         first = f["g_b0_arr"][g] + f["p_t0_arr"][p]
-        blocks = tables[members[0], first:f["g_b0_arr"][g] + f["p_t1_arr"][p]]
-        ntok = min(len(blocks) * B, int(lens[members[0]]) - first * B)  # a last block may be partly filled
-        keys = np.concatenate([K[b, kvh] for b in blocks])[:ntok]
-        vals = np.concatenate([V[b, kvh] for b in blocks])[:ntok]
         pr = f["g_prows_arr"][g]
-        for r in range(ps * pr, min(ps * pr + pr, len(members) * Gq)):
-            s, hh = members[r // Gq], r % Gq
-            records[(p, r % pr)] = _softmax_state(q[s, kvh * Gq + hh] * scale, keys, vals)
+        for off, ts in _lanes(f, p, B, Gq):
+            keys, vals = [], []
+            for t in ts:
+                b = first + t
+                ntok = min(B, int(lens[members[0]]) - b * B)  # a last block may be partly filled
+                keys.append(K[tables[members[0], b], kvh][:ntok])
+                vals.append(V[tables[members[0], b], kvh][:ntok])
+            keys, vals = np.concatenate(keys), np.concatenate(vals)
+            for r in range(ps * pr, min(ps * pr + pr, len(members) * Gq)):
+                s, hh = members[r // Gq], r % Gq
+                records[p * PASS_ROWS + off + r % pr] = _softmax_state(q[s, kvh * Gq + hh] * scale, keys, vals)
     out = np.zeros_like(q)
     roff, rrec = f["r_off_arr"], f["r_rec_arr"]
     assert len(roff) == S * Hq + 1
@@ -265,11 +297,11 @@ def _emulate(f, q, kc, vc, tables, lens, scale):
                 pr = f["g_prows_arr"][g]
                 u = f["g_ubase_arr"][g] + kvh * f["g_passes_arr"][g] + r // pr
                 for p in range(f["u_poff_arr"][u], f["u_poff_arr"][u + 1]):
-                    want.append(p * PASS_ROWS + r % pr)
+                    want += [p * PASS_ROWS + off + r % pr for off, _ in _lanes(f, p, B, Gq)]
             row = s * Hq + h
             got = [int(x) for x in rrec[roff[row]:roff[row + 1]]]
             assert got == want  # the merge's list of the row
-            states = [records[(x // PASS_ROWS, x % PASS_ROWS)] for x in got]
+            states = [records[x] for x in got]
             if states:
                 M = max(m for _, m, _ in states)
                 num = sum(a * np.exp(m - M) for a, m, _ in states)
