@@ -38,7 +38,9 @@ KERNEL_SOURCES = ["paged_kv_cache_170_gb300/csrc/pa_decode_mma.cuh", "paged_kv_c
                   "paged_kv_cache_170_gb300/csrc/pa_mma_tile.cuh",
                   "paged_kv_cache_170_gb300/csrc/pa_common.cuh"]  # the tensor-core decode kernel
 SHARED_SOURCES = KERNEL_SOURCES + ["paged_kv_cache_170_gb300/csrc/pa_decode_shared.cuh",
-                                   "paged_kv_cache_170_gb300/csrc/pa_share.cu"]  # the shared-block decode's two kernels
+                                   "paged_kv_cache_170_gb300/csrc/pa_share.cu",
+                                   "paged_kv_cache_170_gb300/csrc/pa_share_plan.h",
+                                   "paged_kv_cache_170_gb300/csrc/pa_prefill.cuh"]  # the shared-block decode's kernels
 PREFILL_SOURCES = ["paged_kv_cache_170_gb300/csrc/pa_prefill.cuh", "paged_kv_cache_170_gb300/csrc/pa_sched.cuh",
                    "paged_kv_cache_170_gb300/csrc/pa_common.cuh"]  # the tcgen05 prefill kernel
 
@@ -147,12 +149,13 @@ def needs_l2_flush(inp, mode: str = "auto") -> bool:
     return unique_kv_bytes(inp) < 4 * L2_BYTES
 
 
-def decode_kernel_name(inp, shared: bool, fused: bool = False) -> str:
+def decode_kernel_name(inp, shared: bool, fused: bool = False, shared_kernels=None) -> str:
     """The kernel(s) the timed decode call runs: the tensor-core kernel takes
     fp16 / bf16 caches whose block size is a multiple of 16; pa_write_decode
-    runs the write kernel first."""
-    if shared:
-        return "decode_shared_mma_kernel + merge_shared_kernel"
+    runs the write kernel first; the shared decode runs the kernels its plan
+    needs."""
+    if shared and shared_kernels:
+        return " + ".join(shared_kernels)
     name = "decode_partition_mma_kernel" if inp.k_cache.dtype != torch.float32 and inp.k_cache.shape[2] % 16 == 0 \
         else "decode_partition_kernel"
     return "append_last_kernel + " + name + " (pa_write_decode, timed as one call)" if fused else name
@@ -459,17 +462,18 @@ def run_gpu(args) -> dict:
                            "(programmatic dependent launch)" if runner.fused
                            else "slot lookup, K/V write, then decode", runner.launches_per_step,
                            "" if runner.launches_per_step == 1 else "es"),
-                       decode="pa_decode_shared (plan: %d shared and %d own groups, %d pieces)" % (
+                       decode="pa_decode_shared (plan: %d shared and %d own groups, %d pieces, %d tensor-core "
+                              "items)" % (
                            runner.plan_info["num_shared_groups"],
                            runner.plan_info["num_groups"] - runner.plan_info["num_shared_groups"],
-                           runner.plan_info["num_pieces"]) if args.shared
+                           runner.plan_info["num_pieces"], runner.plan_info["num_tc_items"]) if args.shared
                        else "pa_decode"),
         "tokens_per_s": round(sum_over_ranks(float(S), dist) / (step_ms_max * 1e-3), 0),
         "pct_of_nominal_8000_gbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / peaks["hbm_gbs"], 2),
         "decode_kernel_us": round(kernel_ms * 1e3, 2),
         "decode_kernel_us_median": round(statistics.median(kernel_times) * 1e3, 2),
-        "roofline": {"kernel": decode_kernel_name(inp, args.shared, runner.fused), "bound": "hbm", "achieved": round(achieved, 1),
+        "roofline": {"kernel": decode_kernel_name(inp, args.shared, runner.fused, runner.shared_kernels), "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
                      "frac_of_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4),

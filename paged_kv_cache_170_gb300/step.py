@@ -111,6 +111,7 @@ class DecodeStep:
         self.shared = shared
         self.fused = fused and not shared and one_token_per_sequence(inp)
         decode_launches = 1
+        self.shared_kernels = []  # the shared decode's kernels, when it is not the plain decode
         if shared:
             # the plan follows the tables as the decode sees them; this step
             # only writes into private blocks, so it stays valid across replays
@@ -119,7 +120,13 @@ class DecodeStep:
             self.plan_info = {k: v for k, v in ops.plan_fields(self.plan).items() if not k.endswith("_arr")}
             self.workspace = ops.new_shared_workspace(self.plan, S, Hq, Hkv, D, dev)
             if self.plan_info["num_shared_groups"] > 0:
-                decode_launches = 2  # every group's blocks, then the merge
+                # the dense groups on the tensor cores, the other groups' blocks, then the merge
+                f = ops.plan_fields(self.plan)
+                cp, co = f["c_poff_arr"], f["c_opoff_arr"]
+                self.shared_kernels = (["prefill_tc_kernel (dense groups)"] if self.plan_info["num_tc_items"] else []) + \
+                    (["decode_shared_mma_kernel"] if int(cp[-1] - cp[0] + co[-1] - co[0]) > 0 else []) + \
+                    ["merge_shared_kernel"]
+                decode_launches = len(self.shared_kernels)
         else:
             self.workspace = ops.new_workspace(S, Hq, Hkv, D, dev)
         self.slots = torch.empty(inp.new_seq.numel(), dtype=torch.int64, device=dev)
