@@ -248,19 +248,17 @@ pa_status check_decode_call(const void *out, const void *q, const void *k_cache,
   return PA_OK;
 }
 
-// pa_decode, optionally over each sequence's blocks from start_block[s] on,
-// with fp32 output rows (out_f32) and their log2-sum-exp (lse), or (new_key
-// non-null, pa_write_decode) with each sequence's token at position
-// context_lens[s] - 1 written first.  early_launch: the previous kernel in the
-// stream lets this one start launching before it ends (it triggers
-// griddepcontrol.launch_dependents); the decode's producer waits for it
-// before its first copy.
+// pa_decode, or (new_key non-null, pa_write_decode) with each sequence's
+// token at position context_lens[s] - 1 written first.  early_launch: the
+// previous kernel in the stream lets this one start launching before it ends
+// (it triggers griddepcontrol.launch_dependents); the decode's producer waits
+// for it before its first copy.
 static pa_status decode_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
                              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
                              int64_t num_blocks, float scale, pa_dtype dtype, void *workspace, size_t workspace_bytes,
-                             int *debug_err, void *stream, const int32_t *start_block, float *out_f32, float *lse,
-                             const void *new_key = nullptr, const void *new_value = nullptr,
+                             int *debug_err, void *stream, const void *new_key = nullptr,
+                             const void *new_value = nullptr,
                              bool early_launch = false) {
   DecodeShape sh;
   pa_status st = check_decode_call(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
@@ -268,8 +266,7 @@ static pa_status decode_impl(void *out, const void *q, const void *k_cache, cons
                                    workspace, &sh);
   if (st != PA_OK || num_seqs == 0) return st;
   if (workspace_bytes < workspace_bytes_for(num_seqs, num_heads, head_dim, sh.nctas)) return PA_ERR_WORKSPACE;
-  if (new_key != nullptr && (new_value == nullptr || !aligned16(new_key) || !aligned16(new_value) ||
-                             start_block != nullptr))
+  if (new_key != nullptr && (new_value == nullptr || !aligned16(new_key) || !aligned16(new_value)))
     return PA_ERR_INVALID_ARG;
 
   DecodeArgs a;
@@ -299,9 +296,6 @@ static pa_status decode_impl(void *out, const void *q, const void *k_cache, cons
   a.nops = 1;
   a.q_offset = sh.q_offset;
   a.q_bytes = sh.q_bytes;
-  a.start_block = start_block;
-  a.out_f32 = out_f32;
-  a.lse = lse;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   bool early = early_launch && sh.mma;  // the decode may start launching while the previous kernel runs
   if (new_key != nullptr) {
@@ -334,7 +328,7 @@ extern "C" pa_status pa_decode(void *out, const void *q, const void *k_cache, co
                                size_t workspace_bytes, int *debug_err, void *stream) {
   return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_heads,
                      num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace, workspace_bytes,
-                     debug_err, stream, nullptr, nullptr, nullptr);
+                     debug_err, stream);
 }
 
 extern "C" pa_status pa_write_decode(void *out, const void *q, const void *new_key, const void *new_value,
@@ -346,7 +340,7 @@ extern "C" pa_status pa_write_decode(void *out, const void *q, const void *new_k
   if (num_seqs > 0 && (new_key == nullptr || new_value == nullptr)) return PA_ERR_INVALID_ARG;
   return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_heads,
                      num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace, workspace_bytes,
-                     debug_err, stream, nullptr, nullptr, nullptr, new_key, new_value);
+                     debug_err, stream, new_key, new_value);
 }
 
 // ------------------------------------------------------ shared-block decode

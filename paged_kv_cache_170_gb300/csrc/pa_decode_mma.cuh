@@ -301,10 +301,6 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
               store_out1<T>(a, row0 + h1, 16 * mt + g + 8, D, o[mt][3] * i1);
             }
           }
-          if (g == 0) {
-            if (h0 < GT) store_lse(a, row0 + h0, m0, l0);
-            if (h1 < GT) store_lse(a, row0 + h1, m1, l1);
-          }
         } else {
           const int b = nbuf == 2 ? int(dep & 1) : 0;
           const long long use = nbuf == 2 ? (dep >> 1) : dep;

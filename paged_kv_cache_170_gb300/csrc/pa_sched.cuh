@@ -62,32 +62,17 @@ struct DecodeArgs {
   int nops;                // tensor copies per tile (1: one 3-D box; 2: two 2-D halves)
   uint32_t q_offset;       // tensor-core kernel: offset of the q rows inside a slot
   uint32_t q_bytes;        // tensor-core kernel: bytes of q rows of one pair chunk (GT * D * e)
-  // Set only by the shared-block decode, which runs this kernel over each
-  // sequence's own blocks (null in a plain decode):
-  const int32_t *start_block;  // [S] first block of each sequence to read (earlier ones are shared, done elsewhere)
-  float *out_f32;              // [S][Hq][D] fp32 output rows, written instead of `out`
-  float *lse;                  // [S][Hq] log2-sum-exp of each row, m + log2(l); -inf for a row with no tokens
 };
 
-// Output row `row` (= s * Hq + hq), dims d .. d+3, to `out` (or `out_f32`).
+// Output row `row` (= s * Hq + hq), dims d .. d+3 (store_out4) or d.
 template <typename T>
 __device__ __forceinline__ void store_out4(const DecodeArgs &a, long long row, int d, int D, float4 v) {
-  if (a.out_f32 != nullptr)
-    *reinterpret_cast<float4 *>(a.out_f32 + row * D + d) = v;
-  else
-    Elem<T>::store4(static_cast<T *>(a.out) + row * D + d, v);
+  Elem<T>::store4(static_cast<T *>(a.out) + row * D + d, v);
 }
 
 template <typename T>
 __device__ __forceinline__ void store_out1(const DecodeArgs &a, long long row, int d, int D, float v) {
-  if (a.out_f32 != nullptr)
-    a.out_f32[row * D + d] = v;
-  else
-    static_cast<T *>(a.out)[row * D + d] = Elem<T>::from_float(v);
-}
-
-__device__ __forceinline__ void store_lse(const DecodeArgs &a, long long row, float m, float l) {
-  if (a.lse != nullptr) a.lse[row] = l > 0.f ? m + __log2f(l) : -CUDART_INF_F;
+  static_cast<T *>(a.out)[row * D + d] = Elem<T>::from_float(v);
 }
 
 // Wait until ring entry e (slot e % nstage, its u-th use, u = e / nstage) has
@@ -117,19 +102,8 @@ __device__ __forceinline__ int clamped_len(const DecodeArgs &a, int s) {
   return L < 0 ? 0 : (L > cap ? cap : L);
 }
 
-// First block of sequence s this call reads (0 unless start_block is given).
-__device__ __forceinline__ int first_block(const DecodeArgs &a, int s) {
-  return a.start_block != nullptr ? a.start_block[s] : 0;
-}
-
-// Tokens of sequence s this call attends over: its clamped length less the
-// blocks before first_block (full blocks, handled elsewhere).
-__device__ __forceinline__ int eff_len(const DecodeArgs &a, int s) {
-  const int L = clamped_len(a, s);
-  if (a.start_block == nullptr) return L;
-  const long long rest = (long long)L - (long long)first_block(a, s) * a.B;
-  return rest < 0 ? 0 : int(rest);
-}
+// Tokens of sequence s the decode attends over: its clamped length.
+__device__ __forceinline__ int eff_len(const DecodeArgs &a, int s) { return clamped_len(a, s); }
 
 __device__ __forceinline__ int blocks_of(const DecodeArgs &a, int s) {
   return (eff_len(a, s) + a.B - 1) / a.B;
@@ -291,14 +265,12 @@ __device__ __forceinline__ bool phase_range(const Plan &p, int ph, long long *fr
 // Cursor over a CTA's tile range, one segment (consecutive tiles of one
 // (s, pc)) at a time.  Producer and consumers walk identical sequences.
 struct Walk {
-  int s, pc, b, nb, L;  // L: tokens of s this call reads (eff_len, read once per sequence)
-  int fb;               // first_block(s): table index of this call's block 0
+  int s, pc, b, nb, L;  // L: tokens of s (eff_len, read once per sequence)
   long long w;
   long long cp;         // cost position where the current segment starts
   __device__ __forceinline__ void start(const DecodeArgs &a, int s0, long long r0, long long w0, long long c0) {
     s = s0;
     L = eff_len(a, s);
-    fb = first_block(a, s);
     nb = (L + a.B - 1) / a.B;
     pc = int(r0 / nb);
     b = int(r0 % nb);
@@ -321,7 +293,6 @@ struct Walk {
         } while (s < a.S && blocks_of(a, s) == 0);
         if (s < a.S) {
           L = eff_len(a, s);
-          fb = first_block(a, s);
           nb = (L + a.B - 1) / a.B;
         }
       }
@@ -369,7 +340,7 @@ __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, con
       const int n = wk.seg_len(to);
       const int kvh = wk.pc / HC;
       const int L = wk.L;
-      const int32_t *trow = a.tables + (long long)wk.s * a.max_blocks + wk.fb + wk.b;
+      const int32_t *trow = a.tables + (long long)wk.s * a.max_blocks + wk.b;
       int pid_next = lane < n ? trow[lane] : -1;
 #ifdef PA_TRACE
       {
@@ -462,7 +433,6 @@ __device__ __forceinline__ void zero_empty_rows(const DecodeArgs &a, int D, int 
   for (int s = blockIdx.x; s < a.S; s += a.nctas) {
     if (eff_len(a, s) != 0) continue;
     for (int i = tid; i < a.Hq * D; i += nthreads) store_out1<T>(a, (long long)s * a.Hq + i / D, i % D, D, 0.f);
-    for (int i = tid; i < a.Hq; i += nthreads) store_lse(a, (long long)s * a.Hq + i, 0.f, 0.f);
   }
 }
 
@@ -569,7 +539,6 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
       den += __shfl_xor_sync(kFullMask, den, 1);
       den += __shfl_xor_sync(kFullMask, den, 2);
       const float wt = complete ? (mine ? f / den : 0.f) : f;
-      if (complete && lq == 0 && lh < GT) store_lse(a, (long long)s * a.Hq + hq0 + lh, M, den);
       float *rec = nullptr;
       if (!complete) {
         long long ro = ((long long)blockIdx.x * 2 + (first_seg ? 0 : 1)) * 8 * R;
@@ -697,7 +666,6 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
             float den = fv * lv;
             den += __shfl_xor_sync(kFullMask, den, 8);
             const float wv = has ? fv / den : 0.f;  // weight of record rs for head hh
-            if (rs == 0 && hh < GT) store_lse(a, (long long)s * a.Hq + hq0 + hh, Mh, den);
 #pragma unroll
             for (int i = 0; i < kIters; ++i) {
               if (32 * i >= GT * C4) break;
@@ -735,7 +703,6 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
               }
               const float inv = 1.f / dr;
               for (int r = 0; r < nrec; ++r) sh_m[r * 8 + h] *= inv;
-              store_lse(a, (long long)s * a.Hq + hq0 + h, Mr, dr);
             }
             __syncwarp();
             float4 acc[kIters];
@@ -783,7 +750,6 @@ __device__ __forceinline__ void run_merger(const DecodeArgs &a, const Plan &plan
                 dr += fr * __ldcg(rr + D + 1);
               }
               store_out1<T>(a, (long long)s * a.Hq + hq0 + h, d, D, num / dr);
-              if (d == 0) store_lse(a, (long long)s * a.Hq + hq0 + h, Mr, dr);
             }
           }
         }

@@ -150,6 +150,8 @@ def test_shared_decode_own_groups_of_two_passes(ops, B):
     (32, 64, torch.float16, 12, 16, 2, 21),    # 96 rows, two blocks per step
     (64, 128, torch.bfloat16, 9, 32, 8, 7),    # 36 rows, one block per step
     (16, 64, torch.bfloat16, 8, 32, 8, 64),    # exactly 32 rows, a run of 16 whole steps
+    (16, 128, torch.float16, 40, 8, 8, 23),    # one query head per kv head (G = 1): 40 rows
+    (32, 128, torch.bfloat16, 4, 64, 4, 11),   # G = 16: a member's 16 heads fill half a pass
 ])
 def test_shared_decode_tensor_core_groups(ops, B, D, dtype, members, Hq, Hkv, run):
     """Groups with 32 or more query rows per kv head are computed on the
