@@ -1,22 +1,28 @@
-// pa_decode_shared.cuh -- the two kernels of the shared-block decode:
+// pa_decode_shared.cuh -- two of the three kernels of the shared-block decode
+// (the third, for the dense groups, is prefill_tc_kernel's groups mode in
+// pa_prefill.cuh: shared groups of 32 or more query rows per kv head, 128
+// rows against a chunk of the run per CTA, on the tensor cores):
 //
-// decode_shared_mma_kernel (step 1): every group's blocks against the query
-//   rows of all its members: the shared groups' runs of full blocks, and each
-//   sequence's own group (its private blocks, the last one partly filled).  A
-//   CTA walks its pieces (plan: c_poff) in order; one producer warp streams
-//   each piece's K and V tiles into a ring by TMA.  The four consumer warps
-//   take the unit's pass of up to 32 query rows (row = member * G + head) as
-//   wr row-warps of 8 rows times 4 / wr tile-lanes: with 32 rows all four
-//   warps work on every tile, so a tile read once serves 32 rows of up to 32
-//   sequences; with 8 rows (every own group) each warp takes every fourth
-//   tile, and the tile-lanes' states are combined in shared memory at the
-//   piece's end.  Each piece leaves one partial state (acc, m, l) per row of
-//   its pass in `records`.
-//   Every consumer waits for every entry in order, so the ring's mbarrier
-//   parity waits are exact (no warp can lag a full ring behind another).
+// decode_shared_mma_kernel (step 1): every other group's blocks against the
+//   query rows of all its members: the smaller shared groups' runs of full
+//   blocks, and each sequence's own group (its private blocks, the last one
+//   partly filled).  A CTA walks its pieces (plan: c_poff, c_opoff) in
+//   order; one producer warp streams each piece's K and V tiles into a ring
+//   by TMA.  The four consumer warps take the unit's pass of up to 32 query
+//   rows (row = member * G + head) as wr row-warps of 8 rows times 4 / wr
+//   tile-lanes: with 32 rows all four warps work on every tile, so a tile
+//   read once serves 32 rows of up to 32 sequences; with 8 rows (every own
+//   group) each warp takes every fourth tile (tile t of piece p to lane
+//   (t + p) mod 4).  Each tile-lane that got a tile leaves one partial state
+//   (acc, m, l) per row of its pass in `records`, at record row
+//   tl * wr * 8 + row of the piece.  Every consumer waits for every entry in
+//   order, so the ring's mbarrier parity waits are exact (no warp can lag a
+//   full ring behind another).  Launched early beside the tensor-core
+//   kernel when there is one, it waits for that grid before it exits.
 //
-// merge_shared_kernel (step 2): per output row (s, h), the partial states of
-//   every piece of every group s belongs to, merged with a running maximum:
+// merge_shared_kernel (step 2): per output row (s, h), the partial states the
+//   plan lists for it (r_off, r_rec): every tile-lane state of every piece of
+//   every group s belongs to,
 //     M = max_i m_i;  out = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i.
 #pragma once
 

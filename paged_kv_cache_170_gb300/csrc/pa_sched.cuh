@@ -315,9 +315,9 @@ struct Walk {
 //
 // The producer's copies are the kernel's first reads of the pools, so it is
 // where the kernel waits for the grid it depends on (griddepcontrol.wait: a
-// no-op unless the launch allowed an early start, as pa_write_decode's and
-// the shared-block decode's own-block step do, so that the plan and the
-// barriers are set up while the previous kernel runs).
+// no-op unless the launch allowed an early start, as pa_write_decode's does,
+// so that the plan and the barriers are set up while the previous kernel
+// runs).
 template <class Issue>
 __device__ __forceinline__ void produce(const DecodeArgs &a, int PC, int HC, const Plan &plan, int lane,
                                         uint64_t *full_bar, uint64_t *empty_bar, uint32_t *issued,

@@ -119,7 +119,7 @@ def test_shared_decode_edge_cases(ops, dtype):
         ref = native.decode(q, kc, vc, tables.numpy(), lens.numpy(), scale)
         assert_attention_close(out, ref, strict=False)
         assert torch.count_nonzero(out[2]) == 0  # empty sequence: zero row
-        # every sequence's blocks all shared and full: the own-block step has no tiles
+        # every sequence's blocks all shared and full: no own group, no own tiles
         full = torch.tensor([row] * 4, dtype=torch.int32)
         lens_full = torch.full((4,), 144, dtype=torch.int32)
         out, f = _shared(ops, q[:4].to(DEV), args[1], args[2], full.to(DEV), lens_full.to(DEV), scale)
