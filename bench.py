@@ -46,16 +46,45 @@ PREFILL_SOURCES = ["paged_kv_cache_170_gb300/csrc/pa_prefill.cuh", "paged_kv_cac
 
 
 def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
-    """Hash of the kernel's code with comments and blank space removed: an
-    edit of comments alone leaves a profiled kernel the same kernel."""
+    """Hash of the kernel's code with comments, blank space and trace-build
+    blocks (`#ifdef PA_TRACE`, not compiled in a product build) removed: an
+    edit of those alone leaves a profiled kernel the same kernel."""
     h = hashlib.sha256()
     for rel in sources:
         with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
-        h.update("\n".join(line.strip() for line in text.splitlines() if line.strip()).encode())
+        h.update("\n".join(_product_lines(text.splitlines())).encode())
     return h.hexdigest()[:16]
+
+
+def _product_lines(lines):
+    """The stripped, non-blank lines a build without PA_TRACE compiles: the
+    body of each `#ifdef PA_TRACE` is dropped up to its `#else` or `#endif`."""
+    out, depth, skipping = [], 0, False
+    for raw in lines:
+        line = raw.strip()
+        if not line:
+            continue
+        directive = line.split()[0] if line.startswith("#") else ""
+        if skipping:
+            if directive in ("#if", "#ifdef", "#ifndef"):
+                depth += 1
+            elif directive == "#endif":
+                if depth == 0:
+                    skipping = False
+                else:
+                    depth -= 1
+            elif directive == "#else" and depth == 0:
+                skipping = False
+                out.append("#ifndef PA_TRACE")
+            continue
+        if line == "#ifdef PA_TRACE":
+            skipping, depth = True, 0
+            continue
+        out.append(line)
+    return out
 
 
 def measured_peaks() -> dict:

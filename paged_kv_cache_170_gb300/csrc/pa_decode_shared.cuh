@@ -93,6 +93,10 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+#ifdef PA_TRACE
+  unsigned long long tg0, tg_first = 0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tg0));
+#endif
   const int32_t *P = a.plan;
   const SharePlanHeader &h = a.h;
   const int Gq = h.group_size;
@@ -270,6 +274,9 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
       }
       __syncwarp();
       ok = __all_sync(kFullMask, ok);
+#ifdef PA_TRACE
+      if (tg_first == 0) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tg_first));
+#endif
       const uint32_t kt = ring_addr + uint32_t(slot) * a.slot_stride;
 #ifdef PA_TRACE
       const long long tr_m0 = clock64();
@@ -348,6 +355,13 @@ __global__ void __launch_bounds__(kSharedThreads, kCtasPerSm)
 #endif
   }
 #ifdef PA_TRACE
+  if (lane == 0 && warp == 0) {  // every CTA: start, first tile, end of consumer warp 0
+    unsigned long long tg1;
+    unsigned sm;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tg1));
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+    printf("traces1 %d %u %llu %llu %llu %d\n", blockIdx.x, sm, tg0, tg_first, tg1, pl.n);
+  }
   if (lane == 0 && PA_TRACE_CTA(blockIdx.x))
     printf("trace shared cta %d warp %d: pieces %d tiles %lld cycles %lld setup %lld wait %lld math %lld end %lld\n",
            blockIdx.x, warp, pl.n, tr_tiles, clock64() - tr_c0, tr_setup, tr_wait, tr_math, tr_end);
@@ -378,6 +392,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_shared_kernel(const Me
   constexpr int V = D / 32;  // dims per lane
   const long long row = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+#ifdef PA_TRACE
+  unsigned long long tm0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tm0));
+#endif
   if (row >= (long long)a.S * a.Hq) return;
   const int32_t *P = a.plan;
   const SharePlanHeader &h = a.h;
@@ -443,6 +461,13 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_shared_kernel(const Me
   T *o = static_cast<T *>(a.out) + row * D + lane * V;
 #pragma unroll
   for (int v = 0; v < V; ++v) o[v] = Elem<T>::from_float(num[v] * inv);
+#ifdef PA_TRACE
+  if (threadIdx.x == 0) {
+    unsigned long long tm1;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tm1));
+    printf("tracem %d %llu %llu\n", blockIdx.x, tm0, tm1);
+  }
+#endif
 }
 
 }  // namespace pagedkv

@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 #ifdef PA_TRACE
-  unsigned long long tc_g0;
+  unsigned long long tc_g0, tc_gq = 0, tc_ge = 0, tc_gs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tc_g0));
 #endif
   // the shared-block decode's other step may start launching now: it reads
@@ -473,6 +473,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     tc_fence_after();
   }
   const uint32_t tmem = warp != 4 ? tmem_base : 0u;  // the producer never touches TMEM
+#ifdef PA_TRACE
+  if (threadIdx.x == 0) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tc_gq));
+#endif
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
@@ -654,6 +657,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       ok = __all_sync(kFullMask, ok);
       if (!ok) break;
       if (threadIdx.x == 0) TC_TRACE(j, 0);
+#ifdef PA_TRACE
+      if (threadIdx.x == 0 && j < 8) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tc_gs[j]));
+#endif
       tc_fence_after();
       const uint32_t sb = tl + uint32_t(D + kTcStepTokens * (j & 1));
       // a partly filled last block: zero its V rows past the context before the PV MMAs read them
@@ -734,6 +740,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       ok = mbar_wait(&o_done[(nstep - 1) & 1], uint32_t((nstep - 1) >> 1) & 1u, abort_flag);
       ok = __all_sync(kFullMask, ok);
     }
+#ifdef PA_TRACE
+    if (threadIdx.x == 0) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tc_ge));
+#endif
     if (ok && kGroups) {
       // the row's partial state (O, m, l) in the record of its pass's piece:
       // softmax warp w holds pass 4 * (r0 / 128) + w, row lane of it
@@ -803,6 +812,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     pa_prefill_cta_trace[blockIdx.x][0] = tc_g0;
     pa_prefill_cta_trace[blockIdx.x][1] = g1;
     pa_prefill_cta_trace[blockIdx.x][2] = (uint64_t(sm) << 32) | uint32_t(nstep);
+    if (kGroups)  // the groups mode's timeline: start, Q staged, S_0 .. S_3 seen, epilogue, end
+      printf("tracetc %d %u %llu %llu %llu %llu %llu %llu %llu %llu %d\n", blockIdx.x, sm, tc_g0, tc_gq, tc_gs[0],
+             tc_gs[1], tc_gs[2], tc_gs[3], tc_ge, g1, nstep);
   }
 #endif
 }

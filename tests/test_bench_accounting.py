@@ -56,3 +56,12 @@ def test_flush_writes_then_reads_its_buffer():
     buf = torch.zeros(1 << 12, dtype=torch.uint8)
     bench.flush_l2(buf, 300)
     assert int(buf[0]) == 300 & 255 and bool((buf == buf[0]).all())
+
+
+def test_profile_hash_ignores_trace_blocks_but_not_their_else_branch():
+    src = ["int a;", "#ifdef PA_TRACE", "#if X", "t();", "#endif", "u();", "#endif", "int b;",
+           "#ifdef PA_TRACE", "v();", "#else", "w();", "#endif", "  ", "int c;"]
+    assert bench._product_lines(src) == ["int a;", "int b;", "#ifndef PA_TRACE", "w();", "#endif", "int c;"]
+    # a product line inside a trace block's else branch is part of the hash
+    assert bench._product_lines(src[:11] + ["x();"] + src[12:]) != bench._product_lines(src)
+    assert bench._product_lines(["#ifdef PA_TRACE", "z();", "#endif"]) == []
