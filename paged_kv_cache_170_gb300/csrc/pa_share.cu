@@ -187,6 +187,9 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
   // piece is the part of one unit inside one CTA's range of one line; the
   // pieces of a unit are consecutive.
   std::vector<int32_t> punit, pt0, pt1, cpoff(nctas + 1, 0), copoff(nctas + 1, 0), upoff(U + 1, 0);
+  // cumw[c]: the CTAs before c's share of each line, in units of cumw[nctas]
+  std::vector<long long> cumw(nctas + 1);
+  for (int c = 0; c <= nctas; ++c) cumw[c] = c;
   auto split = [&](int ua, int ub, std::vector<int32_t> &coff) {
     std::vector<long long> wp(size_t(ub - ua) + 1, 0);  // cost before each unit of the line
     for (int u = ua; u < ub; ++u)
@@ -195,7 +198,7 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
     std::vector<long long> cs(nctas + 1, utile0[ub]);  // first (flattened) tile of each CTA
     int i = 0;
     for (int c = 0; c < nctas; ++c) {
-      const long long target = (long long)c * Wc / nctas;
+      const long long target = (long long)((__int128)Wc * cumw[c] / cumw[nctas]);
       while (ua + i < ub && wp[i + 1] <= target) ++i;
       if (ua + i == ub) break;
       const int u = ua + i;
@@ -221,7 +224,6 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
   };
   const int Us = num_shared < G ? ubase[num_shared] : U;  // the own groups' units follow the shared ones
   const int Ut = num_mma_shared < G ? ubase[num_mma_shared] : U;  // the tensor-core groups' units, [Ut, Us)
-  split(0, Ut, cpoff);
   // the tensor-core groups' pieces: chunks of their runs, the same for every
   // pass; a chunk is sp steps of 64 tokens.  The items run two per SM
   // (nctas slots at a time): sp is the smallest length at which the items
@@ -236,7 +238,7 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
     for (long long i = 0; i < (long long)Hkv * tiles; ++i) tc_run_steps.push_back(st);
     tc_steps += (long long)Hkv * tiles * st;
   }
-  long long sp = kTcItemMinSteps;
+  long long sp = kTcItemMinSteps, num_items = 0;
   if (tc_steps > 0) {
     const long long slots = nctas;
     const long long waves = std::max<long long>(1, (tc_steps + slots * kTcItemMaxSteps - 1) / (slots * kTcItemMaxSteps));
@@ -247,7 +249,31 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
       return n;
     };
     while (sp < kTcItemMaxSteps && items_of(sp) > waves * slots) ++sp;
+    num_items = items_of(sp);
   }
+  // The CUDA-core step is launched while the tensor-core items run, so its
+  // CTAs that find no room start only as the items end: with n <= nctas
+  // items, one per SM beside one step CTA (or two on an SM beside none), the
+  // last n CTAs of the step (the block scheduler places CTAs in index order)
+  // start about one item's time late.  Those CTAs get that much less of
+  // each line: shares s_e = (W + n C) / nctas and s_e - C, where W is the
+  // step's total cost and C an item's time in the same units, kTcItemFixedCost
+  // + sp * kTcItemStepCost (taken from A/B timings on a GB300: of C = 0, 82,
+  // 123 and 160 for the shared-prefix workload's 4-step items, 82 was the
+  // fastest; the late CTAs then stream alone and run faster than the others).
+  long long W = 0;
+  for (int u = 0; u < U; ++u)
+    if (u < Ut || u >= Us) W += kUnitCost + (utile0[u + 1] - utile0[u]) * ucost[u];
+  if (num_items > 0 && num_items < nctas && W > 0) {
+    const long long n = num_items, C = kTcItemFixedCost + sp * kTcItemStepCost;
+    long long se = W + n * C, sl = se - C * nctas;  // nctas times the shares
+    if (sl < 0) {  // the late CTAs get nothing
+      se = W * nctas / std::max<long long>(1, nctas - n);
+      sl = 0;
+    }
+    for (int c = 0; c < nctas; ++c) cumw[c + 1] = cumw[c] + (c < nctas - n ? se : sl);
+  }
+  split(0, Ut, cpoff);
   const long long chunk_tiles = sp * bps;
   for (int u = Ut; u < Us; ++u) {
     const long long nb = utile0[u + 1] - utile0[u];
@@ -367,6 +393,7 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
   const int NT = int(titems.size()) / kTcItemInts;
   place(h.t_items, (long long)titems.size());
   h.num_tc_items = NT;
+  h.tc_chunk_steps = NT > 0 ? int32_t(sp) : 0;
   // each output row's records: every membership of its sequence, the unit of
   // the row's pass, that unit's pieces
   const int Hq = num_heads;

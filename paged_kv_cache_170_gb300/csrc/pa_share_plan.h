@@ -41,6 +41,8 @@ constexpr int kTcItemRows = 128;                 // query rows of a tensor-core 
 constexpr int kTcStepTokens64 = 64;              // tokens of a step of that kernel
 constexpr int kTcItemMinSteps = 4;               // a chunk's steps: at least this many ...
 constexpr int kTcItemMaxSteps = 64;              // ... and at most this many
+constexpr int kTcItemFixedCost = 50;             // a tensor-core item's time, in CUDA-core step cost units:
+constexpr int kTcItemStepCost = 8;               // this much, plus this much per step
 
 // One work item of the tensor-core kernel: the query rows row0 .. row0 + 127
 // (fewer at the group's end) of one (group, kv head) against a chunk of the
@@ -107,6 +109,7 @@ struct SharePlanHeader {
   int32_t c_opoff, p_desc;    // offsets of c_opoff[nctas+1] and p_desc[P]
   int32_t num_tc_items, t_items;  // the tensor-core kernel's work items and their offset
   int32_t r_off, r_rec;           // offsets of r_off[S*Hq+1] and r_rec[...]
+  int32_t tc_chunk_steps;         // 64-token steps of a tensor-core chunk (the last of a run may be shorter)
 };
 
 constexpr int kSharePlanHeaderInts = int(sizeof(SharePlanHeader) / sizeof(int32_t));
@@ -122,7 +125,9 @@ using pagedkv::kSharePassRows;
 using pagedkv::kSharePlanHeaderInts;
 using pagedkv::kSharePlanMagic;
 using pagedkv::kTcGroupMinRows;
+using pagedkv::kTcItemFixedCost;
 using pagedkv::kTcItemInts;
+using pagedkv::kTcItemStepCost;
 using pagedkv::kTcItemMaxSteps;
 using pagedkv::kTcItemMinSteps;
 using pagedkv::kTcItemRows;

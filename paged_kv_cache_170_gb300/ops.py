@@ -259,7 +259,7 @@ PLAN_FIELDS = ["magic", "total_ints", "num_seqs", "num_groups", "num_units", "nu
                "num_kv_heads", "block_size", "max_blocks", "total_members", "total_memberships", "g_moff",
                "g_members", "g_b0", "g_b1", "g_ubase", "g_passes", "u_group", "u_kvh", "u_pass", "u_poff", "p_unit",
                "p_t0", "p_t1", "c_poff", "s_start", "s_moff", "s_mgroup", "s_midx", "own_tiles", "num_shared_groups",
-               "g_prows", "c_opoff", "p_desc", "num_tc_items", "t_items", "r_off", "r_rec"]
+               "g_prows", "c_opoff", "p_desc", "num_tc_items", "t_items", "r_off", "r_rec", "tc_chunk_steps"]
 
 
 def share_plan(block_tables: torch.Tensor, context_lens: torch.Tensor, block_size: int, num_heads: int,

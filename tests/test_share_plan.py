@@ -159,6 +159,7 @@ def _check_structure(f, tables, lens, B, Hq, Hkv):
     # a unit whose pass has <= 8, <= 16 or more rows costs 3, 4 or 5, and a
     # unit UNIT_COST once), to within one tile and one unit start
     UNIT_COST = 8
+    TC_FIXED_COST, TC_STEP_COST = 50, 8  # a tensor-core item's time in step cost units: fixed + per step
 
     def cost(u):
         g = f["u_group_arr"][u]
@@ -174,15 +175,33 @@ def _check_structure(f, tables, lens, B, Hq, Hkv):
     tc_pieces = list(range(f["c_poff_arr"][N], f["c_opoff_arr"][0]))
     assert f["c_poff_arr"][0] == 0 and f["c_opoff_arr"][N] == P
     assert sorted(tc_pieces) == [p for u in tc_units for p in range(poff[u], poff[u + 1])]
+    # The step's CTAs that start only once the tensor-core items are done
+    # (the last n of them, n = items <= N) get an item's time C less of each
+    # line: shares (W + n C) / N and that minus C, W the cost of both lines
+    line_total = {id(units): sum((b1[f["u_group_arr"][u]] - b0[f["u_group_arr"][u]]) * cost(u) + UNIT_COST
+                                 for u in units) for units in (shared_units, own_units)}
+    W = sum(line_total.values())
+    n = f["num_tc_items"]
+    weights = [1] * N
+    if 0 < n < N and W > 0:
+        C = TC_FIXED_COST + f["tc_chunk_steps"] * TC_STEP_COST
+        se, sl = W + n * C, W + n * C - C * N
+        if sl < 0:
+            se, sl = W * N // max(1, N - n), 0
+        weights = [se] * (N - n) + [sl] * n
+    cum = np.concatenate([[0], np.cumsum(weights)])
     for units, coff in ((shared_units, f["c_poff_arr"]), (own_units, f["c_opoff_arr"])):
         per_cta = [sum((f["p_t1_arr"][p] - f["p_t0_arr"][p]) * cost(f["p_unit_arr"][p]) +
                        (UNIT_COST if f["p_t0_arr"][p] == 0 else 0)
                        for p in range(coff[c], coff[c + 1])) for c in range(N)]
-        total = sum((b1[f["u_group_arr"][u]] - b0[f["u_group_arr"][u]]) * cost(u) + UNIT_COST for u in units)
+        total = line_total[id(units)]
         assert sum(per_cta) == total
         assert all(f["p_unit_arr"][p] in units for p in range(coff[0], coff[N]))
         if units:
-            assert max(per_cta) - total / N <= UNIT_COST + max(cost(u) for u in units)
+            slack = UNIT_COST + max(cost(u) for u in units)
+            done = np.cumsum(per_cta)
+            for c in range(N):  # each CTA's range ends within a tile and a unit start of its weighted share
+                assert abs(done[c] - total * cum[c + 1] / cum[N]) <= slack
     # a tensor-core group's units are all cut into the same chunks; every
     # tensor-core piece belongs to exactly one item, which names the pieces of
     # the passes of its 128 rows against one chunk
