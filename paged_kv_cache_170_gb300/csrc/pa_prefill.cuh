@@ -84,11 +84,15 @@ constexpr int kTcMaxSlots = 4;               // step slots per ring, at most
 // Step slots of the K and V rings: a K slot is free again once its QK is
 // done, early in a step; a V slot only once its PV is done, so V gets one more.
 // With head_dim 128: Q 32 KB + K 2 x 16 KB + V 3 x 16 KB = 112 KB, two CTAs per SM.
-__host__ __device__ constexpr int tc_k_slots(int D) { return D == 128 ? 2 : 4; }
-__host__ __device__ constexpr int tc_v_slots(int D) { return D == 128 ? 3 : 4; }
+// The shared-block decode's items (groups) are a few steps long and start
+// with a chain of dependent loads: their keys are requested three steps ahead
+// (K 3 x 16 KB + V 2 x 16 KB, the same 112 KB).
+__host__ __device__ constexpr int tc_k_slots(int D, bool groups = false) { return D == 128 ? (groups ? 3 : 2) : 4; }
+__host__ __device__ constexpr int tc_v_slots(int D, bool groups = false) { return D == 128 ? (groups ? 2 : 3) : 4; }
 __host__ __device__ constexpr int tc_smem_bytes(int D) {
   return (D / 64) * kTcRows * 128 + (tc_k_slots(D) + tc_v_slots(D)) * (D / 64) * kTcStepTokens * 128;
 }
+static_assert(tc_k_slots(128, true) + tc_v_slots(128, true) == tc_k_slots(128) + tc_v_slots(128), "same footprint");
 constexpr int kTcCols = 256;                 // TMEM columns: O (D) | S/P buffer 0 (64) | S/P buffer 1 (64)
 
 // Shared memory matrix descriptor (tcgen05): 128-byte swizzle, version 1.
@@ -286,7 +290,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   constexpr uint32_t SHALF = kTcStepTokens * 128;  // one 64-column half of a step slot
   static_assert(D + 2 * kTcStepTokens <= kTcCols, "TMEM budget");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  constexpr int NKS = tc_k_slots(D), NVS = tc_v_slots(D);
+  constexpr int NKS = tc_k_slots(D, kGroups), NVS = tc_v_slots(D, kGroups);
   constexpr uint32_t SS = HALVES * SHALF;  // bytes per step slot
   static_assert(NKS <= kTcMaxSlots && NVS <= kTcMaxSlots, "slots");
   __shared__ __align__(8) uint64_t k_full[kTcMaxSlots];
