@@ -39,7 +39,7 @@ constexpr int kUnitCost = 8;                     // fixed cost of a unit in the 
 constexpr int kTcGroupMinRows = 32;              // query rows per kv head from which a shared group takes the tensor cores
 constexpr int kTcItemRows = 128;                 // query rows of a tensor-core work item (one MMA tile, four passes)
 constexpr int kTcStepTokens64 = 64;              // tokens of a step of that kernel
-constexpr int kTcItemMinSteps = 4;               // a chunk's steps: at least this many ...
+constexpr int kTcItemMinSteps = 8;               // a chunk's steps: at least this many ...
 constexpr int kTcItemMaxSteps = 64;              // ... and at most this many
 constexpr int kTcItemFixedCost = 50;             // a tensor-core item's time, in CUDA-core step cost units:
 constexpr int kTcItemStepCost = 8;               // this much, plus this much per step
