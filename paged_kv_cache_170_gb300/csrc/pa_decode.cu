@@ -494,7 +494,9 @@ extern "C" pa_status pa_decode_shared(void *out, const void *q, const void *k_ca
     ta.records = records;
     ta.plan = plan_dev;
     ta.t_items = h->t_items;
-    ta.g_members = h->g_members;
+    ta.t_qrow = h->t_qrow;
+    ta.t_blk = h->t_blk;
+    ta.t_blk_stride = h->t_blk_stride;
     const size_t smem = size_t(tc_smem_bytes(head_dim));
     const dim3 grid{unsigned(h->num_tc_items), 1u, 1u};
     st = dtype == PA_BF16 ? prefill_dispatch<__nv_bfloat16, true>(ta, k_cache, v_cache, dtype, head_dim, smem, grid, s)

@@ -74,7 +74,9 @@ struct PrefillArgs {
   float *records;        // [piece][kSharePassRows][state_row(D)] partial states
   const int32_t *plan;   // device copy of the plan
   int32_t t_items;       // offset of its TcItem array
-  int32_t g_members;     // offset of its member list
+  int32_t t_qrow;        // offset of each item's q rows [item][kTcRows]
+  int32_t t_blk;         // offset of each item's physical blocks [item][t_blk_stride]
+  int32_t t_blk_stride;
 };
 
 constexpr int kTcRows = 128;                 // query rows per CTA (= TMEM lanes)
@@ -290,8 +292,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   constexpr uint32_t SHALF = kTcStepTokens * 128;  // one 64-column half of a step slot
   static_assert(D + 2 * kTcStepTokens <= kTcCols, "TMEM budget");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  constexpr int NKS = tc_k_slots(D, kGroups), NVS = tc_v_slots(D, kGroups);
   constexpr uint32_t SS = HALVES * SHALF;  // bytes per step slot
+  constexpr int NKS = tc_k_slots(D, kGroups), NVS = tc_v_slots(D, kGroups);
   static_assert(NKS <= kTcMaxSlots && NVS <= kTcMaxSlots, "slots");
   __shared__ __align__(8) uint64_t k_full[kTcMaxSlots];
   __shared__ __align__(8) uint64_t v_full[kTcMaxSlots], v_empty[kTcMaxSlots];
@@ -315,23 +317,41 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   // position of its first query row (pos0) and where its q rows start (q0)
   int kvh, rows, r0, ntile, L, pos0 = 0, q0 = 0;
   const int32_t *trow0;
-  const int32_t *members = nullptr;  // kGroups: the group's sequences
-  int piece[4] = {-1, -1, -1, -1};   // kGroups: the record piece of each pass (32 rows)
+  int piece[4] = {-1, -1, -1, -1};  // kGroups: the record piece of each pass (32 rows)
+  // the Q tile's loads: thread t takes 16-byte chunks t + 128 k (k < kPer), a
+  // warp RW rows per k, RK rows apart
+  constexpr int kPer = kTcRows * D / 8 / 128, CPR = D / 8, RW = 32 / CPR, RK = kTcRows / CPR;
+  const int bps = kTcStepTokens / B;         // blocks per step
+  const int kbpw = (bps * HALVES + 3) >> 2;  // K boxes per softmax warp in a full step: 1 or 2
+  const int kfirst = (warp & 3) * kbpw;      // this warp's first box
+  int kpid0[NKS];                            // lane 0 of a softmax warp: its blocks of the first NKS steps
+  int myq = -1;  // kGroups: q row (sequence * Hq + head) of one of this warp's Q rows, -1 past the group's
   if constexpr (kGroups) {
+    // the item's q rows and blocks are at fixed strides: requested together
+    // with the item itself, one round trip before the Q tile and first keys
+    trow0 = a.plan + a.t_blk + (long long)blockIdx.x * a.t_blk_stride;
+    if (warp < 4) {
+      myq = a.plan[a.t_qrow + (long long)blockIdx.x * kTcRows + RW * warp + lane % RW + RK * (lane / RW)];
+      if (lane == 0) {
+#pragma unroll
+        for (int jj = 0; jj < NKS; ++jj) {
+          const int b = jj * bps + kfirst / HALVES;
+          kpid0[jj] = b < a.t_blk_stride ? trow0[b] : -1;
+        }
+      }
+    }
     const int4 *it = reinterpret_cast<const int4 *>(a.plan + a.t_items + (long long)blockIdx.x * kTcItemInts);
     const int4 w0 = it[0], w1 = it[1], w2 = it[2];
     kvh = w0.y;
     r0 = w0.z;
     rows = w0.w;
-    members = a.plan + a.g_members + w1.y;
-    trow0 = a.tables + (long long)w1.x * a.max_blocks + w1.z;
     ntile = w1.w;
     piece[0] = w2.x;
     piece[1] = w2.y;
     piece[2] = w2.z;
     piece[3] = w2.w;
     L = ntile * B;  // shared blocks are full
-    if (ntile <= 0 || r0 >= rows) {
+    if (ntile <= 0 || ntile > a.t_blk_stride || r0 >= rows) {
       if (threadIdx.x == 0) raise_error(a.err, PA_DEVERR_CONTEXT);  // not an item the planner makes
       return;
     }
@@ -360,7 +380,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     ntile = p_last / B + 1;
     trow0 = a.tables + (long long)s * a.max_blocks;
   }
-  const int bps = kTcStepTokens / B;  // blocks per step
   const int nstep = (ntile + bps - 1) / bps;
 
   // shared memory: Q tile, K ring, V ring.  The swizzled tiles need a
@@ -402,8 +421,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   // tokens][128 B]); a warp's boxes lie in one block.  K(j + NKS) goes into
   // the slot of K(j) as soon as the warp sees S_j, i.e. QK(j) done.
   const int32_t *ktrow = trow0;
-  const int kbpw = (bps * HALVES + 3) >> 2;     // boxes per warp in a full step: 1 or 2
-  const int kfirst = (warp & 3) * kbpw;          // this warp's first box
   auto k_entry = [&](int jj) {                   // the table entry of this warp's block of step jj
     const int b = jj * bps + kfirst / HALVES;
     return (jj < nstep && b < ntile) ? ktrow[b] : 0;
@@ -427,26 +444,28 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   if (warp < 4) {
     // ---- the Q tile: rows r0 .. r0 + 127, K-major halves [128 rows][128 B],
     // swizzled; every load is issued before the first store
-    constexpr int kPer = kTcRows * D / 8 / 128;  // 16-byte chunks per thread
-    const int t = threadIdx.x;                    // 0..127
-    int kpid0[NKS];
+    const int t = threadIdx.x;  // 0..127
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_k)) : "memory");
+      if constexpr (!kGroups) {
 #pragma unroll
-      for (int jj = 0; jj < NKS; ++jj) kpid0[jj] = k_entry(jj);
+        for (int jj = 0; jj < NKS; ++jj) kpid0[jj] = k_entry(jj);
+      }
       kpid_next = k_entry(NKS);
     }
     uint4 v[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int i = t + 128 * k;
-      const int r = i / (D / 8), c = i % (D / 8);  // row, 16-byte chunk
+      const int r = i / CPR, c = i % CPR;  // row, 16-byte chunk
       const int gr = r0 + r;
       v[k] = make_uint4(0u, 0u, 0u, 0u);
-      if (gr < rows) {
-        const long long qrow = kGroups ? (long long)members[gr / G] : (long long)(q0 + gr / G);
-        v[k] = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.q) + (qrow * a.Hq + kvh * G + gr % G) * D +
-                                                c * 8);
+      if constexpr (kGroups) {
+        const int qi = __shfl_sync(kFullMask, myq, lane / CPR + RW * k);  // row r's q row
+        if (qi >= 0) v[k] = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.q) + (long long)qi * D + c * 8);
+      } else if (gr < rows) {
+        v[k] = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.q) +
+                                                ((long long)(q0 + gr / G) * a.Hq + kvh * G + gr % G) * D + c * 8);
       }
     }
     if (lane == 0) {  // the first NKS steps' keys, while the Q loads are in flight

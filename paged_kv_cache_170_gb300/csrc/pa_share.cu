@@ -57,6 +57,7 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
       num_heads % num_kv_heads != 0 || nctas <= 0 || plan_ints == nullptr)
     return PA_ERR_INVALID_ARG;
   if (num_seqs > 0 && (block_tables == nullptr || context_lens == nullptr)) return PA_ERR_INVALID_ARG;
+  if ((long long)num_seqs * num_heads > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;  // q rows are int32 in the plan
   const int S = num_seqs, B = block_size, Gq = num_heads / num_kv_heads, Hkv = num_kv_heads;
   const long long cap = (long long)max_blocks_per_seq * B;
 
@@ -394,6 +395,20 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
   place(h.t_items, (long long)titems.size());
   h.num_tc_items = NT;
   h.tc_chunk_steps = NT > 0 ? int32_t(sp) : 0;
+  // each item's q rows and physical blocks, at fixed strides
+  const int blk_stride = NT > 0 ? int(chunk_tiles) : 0;
+  std::vector<int32_t> tqrow((size_t)NT * kTcItemRows, -1), tblk((size_t)NT * blk_stride, -1);
+  for (int i = 0; i < NT; ++i) {
+    const int32_t *it = titems.data() + (size_t)i * kTcItemInts;
+    const int g = it[0], kv = it[1], r0 = it[2], rows = it[3], leader = it[4], blk0 = it[6], nt = it[7];
+    for (int r = 0; r < kTcItemRows && r0 + r < rows; ++r)
+      tqrow[(size_t)i * kTcItemRows + r] =
+          groups[g].members[(r0 + r) / Gq] * num_heads + kv * Gq + (r0 + r) % Gq;
+    for (int j = 0; j < nt; ++j) tblk[(size_t)i * blk_stride + j] = id(leader, blk0 + j);
+  }
+  place(h.t_qrow, (long long)tqrow.size());
+  place(h.t_blk, (long long)tblk.size());
+  h.t_blk_stride = blk_stride;
   // each output row's records: every membership of its sequence, the unit of
   // the row's pass, that unit's pieces
   const int Hq = num_heads;
@@ -494,6 +509,8 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
     put(h.p_desc, d.data(), (long long)d.size());
   }
   put(h.t_items, titems.data(), (long long)titems.size());
+  put(h.t_qrow, tqrow.data(), (long long)tqrow.size());
+  put(h.t_blk, tblk.data(), (long long)tblk.size());
   put(h.r_off, roff.data(), (long long)roff.size());
   put(h.r_rec, rrec.data(), (long long)rrec.size());
   return PA_OK;

@@ -21,7 +21,12 @@
 //             row (s, query head), as record indices piece * kSharePassRows
 //             + row of its pass, for the merge
 //   tc items  t_items[num_tc_items] (one TcItem each, 16-byte aligned): the
-//             work of the tensor-core kernel.  A shared group with at least
+//             work of the tensor-core kernel; per item, at fixed strides so
+//             that the kernel reads them without waiting for the item,
+//             t_qrow[item][kTcItemRows] (each row's q row, sequence * Hq +
+//             query head, or -1 past the group's rows) and
+//             t_blk[item][t_blk_stride] (the chunk's physical blocks, -1 past
+//             its ntile).  A shared group with at least
 //             kTcGroupMinRows query rows per kv head is a dense contraction
 //             (rows x the run's tokens): its units' pieces are token chunks,
 //             cut the same way for the four passes of each 128-row tile, and
@@ -110,6 +115,8 @@ struct SharePlanHeader {
   int32_t num_tc_items, t_items;  // the tensor-core kernel's work items and their offset
   int32_t r_off, r_rec;           // offsets of r_off[S*Hq+1] and r_rec[...]
   int32_t tc_chunk_steps;         // 64-token steps of a tensor-core chunk (the last of a run may be shorter)
+  int32_t t_qrow;                 // offset of t_qrow[num_tc_items][kTcItemRows]
+  int32_t t_blk, t_blk_stride;    // offset of t_blk[num_tc_items][t_blk_stride]
 };
 
 constexpr int kSharePlanHeaderInts = int(sizeof(SharePlanHeader) / sizeof(int32_t));

@@ -259,7 +259,8 @@ PLAN_FIELDS = ["magic", "total_ints", "num_seqs", "num_groups", "num_units", "nu
                "num_kv_heads", "block_size", "max_blocks", "total_members", "total_memberships", "g_moff",
                "g_members", "g_b0", "g_b1", "g_ubase", "g_passes", "u_group", "u_kvh", "u_pass", "u_poff", "p_unit",
                "p_t0", "p_t1", "c_poff", "s_start", "s_moff", "s_mgroup", "s_midx", "own_tiles", "num_shared_groups",
-               "g_prows", "c_opoff", "p_desc", "num_tc_items", "t_items", "r_off", "r_rec", "tc_chunk_steps"]
+               "g_prows", "c_opoff", "p_desc", "num_tc_items", "t_items", "r_off", "r_rec", "tc_chunk_steps",
+               "t_qrow", "t_blk", "t_blk_stride"]
 
 
 def share_plan(block_tables: torch.Tensor, context_lens: torch.Tensor, block_size: int, num_heads: int,
@@ -292,7 +293,8 @@ def plan_fields(plan: torch.Tensor) -> dict:
          "p_t1": hdr["num_pieces"], "c_poff": hdr["nctas"] + 1, "s_start": hdr["num_seqs"],
          "s_moff": hdr["num_seqs"] + 1, "s_mgroup": hdr["total_memberships"], "s_midx": hdr["total_memberships"],
          "g_prows": hdr["num_groups"], "c_opoff": hdr["nctas"] + 1, "p_desc": hdr["num_pieces"] * 12,
-         "t_items": hdr["num_tc_items"] * 12}
+         "t_items": hdr["num_tc_items"] * 12, "t_qrow": hdr["num_tc_items"] * 128,
+         "t_blk": hdr["num_tc_items"] * hdr["t_blk_stride"]}
     out = dict(hdr)
     for k, cnt in n.items():
         out[k + "_arr"] = p[hdr[k]:hdr[k] + cnt]

@@ -230,6 +230,19 @@ def _check_structure(f, tables, lens, B, Hq, Hkv):
             seen.append(p)
     assert sorted(seen) == tc_pieces
     assert list(items[:, 7]) == sorted(items[:, 7], reverse=True)  # the longest chunks first
+    # each item's q rows (sequence * Hq + head, -1 past the group's rows) and
+    # physical blocks (-1 past its chunk), at fixed strides
+    stride = f["t_blk_stride"]
+    qrows = f["t_qrow_arr"].reshape(-1, TC_ITEM_ROWS)
+    blks = f["t_blk_arr"].reshape(-1, stride) if stride else f["t_blk_arr"].reshape(0, 0)
+    assert len(qrows) == len(items) and len(blks) == len(items)
+    assert not len(items) or stride == f["tc_chunk_steps"] * (64 // B)
+    for it, qr, bl in zip(items, qrows, blks):
+        g, kvh, row0, rows, leader, mo, blk0, ntile = (int(x) for x in it[:8])
+        want = [int(mem[moff[g] + r // Gq]) * Hq + kvh * Gq + r % Gq if r < rows else -1
+                for r in range(row0, row0 + TC_ITEM_ROWS)]
+        assert list(qr) == want
+        assert list(bl) == [int(tables[leader, blk0 + j]) if j < ntile else -1 for j in range(stride)]
     # the packed descriptors repeat the piece's unit, tiles and group fields
     desc = f["p_desc_arr"].reshape(P, 12)
     for p in range(P):
