@@ -18,7 +18,7 @@ DEV = "cuda"
 
 
 def assert_prefill_close(got, ref):
-    """The benchmark spec bar for a bf16 / fp16 output: max relative error <= 1e-2
+    """The attention bar for a bf16 / fp16 output: max relative error <= 1e-2
     over |ref| >= 1e-2, and max absolute error <= 2e-3 where |ref| < 0.5.  A
     prompt's early rows see few tokens, so their outputs reach |out| ~ 1..4,
     where the rounding of the output alone (up to 2^-8 relative in bf16)
