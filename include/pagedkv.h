@@ -256,11 +256,16 @@ PA_API size_t pa_decode_shared_workspace_size(const int32_t *plan_host, int num_
  * plus the plan that pa_share_plan built from these tables: plan_host (host
  * copy, read for its sizes) and plan_dev (device copy of the same ints,
  * 16-byte aligned).  fp16 / bf16 caches with block_size a multiple of 16
- * only (else PA_ERR_UNSUPPORTED).  Two launches on `stream`:
- *   1. every group's blocks against the query rows of all its members (a
- *      group is a shared run of full blocks, or one sequence's own blocks):
- *      the four consumer warps of a CTA share each tile, 8 query rows each,
- *      and each piece of the work leaves a partial state (acc, m, l) per row;
+ * only (else PA_ERR_UNSUPPORTED).  Up to three launches on `stream`:
+ *   1a. the shared groups with 32 or more query rows per kv head (block size
+ *      16, 32 or 64), on the tensor cores: one CTA per work item of the plan,
+ *      128 query rows against a chunk of the group's run (the plan holds each
+ *      item's q rows and physical blocks);
+ *   1b. every other group's blocks against the query rows of all its members
+ *      (a group is a shared run of full blocks, or one sequence's own blocks),
+ *      launched to start while 1a runs: the four consumer warps of a CTA
+ *      share each tile, 8 query rows each;
+ *      each piece of 1a and 1b leaves a partial state (acc, m, l) per row;
  *   2. per (sequence, head), the merge of the partial states of every group
  *      it belongs to:
  *      M = max_i m_i;  out = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i.

@@ -356,7 +356,9 @@ static const SharePlanHeader *check_plan(const int32_t *plan_host, int num_seqs,
       h->max_blocks != max_blocks_per_seq || h->nctas <= 0 || h->num_pieces < 0 || h->total_ints < kSharePlanHeaderInts ||
       h->num_shared_groups < 0 || h->num_shared_groups > h->num_groups || (h->p_desc & 3) != 0 ||
       h->num_tc_items < 0 || (h->t_items & 3) != 0 ||
-      (long long)h->t_items + (long long)h->num_tc_items * kTcItemInts > h->total_ints ||
+      (long long)h->t_items + (long long)h->num_tc_items * kTcItemInts > h->total_ints || h->t_qrow < 0 ||
+      (long long)h->t_qrow + (long long)h->num_tc_items * kTcItemRows > h->total_ints || h->t_blk < 0 ||
+      h->t_blk_stride < 0 || (long long)h->t_blk + (long long)h->num_tc_items * h->t_blk_stride > h->total_ints ||
       (long long)h->r_off + (long long)num_seqs * num_heads + 1 > h->total_ints || h->r_rec > h->total_ints)
     return nullptr;
   return h;
