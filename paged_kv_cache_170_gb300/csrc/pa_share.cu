@@ -261,7 +261,8 @@ extern "C" pa_status pa_share_plan(const int32_t *block_tables, int max_blocks_p
   // step's total cost and C an item's time in the same units, kTcItemFixedCost
   // + sp * kTcItemStepCost (taken from A/B timings on a GB300: of C = 0, 82,
   // 123 and 160 for the shared-prefix workload's 4-step items, 82 was the
-  // fastest; the late CTAs then stream alone and run faster than the others).
+  // fastest, and of C = 86, 100, 114 and 130 for its 8-step items, 100; the
+  // late CTAs then stream alone and run faster than the others).
   long long W = 0;
   for (int u = 0; u < U; ++u)
     if (u < Ut || u >= Us) W += kUnitCost + (utile0[u + 1] - utile0[u]) * ucost[u];

@@ -46,7 +46,7 @@ constexpr int kTcItemRows = 128;                 // query rows of a tensor-core 
 constexpr int kTcStepTokens64 = 64;              // tokens of a step of that kernel
 constexpr int kTcItemMinSteps = 8;               // a chunk's steps: at least this many ...
 constexpr int kTcItemMaxSteps = 64;              // ... and at most this many
-constexpr int kTcItemFixedCost = 50;             // a tensor-core item's time, in CUDA-core step cost units:
+constexpr int kTcItemFixedCost = 36;             // a tensor-core item's time, in CUDA-core step cost units:
 constexpr int kTcItemStepCost = 8;               // this much, plus this much per step
 
 // One work item of the tensor-core kernel: the query rows row0 .. row0 + 127

@@ -159,7 +159,7 @@ def _check_structure(f, tables, lens, B, Hq, Hkv):
     # a unit whose pass has <= 8, <= 16 or more rows costs 3, 4 or 5, and a
     # unit UNIT_COST once), to within one tile and one unit start
     UNIT_COST = 8
-    TC_FIXED_COST, TC_STEP_COST = 50, 8  # a tensor-core item's time in step cost units: fixed + per step
+    TC_FIXED_COST, TC_STEP_COST = 36, 8  # a tensor-core item's time in step cost units: fixed + per step
 
     def cost(u):
         g = f["u_group_arr"][u]
