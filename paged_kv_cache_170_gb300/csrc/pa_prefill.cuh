@@ -312,9 +312,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   if constexpr (kGroups) launch_dependents();
   const int G = a.Hq / a.Hkv;
   const int B = a.B;
-  // the CTA's rows r0 .. r0 + 127 (of `rows`), its blocks (ntile, from the
-  // table entry trow0 on), the tokens they hold (L) and, for a prompt, the
-  // position of its first query row (pos0) and where its q rows start (q0)
+  // the CTA's rows r0 .. r0 + 127 (of `rows`), its blocks (ntile physical
+  // block ids from trow0 on: the sequence's table row, or for a group the
+  // item's block list in the plan), the tokens they hold (L) and, for a
+  // prompt, the position of its first query row (pos0) and where its q rows
+  // start (q0)
   int kvh, rows, r0, ntile, L, pos0 = 0, q0 = 0;
   const int32_t *trow0;
   int piece[4] = {-1, -1, -1, -1};  // kGroups: the record piece of each pass (32 rows)
